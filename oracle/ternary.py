@@ -1,0 +1,81 @@
+"""Block-128 absmean ternary quantizer and its packed form. TEST INFRASTRUCTURE ONLY.
+
+Follows ``block_ternary(w, block_size=128, eps=1e-8)`` of "Ternary Bonsai 2",
+section 1.2: per block of 128 consecutive weights along K,
+scale = mean(|w|) + eps and q = clamp(round(w / scale), -1, 1). Readings where
+the page is silent or garbled:
+
+* the ``+`` before ``eps`` was lost in extraction; the scale is mean|w| + 1e-8;
+* ``round`` is round-half-to-even (torch.round);
+* the decision uses the unrounded float64 scale; the stored scale is that
+  value rounded to fp16 (nearest even), which is what dequantization uses;
+* mean|w| is the float64 sum over k = 0..127 in order, divided by 128;
+* an all-zero block has scale 1e-8, q = 0 and a stored fp16 scale of 0
+  (section 3.4 / 5.5 describe such blocks; no flag is stored in this format).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import layout
+from .numerics import f16_bits_to_f64, f64_to_f16_bits
+
+BLOCK = 128
+EPS = 1e-8
+CODE = {0: 0b00, 1: 0b01, -1: 0b10}
+
+
+def quantize(w: np.ndarray):
+    """w float32 [N][K] -> (q int8 [N][K], s_star float64 [N][K/128], s16 uint16 [N][K/128])."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert K % BLOCK == 0
+    blocks = w.astype(np.float64).reshape(N, K // BLOCK, BLOCK)
+    acc = np.zeros((N, K // BLOCK), dtype=np.float64)
+    for k in range(BLOCK):                       # sum |w| in column order
+        acc += np.abs(blocks[:, :, k])
+    s_star = acc / BLOCK + EPS
+    q = np.clip(np.rint(blocks / s_star[:, :, None]), -1, 1).astype(np.int8)
+    return q.reshape(N, K), s_star, f64_to_f16_bits(s_star)
+
+
+def codes_of(q: np.ndarray) -> np.ndarray:
+    q = np.asarray(q)
+    return np.where(q == 1, 1, np.where(q == -1, 2, 0)).astype(np.uint32)
+
+
+def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
+    """Packed ternary buffer (layout in ``oracle.layout``)."""
+    N, K = q.shape
+    c = codes_of(q).reshape(N, K // 16, 16)
+    words = np.zeros((N, K // 16), dtype=np.uint32)
+    for r in range(16):
+        words |= c[:, :, r] << np.uint32(layout.ternary_bit_pos(r))
+    offs, total = layout.sections(layout.ternary_sizes(N, K))
+    buf = bytearray(total)
+    buf[offs[0]:offs[0] + words.nbytes] = words.astype("<u4").tobytes()
+    s = np.asarray(s16, dtype="<u2")
+    buf[offs[1]:offs[1] + s.nbytes] = s.tobytes()
+    return bytes(buf)
+
+
+def unpack(buf: bytes, N: int, K: int):
+    """Inverse of ``pack``: (q int8 [N][K], s16 uint16 [N][K/128]). Code 11 is rejected."""
+    offs, total = layout.sections(layout.ternary_sizes(N, K))
+    assert len(buf) >= total
+    words = np.frombuffer(buf, dtype="<u4", count=N * K // 16, offset=offs[0]).reshape(N, K // 16)
+    c = np.empty((N, K // 16, 16), dtype=np.uint32)
+    for r in range(16):
+        c[:, :, r] = (words >> np.uint32(layout.ternary_bit_pos(r))) & 3
+    if np.any(c == 3):
+        raise ValueError("invalid ternary code 11")
+    q = np.where(c == 1, 1, np.where(c == 2, -1, 0)).astype(np.int8).reshape(N, K)
+    s16 = np.frombuffer(buf, dtype="<u2", count=N * (K // 128), offset=offs[1]).reshape(N, K // 128)
+    return q, s16.copy()
+
+
+def dequant(q: np.ndarray, s16: np.ndarray) -> np.ndarray:
+    """w_hat = q * fp16 scale of its block, float64 [N][K]."""
+    N, K = q.shape
+    s = f16_bits_to_f64(s16)
+    return (q.reshape(N, K // BLOCK, BLOCK).astype(np.float64) * s[:, :, None]).reshape(N, K)
