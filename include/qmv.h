@@ -1,0 +1,220 @@
+/*
+ * qmv.h - C ABI of libqmv: fused dequantize-and-matvec for the decode step of
+ * a compressed LLM, on one GB300 (sm_103a).
+ *
+ * The operation every entry point serves is y = W_hat x at batch 1 up to a
+ * small number M of speculative-verification tokens, where W_hat is a packed,
+ * quantized N x K weight matrix and x holds M bf16 activation rows. Decoding at
+ * low batch reads every active weight once per token, so the packed weight
+ * stream is the cost ("Nemotron 3.5 Bolt", why-only-weights section; "Cassandra",
+ * section 2: FFN weight loading dominates decode).
+ *
+ * Conventions shared by every call:
+ *  - Device pointers point into memory the caller allocated (for example with
+ *    torch); the library never allocates or frees device memory. Host pointers
+ *    are marked "host".
+ *  - Every device buffer must be 16-byte aligned; activation row strides must
+ *    keep each row 16-byte aligned (ldx a multiple of 8 bf16 elements).
+ *  - Calls are asynchronous on the caller's CUDA stream (`stream` is a
+ *    cudaStream_t passed as void*; NULL = legacy default stream) and never
+ *    synchronize. They return a qmv_status and never throw or abort.
+ *  - Argument errors are found on the host before any launch and leave every
+ *    output untouched. Corrupt packed data found by a kernel sets a per-device
+ *    error word (read with qmv_check_status); the kernel still ends normally.
+ *  - qmv_last_error() gives a message for the calling thread's last failure.
+ *  - W is N x K (output rows x input columns). Quantization blocks/groups are
+ *    128 consecutive columns of one row. x is bf16 [M][ldx], y is fp32 [M][ldy].
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMV_ABI_VERSION 1
+#define QMV_GROUP 128          /* block/group size along K for ternary and INT4 */
+#define QMV_MAX_SECTIONS 8
+#define QMV_MAX_M 16           /* activation rows per call */
+#define QMV_MAX_BATCH 448      /* matvecs per qmv_run_batch call */
+
+typedef enum {
+  QMV_OK = 0,
+  QMV_ERR_ARG = -1,          /* bad argument, size or descriptor */
+  QMV_ERR_ALIGN = -2,        /* pointer or stride misaligned */
+  QMV_ERR_UNSUPPORTED = -3,  /* valid request this build does not serve */
+  QMV_ERR_CORRUPT = -4,      /* a kernel met packed data that breaks the format */
+  QMV_ERR_CUDA = -5,         /* a CUDA runtime call failed (message has the CUDA error) */
+  QMV_ERR_TIMEOUT = -6       /* reserved: a bounded device wait gave up */
+} qmv_status;
+
+typedef enum {
+  QMV_TERNARY2 = 1,          /* block-128 absmean ternary, 2 bits + fp16 scale per block */
+  QMV_INT4 = 2,              /* group-128 absmax/7 INT4, 4 bits + fp16 scale per group */
+  QMV_CASS = 3               /* Cassandra lossless bf16 split (speculation + verification) */
+} qmv_format;
+
+/*
+ * Layout descriptor of one packed matrix: a contiguous buffer of sections,
+ * each starting on a 256-byte boundary (off[i] bytes from the start).
+ *
+ * QMV_TERNARY2 ("Ternary Bonsai 2", section 1.2, block_ternary):
+ *   0 codes : N x K/16 uint32; word (n, k/16) holds columns k0..k0+15; column
+ *             r = k%16 at bit r (r even) or bit 15+r (r odd); code 00 = 0,
+ *             01 = +1, 10 = -1 (11 is invalid).
+ *   1 scales: N x K/128 fp16, scale = fp16(mean|w| + 1e-8) of each block.
+ * QMV_INT4 ("GPT-5.4 ..." section 3.2, group-wise quantization):
+ *   0 codes : N x K/8 uint32; column r = k%8 at bit 2r (r even) or 14+2r
+ *             (r odd); 4-bit two's complement, -7..7.
+ *   1 scales: N x K/128 fp16, scale = fp16(max|w| / 7) of each group.
+ * QMV_CASS ("Cassandra", sections 3.1-3.3):
+ *   0 bitmap : N x K/32 uint32, bit j%32 of word j/32 set = value (n, j) kept
+ *   1 signmant: N x K/16 uint32, nibble i = S<<3 | (M>>4) of the i-th kept value
+ *   2 expstream: unary exponent codes (rank r = r zeros then a one), bits
+ *             LSB-first in uint32 words, each row starting 16-byte aligned
+ *   3 rowstart: N+1 uint32, first stream word of each row (last = total)
+ *   4 codebook: 256 bytes, codebook[rank] = exponent field E
+ *   5 pruned : N x K/2 uint16, raw bf16 bits of the pruned values
+ *   6 mlo    : N x K/16 uint32, nibble i = M & 0xF of the i-th kept value
+ *   Sections 0-4 are the speculation data, 5-6 the verification data.
+ */
+typedef struct {
+  uint32_t abi_version;      /* QMV_ABI_VERSION */
+  uint32_t format;           /* qmv_format */
+  int64_t N, K;
+  int32_t group;             /* 128 for ternary/INT4, 0 for Cassandra */
+  int32_t n_symbols;         /* Cassandra: number of codebook entries in use */
+  int64_t off[QMV_MAX_SECTIONS];
+  int64_t bytes[QMV_MAX_SECTIONS];
+  int64_t total_bytes;       /* size of the whole packed buffer */
+  uint64_t flags;            /* 0 */
+} qmv_desc;
+
+/* One matvec of a batch: y[M][ldy] = W x[M][ldx] for the matrix packed in w. */
+typedef struct {
+  const qmv_desc* desc;      /* host pointer */
+  const void* w;             /* device: packed buffer */
+  const void* x;             /* device: bf16 [M][ldx] */
+  float* y;                  /* device: fp32 [M][ldy] */
+  int64_t ldx, ldy;
+} qmv_task;
+
+/*
+ * Layout math only (host, no GPU needed): fill `out` for a ternary or INT4
+ * matrix of N x K with the given group (must be 128). K must be a positive
+ * multiple of 128 and N positive. Returns QMV_ERR_UNSUPPORTED for QMV_CASS,
+ * whose stream length depends on the data (use cass_pack_host).
+ */
+int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out);
+
+/*
+ * Quantize and pack on the GPU (offline step). w: device fp32 [N][K] row-major.
+ * packed: device buffer of desc->total_bytes. Ternary follows block_ternary
+ * ("Ternary Bonsai 2", 1.2): scale* = (sum_k |w_k|)/128 + 1e-8 summed in float64
+ * in column order, q = clamp(rint(w/scale*), -1, 1) in float64, stored scale =
+ * fp16(scale*) rounded to nearest even. INT4 ("GPT-5.4", 3.2): scale* =
+ * max|w|/7 in float64, q = clamp(rint(w/scale*), -7, 7); an all-zero group
+ * stores q = 0 and scale 0. Output bytes are fully determined by w.
+ */
+int qmv_pack_ternary(const qmv_desc* desc, const float* w, void* packed, void* stream);
+int qmv_pack_int4(const qmv_desc* desc, const float* w, void* packed, void* stream);
+
+/*
+ * Decode a packed ternary or INT4 matrix to int8 q [N][K] (device) and its
+ * fp16 scales [N][K/128] (device, nullable) for bit-exact checks. A ternary
+ * code 11 writes 0 to q and sets QMV_ERR_CORRUPT in the device error word.
+ */
+int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* scales, void* stream);
+
+/*
+ * y[m][n] = sum_k W_hat[n][k] * x[m][k] for m < M, n < N, where W_hat = q * scale
+ * of the packed ternary (qmv_run_ternary) or INT4 (qmv_run_int4) matrix.
+ * M in 1..QMV_MAX_M, ldx >= K, ldy >= N. Products and sums use fp16 pairs over
+ * 16-32 columns and fp32 beyond; each row's error stays within the library's
+ * documented bound |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|.
+ */
+int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
+                    float* y, int64_t ldy, void* stream);
+int qmv_run_int4(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
+                 float* y, int64_t ldy, void* stream);
+
+/*
+ * Several independent matvecs of one format and one M in a single persistent
+ * launch (a whole decode stack's q/k/v/o/gate/up/down, or the q|k|v and
+ * gate|up groups that share one x). 1 <= n_tasks <= QMV_MAX_BATCH. The tasks
+ * must not write overlapping y ranges.
+ */
+int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* stream);
+
+/*
+ * Cassandra offline transform on the host ("Cassandra", 3.2-3.3).
+ * w_bf16: host [N][K] bf16 bits; calib_bf16: host [R][K] bf16 calibration
+ * activations. Keeps the K/2 largest Wanda scores |w| * ||X[:,j]||_2 of each
+ * row (float64; equal scores keep the lower column; NaN scores as +inf), splits
+ * kept values into sign + 3 high mantissa bits and 4 low mantissa bits, ranks
+ * exponents of the kept values by frequency (ties: smaller exponent first) and
+ * writes each as a unary code. K must be a positive multiple of 32, N, R > 0.
+ * With out == NULL only `desc` is filled (size query). With out != NULL,
+ * out_capacity must be >= desc->total_bytes. out is host memory.
+ */
+int cass_pack_host(const uint16_t* w_bf16, int64_t N, int64_t K, const uint16_t* calib_bf16,
+                   int64_t R, qmv_desc* desc, void* out, int64_t out_capacity);
+
+/*
+ * Draft path ("Cassandra", 3.2 figure b): reads only the speculation sections
+ * (0-4) of the packed buffer. Draft weight = S<<15 | E<<7 | m_hi<<4 for kept
+ * values (low mantissa bits zero-filled), +0 for pruned values.
+ * y: device fp32 [M][ldy] or NULL; w_draft: device bf16 bits [N][K] or NULL
+ * (materialised draft weights, for bit-exact checks). M in 1..8.
+ * A unary rank beyond the codebook or a bitmap row without exactly K/2 kept
+ * values sets QMV_ERR_CORRUPT.
+ */
+int cass_decode_draft(const qmv_desc* desc, const void* packed, const void* x_bf16, int M,
+                      int64_t ldx, float* y, int64_t ldy, uint16_t* w_draft, void* stream);
+
+/*
+ * Target path ("Cassandra", 3.2 figure c): reads speculation and verification
+ * data and rebuilds every original bf16 bit before the matvec. Same argument
+ * rules as cass_decode_draft; w_out receives the reconstructed bf16 bits.
+ */
+int cass_reconstruct(const qmv_desc* desc, const void* packed, const void* x_bf16, int M,
+                     int64_t ldx, float* y, int64_t ldy, uint16_t* w_out, void* stream);
+
+/*
+ * Mixture-of-experts decode over ternary SwiGLU experts ("Nemotron 3.5 Bolt",
+ * expert top-K routing): per token, the top-k of E router logits (equal logits:
+ * lower expert index first), p = softmax over the k selected logits, and
+ *   y_t = sum_e p_{t,e} * W_down,e ( silu(W_gate,e x_t) * (W_up,e x_t) ).
+ * Only the selected experts' packed weights are read.
+ * experts: device; expert e's record starts at experts + e * expert_stride and
+ * holds the packed [gate; up] matrix (2I x H, described by gateup_desc, rows
+ * 0..I-1 gate and I..2I-1 up) followed, at byte offset down_off, by the packed
+ * down matrix (H x I, down_desc). Both ternary. logits: device fp32 [M][E].
+ * x_bf16: device [M][ldx]; y: device fp32 [M][ldy], overwritten.
+ * workspace: device, >= moe_workspace_size(E, topk, M, H, I) bytes.
+ * 1 <= topk <= 8, topk <= E <= 256, M in 1..8.
+ */
+size_t moe_workspace_size(int E, int topk, int M, int64_t H, int64_t I);
+int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts,
+                int64_t expert_stride, int64_t down_off, int E, const float* logits, int topk,
+                const void* x_bf16, int M, int64_t ldx, float* y, int64_t ldy,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronize `stream`, then read and clear the current device's error word.
+ * *device_code (nullable) receives 0 or a qmv_status the kernels recorded.
+ * Returns QMV_ERR_CUDA if the synchronization failed, else the recorded status.
+ */
+int qmv_check_status(void* stream, int32_t* device_code);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* qmv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

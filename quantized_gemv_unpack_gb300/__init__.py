@@ -1,0 +1,245 @@
+"""Python binding of libqmv (fused dequantize-and-matvec for compressed-LLM decode on GB300).
+
+Argument marshalling only: every function forwards to the C ABI of
+``include/qmv.h`` under the same name. Device buffers are torch CUDA tensors
+(or raw integer addresses); streams default to torch's current stream. A
+failing call raises ``QmvError`` with the library's message. There is no
+fallback: if ``libqmv.so`` has not been built, importing a call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqmv.so")
+
+QMV_ABI_VERSION = 1
+QMV_GROUP = 128
+QMV_MAX_SECTIONS = 8
+QMV_MAX_M = 16
+QMV_MAX_BATCH = 448
+
+QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
+QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
+QMV_TERNARY2, QMV_INT4, QMV_CASS = 1, 2, 3
+
+# the exported C symbols (one per declaration in include/qmv.h)
+EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
+           "qmv_run_int4", "qmv_run_batch", "cass_pack_host", "cass_decode_draft", "cass_reconstruct",
+           "moe_workspace_size", "moe_qmv_run", "qmv_check_status", "qmv_last_error")
+
+
+class QmvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"qmv status {status}: {message}")
+        self.status = status
+
+
+class qmv_desc(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_uint32), ("format", ctypes.c_uint32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("group", ctypes.c_int32), ("n_symbols", ctypes.c_int32),
+                ("off", ctypes.c_int64 * QMV_MAX_SECTIONS), ("bytes", ctypes.c_int64 * QMV_MAX_SECTIONS),
+                ("total_bytes", ctypes.c_int64), ("flags", ctypes.c_uint64)]
+
+    def sections(self):
+        return [(int(self.off[i]), int(self.bytes[i])) for i in range(QMV_MAX_SECTIONS)]
+
+
+class qmv_task(ctypes.Structure):
+    _fields_ = [("desc", ctypes.POINTER(qmv_desc)), ("w", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64)]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+_DESC = ctypes.POINTER(qmv_desc)
+_SIGS = {
+    "qmv_pack_desc": (_I32, [_I32, _I64, _I64, ctypes.c_int32, _DESC]),
+    "qmv_pack_ternary": (_I32, [_DESC, _P, _P, _P]),
+    "qmv_pack_int4": (_I32, [_DESC, _P, _P, _P]),
+    "qmv_unpack": (_I32, [_DESC, _P, _P, _P, _P]),
+    "qmv_run_ternary": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P]),
+    "qmv_run_int4": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P]),
+    "qmv_run_batch": (_I32, [_I32, ctypes.POINTER(qmv_task), _I32, _I32, _P]),
+    "cass_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
+    "cass_decode_draft": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
+    "cass_reconstruct": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
+    "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
+    "moe_qmv_run": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P,
+                           ctypes.c_size_t, _P]),
+    "qmv_check_status": (_I32, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "qmv_last_error": (ctypes.c_char_p, []),
+}
+
+
+def lib():
+    """The loaded libqmv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with quantized_gemv_unpack_gb300.build.build() "
+                              "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def qmv_last_error() -> str:
+    return lib().qmv_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != QMV_OK:
+        raise QmvError(rc, qmv_last_error())
+
+
+def _ptr(t):
+    """Device/host address of a torch tensor, a NumPy array, an int or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if hasattr(t, "ctypes"):
+        return t.ctypes.data
+    raise TypeError(f"cannot take the address of {type(t)}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _rows(t):
+    """(M, leading dimension) of a 2-D (or 1-D) activation/output tensor."""
+    if t.dim() == 1:
+        return 1, t.shape[0]
+    return t.shape[0], t.stride(0)
+
+
+# ----------------------------------------------------------------------------- layout and packing
+
+def qmv_pack_desc(format: int, N: int, K: int, group: int = QMV_GROUP) -> qmv_desc:
+    d = qmv_desc()
+    _check(lib().qmv_pack_desc(format, N, K, group, ctypes.byref(d)))
+    return d
+
+
+def qmv_pack_ternary(desc: qmv_desc, w, packed, stream=None):
+    _check(lib().qmv_pack_ternary(ctypes.byref(desc), _ptr(w), _ptr(packed), _stream(stream)))
+
+
+def qmv_pack_int4(desc: qmv_desc, w, packed, stream=None):
+    _check(lib().qmv_pack_int4(ctypes.byref(desc), _ptr(w), _ptr(packed), _stream(stream)))
+
+
+def qmv_unpack(desc: qmv_desc, packed, q, scales=None, stream=None):
+    _check(lib().qmv_unpack(ctypes.byref(desc), _ptr(packed), _ptr(q), _ptr(scales), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- matvec
+
+def qmv_run_ternary(desc: qmv_desc, w, x, y, stream=None):
+    M, ldx = _rows(x)
+    _, ldy = _rows(y)
+    _check(lib().qmv_run_ternary(ctypes.byref(desc), _ptr(w), _ptr(x), M, ldx, _ptr(y), ldy, _stream(stream)))
+
+
+def qmv_run_int4(desc: qmv_desc, w, x, y, stream=None):
+    M, ldx = _rows(x)
+    _, ldy = _rows(y)
+    _check(lib().qmv_run_int4(ctypes.byref(desc), _ptr(w), _ptr(x), M, ldx, _ptr(y), ldy, _stream(stream)))
+
+
+class Batch:
+    """A prepared qmv_run_batch argument list (keeps the ctypes arrays alive)."""
+
+    def __init__(self, format: int, tasks, M: int):
+        self.format = format
+        self.M = M
+        self.descs = [t[0] for t in tasks]
+        self.arr = (qmv_task * len(tasks))()
+        for i, (d, w, x, y) in enumerate(tasks):
+            _, ldx = _rows(x)
+            _, ldy = _rows(y)
+            self.arr[i] = qmv_task(ctypes.pointer(d), _ptr(w), _ptr(x), _ptr(y), ldx, ldy)
+
+    def run(self, stream=None):
+        _check(lib().qmv_run_batch(self.format, self.arr, len(self.arr), self.M, _stream(stream)))
+
+
+def qmv_run_batch(format: int, tasks, M: int, stream=None):
+    """tasks: list of (desc, w, x, y). Prefer ``Batch`` when the same list runs many times."""
+    Batch(format, tasks, M).run(stream)
+
+
+# ----------------------------------------------------------------------------- Cassandra
+
+def cass_pack_host(w_bf16_bits, calib_bf16_bits):
+    """Host packer: NumPy uint16 [N][K] weights and [R][K] calibration rows -> (desc, uint8 buffer)."""
+    import numpy as np
+    w = np.ascontiguousarray(w_bf16_bits, dtype=np.uint16)
+    c = np.ascontiguousarray(calib_bf16_bits, dtype=np.uint16)
+    N, K = w.shape
+    R = c.shape[0]
+    d = qmv_desc()
+    _check(lib().cass_pack_host(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), None, 0))
+    out = np.zeros(d.total_bytes, dtype=np.uint8)
+    _check(lib().cass_pack_host(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), out.ctypes.data,
+                                out.nbytes))
+    return d, out
+
+
+def cass_decode_draft(desc: qmv_desc, packed, x, y=None, w_draft=None, stream=None):
+    M, ldx = _rows(x)
+    ldy = _rows(y)[1] if y is not None else 0
+    _check(lib().cass_decode_draft(ctypes.byref(desc), _ptr(packed), _ptr(x), M, ldx, _ptr(y), ldy,
+                                   _ptr(w_draft), _stream(stream)))
+
+
+def cass_reconstruct(desc: qmv_desc, packed, x, y=None, w_out=None, stream=None):
+    M, ldx = _rows(x)
+    ldy = _rows(y)[1] if y is not None else 0
+    _check(lib().cass_reconstruct(ctypes.byref(desc), _ptr(packed), _ptr(x), M, ldx, _ptr(y), ldy,
+                                  _ptr(w_out), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- MoE
+
+def moe_workspace_size(E: int, topk: int, M: int, H: int, I: int) -> int:
+    return int(lib().moe_workspace_size(E, topk, M, H, I))
+
+
+def moe_qmv_run(gateup_desc: qmv_desc, down_desc: qmv_desc, experts, expert_stride: int, down_off: int, E: int,
+                logits, topk: int, x, y, workspace, stream=None):
+    M, ldx = _rows(x)
+    _, ldy = _rows(y)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().moe_qmv_run(ctypes.byref(gateup_desc), ctypes.byref(down_desc), _ptr(experts), expert_stride,
+                             down_off, E, _ptr(logits), topk, _ptr(x), M, ldx, _ptr(y), ldy, _ptr(workspace),
+                             ws_bytes, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- status
+
+def qmv_check_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device error word; raises on CUDA failure."""
+    code = ctypes.c_int32(0)
+    rc = lib().qmv_check_status(_stream(stream), ctypes.byref(code))
+    if rc == QMV_ERR_CUDA:
+        _check(rc)
+    return int(code.value)

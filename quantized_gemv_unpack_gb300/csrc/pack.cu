@@ -1,0 +1,208 @@
+// Offline quantize-and-pack kernels (ternary, INT4) and the decode-to-int8
+// kernel used for bit-exact checks of the packed stream.
+//
+// One thread owns one 128-column block of one row: it sums |w| in float64 in
+// column order, divides in float64 and rounds half to even, so the codes and
+// the fp16 scales are fully determined by the input (no reduction-order
+// freedom). The float64 -> fp16 rounding is done on the bit patterns,
+// nearest-even in one step, from the IEEE-754 binary16 definition.
+#include "qmv_internal.cuh"
+
+namespace qmv {
+namespace {
+
+// binary16 bits of a float64, round to nearest, ties to even (no float32 detour)
+__device__ uint16_t f64_to_f16_rne(double d) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(d);
+  const uint32_t sign = (uint32_t)(b >> 63) << 15;
+  const int e = (int)((b >> 52) & 0x7FF);
+  const unsigned long long f = b & ((1ull << 52) - 1);
+  if (e == 0x7FF) return (uint16_t)(sign | (f ? 0x7E00u : 0x7C00u));
+  const int eu = e ? e - 1023 : -1022;                   // value = sig * 2^(eu - 52)
+  const unsigned long long sig = e ? (f | (1ull << 52)) : f;
+  const int shift = eu >= -14 ? 42 : 28 - eu;            // to units of the fp16 ulp
+  if (shift >= 64) return (uint16_t)sign;
+  unsigned long long kept = sig >> shift;
+  const unsigned long long rem = sig & ((1ull << shift) - 1);
+  const unsigned long long half = 1ull << (shift - 1);
+  if (rem > half || (rem == half && (kept & 1ull))) ++kept;
+  unsigned long long enc = eu >= -14 ? ((unsigned long long)(eu + 14) << 10) + kept : kept;
+  if (enc >= 0x7C00ull) enc = 0x7C00ull;
+  return (uint16_t)(sign | (uint32_t)enc);
+}
+
+__global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
+                                    uint16_t* __restrict__ scales) {
+  const int64_t nb = K / 128;
+  const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= N * nb) return;
+  const int64_t n = blk / nb, b = blk % nb;
+  const float4* src = reinterpret_cast<const float4*>(w + n * K + b * 128);
+  double acc = 0.0;
+  for (int i = 0; i < 32; ++i) {
+    const float4 v = src[i];
+    acc += fabs((double)v.x);
+    acc += fabs((double)v.y);
+    acc += fabs((double)v.z);
+    acc += fabs((double)v.w);
+  }
+  const double s = acc / 128.0 + 1e-8;
+  uint32_t words[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) words[j] = 0u;
+  for (int i = 0; i < 32; ++i) {
+    const float4 v = src[i];
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int k = i * 4 + c;
+      const double r = rint((double)vv[c] / s);
+      const uint32_t code = r >= 1.0 ? 1u : (r <= -1.0 ? 2u : 0u);
+      const int rr = k & 15;
+      const int pos = (rr & 1) ? 15 + rr : rr;
+      words[k >> 4] |= code << pos;
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(codes + n * (K / 16) + b * 8);
+  dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+  dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+  scales[n * nb + b] = f64_to_f16_rne(s);
+}
+
+__global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
+                                 uint16_t* __restrict__ scales) {
+  const int64_t nb = K / 128;
+  const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= N * nb) return;
+  const int64_t n = blk / nb, b = blk % nb;
+  const float4* src = reinterpret_cast<const float4*>(w + n * K + b * 128);
+  float mx = 0.f;
+  for (int i = 0; i < 32; ++i) {
+    const float4 v = src[i];
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  const double s = (double)mx / 7.0;
+  uint32_t words[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) words[j] = 0u;
+  for (int i = 0; i < 32; ++i) {
+    const float4 v = src[i];
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int k = i * 4 + c;
+      int q = 0;
+      if (s != 0.0) {
+        const double r = rint((double)vv[c] / s);
+        q = r > 7.0 ? 7 : (r < -7.0 ? -7 : (int)r);
+      }
+      const int rr = k & 7;
+      const int pos = (rr & 1) ? 14 + 2 * rr : 2 * rr;
+      words[k >> 3] |= ((uint32_t)q & 0xFu) << pos;
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(codes + n * (K / 8) + b * 16);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
+  scales[n * nb + b] = f64_to_f16_rne(s);
+}
+
+// One thread per code word: writes the int8 values of its columns.
+__global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, int64_t N, int64_t K,
+                              int8_t* __restrict__ q, int* err) {
+  const int cpw = format == QMV_TERNARY2 ? 16 : 8;
+  const int64_t nw = N * (K / cpw);
+  const int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (wi >= nw) return;
+  const uint32_t w = codes[wi];
+  int8_t* out = q + wi * cpw;                        // row-major: word wi covers columns wi*cpw .. +cpw
+  bool bad = false;
+  for (int r = 0; r < cpw; ++r) {
+    if (format == QMV_TERNARY2) {
+      const int pos = (r & 1) ? 15 + r : r;
+      const uint32_t c = (w >> pos) & 3u;
+      bad |= c == 3u;
+      out[r] = c == 1u ? 1 : (c == 2u ? -1 : 0);
+    } else {
+      const int pos = (r & 1) ? 14 + 2 * r : 2 * r;
+      const int v = (int)((w >> pos) & 0xFu);
+      out[r] = (int8_t)(v >= 8 ? v - 16 : v);
+    }
+  }
+  if (bad) atomicCAS(err, 0, QMV_ERR_CORRUPT);
+}
+
+int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, void* stream) {
+  int rc = check_desc(desc, format);
+  if (rc) return rc;
+  if (!w || !packed) return fail(QMV_ERR_ARG, "NULL w or packed");
+  if (!aligned16(w) || !aligned16(packed)) return fail(QMV_ERR_ALIGN, "w and packed must be 16-byte aligned");
+  char* base = static_cast<char*>(packed);
+  uint32_t* codes = reinterpret_cast<uint32_t*>(base + desc->off[0]);
+  uint16_t* scales = reinterpret_cast<uint16_t*>(base + desc->off[1]);
+  const int64_t blocks = desc->N * (desc->K / 128);
+  const int threads = 128;
+  const int64_t grid = (blocks + threads - 1) / threads;
+  if (grid > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "matrix too large for one pack launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // zero the alignment padding after each section so every byte is determined
+  const int64_t gaps[2][2] = {{desc->off[0] + desc->bytes[0], desc->off[1]},
+                              {desc->off[1] + desc->bytes[1], desc->total_bytes}};
+  for (const auto& gp : gaps) {
+    if (gp[1] > gp[0]) {
+      cudaError_t e = cudaMemsetAsync(base + gp[0], 0, (size_t)(gp[1] - gp[0]), s);
+      if (e != cudaSuccess) return cuda_fail(e, "zero section padding");
+    }
+  }
+  if (format == QMV_TERNARY2)
+    pack_ternary_kernel<<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+  else
+    pack_int4_kernel<<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  return QMV_OK;
+}
+
+}  // namespace
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+int qmv_pack_ternary(const qmv_desc* desc, const float* w, void* packed, void* stream) {
+  return pack_common(QMV_TERNARY2, desc, w, packed, stream);
+}
+
+int qmv_pack_int4(const qmv_desc* desc, const float* w, void* packed, void* stream) {
+  return pack_common(QMV_INT4, desc, w, packed, stream);
+}
+
+int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* scales, void* stream) {
+  if (!desc) return fail(QMV_ERR_ARG, "desc is NULL");
+  const int format = (int)desc->format;
+  if (format != QMV_TERNARY2 && format != QMV_INT4) return fail(QMV_ERR_UNSUPPORTED, "qmv_unpack serves ternary and INT4");
+  int rc = check_desc(desc, format);
+  if (rc) return rc;
+  if (!packed || !q) return fail(QMV_ERR_ARG, "NULL packed or q");
+  if (!aligned16(packed) || !aligned16(q) || (scales && !aligned16(scales)))
+    return fail(QMV_ERR_ALIGN, "buffers must be 16-byte aligned");
+  int* err = device_error_word();
+  if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+  const char* base = static_cast<const char*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int cpw = format == QMV_TERNARY2 ? 16 : 8;
+  const int64_t nw = desc->N * (desc->K / cpw);
+  const int threads = 256;
+  unpack_kernel<<<(unsigned)((nw + threads - 1) / threads), threads, 0, s>>>(
+      format, reinterpret_cast<const uint32_t*>(base + desc->off[0]), desc->N, desc->K, q, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
+  if (scales) {
+    e = cudaMemcpyAsync(scales, base + desc->off[1], desc->bytes[1], cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copy scales");
+  }
+  return QMV_OK;
+}
+
+}  // extern "C"

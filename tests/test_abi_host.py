@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+declared entry point, computes layouts that match the oracle's specification,
+and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_gemv_unpack_gb300 as q
+from oracle import layout
+from quantized_gemv_unpack_gb300 import build
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return q.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared_functions()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in qmv.h but not exported"
+    assert sorted(q.EXPORTS) == declared
+
+
+def test_desc_matches_oracle_layout(L):
+    for fmt, sizes in [(q.QMV_TERNARY2, layout.ternary_sizes), (q.QMV_INT4, layout.int4_sizes)]:
+        for N, K in [(1, 128), (7, 384), (4096, 4096), (1024, 5120), (5120, 25600)]:
+            d = q.qmv_pack_desc(fmt, N, K)
+            offs, total = layout.sections(sizes(N, K))
+            assert [d.off[i] for i in range(2)] == offs
+            assert [d.bytes[i] for i in range(2)] == sizes(N, K)
+            assert d.total_bytes == total
+            assert d.abi_version == q.QMV_ABI_VERSION and d.group == 128
+
+
+@pytest.mark.parametrize("args", [(q.QMV_TERNARY2, 0, 128), (q.QMV_TERNARY2, 4, 100), (q.QMV_INT4, 4, -128),
+                                  (9, 4, 128)])
+def test_pack_desc_rejects_bad_shapes(L, args):
+    with pytest.raises(q.QmvError) as e:
+        q.qmv_pack_desc(*args)
+    assert e.value.status == q.QMV_ERR_ARG
+
+
+def test_cassandra_desc_needs_the_data(L):
+    with pytest.raises(q.QmvError) as e:
+        q.qmv_pack_desc(q.QMV_CASS, 4, 128)
+    assert e.value.status == q.QMV_ERR_UNSUPPORTED
+
+
+def test_run_rejects_bad_arguments_on_the_host(L):
+    d = q.qmv_pack_desc(q.QMV_TERNARY2, 64, 256)
+    # NULL desc, wrong format, misaligned pointers, short ldx and bad M are all found before any launch
+    assert L.qmv_run_ternary(None, 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    assert L.qmv_run_int4(ctypes.byref(d), 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    assert L.qmv_run_ternary(ctypes.byref(d), 258, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ALIGN
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, 256, 1, 128, 256, 64, None) == q.QMV_ERR_ARG
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, 256, 1, 260, 256, 64, None) == q.QMV_ERR_ALIGN
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, 256, 0, 256, 256, 64, None) == q.QMV_ERR_ARG
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, 256, 17, 256, 256, 64, None) == q.QMV_ERR_ARG
+    assert "M=17" in q.qmv_last_error()
+    bad = q.qmv_desc.from_buffer_copy(d)
+    bad.bytes[0] += 4
+    assert L.qmv_run_ternary(ctypes.byref(bad), 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    bad = q.qmv_desc.from_buffer_copy(d)
+    bad.abi_version = 99
+    assert L.qmv_run_ternary(ctypes.byref(bad), 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    assert L.qmv_run_batch(q.QMV_TERNARY2, None, 0, 1, None) == q.QMV_ERR_ARG
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(q, "_lib", None)
+    monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        q.lib()

@@ -1,0 +1,217 @@
+"""GPU parity of the ternary and INT4 paths against the float64 oracle (through the C ABI).
+
+Packed bytes and decoded codes must be bit-identical to the oracle's; matvec
+outputs must satisfy |y - y_ref| <= 2e-3 * sum_k |w_hat_k x_k| for every row.
+"""
+import numpy as np
+import pytest
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+RTOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_gemv_unpack_gb300 as q
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    return q, torch, torch.device("cuda:0")
+
+
+FORMATS = {}
+
+
+def _fmt(q, name):
+    from oracle import int4, ternary
+    if name == "ternary":
+        return q.QMV_TERNARY2, ternary, q.qmv_pack_ternary, q.qmv_run_ternary
+    return q.QMV_INT4, int4, q.qmv_pack_int4, q.qmv_run_int4
+
+
+def _to_dev_bf16(torch, bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def _pack(q, torch, dev, name, w):
+    fmt, ref, pack, run = _fmt(q, name)
+    N, K = w.shape
+    d = q.qmv_pack_desc(fmt, N, K)
+    packed = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
+    pack(d, torch.from_numpy(w).to(dev), packed)
+    return d, packed
+
+
+def _check_bound(y, yr, B, what):
+    err = np.abs(y.astype(np.float64) - yr)
+    worst = float((err / np.maximum(B, 1e-300)).max())
+    assert np.all(err <= RTOL * B), f"{what}: worst |err|/B = {worst:.3e}"
+    return worst
+
+
+@pytest.mark.parametrize("name", ["ternary", "int4"])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (33, 256), (200, 1152), (64, 13824), (4096, 4096)])
+def test_packer_is_bit_exact(env, name, N, K):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    fmt, ref, _, _ = _fmt(q, name)
+    w = synth.student_t4(synth.rng(N * 131 + K), (N, K))
+    w[0, :128] = 0.0                                   # an all-zero block
+    d, packed = _pack(q, torch, dev, name, w)
+    qq, _, s16 = ref.quantize(w)
+    assert np.array_equal(packed.cpu().numpy(), np.frombuffer(ref.pack(qq, s16), np.uint8))
+    # decode on the GPU: int8 codes and scales identical to the oracle's
+    qd = torch.empty((N, K), dtype=torch.int8, device=dev)
+    sd = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+    q.qmv_unpack(d, packed, qd, sd)
+    assert q.qmv_check_status() == 0
+    assert np.array_equal(qd.cpu().numpy(), qq)
+    assert np.array_equal(sd.cpu().numpy().view(np.uint16), s16)
+
+
+def test_unpack_flags_invalid_ternary_code(env):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    w = synth.student_t4(synth.rng(5), (4, 256))
+    d, packed = _pack(q, torch, dev, "ternary", w)
+    packed[5] = 0xFF                                   # codes 11 in word 1 of row 0
+    qd = torch.empty((4, 256), dtype=torch.int8, device=dev)
+    q.qmv_unpack(d, packed, qd)
+    assert q.qmv_check_status() == q.QMV_ERR_CORRUPT
+    assert q.qmv_check_status() == 0                   # the word is cleared after reading
+
+
+@pytest.mark.parametrize("name", ["ternary", "int4"])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (33, 256), (200, 1152), (96, 5120), (40, 13824)])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 16])
+def test_matvec_matches_oracle(env, name, N, K, M):
+    q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    fmt, ref, _, run = _fmt(q, name)
+    g = synth.rng(1000 * M + N + K)
+    w = synth.student_t4(g, (N, K))
+    xb = synth.activations_bf16(g, (M, K))
+    d, packed = _pack(q, torch, dev, name, w)
+    y = torch.full((M, N), float("nan"), device=dev)
+    run(d, packed, _to_dev_bf16(torch, xb, dev), y)
+    qq, _, s16 = ref.quantize(w)
+    yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
+    _check_bound(y.cpu().numpy(), yr, B, f"{name} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("name", ["ternary", "int4"])
+def test_cfg_ternary_4096_square_full(env, name):
+    """The single-matrix workload (4096 x 4096, batch 1), every row against the oracle."""
+    q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    fmt, ref, _, run = _fmt(q, name)
+    g = synth.rng(0)
+    w = synth.student_t4(g, (4096, 4096))
+    xb = synth.activations_bf16(g, (1, 4096))
+    d, packed = _pack(q, torch, dev, name, w)
+    y = torch.empty((1, 4096), device=dev)
+    run(d, packed, _to_dev_bf16(torch, xb, dev), y)
+    qq, _, s16 = ref.quantize(w)
+    yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
+    _check_bound(y.cpu().numpy(), yr, B, f"{name} 4096x4096")
+
+
+def test_activation_range_is_handled(env):
+    """Tiny and huge activations (bf16 range far outside fp16's) stay within the bound."""
+    q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
+    from oracle import ternary
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(77)
+    w = synth.student_t4(g, (64, 1024))
+    d, packed = _pack(q, torch, dev, "ternary", w)
+    qq, _, s16 = ternary.quantize(w)
+    for scale in [1e-30, 1e-6, 1e4, 1e30]:
+        x = synth.to_bf16_bits(g.standard_normal((2, 1024)).astype(np.float32) * np.float32(scale))
+        y = torch.empty((2, 64), device=dev)
+        q.qmv_run_ternary(d, packed, _to_dev_bf16(torch, x, dev), y)
+        yr, B = matvec_bf16x(ternary.dequant(qq, s16), x)
+        _check_bound(y.cpu().numpy(), yr, B, f"x scale {scale}")
+
+
+def test_strided_activations_and_outputs(env):
+    q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
+    from oracle import int4
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(78)
+    N, K, M = 48, 640, 3
+    w = synth.student_t4(g, (N, K))
+    xb = synth.activations_bf16(g, (M, K))
+    d, packed = _pack(q, torch, dev, "int4", w)
+    xbig = torch.zeros((M, K + 64), dtype=torch.bfloat16, device=dev)
+    xbig[:, :K] = _to_dev_bf16(torch, xb, dev)
+    ybig = torch.full((M, N + 12), 7.0, device=dev)
+    q.qmv_run_int4(d, packed, xbig, ybig)
+    qq, _, s16 = int4.quantize(w)
+    yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+    yy = ybig.cpu().numpy()
+    _check_bound(yy[:, :N], yr, B, "strided")
+    assert (yy[:, N:] == 7.0).all()                     # nothing written past N
+
+
+@pytest.mark.parametrize("name", ["ternary", "int4"])
+def test_batch_equals_separate_calls(env, name):
+    """q|k|v sharing one x in a single launch give the same bits as three launches."""
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    fmt, ref, _, run = _fmt(q, name)
+    g = synth.rng(90)
+    K = 1280
+    shapes = [(320, K), (64, K), (64, K), (96, 2560)]
+    mats = [_pack(q, torch, dev, name, synth.student_t4(g, s)) for s in shapes]
+    x1 = _to_dev_bf16(torch, synth.activations_bf16(g, (2, K)), dev)
+    x2 = _to_dev_bf16(torch, synth.activations_bf16(g, (2, 2560)), dev)
+    xs = [x1, x1, x1, x2]
+    ys_b = [torch.empty((2, s[0]), device=dev) for s in shapes]
+    q.qmv_run_batch(fmt, [(d, p, x, y) for (d, p), x, y in zip(mats, xs, ys_b)], 2)
+    for (d, p), x, yb in zip(mats, xs, ys_b):
+        y = torch.empty_like(yb)
+        run(d, p, x, y)
+        assert torch.equal(y, yb)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_int4_gqa_layer_set_sampled(env, M):
+    """The INT4 GQA layer set (hidden 5120, 40/8 heads of 128, SwiGLU 13824) at full size, one batched
+    launch as the benchmark runs it; sampled rows of every matrix against the oracle."""
+    q, torch, dev = env
+    from oracle import int4
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    gen = synth.torch_generator(1, dev)
+    shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824)
+    mats, ws = [], []
+    for name, N, K in shapes:
+        w = synth.student_t4_torch(gen, (N, K), device=dev)
+        d = q.qmv_pack_desc(q.QMV_INT4, N, K)
+        p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
+        q.qmv_pack_int4(d, w, p)
+        mats.append((d, p))
+        ws.append(w)
+    xs = {K: synth.activations_bf16_torch(gen, (M, K), device=dev) for K in {5120, 13824}}
+    ys = [torch.empty((M, N), device=dev) for _, N, _ in shapes]
+    q.qmv_run_batch(q.QMV_INT4, [(d, p, xs[K], y) for (d, p), (_, N, K), y in zip(mats, shapes, ys)], M)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M)
+    for (d, p), (name, N, K), w, y in zip(mats, shapes, ws, ys):
+        rows = np.unique(np.concatenate(([0, N - 1], rng.choice(N, 24, replace=False))))
+        wr = w[torch.from_numpy(rows).to(dev)].cpu().numpy()
+        qq, _, s16 = int4.quantize(wr)
+        # packed codes of the sampled rows are the oracle's codes
+        codes = p[: d.bytes[0]].view(torch.int32).view(N, K // 8)[torch.from_numpy(rows).to(dev)].cpu().numpy()
+        ref_codes = np.frombuffer(int4.pack(qq, s16), "<u4", count=len(rows) * K // 8).reshape(len(rows), K // 8)
+        assert np.array_equal(codes.view(np.uint32), ref_codes), name
+        xb = xs[K].view(torch.int16).cpu().numpy().view(np.uint16)
+        yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+        _check_bound(y[:, torch.from_numpy(rows).to(dev)].cpu().numpy(), yr, B, f"{name} M={M}")
