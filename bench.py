@@ -105,58 +105,66 @@ class ClockSampler:
 def oracle_sample_main():
     """Child process: time the float64 oracle on a bounded sample of the stack (single thread).
 
-    The sample is the q, k, v and o matrices of one layer (57.7M weights); the
-    oracle decodes the packed bytes, dequantizes and forms y in float64. Weights
-    are generated and packed by the oracle before the clock starts.
+    The sample unit is the k and v matrices of one layer (2 x 1024 x 5120 weights):
+    the oracle decodes their packed bytes, dequantizes and forms y in float64.
+    Weights are generated and packed by the oracle before the clock starts.
+    QMV_ORACLE_PASSES fixes the number of passes; otherwise passes repeat until
+    QMV_ORACLE_SECONDS of CPU work have been timed.
     """
     import numpy as np
 
     from oracle import matvec as o_mv
     from oracle import ternary as o_t
     from quantized_gemv_unpack_gb300 import synth
-    reps = int(os.environ.get("QMV_ORACLE_REPS", "1"))
+    passes = int(os.environ.get("QMV_ORACLE_PASSES", "0"))
+    budget = float(os.environ.get("QMV_ORACLE_SECONDS", "10"))
     g = synth.rng(4)
-    shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)[:4]
+    shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)[1:3]
     packed = []
     for _, N, K in shapes:
         w = synth.student_t4(g, (N, K))
         qq, _, s16 = o_t.quantize(w)
         packed.append((o_t.pack(qq, s16), N, K))
-        del w, qq
     x = synth.activations_bf16(g, (1, HIDDEN))
     nbytes = sum(len(b) for b, _, _ in packed) + HIDDEN * 2 + sum(N for _, N, _ in packed) * 4
+    done = 0
     t0 = time.perf_counter()
-    for _ in range(reps):
+    while True:
         for buf, N, K in packed:
             qq, s16 = o_t.unpack(buf, N, K)
             o_mv.matvec_bf16x(o_t.dequant(qq, s16), x)
-    dt = (time.perf_counter() - t0) / reps
-    print(json.dumps({"seconds": dt, "bytes": nbytes, "weights": sum(N * K for _, N, K in packed)}))
+        done += 1
+        el = time.perf_counter() - t0
+        if (passes and done >= passes) or (not passes and el >= budget):
+            break
+    print(json.dumps({"seconds": el / done, "passes": done, "bytes": nbytes,
+                      "weights": sum(N * K for _, N, K in packed)}))
 
 
-def run_oracle_sample(reps=1):
+def run_oracle_sample(passes=0, seconds=10.0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               QMV_ORACLE_REPS=str(reps))
+               QMV_ORACLE_PASSES=str(passes), QMV_ORACLE_SECONDS=str(seconds))
     p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child"], env=env,
                        capture_output=True, text=True, cwd=ROOT)
     if p.returncode:
         raise RuntimeError("oracle sample failed: " + p.stderr[-2000:])
     r = json.loads(p.stdout.strip().splitlines()[-1])
     gbs = r["bytes"] / r["seconds"] / 1e9
-    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"q,k,v,o of one layer ({r['weights'] / 1e6:.1f}M weights, {r['bytes'] / 1e6:.1f} MB packed), "
-                      f"float64 NumPy, single thread, {r['seconds']:.2f} s per pass"}
+    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds_per_pass": r["seconds"],
+            "sample": f"k and v matrices of one stack layer ({r['weights'] / 1e6:.1f}M weights, "
+                      f"{r['bytes'] / 1e6:.2f} MB packed) decoded, dequantized and multiplied in float64 NumPy "
+                      f"on one thread; {r['passes']} passes, {r['seconds']:.3f} s each"}
 
 
 # ----------------------------------------------------------------------------- GPU stack
 
-def build_stack(q, torch, dev, seed=4):
+def build_stack(q, torch, dev, layers=LAYERS, seed=4):
     from quantized_gemv_unpack_gb300 import synth
     gen = synth.torch_generator(seed, dev)
     shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
     tasks, keep = [], []
     nbytes = 0
-    for layer in range(LAYERS):
+    for layer in range(layers):
         x_h = synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)
         x_i = synth.activations_bf16_torch(gen, (1, INTER), device=dev)
         for name, N, K in shapes:
@@ -182,6 +190,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     a = ap.parse_args()
     if a.oracle_child:
@@ -196,21 +205,17 @@ def main():
     if a.impl == "reference":
         if rank != 0:
             return
-        # each step is one pass of the oracle over its bounded sample of the stack
-        reps = a.steps
-        t0 = time.perf_counter()
-        base = run_oracle_sample(reps=reps)
-        wall = time.perf_counter() - t0
+        # each step is one oracle pass over its bounded sample of the stack (warm-up passes untimed)
+        run_oracle_sample(passes=a.warmup)
+        base = run_oracle_sample(passes=a.steps)
         line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
-                "warmup": a.warmup, "ms_per_step": base["sample"] and None, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Student-t(4) weights)",
+                "warmup": a.warmup, "ms_per_step": base["seconds_per_pass"] * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded Student-t(4) std 0.02 weights, N(0,1) bf16 activations)",
                 "config": workload_config(), "impl": "reference",
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
                                  "unit": UNIT},
-                "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-                "wall_s": wall}
-        sec = float(base["sample"].split(", ")[-1].split(" s")[0])
-        line["ms_per_step"] = sec * 1e3
+                "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
@@ -230,7 +235,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    tasks, keep, nbytes = build_stack(q, torch, dev)
+    tasks, keep, nbytes = build_stack(q, torch, dev, a.layers)
     batch = q.Batch(q.QMV_TERNARY2, tasks, 1)
     stream = torch.cuda.current_stream()
 
@@ -298,7 +303,8 @@ def main():
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16x2-f32",
         "data": "synthetic (seeded Student-t(4) std 0.02 weights, N(0,1) bf16 activations)",
-        "config": dict(workload_config(), parallelism="replicas only" if world > 1 else "single GPU"),
+        "config": dict(workload_config(), layers=a.layers,
+                       parallelism="replicas only" if world > 1 else "single GPU"),
         "tok_s": 1000.0 / ms * world, "pct_of_peak": 100.0 * per_launch_gbs / peak,
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": per_launch_gbs, "peak": peak, "unit": "GB/s",

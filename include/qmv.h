@@ -61,15 +61,21 @@ typedef enum {
  * Layout descriptor of one packed matrix: a contiguous buffer of sections,
  * each starting on a 256-byte boundary (off[i] bytes from the start).
  *
- * QMV_TERNARY2 ("Ternary Bonsai 2", section 1.2, block_ternary):
- *   0 codes : N x K/16 uint32; word (n, k/16) holds columns k0..k0+15; column
- *             r = k%16 at bit r (r even) or bit 15+r (r odd); code 00 = 0,
- *             01 = +1, 10 = -1 (11 is invalid).
- *   1 scales: N x K/128 fp16, scale = fp16(mean|w| + 1e-8) of each block.
+ * QMV_TERNARY2 ("Ternary Bonsai 2", section 1.2, block_ternary) and
  * QMV_INT4 ("GPT-5.4 ..." section 3.2, group-wise quantization):
- *   0 codes : N x K/8 uint32; column r = k%8 at bit 2r (r even) or 14+2r
- *             (r odd); 4-bit two's complement, -7..7.
- *   1 scales: N x K/128 fp16, scale = fp16(max|w| / 7) of each group.
+ *   0 codes : row-group records. Rows go in groups of 16 (the last group
+ *             padded with zero codes), columns in steps of 1024 (8 blocks of
+ *             128, the last step possibly fewer: nbk = min(8, K/128 - 8s)).
+ *             Record (group g, step s) = the 16 rows' code blocks of that
+ *             step, row after row; group g starts at byte g*16*K*bits/8 and
+ *             step s inside it at s*16*8*block_bytes. A block is 8 (ternary)
+ *             or 16 (INT4) uint32 words. Ternary word of columns k0..k0+15:
+ *             column r = k%16 at bit r (r even) or 15+r (r odd); code 00 = 0,
+ *             01 = +1, 10 = -1 (11 is invalid). INT4 word of columns
+ *             k0..k0+7: column r = k%8 at bit 2r (r even) or 14+2r (r odd);
+ *             4-bit two's complement, -7..7.
+ *   1 scales: N x K/128 fp16, row-major: ternary fp16(mean|w| + 1e-8), INT4
+ *             fp16(max|w| / 7) of each block/group.
  * QMV_CASS ("Cassandra", sections 3.1-3.3):
  *   0 bitmap : N x K/32 uint32, bit j%32 of word j/32 set = value (n, j) kept
  *   1 signmant: N x K/16 uint32, nibble i = S<<3 | (M>>4) of the i-th kept value

@@ -43,7 +43,8 @@ def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
         words |= nib[:, :, r] << np.uint32(layout.int4_bit_pos(r))
     offs, total = layout.sections(layout.int4_sizes(N, K))
     buf = bytearray(total)
-    buf[offs[0]:offs[0] + words.nbytes] = words.astype("<u4").tobytes()
+    rec = layout.records_from_rows(words, 16)
+    buf[offs[0]:offs[0] + rec.nbytes] = rec.astype("<u4").tobytes()
     s = np.asarray(s16, dtype="<u2")
     buf[offs[1]:offs[1] + s.nbytes] = s.tobytes()
     return bytes(buf)
@@ -52,7 +53,8 @@ def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
 def unpack(buf: bytes, N: int, K: int):
     offs, total = layout.sections(layout.int4_sizes(N, K))
     assert len(buf) >= total
-    words = np.frombuffer(buf, dtype="<u4", count=N * K // 8, offset=offs[0]).reshape(N, K // 8)
+    flat = np.frombuffer(buf, dtype="<u4", count=layout.padded_rows(N) * K // 8, offset=offs[0])
+    words = layout.rows_from_records(flat, N, K, 16, 8)
     q = np.empty((N, K // 8, 8), dtype=np.int8)
     for r in range(8):
         nib = ((words >> np.uint32(layout.int4_bit_pos(r))) & 0xF).astype(np.int32)

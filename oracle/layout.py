@@ -4,18 +4,25 @@ A packed matrix is one contiguous buffer of sections; every section starts at
 a multiple of 256 bytes. W is N x K (output rows x input columns), row-major
 along K; quantization blocks/groups of 128 run along K.
 
-Ternary (2 bits per weight, code 00 = 0, 01 = +1, 10 = -1):
-  section 0 codes : N x K/16 little-endian uint32 words; word (n, k // 16) holds
-                    the 16 codes of k0 .. k0+15. Within a word the low 16 bits
-                    hold the even columns and the high 16 bits the odd columns:
-                    column r = k % 16 sits at bit r if r is even and at bit
-                    15 + r if r is odd (2 bits, bit 0 of the code first).
-  section 1 scales: N x K/128 fp16 bit patterns.
+Ternary (2 bits per weight, code 00 = 0, 01 = +1, 10 = -1) and INT4 (4-bit
+two's complement, values -7 .. 7) share one arrangement:
 
-INT4 (4-bit two's complement, values -7 .. 7):
-  section 0 codes : N x K/8 uint32 words; column r = k % 8 sits at bit 2r if r
-                    is even and at bit 14 + 2r if r is odd (4 bits each).
-  section 1 scales: N x K/128 fp16 bit patterns.
+  section 0 codes : row-group records. Rows are taken in groups of 16 (the
+                    last group padded with all-zero rows), columns in steps of
+                    1024 (8 blocks of 128; the last step may hold fewer). The
+                    record of (group g, step s) holds the 16 rows' codes of
+                    that step, row after row, each row's nbk blocks in column
+                    order (nbk = min(8, K/128 - 8s)). Records follow in (g, s)
+                    order, so group g starts at g * 16 * K * bits / 8 and
+                    step s of it at s * 16 * 8 * block_bytes. A block is
+                    8 (ternary) or 16 (INT4) little-endian uint32 words:
+                    * ternary word of columns k0..k0+15: the low 16 bits hold
+                      the even columns, the high 16 bits the odd ones; column
+                      r = k % 16 sits at bit r (r even) or 15 + r (r odd),
+                      2 bits each, code bit 0 first;
+                    * INT4 word of columns k0..k0+7: column r = k % 8 at bit
+                      2r (r even) or 14 + 2r (r odd), 4 bits each.
+  section 1 scales: N x K/128 fp16 bit patterns, row-major.
 
 Cassandra split (see ``oracle.cassandra`` for the contents):
   0 bitmap    : N x K/32 uint32, bit (j % 32) of word j // 32 = kept(n, j)
@@ -29,6 +36,8 @@ Cassandra split (see ``oracle.cassandra`` for the contents):
   6 mlo       : N x (K/2)/8 uint32, nibble i = M & 0xF of the i-th kept value
 """
 from __future__ import annotations
+
+import numpy as np
 
 ALIGN = 256
 
@@ -47,12 +56,53 @@ def sections(sizes):
     return offs, pos
 
 
+ROW_GROUP = 16
+STEP_BLOCKS = 8
+
+
+def padded_rows(N: int) -> int:
+    return (N + ROW_GROUP - 1) // ROW_GROUP * ROW_GROUP
+
+
 def ternary_sizes(N: int, K: int):
-    return [N * K // 4, N * (K // 128) * 2]
+    return [padded_rows(N) * K // 4, N * (K // 128) * 2]
 
 
 def int4_sizes(N: int, K: int):
-    return [N * K // 2, N * (K // 128) * 2]
+    return [padded_rows(N) * K // 2, N * (K // 128) * 2]
+
+
+def records_from_rows(words, block_words: int):
+    """Row-major code words [N][K/cpw] -> the row-group record order of section 0."""
+    N, W = words.shape
+    KB = W // block_words
+    Np = padded_rows(N)
+    rows = np.zeros((Np, W), dtype=np.uint32)
+    rows[:N] = words
+    out = []
+    for g in range(Np // ROW_GROUP):
+        grp = rows[g * ROW_GROUP:(g + 1) * ROW_GROUP]
+        for s in range(0, KB, STEP_BLOCKS):
+            nbk = min(STEP_BLOCKS, KB - s)
+            out.append(grp[:, s * block_words:(s + nbk) * block_words].ravel())
+    return np.concatenate(out) if out else np.zeros(0, dtype=np.uint32)
+
+
+def rows_from_records(flat, N: int, K: int, block_words: int, cols_per_word: int):
+    """Inverse of records_from_rows: section 0 words -> row-major [N][K/cpw]."""
+    KB = K // 128
+    W = K // cols_per_word
+    Np = padded_rows(N)
+    rows = np.zeros((Np, W), dtype=np.uint32)
+    pos = 0
+    for g in range(Np // ROW_GROUP):
+        for s in range(0, KB, STEP_BLOCKS):
+            nbk = min(STEP_BLOCKS, KB - s)
+            n = ROW_GROUP * nbk * block_words
+            rows[g * ROW_GROUP:(g + 1) * ROW_GROUP, s * block_words:(s + nbk) * block_words] = \
+                flat[pos:pos + n].reshape(ROW_GROUP, nbk * block_words)
+            pos += n
+    return rows[:N]
 
 
 def ternary_bit_pos(k):

@@ -53,7 +53,8 @@ def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
         words |= c[:, :, r] << np.uint32(layout.ternary_bit_pos(r))
     offs, total = layout.sections(layout.ternary_sizes(N, K))
     buf = bytearray(total)
-    buf[offs[0]:offs[0] + words.nbytes] = words.astype("<u4").tobytes()
+    rec = layout.records_from_rows(words, 8)
+    buf[offs[0]:offs[0] + rec.nbytes] = rec.astype("<u4").tobytes()
     s = np.asarray(s16, dtype="<u2")
     buf[offs[1]:offs[1] + s.nbytes] = s.tobytes()
     return bytes(buf)
@@ -63,7 +64,8 @@ def unpack(buf: bytes, N: int, K: int):
     """Inverse of ``pack``: (q int8 [N][K], s16 uint16 [N][K/128]). Code 11 is rejected."""
     offs, total = layout.sections(layout.ternary_sizes(N, K))
     assert len(buf) >= total
-    words = np.frombuffer(buf, dtype="<u4", count=N * K // 16, offset=offs[0]).reshape(N, K // 16)
+    flat = np.frombuffer(buf, dtype="<u4", count=layout.padded_rows(N) * K // 16, offset=offs[0])
+    words = layout.rows_from_records(flat, N, K, 8, 16)
     c = np.empty((N, K // 16, 16), dtype=np.uint32)
     for r in range(16):
         c[:, :, r] = (words >> np.uint32(layout.ternary_bit_pos(r))) & 3

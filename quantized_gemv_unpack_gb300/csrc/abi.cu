@@ -167,21 +167,14 @@ int run_tasks(int format, GemvTask* tasks, int n, int M, cudaStream_t s) {
   static thread_local GemvBatch b;
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mt = M - m0 < 8 ? M - m0 : 8;
-    const int rows = gemv_rows_per_tile(mt);
-    int tiles = 0;
-    int max_K = 0;
     for (int i = 0; i < n; ++i) {
       GemvTask t = tasks[i];
       t.x += (size_t)m0 * t.ldx;
       t.y += (size_t)m0 * t.ldy;
-      t.tile0 = tiles;
-      tiles += (t.N + rows - 1) / rows;
-      if (t.K > max_K) max_K = t.K;
       b.t[i] = t;
     }
     b.n_tasks = n;
-    b.n_tiles = tiles;
-    int rc = launch_gemv(format, b, mt, max_K, s);
+    int rc = launch_gemv(format, b, mt, s);
     if (rc) return rc;
   }
   return QMV_OK;
@@ -217,7 +210,8 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
   out->N = N;
   out->K = K;
   out->group = group;
-  const int64_t codes = format == QMV_TERNARY2 ? N * K / 4 : N * K / 2;
+  const int64_t padded = (N + 15) / 16 * 16;   // row groups of 16
+  const int64_t codes = format == QMV_TERNARY2 ? padded * K / 4 : padded * K / 2;
   const int64_t sizes[2] = {codes, N * (K / QMV_GROUP) * 2};
   fill_sections(out, sizes, 2);
   return QMV_OK;
@@ -242,7 +236,7 @@ int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* s
   for (int i = 0; i < n_tasks; ++i) {
     int rc = build_task(tasks[i].desc, format, tasks[i].w, tasks[i].x, tasks[i].ldx, tasks[i].y, tasks[i].ldy, &t[i]);
     if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
-    tiles += (t[i].N + 7) / 8;
+    tiles += (t[i].N + 3) / 4;
   }
   if (tiles > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
   return run_tasks(format, t, n_tasks, M, static_cast<cudaStream_t>(stream));

@@ -1,33 +1,53 @@
 // Fused dequantize-and-matvec for block-128 ternary and group-128 INT4 weights.
 //
-// One persistent launch walks a table of matvecs (one GEMV, the q|k|v group of
-// a layer, or a whole decode stack). Work is cut into tiles of 8*RW rows;
-// CTA c takes tiles c, c + gridDim.x, ... Each warp owns RW rows of a tile and
-// streams them along K: per step a lane reads 8 bytes of codes per row
-// (32 ternary or 16 INT4 weights) with a non-allocating 64-bit load and the
-// fp16 scale of the block they belong to.
+// One persistent launch (one CTA per SM) walks a table of matvecs: one GEMV,
+// the q|k|v group of a layer, or a whole decode stack. Rows are cut into tiles
+// of kConsumerWarps * RPW rows; the host gives every CTA a contiguous range of
+// tiles holding about the same number of bytes, so a CTA re-stages its
+// activations only when its range crosses into the next matvec.
 //
-// Activations are staged once per (x, chunk) in shared memory as fp16 pairs
-// in exactly the order a lane consumes them, after scaling the chunk by a
-// power of two so its largest magnitude lies in [2^9, 2^10) (ternary) or
-// [2^8, 2^9) (INT4); the scale is undone in fp32.
+// Streaming. A CTA has 16 decode warps. Each warp owns RPW consecutive rows of
+// the tile and a two-slot ring in shared memory; a slot holds one step (1024
+// columns) of its rows. The packed codes are stored in records of 16 rows x
+// one step, so a warp's rows of a step are one contiguous range: lane 0 of the
+// warp fills a slot with a single 1D bulk copy (cp.async.bulk) that completes
+// on the slot's mbarrier, two steps ahead of the step being decoded, walking
+// the same (tile, chunk, step) sequence as the decode loop. Every wait polls a
+// bounded number of times and then records QMV_ERR_TIMEOUT in the device
+// error word instead of spinning on.
 //
-// Decode, per 32-bit code word, without lookup tables:
+// Inside a decode warp, lane = 8*g + p: lane p (0..7) owns one 128-column
+// block of the step and lane group g (0..3) one row of each row quad, so the
+// warp decodes RPW rows x 1024 columns per step.
+//
+// Activations are staged per (x, chunk) in shared memory as fp16 pairs in
+// the order a lane consumes them, after scaling the chunk by a power of two
+// so its largest magnitude lies in [2^9, 2^10) (ternary) or [2^8, 2^9) (INT4);
+// the scale is undone in fp32.
+//
+// Decode, per 32-bit code word, without lookup tables, one shift and one
+// three-input logic op per column pair (mask and base live in registers).
+// The ALU pipe (logic ops, shifts) and the FMA pipe (integer multiply, fp16
+// FMA) each issue 16 lanes per clock per SM sub-partition on this GPU, so of
+// the eight ternary shifts per word four (the left shifts by 9, 7, 5, 1) are
+// integer multiplies by 2^s and four are funnel shifts; the multipliers and
+// amounts arrive as kernel parameters so the assembler keeps that split.
 //  * ternary: the low half holds even columns, the high half odd columns, so a
 //    word gives eight (even, odd) column pairs. Shifting pair i's two 2-bit
 //    codes to bits 9-10 and 25-26 and computing (t & 0x06000600) ^ 0x3C003C00
 //    yields two fp16 values v = 1 + q/2 (code 00 -> 1.0, 01 -> 1.5, 10 -> 0.5):
 //    bit 9 is the mantissa MSB (+0.5), bit 10 the exponent LSB (halves 1.0).
-//    Then sum_k v_k x_k = sum_k x_k + (1/2) sum_k q_k x_k, and the fp16
-//    accumulator is seeded with -sum x over the lane's columns (computed once
-//    per staged chunk), leaving (1/2) sum q x; the factor 2 is applied at the end.
+//    Then sum_k v_k x_k = sum_k x_k + (1/2) sum_k q_k x_k; the fp16
+//    accumulator is seeded with -sum x over the block (computed once per staged
+//    chunk), leaving (1/2) sum q x; the factor 2 is applied at the end.
 //  * INT4: (t & 0x000F000F) ^ 0x64086408 maps a two's-complement nibble q to
 //    the fp16 integer 1032 + q (1024 + offset-binary nibble); subtracting 1032
 //    gives q exactly, which is then multiplied into the fp16 accumulator.
-// Per row and lane step the fp16 pair accumulator is widened to fp32, scaled
-// by the block's fp16 scale and added to an fp32 sum; warp shuffles reduce
-// the 32 lanes at the end of the tile.
-#include <cstring>
+// Two fp16 pair accumulators per block (first and second half of the words)
+// are added, widened to fp32 and scaled by the block's fp16 scale; three warp
+// shuffles reduce the eight lanes of a row at the end of the tile.
+#include <algorithm>
+#include <cstdlib>
 
 #include "qmv_internal.cuh"
 
@@ -38,29 +58,68 @@ template <int FMT>
 struct Fmt;
 template <>
 struct Fmt<QMV_TERNARY2> {
-  static constexpr int KPL = 32;      // columns per lane per step (one 8-byte load)
-  static constexpr int PAIRS = 8;     // column pairs per 32-bit word
-  static constexpr int COLS_PER_WORD = 16;
-  static constexpr int XLOG2 = 9;     // staged |x| max in [2^9, 2^10)
+  static constexpr int WPB = 8;    // 32-bit code words per 128-column block
+  static constexpr int PPW = 8;    // column pairs per word
+  static constexpr int CPW = 16;   // columns per word
+  static constexpr int JW = 2;     // 16-byte activation pieces per word
+  static constexpr int XLOG2 = 9;  // staged |x| max in [2^9, 2^10)
+  static constexpr uint32_t MASK = 0x06000600u, BASE = 0x3C003C00u;
 };
 template <>
 struct Fmt<QMV_INT4> {
-  static constexpr int KPL = 16;
-  static constexpr int PAIRS = 4;
-  static constexpr int COLS_PER_WORD = 8;
+  static constexpr int WPB = 16;
+  static constexpr int PPW = 4;
+  static constexpr int CPW = 8;
+  static constexpr int JW = 1;
   static constexpr int XLOG2 = 8;
+  static constexpr uint32_t MASK = 0x000F000Fu, BASE = 0x64086408u;
 };
 
-__host__ __device__ constexpr int rows_per_warp(int mt) { return mt <= 2 ? 4 : (mt <= 4 ? 2 : 1); }
+constexpr int kGroups = 4;            // lane groups (rows of a row quad)
+constexpr int kBlocksPerStep = 8;     // lanes per row
+constexpr int kStep = kBlocksPerStep * 128;
+constexpr int kSlots = 2;             // ring slots per decode warp
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr uint32_t kWaitLimit = 1u << 26;  // polls before a wait is declared lost
 
-__device__ __forceinline__ uint2 ld_stream_u2(const uint32_t* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+// (a & b) ^ c as one logic op
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// a * m on the integer-multiply unit (m a run-time power of two: a left shift)
+__device__ __forceinline__ uint32_t mul_lo(uint32_t a, uint32_t m) {
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(m));
+  return d;
+}
+// shifts by a run-time amount on the shift unit
+__device__ __forceinline__ uint32_t shl_r(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(s));
+  return d;
+}
+__device__ __forceinline__ uint32_t shr_r(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(s));
+  return d;
 }
 
+// decode constants held in registers for the whole kernel
+struct DecodeK {
+  uint32_t mask, base;
+  uint32_t m9, m7, m5, m1;  // 2^9, 2^7, 2^5, 2^1
+  uint32_t s1, s3, s5;      // shift amounts 1, 3, 5 (INT4: 4, 8, 12)
+};
+
 __device__ __forceinline__ __half2 as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
 __device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+// 2^e as a float, e in [-126, 127]
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
 __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
   int lo = 0, hi = b.n_tasks - 1;
@@ -71,83 +130,186 @@ __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
   return lo;
 }
 
-// power of two 2^e as a float, e in [-126, 127]
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
-
 template <int FMT>
-__device__ __forceinline__ __half2 decode_pair(uint32_t w, int i) {
+__device__ __forceinline__ __half2 decode_pair(uint32_t w, int i, const DecodeK& k) {
   if constexpr (FMT == QMV_TERNARY2) {
-    // pair i: even column code at bits 2i..2i+1, odd column code at 16+2i..17+2i
-    uint32_t t = (i <= 4) ? (w << (9 - 2 * i)) : (w >> (2 * i - 9));
-    return as_h2((t & 0x06000600u) ^ 0x3C003C00u);
+    // pair i: even column code at bits 2i..2i+1, odd column code at 16+2i..17+2i;
+    // shift both to bits 9-10 / 25-26
+    uint32_t t;
+    switch (i) {
+      case 0: t = mul_lo(w, k.m9); break;
+      case 1: t = mul_lo(w, k.m7); break;
+      case 2: t = mul_lo(w, k.m5); break;
+      case 3: t = shl_r(w, k.s3); break;
+      case 4: t = mul_lo(w, k.m1); break;
+      case 5: t = shr_r(w, k.s1); break;
+      case 6: t = shr_r(w, k.s3); break;
+      default: t = shr_r(w, k.s5); break;
+    }
+    return as_h2(and_xor(t, k.mask, k.base));
   } else {
-    uint32_t t = w >> (4 * i);
-    __half2 v = as_h2((t & 0x000F000Fu) ^ 0x64086408u);
-    return __hsub2(v, __floats2half2_rn(1032.f, 1032.f));
+    const uint32_t t = i == 0 ? w : shr_r(w, i == 1 ? k.s1 : (i == 2 ? k.s3 : k.s5));
+    return __hsub2(as_h2(and_xor(t, k.mask, k.base)), __floats2half2_rn(1032.f, 1032.f));
   }
 }
 
-template <int FMT, int MT>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvBatch b) {
+// ---- mbarrier and bulk-copy helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait: false (and the device error word set) if the phase never completes
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  for (uint32_t polls = 0; polls < kWaitLimit; ++polls)
+    if (mbar_try_wait(bar, parity)) return true;
+  atomicCAS(err, 0, (int)QMV_ERR_TIMEOUT);
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+template <int FMT, int RPW>
+struct Geometry {
+  static constexpr int BLOCK_BYTES = Fmt<FMT>::WPB * 4;
+  static constexpr int ROW_STEP_BYTES = kBlocksPerStep * BLOCK_BYTES;   // one step of one row
+  static constexpr int SLOT = RPW * ROW_STEP_BYTES;
+  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
+  static constexpr int BARS = kConsumerWarps * kSlots * 8;
+  static constexpr int TILE_ROWS = kConsumerWarps * RPW;
+};
+
+template <int FMT, int MT, int RPW>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvBatch b) {
   using F = Fmt<FMT>;
-  constexpr int KPL = F::KPL;
-  constexpr int STEP = 32 * KPL;          // columns per warp step
-  constexpr int J = KPL / 8;              // 16-byte activation pieces per lane step
-  constexpr int RW = rows_per_warp(MT);
-  constexpr int ROWS = (kThreads / 32) * RW;
+  using G = Geometry<FMT, RPW>;
+  constexpr int WPB = F::WPB;
+  constexpr int JW = F::JW;
+  constexpr int RQ = RPW / kGroups;          // row quads per decode warp
   constexpr bool TERN = FMT == QMV_TERNARY2;
 
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw;                                             // [warp][slot][RPW rows of a step]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + G::RING);          // [warp][slot]
   const int KC = b.kc;
-  const int S = KC / STEP;
-  uint4* xs = reinterpret_cast<uint4*>(smem);                        // [MT][S][J][32]
-  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * J * 32);  // [MT][S][32]
-  __shared__ float s_red[kThreads / 32][MT];
+  const int S = KC / kStep;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);        // [MT][S][WPB][JW][8]
+  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8]
+  __shared__ float s_red[kConsumerWarps][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int tile_begin = b.cta_tile[blockIdx.x];
+  const int tile_end = b.cta_tile[blockIdx.x + 1];
+  unsigned char* wring = ring + (size_t)warp * kSlots * G::SLOT;
+  uint64_t* wfull = full + warp * kSlots;
 
-  const uint16_t* staged_x = nullptr;
-  int staged_c = -1;
-  int staged_K = -1;
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(&wfull[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
-  for (int tile = blockIdx.x; tile < b.n_tiles; tile += gridDim.x) {
-    const int ti = find_task(b, tile);
-    const GemvTask& T = b.t[ti];
+  // ---- producer side of this warp: copy the warp's rows of one step into a slot
+  constexpr int kStepWords = kBlocksPerStep * WPB;
+  int p_tile = tile_begin, p_ti = 0, p_kc0 = 0, p_s = 0;
+  if (p_tile < tile_end) p_ti = find_task(b, p_tile);
+  uint32_t n_issued = 0;
+  auto issue_one = [&]() {
+    if (p_tile >= tile_end) return;
+    const GemvTask& T = b.t[p_ti];
     const int K = T.K;
-    const int KW = K / F::COLS_PER_WORD;
-    const int KB = K / 128;
-    const int rbase = (tile - T.tile0) * ROWS + warp * RW;
-    const int nchunks = (K + KC - 1) / KC;
+    const int nb = min(KC, K - p_kc0) / 128;
+    const int nbk = min(kBlocksPerStep, nb - p_s * kBlocksPerStep);
+    const int blk0 = p_kc0 / 128 + p_s * kBlocksPerStep;
+    const int wrow0 = (p_tile - T.tile0) * G::TILE_ROWS + warp * RPW;
+    const int N16 = (T.N + 15) / 16 * 16;
+    // the warp's RPW rows lie inside one 16-row group: one contiguous piece of
+    // the (group, step) record; rows past the padded end are not copied
+    const uint32_t bytes = wrow0 < N16 ? (uint32_t)(RPW * nbk * G::BLOCK_BYTES) : 0u;
+    const int slot = n_issued % kSlots;
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the slot precede the copy
+      mbar_arrive_expect_tx(&wfull[slot], bytes);
+      if (bytes) {
+        const size_t off = (size_t)(wrow0 / 16) * 16 * (K / F::CPW) + (size_t)(blk0 / kBlocksPerStep) * 16 * kStepWords +
+                           (size_t)(wrow0 % 16) * nbk * WPB;
+        bulk_g2s(wring + (size_t)slot * G::SLOT, T.codes + off, bytes, &wfull[slot]);
+      }
+    }
+    ++n_issued;
+    if (++p_s * kBlocksPerStep >= nb) {
+      p_s = 0;
+      p_kc0 += KC;
+      if (p_kc0 >= K) {
+        p_kc0 = 0;
+        if (++p_tile < tile_end) p_ti = find_task(b, p_tile);
+      }
+    }
+  };
+  for (int i = 0; i < kSlots; ++i) issue_one();
 
-    float acc[RW][MT];
+  // ===================== decode warps
+  const int g = lane >> 3;
+  const int p = lane & 7;
+  const DecodeK dk{b.magic[0], b.magic[1], b.magic[2], b.magic[3], b.magic[4],
+                   b.magic[5], b.magic[6], b.magic[7], b.magic[8]};  // mask base 2^9 2^7 2^5 2^1 s1 s3 s5
+  const uint16_t* staged_x = nullptr;
+  int staged_kc0 = -1;
+  int staged_K = -1;
+  uint32_t it = 0;
+
+  for (int tile = tile_begin; tile < tile_end; ++tile) {
+    const int ti = find_task(b, tile);
+    const unsigned short* __restrict__ scales = reinterpret_cast<const unsigned short*>(b.t[ti].scales);
+    const uint16_t* __restrict__ x = b.t[ti].x;
+    float* __restrict__ y = b.t[ti].y;
+    const int N = b.t[ti].N, K = b.t[ti].K, ldx = b.t[ti].ldx, ldy = b.t[ti].ldy;
+    const int KB = K / 128;
+    const int wrow0 = (tile - b.t[ti].tile0) * G::TILE_ROWS + warp * RPW;
+
+    float acc[RQ][MT];
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
+    for (int r = 0; r < RQ; ++r)
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
 
-    for (int c = 0; c < nchunks; ++c) {
-      const int kc0 = c * KC;
+    for (int kc0 = 0; kc0 < K; kc0 += KC) {
       const int kcn = min(KC, K - kc0);
+      const int nb = kcn / 128;
 
-      if (T.x != staged_x || c != staged_c || K != staged_K || nchunks > 1) {
-        // ---- stage activations of this chunk (all threads of the CTA)
+      if (x != staged_x || kc0 != staged_kc0 || K != staged_K) {
+        // ---- stage the activations of this chunk
         __syncthreads();
         const int ngroups = kcn / 8;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           float mx = 0.f;
-          const uint16_t* xr = T.x + (size_t)m * T.ldx + kc0;
-          for (int g = tid; g < ngroups; g += kThreads) {
-            uint4 raw = *reinterpret_cast<const uint4*>(xr + g * 8);
-            uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+          const uint16_t* xr = x + (size_t)m * ldx + kc0;
+          for (int q = tid; q < ngroups; q += kConsumerThreads) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(xr + q * 8);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              mx = fmaxf(mx, fabsf(bf16_to_f32(wv[q] & 0xFFFFu)));
-              mx = fmaxf(mx, fabsf(bf16_to_f32(wv[q] >> 16)));
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t wv = word_of(raw, e);
+              mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(wv & 0xFFFFu)), fabsf(bf16_to_f32(wv >> 16))));
             }
           }
 #pragma unroll
@@ -158,13 +320,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         if (tid < MT) {
           float mx = 0.f;
 #pragma unroll
-          for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, s_red[w][tid]);
+          for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_red[w][tid]);
           int e = 0;
           if (mx > 0.f && mx <= 3.4e38f) {
             int ex;
-            frexpf(mx, &ex);                         // mx = f * 2^ex, f in [0.5, 1)
-            e = F::XLOG2 - (ex - 1);
-            e = max(-120, min(120, e));
+            frexpf(mx, &ex);  // mx = f * 2^ex, f in [0.5, 1)
+            e = max(-120, min(120, F::XLOG2 - (ex - 1)));
           }
           s_xscale[tid] = exp2i(e);
           s_xinv[tid] = exp2i(-e);
@@ -173,164 +334,228 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const float xsc = s_xscale[m];
-          const uint16_t* xr = T.x + (size_t)m * T.ldx + kc0;
-          for (int g = tid; g < ngroups; g += kThreads) {
-            uint4 raw = *reinterpret_cast<const uint4*>(xr + g * 8);
-            uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+          const uint16_t* xr = x + (size_t)m * ldx + kc0;
+          for (int q = tid; q < ngroups; q += kConsumerThreads) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(xr + q * 8);
             uint32_t hv[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              __half2 h = __floats2half2_rn(bf16_to_f32(wv[q] & 0xFFFFu) * xsc, bf16_to_f32(wv[q] >> 16) * xsc);
-              hv[q] = *reinterpret_cast<uint32_t*>(&h);
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t wv = word_of(raw, e);
+              __half2 h = __floats2half2_rn(bf16_to_f32(wv & 0xFFFFu) * xsc, bf16_to_f32(wv >> 16) * xsc);
+              hv[e] = *reinterpret_cast<uint32_t*>(&h);
             }
-            const int k = g * 8;
-            const int s = k / STEP;
-            const int l = (k % STEP) / KPL;
-            const int j = (k % KPL) / 8;
-            xs[(((size_t)m * S + s) * J + j) * 32 + l] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            const int k = q * 8;
+            const int blk = k / 128, cc = k % 128;
+            const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
+            const int h = cc / F::CPW, j = (cc % F::CPW) / 8;
+            xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
           }
         }
         if constexpr (TERN) {
           __syncthreads();
-          for (int g = tid; g < MT * S * 32; g += kThreads) {
-            const int m = g / (S * 32);
-            const int s = (g / 32) % S;
-            const int l = g % 32;
+          for (int q = tid; q < MT * S * kBlocksPerStep; q += kConsumerThreads) {
+            const int m = q / (S * kBlocksPerStep);
+            const int blk = q % (S * kBlocksPerStep);
+            const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
             float se = 0.f, so = 0.f;
-            if (s * STEP + l * KPL < kcn) {
+            if (blk < nb) {
+              for (int h = 0; h < WPB; ++h)
 #pragma unroll
-              for (int j = 0; j < J; ++j) {
-                uint4 p = xs[(((size_t)m * S + s) * J + j) * 32 + l];
-                uint32_t pv[4] = {p.x, p.y, p.z, p.w};
+                for (int j = 0; j < JW; ++j) {
+                  const uint4 pc = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  float2 f = __half22float2(as_h2(pv[q]));
-                  se += f.x;
-                  so += f.y;
+                  for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(as_h2(word_of(pc, e)));
+                    se += f.x;
+                    so += f.y;
+                  }
                 }
-              }
             }
-            negs[g] = __floats2half2_rn(-se, -so);
+            negs[q] = __floats2half2_rn(-se, -so);
           }
         }
         __syncthreads();
-        staged_x = T.x;
-        staged_c = c;
+        staged_x = x;
+        staged_kc0 = kc0;
         staged_K = K;
       }
 
-      // ---- stream the rows of this warp over the chunk
-      float xinv[MT];
+      // ---- decode this warp's rows over the chunk, one ring slot per step
+      const unsigned short* sp[RQ];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) xinv[m] = s_xinv[m];
-      const int nsteps = (kcn + STEP - 1) / STEP;
+      for (int r = 0; r < RQ; ++r) {
+        const int row = min(wrow0 + r * kGroups + g, N - 1);  // rows past N read the last row, never stored
+        sp[r] = scales + (size_t)row * KB + kc0 / 128 + p;
+      }
+      float accc[RQ][MT];
+#pragma unroll
+      for (int r = 0; r < RQ; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) accc[r][m] = 0.f;
+      const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
+      unsigned short scn[RQ];
+#pragma unroll
+      for (int r = 0; r < RQ; ++r) scn[r] = p < nb ? __ldg(sp[r]) : (unsigned short)0;
 
-      uint2 cw_n[RW];
-      uint16_t sc_n[RW];
-      auto load_step = [&](int s, uint2* cw, uint16_t* sc) {
-        const int kl = s * STEP + lane * KPL;
-        const int k0 = kc0 + kl;
+      for (int s = 0; s < nsteps; ++s, ++it) {
+        const bool active = s * kBlocksPerStep + p < nb;
+        unsigned short sc[RQ];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          const int row = rbase + r;
-          if (row < T.N && kl < kcn) {
-            cw[r] = ld_stream_u2(T.codes + (size_t)row * KW + k0 / F::COLS_PER_WORD);
-            sc[r] = __ldg(reinterpret_cast<const unsigned short*>(T.scales) + (size_t)row * KB + k0 / 128);
-          } else {
-            cw[r] = make_uint2(0u, 0u);
-            sc[r] = 0;
+        for (int r = 0; r < RQ; ++r) {
+          sc[r] = scn[r];
+          if ((s + 1) * kBlocksPerStep + p < nb) scn[r] = __ldg(sp[r] + (s + 1) * kBlocksPerStep);
+        }
+        const int slot = it % kSlots;
+        mbar_wait(&wfull[slot], (it / kSlots) & 1u, b.err);
+        if (active) {
+          // rows of the step are nbk blocks apart in the slot
+          const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
+          const unsigned char* sb = wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES;
+          uint4 cw[RQ][WPB / 4];
+#pragma unroll
+          for (int r = 0; r < RQ; ++r)
+#pragma unroll
+            for (int u = 0; u < WPB / 4; ++u)
+              cw[r][u] = *reinterpret_cast<const uint4*>(sb + (r * kGroups + g) * row_bytes + u * 16);
+          __half2 a0[RQ][MT], a1[RQ][MT];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const __half2 init = TERN ? negs[((size_t)m * S + s) * kBlocksPerStep + p] : __floats2half2_rn(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < RQ; ++r) {
+              a0[r][m] = init;
+              a1[r][m] = __floats2half2_rn(0.f, 0.f);
+            }
           }
-        }
-      };
-      load_step(0, cw_n, sc_n);
-
-      for (int s = 0; s < nsteps; ++s) {
-        uint2 cw[RW];
-        uint16_t sc[RW];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          cw[r] = cw_n[r];
-          sc[r] = sc_n[r];
-        }
-        if (s + 1 < nsteps) load_step(s + 1, cw_n, sc_n);
-        const int kl = s * STEP + lane * KPL;
-        if (kl >= kcn) continue;
-
-        __half2 a2[RW][MT];
+          for (int h = 0; h < WPB; ++h) {
+            uint4 xw[MT][JW];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          __half2 init = TERN ? negs[((size_t)m * S + s) * 32 + lane] : __floats2half2_rn(0.f, 0.f);
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int r = 0; r < RW; ++r) a2[r][m] = init;
-        }
+              for (int j = 0; j < JW; ++j) xw[m][j] = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + p];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          constexpr int JW = J / 2;     // pieces per word
-          uint4 xw[MT][JW];
+            for (int r = 0; r < RQ; ++r) {
+              const uint32_t w = word_of(cw[r][h / 4], h % 4);
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
+              for (int i = 0; i < F::PPW; ++i) {
+                const __half2 v = decode_pair<FMT>(w, i, dk);
 #pragma unroll
-            for (int j = 0; j < JW; ++j) xw[m][j] = xs[(((size_t)m * S + s) * J + h * JW + j) * 32 + lane];
-#pragma unroll
-          for (int r = 0; r < RW; ++r) {
-            const uint32_t w = h ? cw[r].y : cw[r].x;
-#pragma unroll
-            for (int i = 0; i < F::PAIRS; ++i) {
-              const __half2 v = decode_pair<FMT>(w, i);
-#pragma unroll
-              for (int m = 0; m < MT; ++m) {
-                const uint4 p = xw[m][i / 4];
-                const uint32_t pv = (i % 4 == 0) ? p.x : (i % 4 == 1) ? p.y : (i % 4 == 2) ? p.z : p.w;
-                a2[r][m] = __hfma2(v, as_h2(pv), a2[r][m]);
+                for (int m = 0; m < MT; ++m) {
+                  const __half2 xv = as_h2(word_of(xw[m][i / 4], i % 4));
+                  if (h < WPB / 2) a0[r][m] = __hfma2(v, xv, a0[r][m]);
+                  else a1[r][m] = __hfma2(v, xv, a1[r][m]);
+                }
               }
             }
           }
-        }
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          const float scf = __half2float(__ushort_as_half(sc[r]));
+          for (int r = 0; r < RQ; ++r) {
+            const float scf = __half2float(__ushort_as_half(sc[r]));
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const float2 f = __half22float2(a2[r][m]);
-            acc[r][m] = fmaf(f.x + f.y, scf * xinv[m], acc[r][m]);
+            for (int m = 0; m < MT; ++m) {
+              const __half2 t = __hadd2(a0[r][m], a1[r][m]);
+              accc[r][m] = fmaf(__low2float(t) + __high2float(t), scf, accc[r][m]);
+            }
           }
         }
+        __syncwarp();  // every lane is done with the slot before it is refilled
+        issue_one();
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float xinv = s_xinv[m];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) acc[r][m] = fmaf(accc[r][m], xinv, acc[r][m]);
       }
     }
 
-    // ---- reduce over lanes, write y
+    // ---- reduce the eight lanes of each row, write y
     constexpr float kFactor = TERN ? 2.f : 1.f;
 #pragma unroll
-    for (int r = 0; r < RW; ++r) {
+    for (int r = 0; r < RQ; ++r) {
+      const int row = wrow0 + r * kGroups + g;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         float v = acc[r][m];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        const int row = rbase + r;
-        if (lane == 0 && row < T.N) T.y[(size_t)m * T.ldy + row] = kFactor * v;
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        if (p == 0 && row < N) y[(size_t)m * ldy + row] = kFactor * v;
       }
     }
   }
 }
 
-template <int FMT, int MT>
-int launch_t(GemvBatch& b, int max_K, cudaStream_t s) {
-  constexpr int KPL = Fmt<FMT>::KPL;
-  constexpr int STEP = 32 * KPL;
-  // activation chunk: as much of K as fits a ~112 KB budget, in whole warp steps
-  int kc_cap = (57344 / MT) / STEP * STEP;
-  int kc = ((max_K + STEP - 1) / STEP) * STEP;
+// rows per decode warp: large for one activation row, small when the launch is
+// too small to give every SM a tile or when many activation rows need registers
+template <int FMT>
+int pick_rpw(int M, int64_t total_rows) {
+  const int big = M == 1 ? (FMT == QMV_TERNARY2 ? 16 : 8) : (M == 2 ? 8 : 4);
+  if (big > 4 && total_rows / ((int64_t)kConsumerWarps * big) < sm_count()) return 4;
+  return big;
+}
+
+template <int FMT, int MT, int RPW>
+int launch_t(GemvBatch& b, cudaStream_t s) {
+  using F = Fmt<FMT>;
+  using G = Geometry<FMT, RPW>;
+  constexpr size_t kSmemMax = 227 * 1024;
+  // tiles, numbered across tasks
+  int tiles = 0;
+  int max_K = 0;
+  for (int i = 0; i < b.n_tasks; ++i) {
+    b.t[i].tile0 = tiles;
+    tiles += (b.t[i].N + G::TILE_ROWS - 1) / G::TILE_ROWS;
+    max_K = std::max(max_K, (int)b.t[i].K);
+  }
+  b.n_tiles = tiles;
+  b.rows_per_tile = G::TILE_ROWS;
+  // activation chunk: as much of K as fits next to the ring, in whole steps;
+  // per staged column: MT fp16 values, plus one fp16 pair per 128 columns and row
+  const size_t fixed = G::RING + G::BARS;
+  const size_t budget = kSmemMax - fixed - 1024;
+  int kc_cap = (int)(budget / ((size_t)MT * 2 + ((size_t)MT * 4 + 127) / 128)) / kStep * kStep;
+  int kc = ((max_K + kStep - 1) / kStep) * kStep;
   if (kc > kc_cap) kc = kc_cap;
+  if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", MT);
   b.kc = kc;
-  const size_t S = kc / STEP;
-  size_t smem = (size_t)MT * kc * 2 + (FMT == QMV_TERNARY2 ? (size_t)MT * S * 32 * 4 : 0);
-  auto kern = gemv_kernel<FMT, MT>;
+  const size_t S = kc / kStep;
+  const size_t smem = fixed + (size_t)MT * kc * 2 + (size_t)MT * S * kBlocksPerStep * 4;
+  // decode constants
+  b.magic[0] = F::MASK;
+  b.magic[1] = F::BASE;
+  b.magic[2] = 1u << 9;
+  b.magic[3] = 1u << 7;
+  b.magic[4] = 1u << 5;
+  b.magic[5] = 1u << 1;
+  const bool tern = FMT == QMV_TERNARY2;
+  b.magic[6] = tern ? 1 : 4;
+  b.magic[7] = tern ? 3 : 8;
+  b.magic[8] = tern ? 5 : 12;
+  b.magic[9] = 0;
+  b.err = device_error_word();
+  if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+  auto kern = gemv_kernel<FMT, MT, RPW>;
   int per_sm = 0;
   int rc = kernel_fit((const void*)kern, kThreads, smem, &per_sm);
   if (rc != QMV_OK) return rc;
-  int grid = sm_count() * per_sm;
-  if (grid > b.n_tiles) grid = b.n_tiles;
+  // persistent grid, one CTA per SM; contiguous tile ranges of about equal bytes
+  const int grid = std::min(std::min(sm_count(), kMaxCtas), tiles);
+  double total = 0;
+  for (int i = 0; i < b.n_tasks; ++i) total += (double)b.t[i].N * b.t[i].K;
+  b.n_ctas = grid;
+  b.cta_tile[0] = 0;
+  int c = 1;
+  double done = 0;
+  for (int i = 0; i < b.n_tasks && c < grid; ++i) {
+    const int nt = (b.t[i].N + G::TILE_ROWS - 1) / G::TILE_ROWS;
+    for (int j = 0; j < nt && c < grid; ++j) {
+      done += (double)std::min(G::TILE_ROWS, (int)b.t[i].N - j * G::TILE_ROWS) * b.t[i].K;
+      while (c < grid && done >= total * c / grid) b.cta_tile[c++] = b.t[i].tile0 + j + 1;
+    }
+  }
+  for (; c <= grid; ++c) b.cta_tile[c] = tiles;
   kern<<<grid, kThreads, smem, s>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
@@ -338,27 +563,29 @@ int launch_t(GemvBatch& b, int max_K, cudaStream_t s) {
 }
 
 template <int FMT>
-int launch_fmt(GemvBatch& b, int M, int max_K, cudaStream_t s) {
+int launch_fmt(GemvBatch& b, int M, cudaStream_t s) {
+  int64_t rows = 0;
+  for (int i = 0; i < b.n_tasks; ++i) rows += b.t[i].N;
+  const int rpw = pick_rpw<FMT>(M, rows);
+  constexpr int BIG1 = FMT == QMV_TERNARY2 ? 16 : 8;
   switch (M) {
-    case 1: return launch_t<FMT, 1>(b, max_K, s);
-    case 2: return launch_t<FMT, 2>(b, max_K, s);
-    case 3: return launch_t<FMT, 3>(b, max_K, s);
-    case 4: return launch_t<FMT, 4>(b, max_K, s);
-    case 5: return launch_t<FMT, 5>(b, max_K, s);
-    case 6: return launch_t<FMT, 6>(b, max_K, s);
-    case 7: return launch_t<FMT, 7>(b, max_K, s);
-    case 8: return launch_t<FMT, 8>(b, max_K, s);
+    case 1: return rpw == 4 ? launch_t<FMT, 1, 4>(b, s) : launch_t<FMT, 1, BIG1>(b, s);
+    case 2: return rpw == 4 ? launch_t<FMT, 2, 4>(b, s) : launch_t<FMT, 2, 8>(b, s);
+    case 3: return launch_t<FMT, 3, 4>(b, s);
+    case 4: return launch_t<FMT, 4, 4>(b, s);
+    case 5: return launch_t<FMT, 5, 4>(b, s);
+    case 6: return launch_t<FMT, 6, 4>(b, s);
+    case 7: return launch_t<FMT, 7, 4>(b, s);
+    case 8: return launch_t<FMT, 8, 4>(b, s);
     default: return fail(QMV_ERR_ARG, "M=%d outside 1..8 for one launch", M);
   }
 }
 
 }  // namespace
 
-int gemv_rows_per_tile(int M) { return (kThreads / 32) * rows_per_warp(M); }
-
-int launch_gemv(int format, GemvBatch& b, int M, int max_K, cudaStream_t s) {
-  if (format == QMV_TERNARY2) return launch_fmt<QMV_TERNARY2>(b, M, max_K, s);
-  if (format == QMV_INT4) return launch_fmt<QMV_INT4>(b, M, max_K, s);
+int launch_gemv(int format, GemvBatch& b, int M, cudaStream_t s) {
+  if (format == QMV_TERNARY2) return launch_fmt<QMV_TERNARY2>(b, M, s);
+  if (format == QMV_INT4) return launch_fmt<QMV_INT4>(b, M, s);
   return fail(QMV_ERR_UNSUPPORTED, "format %d has no matvec kernel", format);
 }
 

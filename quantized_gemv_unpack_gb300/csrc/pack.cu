@@ -31,6 +31,15 @@ __device__ uint16_t f64_to_f16_rne(double d) {
   return (uint16_t)(sign | (uint32_t)enc);
 }
 
+// Word offset of block b of row n in the row-group record layout of the codes
+// section: groups of 16 rows, steps of 8 blocks, each record row-major.
+__device__ __forceinline__ int64_t record_word(int64_t n, int64_t b, int64_t K, int block_words) {
+  const int64_t KB = K / 128;
+  const int64_t g = n / 16, r = n % 16, st = b / 8, j = b % 8;
+  const int64_t nbk = KB - st * 8 < 8 ? KB - st * 8 : 8;
+  return ((g * 16 * KB + st * 16 * 8) + r * nbk + j) * block_words;
+}
+
 __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
                                     uint16_t* __restrict__ scales) {
   const int64_t nb = K / 128;
@@ -63,7 +72,7 @@ __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int6
       words[k >> 4] |= code << pos;
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + n * (K / 16) + b * 8);
+  uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 8));
   dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
   dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
   scales[n * nb + b] = f64_to_f16_rne(s);
@@ -101,32 +110,38 @@ __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t
       words[k >> 3] |= ((uint32_t)q & 0xFu) << pos;
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + n * (K / 8) + b * 16);
+  uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 16));
 #pragma unroll
   for (int j = 0; j < 4; ++j) dst[j] = make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
   scales[n * nb + b] = f64_to_f16_rne(s);
 }
 
-// One thread per code word: writes the int8 values of its columns.
+// One thread per (row, block): decodes the block's columns to int8.
 __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, int64_t N, int64_t K,
                               int8_t* __restrict__ q, int* err) {
-  const int cpw = format == QMV_TERNARY2 ? 16 : 8;
-  const int64_t nw = N * (K / cpw);
-  const int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (wi >= nw) return;
-  const uint32_t w = codes[wi];
-  int8_t* out = q + wi * cpw;                        // row-major: word wi covers columns wi*cpw .. +cpw
+  const int64_t KB = K / 128;
+  const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= N * KB) return;
+  const int64_t n = blk / KB, b = blk % KB;
+  const int bw = format == QMV_TERNARY2 ? 8 : 16;
+  const uint32_t* src = codes + record_word(n, b, K, bw);
+  int8_t* out = q + n * K + b * 128;
   bool bad = false;
-  for (int r = 0; r < cpw; ++r) {
+  for (int wi = 0; wi < bw; ++wi) {
+    const uint32_t w = src[wi];
     if (format == QMV_TERNARY2) {
-      const int pos = (r & 1) ? 15 + r : r;
-      const uint32_t c = (w >> pos) & 3u;
-      bad |= c == 3u;
-      out[r] = c == 1u ? 1 : (c == 2u ? -1 : 0);
+      for (int r = 0; r < 16; ++r) {
+        const int pos = (r & 1) ? 15 + r : r;
+        const uint32_t c = (w >> pos) & 3u;
+        bad |= c == 3u;
+        out[wi * 16 + r] = c == 1u ? 1 : (c == 2u ? -1 : 0);
+      }
     } else {
-      const int pos = (r & 1) ? 14 + 2 * r : 2 * r;
-      const int v = (int)((w >> pos) & 0xFu);
-      out[r] = (int8_t)(v >= 8 ? v - 16 : v);
+      for (int r = 0; r < 8; ++r) {
+        const int pos = (r & 1) ? 14 + 2 * r : 2 * r;
+        const int v = (int)((w >> pos) & 0xFu);
+        out[wi * 8 + r] = (int8_t)(v >= 8 ? v - 16 : v);
+      }
     }
   }
   if (bad) atomicCAS(err, 0, QMV_ERR_CORRUPT);
@@ -145,7 +160,12 @@ int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, 
   const int64_t grid = (blocks + threads - 1) / threads;
   if (grid > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "matrix too large for one pack launch");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // zero the alignment padding after each section so every byte is determined
+  // zero the padding rows of the last row group and the alignment padding after
+  // each section, so every byte is determined
+  if (desc->N % 16) {
+    cudaError_t e = cudaMemsetAsync(base + desc->off[0], 0, (size_t)desc->bytes[0], s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero padding rows");
+  }
   const int64_t gaps[2][2] = {{desc->off[0] + desc->bytes[0], desc->off[1]},
                               {desc->off[1] + desc->bytes[1], desc->total_bytes}};
   for (const auto& gp : gaps) {
@@ -191,10 +211,9 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
   if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   const char* base = static_cast<const char*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int cpw = format == QMV_TERNARY2 ? 16 : 8;
-  const int64_t nw = desc->N * (desc->K / cpw);
-  const int threads = 256;
-  unpack_kernel<<<(unsigned)((nw + threads - 1) / threads), threads, 0, s>>>(
+  const int64_t nblk = desc->N * (desc->K / 128);
+  const int threads = 128;
+  unpack_kernel<<<(unsigned)((nblk + threads - 1) / threads), threads, 0, s>>>(
       format, reinterpret_cast<const uint32_t*>(base + desc->off[0]), desc->N, desc->K, q, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "unpack launch");

@@ -30,11 +30,13 @@ int kernel_fit(const void* kernel, int threads, size_t smem, int* per_sm);
 
 // ----------------------------------------------------------------------------- matvec batch
 
-constexpr int kThreads = 256;      // 8 warps per CTA
+constexpr int kConsumerWarps = 16;                      // decode warps per CTA (4 per SM sub-partition)
+constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kMaxTasks = QMV_MAX_BATCH;
+constexpr int kMaxCtas = 256;                           // persistent grid: at most one CTA per SM
 
-// One matvec of a persistent launch. Tiles of gemv_rows_per_tile(M) rows are
-// numbered across tasks: task i owns tiles [tile0, tile0 + ceil(N / rows)).
+// One matvec of a persistent launch. Tiles of rows_per_tile rows are numbered
+// across tasks: task i owns tiles [tile0, tile0 + ceil(N / rows_per_tile)).
 struct GemvTask {
   const uint32_t* codes;   // section 0
   const uint16_t* scales;  // section 1 (fp16 bits)
@@ -50,14 +52,23 @@ struct GemvBatch {
   int32_t n_tasks;
   int32_t n_tiles;
   int32_t kc;              // activation chunk staged in shared memory (elements)
-  int32_t pad;
+  int32_t rows_per_tile;
+  int32_t n_ctas;
+  int32_t pad0;
+  // CTA c processes the contiguous tile range [cta_tile[c], cta_tile[c+1]),
+  // cut so every CTA streams about the same number of bytes
+  int32_t cta_tile[kMaxCtas + 1];
+  // decode constants, passed at run time so they live in registers: {mask,
+  // base} make each decode a single three-input logic op, and the shift
+  // multipliers/amounts pin each shift to the integer-multiply or the
+  // shift unit (see gemv.cu)
+  uint32_t magic[10];
+  int* err;                // device error word (timeouts of bounded waits)
   GemvTask t[kMaxTasks];
 };
 
-// Rows per tile of the persistent matvec kernel for M activation rows.
-int gemv_rows_per_tile(int M);
-// Launch the persistent matvec kernel for `format` (QMV_TERNARY2 / QMV_INT4);
-// sets b.kc. M in 1..8.
-int launch_gemv(int format, GemvBatch& b, int M, int max_K, cudaStream_t s);
+// Launch the persistent matvec kernel for `format` (QMV_TERNARY2 / QMV_INT4)
+// over b.t[0 .. b.n_tasks); fills the tiling fields of b. M in 1..8.
+int launch_gemv(int format, GemvBatch& b, int M, cudaStream_t s);
 
 }  // namespace qmv

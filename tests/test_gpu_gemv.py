@@ -208,10 +208,13 @@ def test_int4_gqa_layer_set_sampled(env, M):
         rows = np.unique(np.concatenate(([0, N - 1], rng.choice(N, 24, replace=False))))
         wr = w[torch.from_numpy(rows).to(dev)].cpu().numpy()
         qq, _, s16 = int4.quantize(wr)
-        # packed codes of the sampled rows are the oracle's codes
-        codes = p[: d.bytes[0]].view(torch.int32).view(N, K // 8)[torch.from_numpy(rows).to(dev)].cpu().numpy()
-        ref_codes = np.frombuffer(int4.pack(qq, s16), "<u4", count=len(rows) * K // 8).reshape(len(rows), K // 8)
-        assert np.array_equal(codes.view(np.uint32), ref_codes), name
+        # decoded codes and scales of the sampled rows are the oracle's
+        qd = torch.empty((N, K), dtype=torch.int8, device=dev)
+        sd = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+        q.qmv_unpack(d, p, qd, sd)
+        idx = torch.from_numpy(rows).to(dev)
+        assert np.array_equal(qd[idx].cpu().numpy(), qq), name
+        assert np.array_equal(sd[idx].cpu().numpy().view(np.uint16), s16), name
         xb = xs[K].view(torch.int16).cpu().numpy().view(np.uint16)
         yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
         _check_bound(y[:, torch.from_numpy(rows).to(dev)].cpu().numpy(), yr, B, f"{name} M={M}")

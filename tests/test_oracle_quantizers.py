@@ -137,6 +137,21 @@ def test_ternary_pack_layout_hand_word():
     assert word == (0b01 << 0) | (0b10 << 16) | (0b10 << 2) | (0b01 << 30)
 
 
+def test_ternary_record_layout_hand_position():
+    # N=20 rows (2 row groups, the second padded), K=1280 (10 blocks: steps of 8 and 2).
+    # q = +1 at row 17, column 1100: group 1, row 1 of the group; block 8 -> step 1 (nbk = 2),
+    # block 0 of the step; column 76 of the block -> word 4, bit 12 (even column).
+    # byte offset = 1*16*(1280/4) + 16*8*32 + 1*2*32 + 0*32 + 4*4 = 5120 + 4096 + 64 + 16 = 9296
+    q = np.zeros((20, 1280), np.int8)
+    q[17, 1100] = 1
+    buf = ternary.pack(q, np.zeros((20, 10), np.uint16))
+    words = np.frombuffer(buf, "<u4", count=32 * 1280 // 16)
+    assert np.flatnonzero(words).tolist() == [9296 // 4]
+    assert words[9296 // 4] == 1 << 12
+    # the padded rows 20..31 are all-zero codes
+    assert len(buf) >= 32 * 1280 // 4
+
+
 def test_ternary_pack_roundtrip_and_size():
     g = synth.rng(3)
     q = g.integers(-1, 2, (5, 384)).astype(np.int8)
@@ -149,9 +164,9 @@ def test_ternary_pack_roundtrip_and_size():
     iq = bpw["iq2_xxs"]
     assert iq["data_bits"] + iq["scale_bits"] / iq["block"] == iq["bits_per_weight"]
     t = bpw["this_library"]["ternary_block128_fp16"]
-    assert sum(layout.ternary_sizes(5, 384)) * 8 / (5 * 384) == t["bits_per_weight"]
+    assert sum(layout.ternary_sizes(32, 384)) * 8 / (32 * 384) == t["bits_per_weight"]
     t = bpw["this_library"]["int4_group128_fp16"]
-    assert sum(layout.int4_sizes(5, 384)) * 8 / (5 * 384) == t["bits_per_weight"]
+    assert sum(layout.int4_sizes(32, 384)) * 8 / (32 * 384) == t["bits_per_weight"]
 
 
 def test_ternary_unpack_rejects_code_11():
