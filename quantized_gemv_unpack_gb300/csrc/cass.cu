@@ -1,20 +1,439 @@
-// Cassandra lossless bf16 split: host packer and GPU draft/target kernels.
+// Cassandra lossless bf16 split ("Cassandra", sections 3.1-3.3): the host-side
+// offline transform and the GPU draft / target paths.
+//
+// Offline (host): Wanda value pruning keeps the K/2 largest |w| * ||X[:,j]||_2
+// of every row (bitmap), kept values keep sign + 3 high mantissa bits in the
+// speculation data and 4 low mantissa bits in the verification data, their
+// exponents are ranked by frequency over the whole tensor and written as unary
+// codes (rank r = r zeros then a one), pruned values go to the verification
+// data as raw bf16.
+//
+// GPU: one warp per row, rows strided over a persistent grid. Phase A decodes
+// the row's unary exponent stream: each lane takes one 32-bit word, counts the
+// codewords ending in it (__popc), an inclusive warp scan turns the counts into
+// codeword indices, and an exclusive warp max-scan of each word's last one bit
+// (carried across 32-word chunks) gives every codeword's start, so a lane can
+// turn each set bit into a rank = zeros since the previous one and look the
+// exponent up in the codebook. Exponents land in shared memory in kept-value
+// order. Phase B walks the bitmap 32 columns at a time: lane l owns column
+// 32*i + l, its kept index is the number of kept columns before it
+// (__popc(word & lanemask_lt) plus the running count), its pruned index is
+// column - kept index. The draft value is S<<15 | E<<7 | m_hi<<4 (pruned: +0),
+// the target value adds m_lo (pruned: the raw verification bits); either is
+// widened to fp32 (exact) and multiplied into fp32 accumulators per activation
+// row. Every loop is bounded by the row's sizes; inconsistent streams set
+// QMV_ERR_CORRUPT in the device error word.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
 #include "qmv_internal.cuh"
+
+namespace qmv {
+namespace {
+
+constexpr int kCassWarpsMax = 16;
+
+struct CassArgs {
+  const uint32_t* bitmap;    // [N][K/32]
+  const uint32_t* signmant;  // [N][K/16]
+  const uint32_t* stream;    // unary words
+  const uint32_t* rowstart;  // [N+1]
+  const uint8_t* codebook;   // [256]
+  const uint16_t* pruned;    // [N][K/2]
+  const uint32_t* mlo;       // [N][K/16]
+  const uint16_t* x;         // bf16 [M][ldx]
+  float* y;                  // [M][ldy] or null
+  uint16_t* w_out;           // [N][K] or null
+  int64_t stream_words;
+  int N, K, ldx, ldy, n_symbols;
+  int* err;
+};
+
+__device__ __forceinline__ void flag(int* err) { atomicCAS(err, 0, (int)QMV_ERR_CORRUPT); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+template <int MT, bool TARGET>
+__global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int K = a.K;
+  const int K2 = K / 2;
+  const int nwarps = blockDim.x / 32;
+  float* xs = reinterpret_cast<float*>(smem);                       // [MT][K] fp32
+  uint8_t* cb = smem + (size_t)MT * K * 4;                           // [256]
+  // per-warp buffers: bitmap[K/32] words, signmant[K/16] words, (target: mlo[K/16] words,
+  // pruned[K/2] halves), exps[K/2] bytes
+  const size_t per_warp = ((size_t)K2 + (size_t)K / 8 + (size_t)K / 4 + (TARGET ? (size_t)K / 4 + (size_t)K : 0) + 15) / 16 * 16;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  unsigned char* wb = smem + (size_t)MT * K * 4 + 256 + (size_t)warp * per_warp;
+  uint32_t* bm_s = reinterpret_cast<uint32_t*>(wb);
+  uint32_t* sm_s = bm_s + K / 32;
+  uint32_t* lo_s = sm_s + K / 16;
+  uint16_t* pr_s = reinterpret_cast<uint16_t*>(lo_s + (TARGET ? K / 16 : 0));
+  uint8_t* exps = reinterpret_cast<uint8_t*>(pr_s + (TARGET ? K2 : 0));
+
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) cb[i] = a.codebook[i];
+  for (int m = 0; m < MT; ++m)
+    for (int j = threadIdx.x; j < K; j += blockDim.x)
+      xs[(size_t)m * K + j] = __uint_as_float((uint32_t)a.x[(size_t)m * a.ldx + j] << 16);
+  __syncthreads();
+
+  const uint32_t below = lanemask_lt();
+  const int gw = blockIdx.x * nwarps + warp;
+  const int stride = gridDim.x * nwarps;
+  for (int n = gw; n < a.N; n += stride) {
+    // ---- stage the row's fixed-size sections (all loads in flight together);
+    // rows are 16-byte aligned in global memory when K is a multiple of 128
+    if (K % 128 == 0) {
+      const uint4* bm = reinterpret_cast<const uint4*>(a.bitmap + (size_t)n * (K / 32));
+      const uint4* sm = reinterpret_cast<const uint4*>(a.signmant + (size_t)n * (K / 16));
+      for (int i = lane; i < K / 128; i += 32) reinterpret_cast<uint4*>(bm_s)[i] = __ldg(bm + i);
+      for (int i = lane; i < K / 64; i += 32) reinterpret_cast<uint4*>(sm_s)[i] = __ldg(sm + i);
+      if (TARGET) {
+        const uint4* lo = reinterpret_cast<const uint4*>(a.mlo + (size_t)n * (K / 16));
+        const uint4* pr = reinterpret_cast<const uint4*>(a.pruned + (size_t)n * K2);
+        for (int i = lane; i < K / 64; i += 32) reinterpret_cast<uint4*>(lo_s)[i] = __ldg(lo + i);
+        for (int i = lane; i < K / 16; i += 32) reinterpret_cast<uint4*>(pr_s)[i] = __ldg(pr + i);
+      }
+    } else {
+      const uint32_t* bm = a.bitmap + (size_t)n * (K / 32);
+      const uint32_t* sm = a.signmant + (size_t)n * (K / 16);
+      for (int i = lane; i < K / 32; i += 32) bm_s[i] = __ldg(bm + i);
+      for (int i = lane; i < K / 16; i += 32) sm_s[i] = __ldg(sm + i);
+      if (TARGET) {
+        const uint32_t* lo = a.mlo + (size_t)n * (K / 16);
+        const uint16_t* pr = a.pruned + (size_t)n * K2;
+        for (int i = lane; i < K / 16; i += 32) lo_s[i] = __ldg(lo + i);
+        for (int i = lane; i < K2; i += 32) pr_s[i] = __ldg(pr + i);
+      }
+    }
+
+    // ---- phase A: unary exponent codes -> exps[kept index]
+    uint32_t s0 = __ldg(a.rowstart + n), s1 = __ldg(a.rowstart + n + 1);
+    if (s1 < s0 || (int64_t)s1 > a.stream_words) {
+      if (lane == 0) flag(a.err);
+      s1 = s0;
+    }
+    const int nwords = (int)(s1 - s0);
+    int count = 0;       // codewords so far (warp-uniform)
+    int carry = -1;      // row-relative bit position of the last one so far
+    for (int c = 0; c < nwords; c += 32) {
+      const int wi = c + lane;
+      const uint32_t w = wi < nwords ? __ldg(a.stream + s0 + wi) : 0u;
+      const int cnt = __popc(w);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int lastpos = w ? wi * 32 + 31 - __clz(w) : -1;
+      int mx = lastpos;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, mx, o);
+        if (lane >= o) mx = max(mx, t);
+      }
+      int prev = __shfl_up_sync(0xffffffffu, mx, 1);
+      prev = lane == 0 ? carry : max(prev, carry);
+      int k = count + incl - cnt;
+      uint32_t bits = w;
+      bool bad = false;
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int pos = wi * 32 + b;
+        const int rank = pos - prev - 1;
+        prev = pos;
+        uint8_t e = 0;
+        if (rank < a.n_symbols) e = cb[rank]; else bad = true;
+        if (k < K2) exps[k] = e; else bad = true;
+        ++k;
+      }
+      if (bad) flag(a.err);
+      count += __shfl_sync(0xffffffffu, incl, 31);
+      carry = max(carry, __shfl_sync(0xffffffffu, mx, 31));
+    }
+    if (count != K2 && lane == 0) flag(a.err);
+    __syncwarp();
+
+    // ---- phase B: rebuild each column's bf16 value and accumulate w * x,
+    // four bitmap words per iteration (their kept counts prefix-summed first)
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    int kbase = 0;
+    uint16_t* wrow = a.w_out ? a.w_out + (size_t)n * K : nullptr;
+    auto column = [&](uint32_t word, int it, int kb) {
+      const int j = it * 32 + lane;
+      const bool kept = (word >> lane) & 1u;
+      const int kidx = kb + __popc(word & below);
+      uint32_t v = 0;
+      if (kept) {
+        if (kidx < K2) {
+          const uint32_t nib = (sm_s[kidx >> 3] >> ((kidx & 7) * 4)) & 0xFu;
+          v = ((nib >> 3) << 15) | ((uint32_t)exps[kidx] << 7) | ((nib & 7u) << 4);
+          if (TARGET) v |= (lo_s[kidx >> 3] >> ((kidx & 7) * 4)) & 0xFu;
+        }
+      } else if (TARGET) {
+        const int pidx = j - kidx;
+        if (pidx < K2) v = pr_s[pidx];
+      }
+      if (wrow) wrow[j] = (uint16_t)v;
+      const float wf = __uint_as_float(v << 16);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[m] = fmaf(wf, xs[(size_t)m * K + j], acc[m]);
+    };
+    int it = 0;
+    for (; it + 4 <= K / 32; it += 4) {
+      const uint4 w4 = reinterpret_cast<const uint4*>(bm_s)[it >> 2];
+      const int k1 = kbase + __popc(w4.x), k2 = k1 + __popc(w4.y), k3 = k2 + __popc(w4.z);
+      column(w4.x, it, kbase);
+      column(w4.y, it + 1, k1);
+      column(w4.z, it + 2, k2);
+      column(w4.w, it + 3, k3);
+      kbase = k3 + __popc(w4.w);
+    }
+    for (; it < K / 32; ++it) {
+      const uint32_t word = bm_s[it];
+      column(word, it, kbase);
+      kbase += __popc(word);
+    }
+    if (kbase != K2 && lane == 0) flag(a.err);
+    if (a.y) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float v = acc[m];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) a.y[(size_t)m * a.ldy + n] = v;
+      }
+    }
+    __syncwarp();  // the staged row buffers are reused by the next row
+  }
+}
+
+template <bool TARGET>
+int launch_cass(const CassArgs& a, int M, cudaStream_t s) {
+  const size_t K = a.K;
+  const size_t per_warp = (K / 2 + K / 8 + K / 4 + (TARGET ? K / 4 + K : 0) + 15) / 16 * 16;
+  const size_t fixed = (size_t)M * K * 4 + 256;
+  const size_t cap = 227 * 1024 - 1024;
+  if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%zu with M=%d does not fit shared memory", K, M);
+  const int warps = (int)std::min<size_t>(kCassWarpsMax, (cap - fixed) / per_warp);
+  const size_t smem = fixed + per_warp * warps;
+  const void* kern = nullptr;
+  switch (M) {
+#define QMV_CASS_CASE(m) \
+  case m: kern = (const void*)cass_kernel<m, TARGET>; break;
+    QMV_CASS_CASE(1) QMV_CASS_CASE(2) QMV_CASS_CASE(3) QMV_CASS_CASE(4)
+    QMV_CASS_CASE(5) QMV_CASS_CASE(6) QMV_CASS_CASE(7) QMV_CASS_CASE(8)
+#undef QMV_CASS_CASE
+    default: return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
+  }
+  int per_sm = 0;
+  int rc = kernel_fit(kern, warps * 32, smem, &per_sm);
+  if (rc) return rc;
+  const int grid = std::max(1, std::min(sm_count() * per_sm, (a.N + warps - 1) / warps));
+  void* args[] = {const_cast<CassArgs*>(&a)};
+  cudaError_t e = cudaLaunchKernel(kern, grid, warps * 32, args, smem, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cassandra launch");
+  return QMV_OK;
+}
+
+int check_cass_desc(const qmv_desc* d) {
+  if (!d) return fail(QMV_ERR_ARG, "desc is NULL");
+  if (d->abi_version != QMV_ABI_VERSION || d->format != QMV_CASS) return fail(QMV_ERR_ARG, "not a Cassandra descriptor");
+  if (d->N <= 0 || d->K <= 0 || d->K % 32) return fail(QMV_ERR_ARG, "N=%lld K=%lld (K must be a multiple of 32)", (long long)d->N, (long long)d->K);
+  if (d->N > INT32_MAX / 2 || d->K > (1 << 20)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
+  const int64_t N = d->N, K = d->K;
+  const int64_t want[7] = {N * K / 8, N * K / 4, -1, (N + 1) * 4, 256, N * K, N * K / 4};
+  for (int i = 0; i < 7; ++i) {
+    if (want[i] >= 0 && d->bytes[i] != want[i]) return fail(QMV_ERR_ARG, "Cassandra section %d has %lld bytes, expected %lld", i, (long long)d->bytes[i], (long long)want[i]);
+    if (d->off[i] % 256 || d->off[i] + d->bytes[i] > d->total_bytes) return fail(QMV_ERR_ARG, "Cassandra section %d outside the buffer", i);
+  }
+  if (d->bytes[2] % 16) return fail(QMV_ERR_ARG, "exponent stream size must be a multiple of 16 bytes");
+  if (d->n_symbols < 1 || d->n_symbols > 256) return fail(QMV_ERR_ARG, "n_symbols=%d", d->n_symbols);
+  return QMV_OK;
+}
+
+int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, int M, int64_t ldx, float* y,
+             int64_t ldy, uint16_t* w_out, void* stream) {
+  int rc = check_cass_desc(d);
+  if (rc) return rc;
+  if (M < 1 || M > 8) return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
+  if (!packed || !x) return fail(QMV_ERR_ARG, "NULL packed or x");
+  if (!aligned16(packed) || !aligned16(x) || (y && !aligned16(y)) || (w_out && !aligned16(w_out)))
+    return fail(QMV_ERR_ALIGN, "buffers must be 16-byte aligned");
+  if (ldx < d->K || (y && ldy < d->N)) return fail(QMV_ERR_ARG, "ldx < K or ldy < N");
+  if (ldx > INT32_MAX || ldy > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "leading dimension too large");
+  int* err = device_error_word();
+  if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+  const char* b = static_cast<const char*>(packed);
+  CassArgs a;
+  a.bitmap = reinterpret_cast<const uint32_t*>(b + d->off[0]);
+  a.signmant = reinterpret_cast<const uint32_t*>(b + d->off[1]);
+  a.stream = reinterpret_cast<const uint32_t*>(b + d->off[2]);
+  a.rowstart = reinterpret_cast<const uint32_t*>(b + d->off[3]);
+  a.codebook = reinterpret_cast<const uint8_t*>(b + d->off[4]);
+  a.pruned = reinterpret_cast<const uint16_t*>(b + d->off[5]);
+  a.mlo = reinterpret_cast<const uint32_t*>(b + d->off[6]);
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = y;
+  a.w_out = w_out;
+  a.stream_words = d->bytes[2] / 4;
+  a.N = (int)d->N;
+  a.K = (int)d->K;
+  a.ldx = (int)ldx;
+  a.ldy = (int)(y ? ldy : 0);
+  a.n_symbols = d->n_symbols;
+  a.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return target ? launch_cass<true>(a, M, s) : launch_cass<false>(a, M, s);
+}
+
+// ----------------------------------------------------------------------------- host packer
+
+int64_t align256(int64_t n) { return (n + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace qmv
 
 using namespace qmv;
 
 extern "C" {
 
-int cass_pack_host(const uint16_t*, int64_t, int64_t, const uint16_t*, int64_t, qmv_desc*, void*, int64_t) {
-  return fail(QMV_ERR_UNSUPPORTED, "cass_pack_host: not built yet");
+int cass_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X, int64_t R, qmv_desc* desc, void* out,
+                   int64_t out_capacity) {
+  if (!w || !X || !desc) return fail(QMV_ERR_ARG, "NULL w, calibration or desc");
+  if (N <= 0 || K <= 0 || K % 32 || R <= 0) return fail(QMV_ERR_ARG, "N=%lld K=%lld R=%lld (K must be a positive multiple of 32)", (long long)N, (long long)K, (long long)R);
+  if (N > INT32_MAX / 2 || K > (1 << 20)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
+  const int64_t K2 = K / 2;
+  auto value = [](uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+  };
+  // 1. calibration column norms, rows summed in order
+  std::vector<double> c(K, 0.0);
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t j = 0; j < K; ++j) {
+      const double v = value(X[r * K + j]);
+      c[j] += v * v;
+    }
+  for (int64_t j = 0; j < K; ++j) c[j] = std::sqrt(c[j]);
+
+  // 2. Wanda selection per row + 3. split of the kept values
+  std::vector<uint8_t> keep((size_t)(N * K), 0);
+  std::vector<uint8_t> ek((size_t)(N * K2));
+  std::vector<int64_t> hist(256, 0);
+  std::vector<double> score(K);
+  std::vector<int32_t> idx(K);
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = w + n * K;
+    for (int64_t j = 0; j < K; ++j) {
+      const double s = std::fabs(value(row[j])) * c[j];
+      score[j] = std::isnan(s) ? HUGE_VAL : s;
+      idx[j] = (int32_t)j;
+    }
+    auto before = [&](int32_t a2, int32_t b2) { return score[a2] > score[b2] || (score[a2] == score[b2] && a2 < b2); };
+    std::nth_element(idx.begin(), idx.begin() + K2, idx.end(), before);
+    for (int64_t i = 0; i < K2; ++i) keep[n * K + idx[i]] = 1;
+    int64_t k = 0;
+    for (int64_t j = 0; j < K; ++j)
+      if (keep[n * K + j]) {
+        const uint8_t e = (uint8_t)((row[j] >> 7) & 0xFF);
+        ek[n * K2 + k++] = e;
+        ++hist[e];
+      }
+  }
+  // 4. exponent ranks: count descending, equal counts smaller exponent first
+  std::vector<int> order;
+  for (int e = 0; e < 256; ++e)
+    if (hist[e]) order.push_back(e);
+  std::stable_sort(order.begin(), order.end(), [&](int a2, int b2) { return hist[a2] > hist[b2]; });
+  std::vector<int> rank_of(256, -1);
+  for (size_t r = 0; r < order.size(); ++r) rank_of[order[r]] = (int)r;
+  // 5. unary stream length: sum (rank + 1) bits per row, rows padded to 4 words
+  std::vector<uint32_t> rowstart((size_t)N + 1, 0);
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t bits = 0;
+    for (int64_t k = 0; k < K2; ++k) bits += rank_of[ek[n * K2 + k]] + 1;
+    const int64_t words = ((bits + 31) / 32 + 3) / 4 * 4;
+    if ((int64_t)rowstart[n] + words > (int64_t)UINT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "exponent stream too long");
+    rowstart[n + 1] = rowstart[n] + (uint32_t)words;
+  }
+  // layout
+  const int64_t sizes[7] = {N * K / 8, N * K / 4, (int64_t)rowstart[N] * 4, (N + 1) * 4, 256, N * K, N * K / 4};
+  memset(desc, 0, sizeof(*desc));
+  desc->abi_version = QMV_ABI_VERSION;
+  desc->format = QMV_CASS;
+  desc->N = N;
+  desc->K = K;
+  desc->group = 0;
+  desc->n_symbols = (int32_t)order.size();
+  int64_t pos = 0;
+  for (int i = 0; i < 7; ++i) {
+    desc->off[i] = pos;
+    desc->bytes[i] = sizes[i];
+    pos = align256(pos + sizes[i]);
+  }
+  desc->total_bytes = pos;
+  if (!out) return QMV_OK;
+  if (out_capacity < desc->total_bytes) return fail(QMV_ERR_ARG, "out_capacity %lld < %lld", (long long)out_capacity, (long long)desc->total_bytes);
+
+  unsigned char* o = static_cast<unsigned char*>(out);
+  memset(o, 0, (size_t)desc->total_bytes);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(o + desc->off[0]);
+  uint32_t* signmant = reinterpret_cast<uint32_t*>(o + desc->off[1]);
+  uint32_t* stream = reinterpret_cast<uint32_t*>(o + desc->off[2]);
+  uint32_t* rs = reinterpret_cast<uint32_t*>(o + desc->off[3]);
+  uint8_t* codebook = o + desc->off[4];
+  uint16_t* pruned = reinterpret_cast<uint16_t*>(o + desc->off[5]);
+  uint32_t* mlo = reinterpret_cast<uint32_t*>(o + desc->off[6]);
+  for (size_t r = 0; r < order.size(); ++r) codebook[r] = (uint8_t)order[r];
+  memcpy(rs, rowstart.data(), (size_t)(N + 1) * 4);
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = w + n * K;
+    int64_t k = 0, p = 0;
+    uint64_t bit = (uint64_t)rowstart[n] * 32;
+    for (int64_t j = 0; j < K; ++j) {
+      const uint16_t v = row[j];
+      if (keep[n * K + j]) {
+        bitmap[n * (K / 32) + j / 32] |= 1u << (j % 32);
+        const uint32_t S = v >> 15, M = v & 0x7F;
+        const int64_t ki = n * K2 + k;
+        signmant[ki / 8] |= ((S << 3) | (M >> 4)) << ((ki % 8) * 4);
+        mlo[ki / 8] |= (M & 0xF) << ((ki % 8) * 4);
+        bit += (uint64_t)rank_of[(v >> 7) & 0xFF];            // rank zeros ...
+        stream[bit / 32] |= 1u << (bit % 32);                  // ... then a one
+        ++bit;
+        ++k;
+      } else {
+        pruned[n * K2 + p++] = v;
+      }
+    }
+  }
+  return QMV_OK;
 }
 
-int cass_decode_draft(const qmv_desc*, const void*, const void*, int, int64_t, float*, int64_t, uint16_t*, void*) {
-  return fail(QMV_ERR_UNSUPPORTED, "cass_decode_draft: not built yet");
+int cass_decode_draft(const qmv_desc* desc, const void* packed, const void* x_bf16, int M, int64_t ldx, float* y,
+                      int64_t ldy, uint16_t* w_draft, void* stream) {
+  return run_cass(false, desc, packed, x_bf16, M, ldx, y, ldy, w_draft, stream);
 }
 
-int cass_reconstruct(const qmv_desc*, const void*, const void*, int, int64_t, float*, int64_t, uint16_t*, void*) {
-  return fail(QMV_ERR_UNSUPPORTED, "cass_reconstruct: not built yet");
+int cass_reconstruct(const qmv_desc* desc, const void* packed, const void* x_bf16, int M, int64_t ldx, float* y,
+                     int64_t ldy, uint16_t* w_out, void* stream) {
+  return run_cass(true, desc, packed, x_bf16, M, ldx, y, ldy, w_out, stream);
 }
 
 }  // extern "C"

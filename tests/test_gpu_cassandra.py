@@ -1,0 +1,159 @@
+"""GPU parity of the Cassandra draft and target paths (through the C ABI).
+
+Materialised draft weights must equal the oracle's bit for bit, reconstructed
+weights must equal the original bf16 bits (the lossless invariant), and the
+fused matvecs must satisfy |y - y_ref| <= 2e-3 * sum_k |w_k x_k|.
+"""
+import numpy as np
+import pytest
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+RTOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_gemv_unpack_gb300 as q
+    assert torch.cuda.is_available()
+    return q, torch, torch.device("cuda:0")
+
+
+def _dev(torch, a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _bf16(torch, bits, dev):
+    return _dev(torch, bits.view(np.int16), dev).view(torch.bfloat16)
+
+
+def _u16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def _run(q, torch, dev, W, X, M, seed):
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = W.shape
+    d, buf = q.cass_pack_host(W, X)
+    packed = _dev(torch, buf, dev)
+    xb = synth.activations_bf16(synth.rng(seed), (M, K))
+    x = _bf16(torch, xb, dev)
+    yd = torch.full((M, N), float("nan"), device=dev)
+    yt = torch.full((M, N), float("nan"), device=dev)
+    wd = torch.empty((N, K), dtype=torch.int16, device=dev)
+    wt = torch.empty((N, K), dtype=torch.int16, device=dev)
+    q.cass_decode_draft(d, packed, x, yd, wd)
+    q.cass_reconstruct(d, packed, x, yt, wt)
+    assert q.qmv_check_status() == 0
+    return d, packed, xb, yd.cpu().numpy(), yt.cpu().numpy(), _u16(wd), _u16(wt)
+
+
+@pytest.mark.parametrize("N,K,M", [(1, 32, 1), (24, 256, 1), (40, 512, 5), (33, 1024, 3), (7, 160, 2), (19, 96, 4), (130, 4096, 8)])
+def test_draft_and_target_match_oracle(env, N, K, M):
+    q, torch, dev = env
+    from oracle import cassandra as cs
+    from oracle.matvec import matvec_bf16x
+    from oracle.numerics import bf16_bits_to_f64
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(N * 7 + K)
+    W = synth.to_bf16_bits(synth.student_t4(g, (N, K)))
+    X, _ = synth.calibration_bf16(g, 128, K)
+    d, packed, xb, yd, yt, wd, wt = _run(q, torch, dev, W, X, M, N + M)
+    ref, meta = cs.pack(W, X)
+    assert np.array_equal(wd, cs.draft(ref, meta))
+    assert np.array_equal(wt, W)
+    for y, wbits in [(yd, cs.draft(ref, meta)), (yt, W)]:
+        yr, B = matvec_bf16x(bf16_bits_to_f64(wbits), xb)
+        assert np.all(np.abs(y - yr) <= RTOL * B)
+
+
+def test_special_values_roundtrip(env):
+    """All 65,536 bf16 patterns come back bit-exactly through the target path."""
+    q, torch, dev = env
+    from oracle import cassandra as cs
+    from quantized_gemv_unpack_gb300 import synth
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    W = allp.reshape(2048, 32)
+    X = synth.to_bf16_bits(np.ones((2, 32), np.float32))
+    d, buf = q.cass_pack_host(W, X)
+    packed = _dev(torch, buf, dev)
+    x = _bf16(torch, synth.activations_bf16(synth.rng(1), (1, 32)), dev)
+    wt = torch.empty((2048, 32), dtype=torch.int16, device=dev)
+    wd = torch.empty((2048, 32), dtype=torch.int16, device=dev)
+    q.cass_reconstruct(d, packed, x, None, wt)
+    q.cass_decode_draft(d, packed, x, None, wd)
+    assert q.qmv_check_status() == 0
+    assert np.array_equal(_u16(wt), W)
+    ref, meta = cs.pack(W, X)
+    assert np.array_equal(_u16(wd), cs.draft(ref, meta))
+
+
+def test_mlp_matrix_full_size_sampled(env):
+    """The 14336 x 4096 MLP matrix with 128 calibration rows (1% outlier channels x20): draft at M=1,
+    target at M=5; reconstruction checked on every weight, draft weights and outputs on sampled rows."""
+    q, torch, dev = env
+    from oracle import cassandra as cs
+    from oracle.matvec import matvec_bf16x
+    from oracle.numerics import bf16_bits_to_f64
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(2)
+    N, K = 14336, 4096
+    W = synth.to_bf16_bits(synth.student_t4(g, (N, K)))
+    X, chans = synth.calibration_bf16(g, 128, K)
+    d, buf = q.cass_pack_host(W, X)
+    packed = _dev(torch, buf, dev)
+    x1 = synth.activations_bf16(g, (1, K))
+    x5 = synth.activations_bf16(g, (5, K))
+    yd = torch.empty((1, N), device=dev)
+    yt = torch.empty((5, N), device=dev)
+    wd = torch.empty((N, K), dtype=torch.int16, device=dev)
+    wt = torch.empty((N, K), dtype=torch.int16, device=dev)
+    q.cass_decode_draft(d, packed, _bf16(torch, x1, dev), yd, wd)
+    q.cass_reconstruct(d, packed, _bf16(torch, x5, dev), yt, wt)
+    assert q.qmv_check_status() == 0
+    assert np.array_equal(_u16(wt), W)                          # lossless, every bit
+    rows = np.unique(np.concatenate(([0, N - 1], np.random.default_rng(0).choice(N, 40, replace=False))))
+    keep = cs.wanda_keep(W[rows], cs.column_norms(X))
+    draft_ref = np.where(keep, W[rows] & np.uint16(0xFFF0), np.uint16(0))
+    assert np.array_equal(_u16(wd)[rows], draft_ref)
+    yr, B = matvec_bf16x(bf16_bits_to_f64(draft_ref), x1)
+    assert np.all(np.abs(yd.cpu().numpy()[:, rows] - yr) <= RTOL * B)
+    yr, B = matvec_bf16x(bf16_bits_to_f64(W[rows]), x5)
+    assert np.all(np.abs(yt.cpu().numpy()[:, rows] - yr) <= RTOL * B)
+    # the speculation data is what the draft reads: far smaller than the dense bf16 matrix
+    spec = sum(d.bytes[i] for i in range(5))
+    assert spec < 0.35 * N * K * 2
+
+
+def test_corrupt_streams_are_reported(env):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(9)
+    W = synth.to_bf16_bits(synth.student_t4(g, (16, 256)))
+    X, _ = synth.calibration_bf16(g, 8, 256)
+    d, buf = q.cass_pack_host(W, X)
+    x = _bf16(torch, synth.activations_bf16(g, (1, 256)), dev)
+    y = torch.empty((1, 16), device=dev)
+    # no codeword ends in the exponent stream
+    bad = buf.copy()
+    bad[d.off[2]:d.off[2] + d.bytes[2]] = 0
+    q.cass_decode_draft(d, _dev(torch, bad, dev), x, y)
+    assert q.qmv_check_status() == q.QMV_ERR_CORRUPT
+    # a bitmap row keeping every column
+    bad = buf.copy()
+    bad[d.off[0]:d.off[0] + 32] = 0xFF
+    q.cass_reconstruct(d, _dev(torch, bad, dev), x, y)
+    assert q.qmv_check_status() == q.QMV_ERR_CORRUPT
+    # a unary rank past the codebook: a long run of zeros before the first one
+    bad = buf.copy()
+    bad[d.off[2]:d.off[2] + 64] = 0
+    bad[d.off[2] + 64] = 1
+    q.cass_decode_draft(d, _dev(torch, bad, dev), x, y)
+    assert q.qmv_check_status() == q.QMV_ERR_CORRUPT
+    # the untouched buffer is clean
+    q.cass_decode_draft(d, _dev(torch, buf, dev), x, y)
+    assert q.qmv_check_status() == 0
