@@ -1,17 +1,25 @@
 """Benchmark: batch-1 dequantize-and-matvec weight stream on GB300.
 
-Default workload: the 27B-shaped ternary decode stack - 60 layers of a GQA
-transformer (hidden 5120, 40 query / 8 KV heads of dim 128, SwiGLU
-intermediate 25600), every linear map in block-128 absmean ternary with fp16
-scales (7.27 GB packed), one bf16 activation vector per layer (one of width
-5120 for q/k/v/o/gate/up and one of width 25600 for down). A step is one
-batch-1 pass over all 420 matvecs, issued as one persistent launch.
+Default workload (the line the metric is quoted on): the 27B-shaped ternary
+decode stack - 60 layers of a GQA transformer (hidden 5120, 40 query / 8 KV
+heads of dim 128, SwiGLU intermediate 25600), every linear map in block-128
+absmean ternary with fp16 scales (7.27 GB packed), one bf16 activation vector
+per layer (one of width 5120 for q/k/v/o/gate/up and one of width 25600 for
+down). A step is one batch-1 pass over all 420 matvecs, issued as one
+persistent launch.
+
+Other workloads (--workload) measure the remaining hot-path rows in the same
+format: the 4096 x 4096 ternary matrix, the INT4 GQA layer set (M = 1 or 4),
+the Cassandra draft (M = 1) and target (M = 5) paths on the 14336 x 4096 MLP
+matrix, and the 128-expert ternary MoE (M = 1, 2, 4, 8). Workloads smaller
+than L2 rotate over enough copies of the packed weights that every step
+streams from HBM.
 
 Printed: one JSON line with the achieved HBM GB/s on the algorithmic bytes
-(packed codes + scales + activations + outputs), the equivalent decode
-tokens/s, the roofline of the dominant kernel against the measured copy
-bandwidth, an end-to-end figure through host buffers, and the float64 CPU
-oracle timed on a bounded sample as the CPU baseline.
+(packed weight bytes + activations + outputs), the roofline of the dominant
+kernel against the measured copy bandwidth, an end-to-end figure through host
+buffers, clocks sampled during the timed region, and (default workload) the
+float64 CPU oracle timed on a bounded sample as the CPU baseline.
 
 --impl reference times that oracle alone on the host cores (the reference arm).
 """
@@ -32,15 +40,8 @@ METRIC = "batch-1 dequant-GEMV achieved HBM GB/s (% of GB300 peak); equiv. decod
 UNIT = "GB/s"
 HIDDEN, NQ, NKV, HD, INTER, LAYERS = 5120, 40, 8, 128, 25600, 60
 FALLBACK_HBM_GBS = 6800.0
-
-
-def workload_config():
-    return {"workload": "27B-shaped ternary decode stack: 60 layers x {q,k,v,o,gate,up,down}, hidden 5120, "
-                        "40/8 heads x 128, SwiGLU 25600, block-128 absmean ternary + fp16 scales, batch 1",
-            "layers": LAYERS, "hidden": HIDDEN, "heads": [NQ, NKV, HD], "intermediate": INTER,
-            "batch": 1, "matvecs_per_step": 7 * LAYERS,
-            "l2": "inputs larger than L2 (7.27 GB of packed weights per step; no flush needed)",
-            "seed": 4}
+L2_BYTES = 129 * 2 ** 20
+DATA = "synthetic (seeded Student-t(4) std 0.02 weights, N(0,1) bf16 activations)"
 
 
 def peaks():
@@ -49,6 +50,11 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def copies_for(nbytes: int) -> int:
+    """Rotation depth so consecutive steps never find their weights in L2."""
+    return max(1, -(-3 * L2_BYTES // nbytes))
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -111,8 +117,6 @@ def oracle_sample_main():
     QMV_ORACLE_PASSES fixes the number of passes; otherwise passes repeat until
     QMV_ORACLE_SECONDS of CPU work have been timed.
     """
-    import numpy as np
-
     from oracle import matvec as o_mv
     from oracle import ternary as o_t
     from quantized_gemv_unpack_gb300 import synth
@@ -156,32 +160,242 @@ def run_oracle_sample(passes=0, seconds=10.0):
                       f"on one thread; {r['passes']} passes, {r['seconds']:.3f} s each"}
 
 
-# ----------------------------------------------------------------------------- GPU stack
+# ----------------------------------------------------------------------------- workloads
 
-def build_stack(q, torch, dev, layers=LAYERS, seed=4):
-    from quantized_gemv_unpack_gb300 import synth
-    gen = synth.torch_generator(seed, dev)
-    shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
-    tasks, keep = [], []
-    nbytes = 0
-    for layer in range(layers):
-        x_h = synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)
-        x_i = synth.activations_bf16_torch(gen, (1, INTER), device=dev)
-        for name, N, K in shapes:
-            d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+class Workload:
+    """One batch of synthetic input resident in HBM; step() launches one pass of the hot path."""
+    name = ""
+    kernel = ""
+    tok_s = False
+
+    def config(self):
+        raise NotImplementedError
+
+    def step(self, i, stream):
+        raise NotImplementedError
+
+    def bytes(self, i):
+        return self.nbytes
+
+    def host_io(self):
+        """(device inputs, device outputs) that an end-to-end step copies from / to pinned host memory."""
+        raise NotImplementedError
+
+
+class Stack(Workload):
+    name = "stack"
+    kernel = "gemv_kernel<ternary, M=1>"
+    tok_s = True
+
+    def __init__(self, q, torch, dev, layers=LAYERS, seed=4):
+        from quantized_gemv_unpack_gb300 import synth
+        gen = synth.torch_generator(seed, dev)
+        shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
+        tasks, xs = [], []
+        nbytes = 0
+        for _ in range(layers):
+            x_h = synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)
+            x_i = synth.activations_bf16_torch(gen, (1, INTER), device=dev)
+            for _, N, K in shapes:
+                d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+                p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
+                w = synth.student_t4_torch(gen, (N, K), device=dev)
+                q.qmv_pack_ternary(d, w, p)
+                del w
+                y = torch.empty((1, N), dtype=torch.float32, device=dev)
+                tasks.append((d, p, x_i if K == INTER else x_h, y))
+                nbytes += d.bytes[0] + d.bytes[1] + N * 4
+            nbytes += (HIDDEN + INTER) * 2
+            xs += [x_h, x_i]
+        torch.cuda.synchronize()
+        self.batch = q.Batch(q.QMV_TERNARY2, tasks, 1)
+        self.xs, self.ys = xs, [t[3] for t in tasks]
+        self.nbytes = nbytes
+        self.layers = layers
+
+    @staticmethod
+    def stack_config(layers):
+        return {"workload": f"27B-shaped ternary decode stack: {layers} layers x {{q,k,v,o,gate,up,down}}, "
+                            "hidden 5120, 40/8 heads x 128, SwiGLU 25600, block-128 absmean ternary + fp16 scales, "
+                            "batch 1",
+                "layers": layers, "hidden": HIDDEN, "heads": [NQ, NKV, HD], "intermediate": INTER,
+                "batch": 1, "matvecs_per_step": 7 * layers, "seed": 4,
+                "l2": "inputs larger than L2 (7.27 GB of packed weights per step; no flush needed)"}
+
+    def config(self):
+        return self.stack_config(self.layers)
+
+    def step(self, i, stream):
+        self.batch.run(stream)
+
+    def host_io(self):
+        return self.xs, self.ys
+
+
+class Ternary4096(Workload):
+    name = "ternary-4096"
+    kernel = "gemv_kernel<ternary, M=1>"
+
+    def __init__(self, q, torch, dev, M=1):
+        from quantized_gemv_unpack_gb300 import synth
+        gen = synth.torch_generator(0, dev)
+        N = K = 4096
+        self.d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+        one = torch.empty(self.d.total_bytes, dtype=torch.uint8, device=dev)
+        q.qmv_pack_ternary(self.d, synth.student_t4_torch(gen, (N, K), device=dev), one)
+        self.copies = copies_for(self.d.total_bytes)
+        self.ps = [one.clone() for _ in range(self.copies)]
+        self.x = synth.activations_bf16_torch(gen, (M, K), device=dev)
+        self.y = torch.empty((M, N), device=dev)
+        self.nbytes = self.d.bytes[0] + self.d.bytes[1] + M * K * 2 + M * N * 4
+        self.M = M
+        self.q = q
+
+    def config(self):
+        return {"workload": f"ternary GEMV 4096 x 4096, block-128 absmean + fp16 scales, M={self.M}", "M": self.M,
+                "seed": 0, "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
+
+    def step(self, i, stream):
+        self.q.qmv_run_ternary(self.d, self.ps[i % self.copies], self.x, self.y, stream)
+
+    def host_io(self):
+        return [self.x], [self.y]
+
+
+class Int4Layer(Workload):
+    name = "int4-layer"
+    kernel = "gemv_kernel<int4, M>"
+
+    def __init__(self, q, torch, dev, M=1):
+        from quantized_gemv_unpack_gb300 import synth
+        gen = synth.torch_generator(1, dev)
+        shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824)
+        one = []
+        for _, N, K in shapes:
+            d = q.qmv_pack_desc(q.QMV_INT4, N, K)
             p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
-            w = synth.student_t4_torch(gen, (N, K), device=dev)
-            q.qmv_pack_ternary(d, w, p)
-            del w
-            y = torch.empty((1, N), dtype=torch.float32, device=dev)
-            x = x_i if K == INTER else x_h
-            tasks.append((d, p, x, y))
-            nbytes += d.bytes[0] + d.bytes[1] + N * 4
-        nbytes += (HIDDEN + INTER) * 2
-        keep.append((x_h, x_i))
-    torch.cuda.synchronize()
-    return tasks, keep, nbytes
+            q.qmv_pack_int4(d, synth.student_t4_torch(gen, (N, K), device=dev), p)
+            one.append((d, p, N, K))
+        layer_bytes = sum(d.total_bytes for d, _, _, _ in one)
+        self.copies = copies_for(layer_bytes)
+        self.xs = {K: synth.activations_bf16_torch(gen, (M, K), device=dev) for K in (5120, 13824)}
+        self.ys = [torch.empty((M, N), device=dev) for _, _, N, _ in one]
+        self.batches = []
+        for c in range(self.copies):
+            tasks = [(d, p if c == 0 else p.clone(), self.xs[K], y) for (d, p, N, K), y in zip(one, self.ys)]
+            self.batches.append(q.Batch(q.QMV_INT4, tasks, M))
+        self.nbytes = sum(d.bytes[0] + d.bytes[1] + M * N * 4 for d, _, N, _ in one) + M * (5120 + 13824) * 2
+        self.M = M
 
+    def config(self):
+        return {"workload": f"INT4 GQA layer set (hidden 5120, 40/8 heads x 128, SwiGLU 13824), group-128 absmax/7, "
+                            f"M={self.M}", "M": self.M, "seed": 1, "matvecs_per_step": 7,
+                "l2": f"rotating {self.copies} copies of the layer (>= 3x L2)"}
+
+    def step(self, i, stream):
+        self.batches[i % self.copies].run(stream)
+
+    def host_io(self):
+        return list(self.xs.values()), self.ys
+
+
+class Cassandra(Workload):
+    kernel = "cass_kernel"
+
+    def __init__(self, q, torch, dev, target=False):
+        from quantized_gemv_unpack_gb300 import synth
+        g = synth.rng(2)
+        N, K = 14336, 4096
+        W = synth.to_bf16_bits(synth.student_t4(g, (N, K)))
+        X, _ = synth.calibration_bf16(g, 128, K)
+        self.d, buf = q.cass_pack_host(W, X)
+        one = torch.from_numpy(buf).to(dev)
+        self.copies = copies_for(self.d.total_bytes)
+        self.ps = [one] + [one.clone() for _ in range(self.copies - 1)]
+        self.M = 5 if target else 1
+        self.x = torch.from_numpy(synth.activations_bf16(g, (self.M, K)).view("int16")).to(dev).view(torch.bfloat16)
+        self.y = torch.empty((self.M, N), device=dev)
+        spec = sum(self.d.bytes[i] for i in range(5))
+        verif = self.d.bytes[5] + self.d.bytes[6]
+        self.nbytes = (spec + (verif if target else 0)) + self.M * K * 2 + self.M * N * 4
+        self.target = target
+        self.fn = q.cass_reconstruct if target else q.cass_decode_draft
+        self.name = "cass-target" if target else "cass-draft"
+        self.dense = N * K * 2
+
+    def config(self):
+        path = "target (speculation + verification, bit-exact rebuild)" if self.target else "draft (speculation only)"
+        return {"workload": f"Cassandra split 14336 x 4096 MLP matrix, {path}, M={self.M}", "M": self.M, "seed": 2,
+                "dense_bf16_bytes": self.dense, "n_symbols": self.d.n_symbols,
+                "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
+
+    def step(self, i, stream):
+        self.fn(self.d, self.ps[i % self.copies], self.x, self.y, None, stream)
+
+    def host_io(self):
+        return [self.x], [self.y]
+
+
+class Moe(Workload):
+    name = "moe"
+    kernel = "moe_expert_kernel"
+
+    def __init__(self, q, torch, dev, M=1, n_logits=64):
+        from quantized_gemv_unpack_gb300 import synth
+        E, H, I, topk = 128, 4096, 2048, 8
+        gen = synth.torch_generator(3, dev)
+        self.gu = q.qmv_pack_desc(q.QMV_TERNARY2, 2 * I, H)
+        self.dn = q.qmv_pack_desc(q.QMV_TERNARY2, H, I)
+        self.down_off = self.gu.total_bytes
+        self.stride = self.down_off + self.dn.total_bytes
+        self.buf = torch.empty(E * self.stride, dtype=torch.uint8, device=dev)
+        for e in range(E):
+            rec = self.buf[e * self.stride:(e + 1) * self.stride]
+            q.qmv_pack_ternary(self.gu, synth.student_t4_torch(gen, (2 * I, H), device=dev), rec[:self.down_off])
+            q.qmv_pack_ternary(self.dn, synth.student_t4_torch(gen, (H, I), device=dev), rec[self.down_off:])
+        self.logits = [synth.router_logits_torch(gen, M, E, device=dev) for _ in range(n_logits)]
+        self.active = [len(set(torch.topk(lg, topk, dim=1).indices.flatten().tolist())) for lg in self.logits]
+        self.x = synth.activations_bf16_torch(gen, (M, H), device=dev)
+        self.y = torch.empty((M, H), device=dev)
+        self.ws = torch.zeros(q.moe_workspace_size(E, topk, M, H, I), dtype=torch.uint8, device=dev)
+        self.per_expert = self.gu.bytes[0] + self.gu.bytes[1] + self.dn.bytes[0] + self.dn.bytes[1]
+        self.E, self.H, self.I, self.topk, self.M = E, H, I, topk, M
+        self.q = q
+
+    def config(self):
+        return {"workload": f"MoE decode, 128 ternary SwiGLU experts (hidden 4096, 2048), top-8 softmax, M={self.M}",
+                "M": self.M, "seed": 3, "mean_active_experts": sum(self.active) / len(self.active),
+                "l2": f"router logits rotate over {len(self.logits)} draws; experts total "
+                      f"{self.E * self.stride / 1e6:.0f} MB (> L2)"}
+
+    def bytes(self, i):
+        return self.active[i % len(self.active)] * self.per_expert + self.M * self.H * (2 + 4)
+
+    def step(self, i, stream):
+        self.q.moe_qmv_run(self.gu, self.dn, self.buf, self.stride, self.down_off, self.E,
+                           self.logits[i % len(self.logits)], self.topk, self.x, self.y, self.ws, stream)
+
+    def host_io(self):
+        return [self.x], [self.y]
+
+
+def make_workload(name, q, torch, dev, a):
+    if name == "stack":
+        return Stack(q, torch, dev, a.layers)
+    if name == "ternary-4096":
+        return Ternary4096(q, torch, dev, a.M or 1)
+    if name == "int4-layer":
+        return Int4Layer(q, torch, dev, a.M or 1)
+    if name == "cass-draft":
+        return Cassandra(q, torch, dev, target=False)
+    if name == "cass-target":
+        return Cassandra(q, torch, dev, target=True)
+    if name == "moe":
+        return Moe(q, torch, dev, a.M or 1)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ----------------------------------------------------------------------------- main
 
 def main():
     ap = argparse.ArgumentParser()
@@ -189,6 +403,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
+    ap.add_argument("--workload", default="stack",
+                    choices=["stack", "ternary-4096", "int4-layer", "cass-draft", "cass-target", "moe"])
+    ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
@@ -210,9 +427,8 @@ def main():
         base = run_oracle_sample(passes=a.steps)
         line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": base["seconds_per_pass"] * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded Student-t(4) std 0.02 weights, N(0,1) bf16 activations)",
-                "config": workload_config(), "impl": "reference",
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+                "config": Stack.stack_config(LAYERS), "impl": "reference",
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
                                  "unit": UNIT},
                 "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -221,7 +437,7 @@ def main():
 
     # CPU baseline first: a fresh interpreter (fork+exec) before any CUDA work
     cpu = None
-    if rank == 0 and not a.no_cpu_baseline:
+    if rank == 0 and a.workload == "stack" and not a.no_cpu_baseline:
         cpu = run_oracle_sample()
 
     import torch
@@ -235,8 +451,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    tasks, keep, nbytes = build_stack(q, torch, dev, a.layers)
-    batch = q.Batch(q.QMV_TERNARY2, tasks, 1)
+    wl = make_workload(a.workload, q, torch, dev, a)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -244,8 +459,8 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(a.warmup):
-        batch.run(stream)
+    for i in range(a.warmup):
+        wl.step(i, stream)
     assert q.qmv_check_status() == 0
     barrier()
     clocks = ClockSampler(local_rank)
@@ -254,40 +469,41 @@ def main():
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(a.steps):
-        batch.run(stream)
+    for i in range(a.steps):
+        wl.step(i, stream)
     ev1.record(stream)
     barrier()
     ms = ev0.elapsed_time(ev1) / a.steps
     clk = clocks.stop()
-    launches = a.steps
+    assert q.qmv_check_status() == 0
+    nbytes = sum(wl.bytes(i) for i in range(a.steps)) / a.steps
 
-    # end to end through host buffers: x from pinned host memory in, y back to pinned host memory
-    xs_dev = [t for pair in keep for t in pair]
-    xs_host = [t.cpu().pin_memory() for t in xs_dev]
-    ys_dev = [t[3] for t in tasks]
-    ys_host = [torch.empty_like(y, device="cpu").pin_memory() for y in ys_dev]
-    h2d = sum(t.numel() * t.element_size() for t in xs_host)
-    d2h = sum(t.numel() * t.element_size() for t in ys_host)
+    # end to end through host buffers: inputs from pinned host memory, outputs back to pinned host memory
+    ins, outs = wl.host_io()
+    ins_h = [t.cpu().pin_memory() for t in ins]
+    outs_h = [torch.empty_like(y, device="cpu").pin_memory() for y in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins_h)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
-    def e2e_step():
-        for h, d_ in zip(xs_host, xs_dev):
+    def e2e_step(i):
+        for h, d_ in zip(ins_h, ins):
             d_.copy_(h, non_blocking=True)
-        batch.run(stream)
-        for d_, h in zip(ys_dev, ys_host):
+        wl.step(i, stream)
+        for d_, h in zip(outs, outs_h):
             h.copy_(d_, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_e2e = max(3, a.steps // 4)
     e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
+    for i in range(n_e2e):
+        e2e_step(i)
     e1.record(stream)
     barrier()
     ms_e2e = e0.elapsed_time(e1) / n_e2e
+    e2e_bytes = sum(wl.bytes(i) for i in range(n_e2e)) / n_e2e
 
     if dist is not None:
         t = torch.tensor([ms, ms_e2e], device=dev)
@@ -296,26 +512,28 @@ def main():
     if rank != 0:
         dist.destroy_process_group()
         return
-    gbs = nbytes * world / (ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
-    per_launch_gbs = nbytes / (ms * 1e-3) / 1e9
+    per_gpu = nbytes / (ms * 1e-3) / 1e9
+    launches = {"stack": 1, "ternary-4096": 1, "int4-layer": 1 if (a.M or 1) <= 8 else 2, "cass-draft": 1,
+                "cass-target": 1, "moe": 3}[a.workload]
     line = {
-        "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16x2-f32",
-        "data": "synthetic (seeded Student-t(4) std 0.02 weights, N(0,1) bf16 activations)",
-        "config": dict(workload_config(), layers=a.layers,
-                       parallelism="replicas only" if world > 1 else "single GPU"),
-        "tok_s": 1000.0 / ms * world, "pct_of_peak": 100.0 * per_launch_gbs / peak,
+        "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16x2-f32" if a.workload in ("stack", "ternary-4096", "int4-layer", "moe") else "f32",
+        "data": DATA,
+        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU"),
+        "pct_of_peak": 100.0 * per_gpu / peak,
         "algorithmic_bytes_per_step": nbytes,
-        "roofline": {"bound": "hbm", "achieved": per_launch_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": per_launch_gbs / peak, "traffic": None,
-                     "kernel": "gemv_kernel<ternary, M=1>", "peak_kind": f"copy bandwidth, {peak_kind}"},
-        "e2e": {"value": nbytes * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
+                     "traffic": None, "kernel": wl.kernel, "peak_kind": f"copy bandwidth, {peak_kind}"},
+        "e2e": {"value": e2e_bytes / (ms_e2e * 1e-3) / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": launches,
+        "gpu_launches": launches * a.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if wl.tok_s:
+        line["tok_s"] = 1000.0 / ms * world
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -49,77 +49,15 @@
 #include <algorithm>
 #include <cstdlib>
 
-#include "qmv_internal.cuh"
+#include <algorithm>
+#include <cstdlib>
+
+#include "gemv_core.cuh"
 
 namespace qmv {
 namespace {
 
-template <int FMT>
-struct Fmt;
-template <>
-struct Fmt<QMV_TERNARY2> {
-  static constexpr int WPB = 8;    // 32-bit code words per 128-column block
-  static constexpr int PPW = 8;    // column pairs per word
-  static constexpr int CPW = 16;   // columns per word
-  static constexpr int JW = 2;     // 16-byte activation pieces per word
-  static constexpr int XLOG2 = 9;  // staged |x| max in [2^9, 2^10)
-  static constexpr uint32_t MASK = 0x06000600u, BASE = 0x3C003C00u;
-};
-template <>
-struct Fmt<QMV_INT4> {
-  static constexpr int WPB = 16;
-  static constexpr int PPW = 4;
-  static constexpr int CPW = 8;
-  static constexpr int JW = 1;
-  static constexpr int XLOG2 = 8;
-  static constexpr uint32_t MASK = 0x000F000Fu, BASE = 0x64086408u;
-};
-
-constexpr int kGroups = 4;            // lane groups (rows of a row quad)
-constexpr int kBlocksPerStep = 8;     // lanes per row
-constexpr int kStep = kBlocksPerStep * 128;
-constexpr int kSlots = 2;             // ring slots per decode warp
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr uint32_t kWaitLimit = 1u << 26;  // polls before a wait is declared lost
-
-// (a & b) ^ c as one logic op
-__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-// a * m on the integer-multiply unit (m a run-time power of two: a left shift)
-__device__ __forceinline__ uint32_t mul_lo(uint32_t a, uint32_t m) {
-  uint32_t d;
-  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(m));
-  return d;
-}
-// shifts by a run-time amount on the shift unit
-__device__ __forceinline__ uint32_t shl_r(uint32_t a, uint32_t s) {
-  uint32_t d;
-  asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(s));
-  return d;
-}
-__device__ __forceinline__ uint32_t shr_r(uint32_t a, uint32_t s) {
-  uint32_t d;
-  asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(s));
-  return d;
-}
-
-// decode constants held in registers for the whole kernel
-struct DecodeK {
-  uint32_t mask, base;
-  uint32_t m9, m7, m5, m1;  // 2^9, 2^7, 2^5, 2^1
-  uint32_t s1, s3, s5;      // shift amounts 1, 3, 5 (INT4: 4, 8, 12)
-};
-
-__device__ __forceinline__ __half2 as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-__device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
-// 2^e as a float, e in [-126, 127]
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+using namespace core;
 
 __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
   int lo = 0, hi = b.n_tasks - 1;
@@ -130,69 +68,6 @@ __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
   return lo;
 }
 
-template <int FMT>
-__device__ __forceinline__ __half2 decode_pair(uint32_t w, int i, const DecodeK& k) {
-  if constexpr (FMT == QMV_TERNARY2) {
-    // pair i: even column code at bits 2i..2i+1, odd column code at 16+2i..17+2i;
-    // shift both to bits 9-10 / 25-26
-    uint32_t t;
-    switch (i) {
-      case 0: t = mul_lo(w, k.m9); break;
-      case 1: t = mul_lo(w, k.m7); break;
-      case 2: t = mul_lo(w, k.m5); break;
-      case 3: t = shl_r(w, k.s3); break;
-      case 4: t = mul_lo(w, k.m1); break;
-      case 5: t = shr_r(w, k.s1); break;
-      case 6: t = shr_r(w, k.s3); break;
-      default: t = shr_r(w, k.s5); break;
-    }
-    return as_h2(and_xor(t, k.mask, k.base));
-  } else {
-    const uint32_t t = i == 0 ? w : shr_r(w, i == 1 ? k.s1 : (i == 2 ? k.s3 : k.s5));
-    return __hsub2(as_h2(and_xor(t, k.mask, k.base)), __floats2half2_rn(1032.f, 1032.f));
-  }
-}
-
-// ---- mbarrier and bulk-copy helpers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait: false (and the device error word set) if the phase never completes
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t polls = 0; polls < kWaitLimit; ++polls)
-    if (mbar_try_wait(bar, parity)) return true;
-  atomicCAS(err, 0, (int)QMV_ERR_TIMEOUT);
-  return false;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-
-template <int FMT, int RPW>
-struct Geometry {
-  static constexpr int BLOCK_BYTES = Fmt<FMT>::WPB * 4;
-  static constexpr int ROW_STEP_BYTES = kBlocksPerStep * BLOCK_BYTES;   // one step of one row
-  static constexpr int SLOT = RPW * ROW_STEP_BYTES;
-  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
-  static constexpr int BARS = kConsumerWarps * kSlots * 8;
-  static constexpr int TILE_ROWS = kConsumerWarps * RPW;
-};
 
 template <int FMT, int MT, int RPW>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvBatch b) {
@@ -270,8 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   // ===================== decode warps
   const int g = lane >> 3;
   const int p = lane & 7;
-  const DecodeK dk{b.magic[0], b.magic[1], b.magic[2], b.magic[3], b.magic[4],
-                   b.magic[5], b.magic[6], b.magic[7], b.magic[8]};  // mask base 2^9 2^7 2^5 2^1 s1 s3 s5
+  const DecodeK dk = load_decode_k(b.magic);
   const uint16_t* staged_x = nullptr;
   int staged_kc0 = -1;
   int staged_K = -1;
@@ -298,83 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
       if (x != staged_x || kc0 != staged_kc0 || K != staged_K) {
         // ---- stage the activations of this chunk
-        __syncthreads();
-        const int ngroups = kcn / 8;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          float mx = 0.f;
-          const uint16_t* xr = x + (size_t)m * ldx + kc0;
-          for (int q = tid; q < ngroups; q += kConsumerThreads) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(xr + q * 8);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t wv = word_of(raw, e);
-              mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(wv & 0xFFFFu)), fabsf(bf16_to_f32(wv >> 16))));
-            }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          if (lane == 0) s_red[warp][m] = mx;
-        }
-        __syncthreads();
-        if (tid < MT) {
-          float mx = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, s_red[w][tid]);
-          int e = 0;
-          if (mx > 0.f && mx <= 3.4e38f) {
-            int ex;
-            frexpf(mx, &ex);  // mx = f * 2^ex, f in [0.5, 1)
-            e = max(-120, min(120, F::XLOG2 - (ex - 1)));
-          }
-          s_xscale[tid] = exp2i(e);
-          s_xinv[tid] = exp2i(-e);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const float xsc = s_xscale[m];
-          const uint16_t* xr = x + (size_t)m * ldx + kc0;
-          for (int q = tid; q < ngroups; q += kConsumerThreads) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(xr + q * 8);
-            uint32_t hv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t wv = word_of(raw, e);
-              __half2 h = __floats2half2_rn(bf16_to_f32(wv & 0xFFFFu) * xsc, bf16_to_f32(wv >> 16) * xsc);
-              hv[e] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            const int k = q * 8;
-            const int blk = k / 128, cc = k % 128;
-            const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
-            const int h = cc / F::CPW, j = (cc % F::CPW) / 8;
-            xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          }
-        }
-        if constexpr (TERN) {
-          __syncthreads();
-          for (int q = tid; q < MT * S * kBlocksPerStep; q += kConsumerThreads) {
-            const int m = q / (S * kBlocksPerStep);
-            const int blk = q % (S * kBlocksPerStep);
-            const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
-            float se = 0.f, so = 0.f;
-            if (blk < nb) {
-              for (int h = 0; h < WPB; ++h)
-#pragma unroll
-                for (int j = 0; j < JW; ++j) {
-                  const uint4 pc = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp];
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(as_h2(word_of(pc, e)));
-                    se += f.x;
-                    so += f.y;
-                  }
-                }
-            }
-            negs[q] = __floats2half2_rn(-se, -so);
-          }
-        }
-        __syncthreads();
+        stage_chunk<FMT, MT, kThreads>(Bf16Rows{x, ldx, kc0}, kcn, S, xs, negs, s_red, s_xscale, s_xinv);
         staged_x = x;
         staged_kc0 = kc0;
         staged_K = K;
@@ -410,54 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         if (active) {
           // rows of the step are nbk blocks apart in the slot
           const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
-          const unsigned char* sb = wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES;
-          uint4 cw[RQ][WPB / 4];
-#pragma unroll
-          for (int r = 0; r < RQ; ++r)
-#pragma unroll
-            for (int u = 0; u < WPB / 4; ++u)
-              cw[r][u] = *reinterpret_cast<const uint4*>(sb + (r * kGroups + g) * row_bytes + u * 16);
-          __half2 a0[RQ][MT], a1[RQ][MT];
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const __half2 init = TERN ? negs[((size_t)m * S + s) * kBlocksPerStep + p] : __floats2half2_rn(0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < RQ; ++r) {
-              a0[r][m] = init;
-              a1[r][m] = __floats2half2_rn(0.f, 0.f);
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < WPB; ++h) {
-            uint4 xw[MT][JW];
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-              for (int j = 0; j < JW; ++j) xw[m][j] = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + p];
-#pragma unroll
-            for (int r = 0; r < RQ; ++r) {
-              const uint32_t w = word_of(cw[r][h / 4], h % 4);
-#pragma unroll
-              for (int i = 0; i < F::PPW; ++i) {
-                const __half2 v = decode_pair<FMT>(w, i, dk);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                  const __half2 xv = as_h2(word_of(xw[m][i / 4], i % 4));
-                  if (h < WPB / 2) a0[r][m] = __hfma2(v, xv, a0[r][m]);
-                  else a1[r][m] = __hfma2(v, xv, a1[r][m]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < RQ; ++r) {
-            const float scf = __half2float(__ushort_as_half(sc[r]));
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const __half2 t = __hadd2(a0[r][m], a1[r][m]);
-              accc[r][m] = fmaf(__low2float(t) + __high2float(t), scf, accc[r][m]);
-            }
-          }
+          decode_step<FMT, MT, RQ>(wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, negs, S, s, g,
+                                   p, dk, sc, accc);
         }
         __syncwarp();  // every lane is done with the slot before it is refilled
         issue_one();
@@ -522,18 +274,7 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   b.kc = kc;
   const size_t S = kc / kStep;
   const size_t smem = fixed + (size_t)MT * kc * 2 + (size_t)MT * S * kBlocksPerStep * 4;
-  // decode constants
-  b.magic[0] = F::MASK;
-  b.magic[1] = F::BASE;
-  b.magic[2] = 1u << 9;
-  b.magic[3] = 1u << 7;
-  b.magic[4] = 1u << 5;
-  b.magic[5] = 1u << 1;
-  const bool tern = FMT == QMV_TERNARY2;
-  b.magic[6] = tern ? 1 : 4;
-  b.magic[7] = tern ? 3 : 8;
-  b.magic[8] = tern ? 5 : 12;
-  b.magic[9] = 0;
+  fill_magic<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   auto kern = gemv_kernel<FMT, MT, RPW>;

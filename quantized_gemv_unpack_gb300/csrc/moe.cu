@@ -1,15 +1,485 @@
-// Mixture-of-experts decode over ternary SwiGLU experts.
-#include "qmv_internal.cuh"
+// Mixture-of-experts decode over ternary SwiGLU experts ("Nemotron 3.5 Bolt",
+// expert top-K routing): only the experts the router selects are read.
+//
+// Three launches on the caller's stream, all state in the caller's workspace:
+//  1. route: one warp per token takes the top-k of its E logits (equal logits:
+//     lower expert first) by k rounds of a warp arg-max, softmax over the k
+//     selected logits in fp32; one thread then orders the (token, expert)
+//     pairs by expert and token and lists each active expert once (a slot),
+//     and the CTA zeroes y.
+//  2. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
+//     tile of 64 rows of the [gate; up] matrix) into equal contiguous ranges;
+//     a CTA stages the slot's token rows of x (gathered) once per slot and
+//     decodes its rows with the same per-warp TMA ring and decode step as the
+//     matvec batch (prefetching across unit boundaries), writing g and u per
+//     (token, expert) pair to the workspace in fp32.
+//  3. down: the same over the down matrices; staging computes h = silu(g) * u
+//     (fp32) per pair, and the decoded rows are added into y[token] with
+//     weight p by fp32 atomics (their order varies between runs; the sum stays
+//     within the documented bound).
+#include <algorithm>
+
+#include "gemv_core.cuh"
+
+namespace qmv {
+namespace {
+
+using namespace core;
+
+constexpr int kMoeRPW = 4;                              // rows per decode warp
+constexpr int kMoeTileRows = kConsumerWarps * kMoeRPW;  // 64
+constexpr int kMaxTopk = 8;
+constexpr int kMaxTokens = 8;
+constexpr int kMaxExperts = 256;
+
+// Workspace layout (all offsets in bytes from the workspace base).
+struct MoeLayout {
+  int64_t hdr, slot_expert, slot_first, slot_count, pair_token, pair_prob, gu, total;
+  MoeLayout(int E, int topk, int M, int64_t I) {
+    const int P = M * topk;
+    const int S = std::min(E, P);
+    auto al = [](int64_t v) { return (v + 255) / 256 * 256; };
+    hdr = 0;
+    slot_expert = al(hdr + 16);
+    slot_first = al(slot_expert + 4 * S);
+    slot_count = al(slot_first + 4 * S);
+    pair_token = al(slot_count + 4 * S);
+    pair_prob = al(pair_token + 4 * P);
+    gu = al(pair_prob + 4 * P);
+    total = al(gu + (int64_t)P * 2 * I * 4);
+  }
+};
+
+struct MoeArgs {
+  const uint32_t* gu_codes;   // expert 0's [gate; up] codes; expert e at + e * stride_words
+  const uint16_t* gu_scales;
+  const uint32_t* dn_codes;
+  const uint16_t* dn_scales;
+  int64_t stride_words;       // expert record stride in 32-bit words
+  int64_t stride_halves;      // the same stride in 16-bit units
+  const float* logits;        // [M][E]
+  const uint16_t* x;          // bf16 [M][ldx]
+  float* y;                   // [M][ldy]
+  unsigned char* ws;
+  int E, topk, M, H, I, ldx, ldy, max_slots;
+  int64_t off_slot_expert, off_slot_first, off_slot_count, off_pair_token, off_pair_prob, off_gu;
+  uint32_t magic[10];
+  int* err;
+};
+
+__global__ void __launch_bounds__(256) moe_route_kernel(const MoeArgs a) {
+  __shared__ int s_exp[kMaxTokens][kMaxTopk];
+  __shared__ float s_prob[kMaxTokens][kMaxTopk];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* slot_expert = reinterpret_cast<int*>(a.ws + a.off_slot_expert);
+  int* slot_first = reinterpret_cast<int*>(a.ws + a.off_slot_first);
+  int* slot_count = reinterpret_cast<int*>(a.ws + a.off_slot_count);
+  int* pair_token = reinterpret_cast<int*>(a.ws + a.off_pair_token);
+  float* pair_prob = reinterpret_cast<float*>(a.ws + a.off_pair_prob);
+  int* n_slots = reinterpret_cast<int*>(a.ws);
+
+  if (warp < a.M) {
+    const float* lg = a.logits + (size_t)warp * a.E;
+    float v[kMaxExperts / 32];
+    bool used[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = i * 32 + lane;
+      v[i] = e < a.E ? lg[e] : -INFINITY;
+      used[i] = e >= a.E;
+    }
+    for (int r = 0; r < a.topk; ++r) {
+      // best remaining (value, index) of this lane, then across the warp
+      float bv = -INFINITY;
+      int bi = 1 << 30;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = i * 32 + lane;
+        if (!used[i] && (v[i] > bv || (v[i] == bv && e < bi) || bi == (1 << 30))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (bi < a.E && (bi & 31) == lane) used[bi >> 5] = true;
+      if (lane == 0) {
+        s_exp[warp][r] = bi < a.E ? bi : 0;
+        s_prob[warp][r] = bv;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const float mx = s_prob[warp][0];
+      float z = 0.f;
+      for (int r = 0; r < a.topk; ++r) {
+        s_prob[warp][r] = expf(s_prob[warp][r] - mx);
+        z += s_prob[warp][r];
+      }
+      for (int r = 0; r < a.topk; ++r) s_prob[warp][r] /= z;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // pairs ordered by expert, then token: one slot per active expert
+    int ns = 0, np = 0;
+    for (int e = 0; e < a.E; ++e) {
+      int first = np;
+      for (int t = 0; t < a.M; ++t)
+        for (int r = 0; r < a.topk; ++r)
+          if (s_exp[t][r] == e) {
+            pair_token[np] = t;
+            pair_prob[np] = s_prob[t][r];
+            ++np;
+          }
+      if (np > first) {
+        slot_expert[ns] = e;
+        slot_first[ns] = first;
+        slot_count[ns] = np - first;
+        ++ns;
+      }
+    }
+    *n_slots = ns;
+  }
+  for (int i = threadIdx.x; i < a.M * a.H; i += blockDim.x) a.y[(size_t)(i / a.H) * a.ldy + i % a.H] = 0.f;
+}
+
+// activation sources of the two expert phases
+struct GatherRows {  // x rows of the slot's tokens
+  const uint16_t* x;
+  int ldx;
+  const int* tok;    // shared memory, MT entries
+  __device__ __forceinline__ void load8(int m, int k, float v[8]) const {
+    Bf16Rows{x + (size_t)tok[m] * ldx, 0, 0}.load8(0, k, v);
+  }
+};
+struct SwiGlu {  // h = silu(g) * u from the workspace, pair rows [first + m]
+  const float* gu;
+  int I, first;
+  __device__ __forceinline__ void load8(int m, int k, float v[8]) const {
+    const float* gr = gu + (size_t)(first + m) * 2 * I + k;
+    const float4 g0 = *reinterpret_cast<const float4*>(gr), g1 = *reinterpret_cast<const float4*>(gr + 4);
+    const float4 u0 = *reinterpret_cast<const float4*>(gr + I), u1 = *reinterpret_cast<const float4*>(gr + I + 4);
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = g[e] / (1.f + __expf(-g[e])) * u[e];
+  }
+};
+
+// Per-warp producer over the CTA's sequence of (unit, step), unit = (slot,
+// tile): lane 0 copies the warp's 4 rows of one step of the unit's expert
+// matrix into the next ring slot (one bulk copy, completes on the slot's
+// mbarrier), two steps ahead of the decode.
+struct UnitProducer {
+  const uint32_t* codes0;   // expert 0's codes; expert e at + e * stride_words
+  int64_t stride_words;
+  const int* slot_expert;
+  int N, K, tiles, u, u_end, s, nsteps, warp, lane;
+  uint32_t n_issued;
+  unsigned char* wring;
+  uint64_t* wfull;
+  __device__ __forceinline__ void issue() {
+    using F = Fmt<QMV_TERNARY2>;
+    using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+    constexpr int kStepWords = kBlocksPerStep * F::WPB;
+    if (u >= u_end) return;
+    const int nb = K / 128;
+    const int nbk = min(kBlocksPerStep, nb - s * kBlocksPerStep);
+    const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
+    const int N16 = (N + 15) / 16 * 16;
+    const uint32_t bytes = wrow0 < N16 ? (uint32_t)(kMoeRPW * nbk * G::BLOCK_BYTES) : 0u;
+    const int slot = n_issued % kSlots;
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&wfull[slot], bytes);
+      if (bytes) {
+        const uint32_t* codes = codes0 + (size_t)slot_expert[u / tiles] * stride_words;
+        const size_t off = (size_t)(wrow0 / 16) * 16 * (K / F::CPW) + (size_t)s * 16 * kStepWords +
+                           (size_t)(wrow0 % 16) * nbk * F::WPB;
+        bulk_g2s(wring + (size_t)slot * G::SLOT, codes + off, bytes, &wfull[slot]);
+      }
+    }
+    ++n_issued;
+    if (++s >= nsteps) {
+      s = 0;
+      ++u;
+    }
+  }
+};
+
+// Decode the units [u, u_end) of one slot (all tiles of one expert matrix for
+// the slot's MT tokens); out(m, row, value) receives sum_k w_hat x.
+template <int MT, class Src, class Out>
+__device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u, int u_end, const Src& src,
+                         const Out& out, unsigned char* smem_raw, const DecodeK& dk, UnitProducer& prod,
+                         uint32_t& it, int* err) {
+  constexpr int FMT = QMV_TERNARY2;
+  using F = Fmt<FMT>;
+  using G = Geometry<FMT, kMoeRPW>;
+  constexpr int RQ = kMoeRPW / kGroups;
+  __shared__ float s_red[kConsumerWarps][MT];
+  __shared__ float s_xinv[MT];
+  __shared__ float s_xscale[MT];
+  const int S = (K + kStep - 1) / kStep;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);
+  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 3, p = lane & 7;
+  const int nb = K / 128;
+  const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
+  const int KB = K / 128;
+
+  stage_chunk<FMT, MT, kThreads>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
+
+  for (; u < u_end; ++u) {
+    const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
+    const unsigned short* sp[RQ];
+#pragma unroll
+    for (int r = 0; r < RQ; ++r)
+      sp[r] = reinterpret_cast<const unsigned short*>(scales) + (size_t)min(wrow0 + r * kGroups + g, N - 1) * KB + p;
+    float accc[RQ][MT];
+#pragma unroll
+    for (int r = 0; r < RQ; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) accc[r][m] = 0.f;
+    for (int s = 0; s < nsteps; ++s, ++it) {
+      const bool active = s * kBlocksPerStep + p < nb;
+      unsigned short sc[RQ];
+#pragma unroll
+      for (int r = 0; r < RQ; ++r) sc[r] = active ? __ldg(sp[r] + s * kBlocksPerStep) : (unsigned short)0;
+      const int slot = it % kSlots;
+      mbar_wait(&prod.wfull[slot], (it / kSlots) & 1u, err);
+      if (active) {
+        const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
+        decode_step<FMT, MT, RQ>(prod.wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, negs, S,
+                                 s, g, p, dk, sc, accc);
+      }
+      __syncwarp();
+      prod.issue();
+    }
+#pragma unroll
+    for (int r = 0; r < RQ; ++r) {
+      const int row = wrow0 + r * kGroups + g;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float v = accc[r][m];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        if (p == 0 && row < N) out(m, row, 2.f * v * s_xinv[m]);
+      }
+    }
+  }
+}
+
+struct GuOut {  // g|u of pair first + m
+  float* gu;
+  int I2, first;
+  __device__ __forceinline__ void operator()(int m, int row, float v) const {
+    gu[(size_t)(first + m) * I2 + row] = v;
+  }
+};
+struct DownOut {  // y[token] += p * value
+  float* y;
+  int ldy;
+  const int* tok;
+  const float* prob;
+  __device__ __forceinline__ void operator()(int m, int row, float v) const {
+    atomicAdd(y + (size_t)tok[m] * ldy + row, prob[m] * v);
+  }
+};
+
+// Persistent: CTA c takes the contiguous unit range [c*U/G, (c+1)*U/G) of the
+// U = n_slots * tiles units of this phase (all units are the same size).
+template <int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a) {
+  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ int s_tok[kMaxTokens];
+  __shared__ float s_prob[kMaxTokens];
+  const int ns = *reinterpret_cast<const int*>(a.ws);
+  const int* slot_expert = reinterpret_cast<const int*>(a.ws + a.off_slot_expert);
+  const int* slot_first = reinterpret_cast<const int*>(a.ws + a.off_slot_first);
+  const int* slot_count = reinterpret_cast<const int*>(a.ws + a.off_slot_count);
+  const int N = PHASE == 0 ? 2 * a.I : a.H;
+  const int K = PHASE == 0 ? a.H : a.I;
+  const int tiles = (N + kMoeTileRows - 1) / kMoeTileRows;
+  const int total = ns * tiles;
+  const int u_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int u_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  if (u_begin >= u_end) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  UnitProducer prod;
+  prod.codes0 = PHASE == 0 ? a.gu_codes : a.dn_codes;
+  prod.stride_words = a.stride_words;
+  prod.slot_expert = slot_expert;
+  prod.N = N;
+  prod.K = K;
+  prod.tiles = tiles;
+  prod.u = u_begin;
+  prod.u_end = u_end;
+  prod.s = 0;
+  prod.nsteps = (K / 128 + kBlocksPerStep - 1) / kBlocksPerStep;
+  prod.warp = warp;
+  prod.lane = lane;
+  prod.n_issued = 0;
+  prod.wring = smem_raw + (size_t)warp * kSlots * G::SLOT;
+  prod.wfull = reinterpret_cast<uint64_t*>(smem_raw + G::RING) + warp * kSlots;
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(&prod.wfull[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  for (int i = 0; i < kSlots; ++i) prod.issue();
+
+  const DecodeK dk = load_decode_k(a.magic);
+  float* gu = reinterpret_cast<float*>(a.ws + a.off_gu);
+  const uint16_t* scales0 = PHASE == 0 ? a.gu_scales : a.dn_scales;
+  uint32_t it = 0;
+  for (int u = u_begin; u < u_end;) {
+    const int slot = u / tiles;
+    const int u_stop = min(u_end, (slot + 1) * tiles);
+    const int e = slot_expert[slot];
+    const int first = slot_first[slot];
+    const int cnt = slot_count[slot];
+    __syncthreads();  // the previous slot's token table is no longer read
+    if (threadIdx.x < cnt) {
+      s_tok[threadIdx.x] = reinterpret_cast<const int*>(a.ws + a.off_pair_token)[first + threadIdx.x];
+      s_prob[threadIdx.x] = reinterpret_cast<const float*>(a.ws + a.off_pair_prob)[first + threadIdx.x];
+    }
+    __syncthreads();
+    const uint16_t* scales = scales0 + (size_t)e * a.stride_halves;
+    if (PHASE == 0) {
+      const GatherRows src{a.x, a.ldx, s_tok};
+      const GuOut out{gu, 2 * a.I, first};
+      switch (cnt) {
+#define QMV_MOE_CASE(m) \
+  case m: run_slot<m>(scales, N, K, tiles, u, u_stop, src, out, smem_raw, dk, prod, it, a.err); break;
+        QMV_MOE_CASE(1) QMV_MOE_CASE(2) QMV_MOE_CASE(3) QMV_MOE_CASE(4)
+        QMV_MOE_CASE(5) QMV_MOE_CASE(6) QMV_MOE_CASE(7) QMV_MOE_CASE(8)
+#undef QMV_MOE_CASE
+        default: break;
+      }
+    } else {
+      const SwiGlu src{gu, a.I, first};
+      const DownOut out{a.y, a.ldy, s_tok, s_prob};
+      switch (cnt) {
+#define QMV_MOE_CASE(m) \
+  case m: run_slot<m>(scales, N, K, tiles, u, u_stop, src, out, smem_raw, dk, prod, it, a.err); break;
+        QMV_MOE_CASE(1) QMV_MOE_CASE(2) QMV_MOE_CASE(3) QMV_MOE_CASE(4)
+        QMV_MOE_CASE(5) QMV_MOE_CASE(6) QMV_MOE_CASE(7) QMV_MOE_CASE(8)
+#undef QMV_MOE_CASE
+        default: break;
+      }
+    }
+    u = u_stop;
+  }
+}
+
+size_t expert_smem(int64_t K) {
+  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+  const int64_t S = (K + kStep - 1) / kStep;
+  return G::RING + G::BARS + (size_t)kMaxTokens * S * kStep * 2 + (size_t)kMaxTokens * S * kBlocksPerStep * 4;
+}
+
+}  // namespace
+}  // namespace qmv
 
 using namespace qmv;
 
 extern "C" {
 
-size_t moe_workspace_size(int, int, int, int64_t, int64_t) { return 0; }
+size_t moe_workspace_size(int E, int topk, int M, int64_t H, int64_t I) {
+  (void)H;
+  if (E < 1 || topk < 1 || M < 1 || I < 1) return 0;
+  return (size_t)MoeLayout(E, topk, M, I).total;
+}
 
-int moe_qmv_run(const qmv_desc*, const qmv_desc*, const void*, int64_t, int64_t, int, const float*, int,
-                const void*, int, int64_t, float*, int64_t, void*, size_t, void*) {
-  return fail(QMV_ERR_UNSUPPORTED, "moe_qmv_run: not built yet");
+int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts, int64_t expert_stride,
+                int64_t down_off, int E, const float* logits, int topk, const void* x_bf16, int M, int64_t ldx,
+                float* y, int64_t ldy, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_desc(gateup_desc, QMV_TERNARY2);
+  if (rc) return fail(rc, "gate|up descriptor: %s", qmv_last_error());
+  rc = check_desc(down_desc, QMV_TERNARY2);
+  if (rc) return fail(rc, "down descriptor: %s", qmv_last_error());
+  const int64_t H = gateup_desc->K, I2 = gateup_desc->N;
+  if (I2 % 2 || down_desc->N != H || down_desc->K != I2 / 2)
+    return fail(QMV_ERR_ARG, "shapes: [gate; up] must be 2I x H and down H x I");
+  const int64_t I = I2 / 2;
+  if (I % 128) return fail(QMV_ERR_ARG, "I=%lld must be a multiple of 128", (long long)I);
+  if (E < 1 || E > kMaxExperts || topk < 1 || topk > kMaxTopk || topk > E || M < 1 || M > kMaxTokens)
+    return fail(QMV_ERR_ARG, "E=%d topk=%d M=%d outside 1..256, 1..8 (<= E), 1..8", E, topk, M);
+  if (!experts || !logits || !x_bf16 || !y || !workspace) return fail(QMV_ERR_ARG, "NULL pointer");
+  if (!aligned16(experts) || !aligned16(logits) || !aligned16(x_bf16) || !aligned16(y) || !aligned16(workspace))
+    return fail(QMV_ERR_ALIGN, "buffers must be 16-byte aligned");
+  if (expert_stride % 256 || down_off % 256 || down_off < gateup_desc->total_bytes ||
+      down_off + down_desc->total_bytes > expert_stride)
+    return fail(QMV_ERR_ARG, "expert record: stride and down_off must be multiples of 256 and hold both matrices");
+  if (ldx < H || ldx % 8 || ldy < H) return fail(QMV_ERR_ARG, "ldx/ldy");
+  if (H > INT32_MAX || ldx > INT32_MAX || ldy > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "sizes too large");
+  const MoeLayout L(E, topk, M, I);
+  if (ws_bytes < (size_t)L.total) return fail(QMV_ERR_ARG, "workspace %zu < %lld bytes", ws_bytes, (long long)L.total);
+  const size_t smem_gu = expert_smem(H), smem_dn = expert_smem(I);
+  if (std::max(smem_gu, smem_dn) > 227 * 1024 - 1024) return fail(QMV_ERR_UNSUPPORTED, "hidden size too large for one CTA");
+  int* err = device_error_word();
+  if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+
+  MoeArgs a;
+  const char* base = static_cast<const char*>(experts);
+  a.gu_codes = reinterpret_cast<const uint32_t*>(base + gateup_desc->off[0]);
+  a.gu_scales = reinterpret_cast<const uint16_t*>(base + gateup_desc->off[1]);
+  a.dn_codes = reinterpret_cast<const uint32_t*>(base + down_off + down_desc->off[0]);
+  a.dn_scales = reinterpret_cast<const uint16_t*>(base + down_off + down_desc->off[1]);
+  a.stride_words = expert_stride / 4;
+  a.stride_halves = expert_stride / 2;
+  a.logits = logits;
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.y = y;
+  a.ws = static_cast<unsigned char*>(workspace);
+  a.E = E;
+  a.topk = topk;
+  a.M = M;
+  a.H = (int)H;
+  a.I = (int)I;
+  a.ldx = (int)ldx;
+  a.ldy = (int)ldy;
+  a.max_slots = std::min(E, M * topk);
+  a.off_slot_expert = L.slot_expert;
+  a.off_slot_first = L.slot_first;
+  a.off_slot_count = L.slot_count;
+  a.off_pair_token = L.pair_token;
+  a.off_pair_prob = L.pair_prob;
+  a.off_gu = L.gu;
+  core::fill_magic<QMV_TERNARY2>(a.magic);
+  a.err = err;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe_route_kernel<<<1, 256, 0, s>>>(a);
+  cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return cuda_fail(ce, "moe route launch");
+  int per_sm = 0;
+  rc = kernel_fit((const void*)moe_expert_kernel<0>, kThreads, smem_gu, &per_sm);
+  if (rc) return rc;
+  rc = kernel_fit((const void*)moe_expert_kernel<1>, kThreads, smem_dn, &per_sm);
+  if (rc) return rc;
+  // persistent grids: one CTA per SM, capped by the largest possible unit count
+  const int units_gu = a.max_slots * (int)((I2 + kMoeTileRows - 1) / kMoeTileRows);
+  const int units_dn = a.max_slots * (int)((H + kMoeTileRows - 1) / kMoeTileRows);
+  moe_expert_kernel<0><<<std::min(sm_count(), units_gu), kThreads, smem_gu, s>>>(a);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return cuda_fail(ce, "moe gate|up launch");
+  moe_expert_kernel<1><<<std::min(sm_count(), units_dn), kThreads, smem_dn, s>>>(a);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
+  return QMV_OK;
 }
 
 }  // extern "C"
