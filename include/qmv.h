@@ -210,6 +210,31 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The same MoE decode as moe_qmv_run, for callers that cannot allocate device
+ * memory themselves: for example a plugin inside a host application that owns
+ * every device allocation, or a latency-critical loop that must not pay for
+ * cudaMalloc. Instead of a caller workspace it uses one fixed scratch array of
+ * QMV_MOE_STATIC_SCRATCH_BYTES bytes that lives in this library's own device
+ * memory (every GPU that loads the library holds it until the process exits).
+ * The pages have no counterpart to this entry point; it exists only for such
+ * callers.
+ *  - It allocates nothing and frees nothing. The first call on a device looks up
+ *    the array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *    first call before any stream capture.
+ *  - A call whose scratch need (moe_workspace_size) exceeds the array is
+ *    rejected with QMV_ERR_ARG before any launch.
+ *  - All calls share the one array and it keeps the previous call's contents;
+ *    each call rewrites everything it reads, so nothing needs clearing. Calls
+ *    that overlap on the GPU (for example on two streams) race on the array:
+ *    issue them in one stream order.
+ * Other arguments, layouts and errors are those of moe_qmv_run.
+ */
+#define QMV_MOE_STATIC_SCRATCH_BYTES (2u * 1024u * 1024u)
+int moe_qmv_run_static(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts,
+                       int64_t expert_stride, int64_t down_off, int E, const float* logits, int topk,
+                       const void* x_bf16, int M, int64_t ldx, float* y, int64_t ldy, void* stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *device_code (nullable) receives 0 or a qmv_status the kernels recorded.
  * Returns QMV_ERR_CUDA if the synchronization failed, else the recorded status.

@@ -27,7 +27,7 @@ QMV_TERNARY2, QMV_INT4, QMV_CASS = 1, 2, 3
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
            "qmv_run_int4", "qmv_run_batch", "cass_pack_host", "cass_decode_draft", "cass_reconstruct",
-           "moe_workspace_size", "moe_qmv_run", "qmv_check_status", "qmv_last_error")
+           "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
 
 
 class QmvError(RuntimeError):
@@ -72,6 +72,7 @@ _SIGS = {
     "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
     "moe_qmv_run": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P,
                            ctypes.c_size_t, _P]),
+    "moe_qmv_run_static": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P]),
     "qmv_check_status": (_I32, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "qmv_last_error": (ctypes.c_char_p, []),
 }
@@ -232,6 +233,20 @@ def moe_qmv_run(gateup_desc: qmv_desc, down_desc: qmv_desc, experts, expert_stri
     _check(lib().moe_qmv_run(ctypes.byref(gateup_desc), ctypes.byref(down_desc), _ptr(experts), expert_stride,
                              down_off, E, _ptr(logits), topk, _ptr(x), M, ldx, _ptr(y), ldy, _ptr(workspace),
                              ws_bytes, _stream(stream)))
+
+
+QMV_MOE_STATIC_SCRATCH_BYTES = 2 * 1024 * 1024
+
+
+def moe_qmv_run_static(gateup_desc: qmv_desc, down_desc: qmv_desc, experts, expert_stride: int, down_off: int,
+                       E: int, logits, topk: int, x, y, stream=None):
+    """moe_qmv_run without a caller workspace: for callers that cannot allocate device memory, the
+    library's fixed device scratch array is used instead (see include/qmv.h)."""
+    M, ldx = _rows(x)
+    _, ldy = _rows(y)
+    _check(lib().moe_qmv_run_static(ctypes.byref(gateup_desc), ctypes.byref(down_desc), _ptr(experts),
+                                    expert_stride, down_off, E, _ptr(logits), topk, _ptr(x), M, ldx, _ptr(y), ldy,
+                                    _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- status

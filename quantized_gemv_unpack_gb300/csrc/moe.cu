@@ -18,6 +18,8 @@
 //     weight p by fp32 atomics (their order varies between runs; the sum stays
 //     within the documented bound).
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "gemv_core.cuh"
 
@@ -390,6 +392,30 @@ size_t expert_smem(int64_t K) {
   return G::RING + G::BARS + (size_t)kMaxTokens * S * kStep * 2 + (size_t)kMaxTokens * S * kBlocksPerStep * 4;
 }
 
+// Scratch for moe_qmv_run_static: one fixed array per device, in the module's
+// own global memory, for callers that cannot allocate device memory.
+__device__ __align__(256) unsigned char g_moe_static_scratch[QMV_MOE_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+std::vector<void*> g_static_ptr;  // device address of the scratch, per device ordinal
+
+// Device address of the scratch array on the current device (looked up once).
+int static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if ((int)g_static_ptr.size() <= dev) g_static_ptr.resize(dev + 1, nullptr);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_moe_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(MoE static scratch)");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return QMV_OK;
+}
+
 }  // namespace
 }  // namespace qmv
 
@@ -480,6 +506,22 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
   return QMV_OK;
+}
+
+int moe_qmv_run_static(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts,
+                       int64_t expert_stride, int64_t down_off, int E, const float* logits, int topk,
+                       const void* x_bf16, int M, int64_t ldx, float* y, int64_t ldy, void* stream) {
+  if (!gateup_desc) return fail(QMV_ERR_ARG, "gate|up descriptor is NULL");
+  const size_t need = moe_workspace_size(E, topk, M, gateup_desc->K, gateup_desc->N / 2);
+  if (need == 0) return fail(QMV_ERR_ARG, "E=%d topk=%d M=%d", E, topk, M);
+  if (need > (size_t)QMV_MOE_STATIC_SCRATCH_BYTES)
+    return fail(QMV_ERR_ARG, "this MoE call needs %zu bytes of scratch; the static scratch holds %zu (use moe_qmv_run "
+                "with a caller workspace)", need, (size_t)QMV_MOE_STATIC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  int rc = static_scratch(&scratch);
+  if (rc) return rc;
+  return moe_qmv_run(gateup_desc, down_desc, experts, expert_stride, down_off, E, logits, topk, x_bf16, M, ldx, y,
+                     ldy, scratch, (size_t)QMV_MOE_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"
