@@ -96,8 +96,19 @@ typedef struct {
   int64_t off[QMV_MAX_SECTIONS];
   int64_t bytes[QMV_MAX_SECTIONS];
   int64_t total_bytes;       /* size of the whole packed buffer */
-  uint64_t flags;            /* 0 */
+  uint64_t flags;            /* 0, or one QMV_FLAG_PATH_* bit (ternary/INT4 matvec) */
 } qmv_desc;
+
+/*
+ * Kernel choice of the ternary/INT4 matvec entry points (qmv_desc.flags; the
+ * packers leave it 0). With 0 the library picks by M: the fp16-FMA kernel,
+ * whose cost grows with M, below 4 activation rows, and the tensor-core kernel
+ * (mma.sync m16n8k16, decode cost independent of M) from 4 on. Setting one bit
+ * forces a kernel, for testing and tuning; both bits set is QMV_ERR_ARG.
+ * Results of both kernels satisfy the same error bound.
+ */
+#define QMV_FLAG_PATH_FMA 1u
+#define QMV_FLAG_PATH_MMA 2u
 
 /* One matvec of a batch: y[M][ldy] = W x[M][ldx] for the matrix packed in w. */
 typedef struct {
@@ -138,9 +149,12 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
 /*
  * y[m][n] = sum_k W_hat[n][k] * x[m][k] for m < M, n < N, where W_hat = q * scale
  * of the packed ternary (qmv_run_ternary) or INT4 (qmv_run_int4) matrix.
- * M in 1..QMV_MAX_M, ldx >= K, ldy >= N. Products and sums use fp16 pairs over
- * 16-32 columns and fp32 beyond; each row's error stays within the library's
- * documented bound |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|.
+ * M in 1..QMV_MAX_M, ldx >= K, ldy >= N. Activations are rounded to fp16 after
+ * a power-of-two scaling per row and chunk of K; the fp16-FMA kernel sums
+ * products in fp16 pairs over 16-32 columns and in fp32 beyond, the
+ * tensor-core kernel (M >= 4, see QMV_FLAG_PATH_*) in fp32 from the start. Each
+ * row's error stays within the library's documented bound
+ * |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|.
  */
 int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
                     float* y, int64_t ldy, void* stream);
@@ -151,7 +165,8 @@ int qmv_run_int4(const qmv_desc* desc, const void* w, const void* x_bf16, int M,
  * Several independent matvecs of one format and one M in a single persistent
  * launch (a whole decode stack's q/k/v/o/gate/up/down, or the q|k|v and
  * gate|up groups that share one x). 1 <= n_tasks <= QMV_MAX_BATCH. The tasks
- * must not write overlapping y ranges.
+ * must not write overlapping y ranges. The kernel choice follows the OR of the
+ * descriptors' QMV_FLAG_PATH_* bits.
  */
 int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* stream);
 

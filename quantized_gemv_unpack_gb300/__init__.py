@@ -23,6 +23,7 @@ QMV_MAX_BATCH = 448
 QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
 QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
 QMV_TERNARY2, QMV_INT4, QMV_CASS = 1, 2, 3
+QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-FMA or the tensor-core matvec kernel
 
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",

@@ -28,6 +28,15 @@ struct FitEntry {
   int per_sm;
 };
 std::vector<FitEntry> g_fit;
+// the largest dynamic shared memory size a kernel has been allowed on a device:
+// the attribute is only ever raised, so a smaller launch cannot lower it under
+// a larger cached one
+struct SmemAttr {
+  int dev;
+  const void* kernel;
+  size_t smem;
+};
+std::vector<SmemAttr> g_smem_attr;
 
 int current_device() {
   int d = 0;
@@ -76,23 +85,27 @@ int sm_count() {
 
 int kernel_fit(const void* kernel, int threads, size_t smem, int* per_sm) {
   const int d = current_device();
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    for (const FitEntry& f : g_fit)
-      if (f.dev == d && f.kernel == kernel && f.threads == threads && f.smem == smem) {
-        *per_sm = f.per_sm;
-        return QMV_OK;
-      }
-  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const FitEntry& f : g_fit)
+    if (f.dev == d && f.kernel == kernel && f.threads == threads && f.smem == smem) {
+      *per_sm = f.per_sm;
+      return QMV_OK;
+    }
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    SmemAttr* a = nullptr;
+    for (SmemAttr& x : g_smem_attr)
+      if (x.dev == d && x.kernel == kernel) a = &x;
+    if (!a || a->smem < smem) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+      if (a) a->smem = smem;
+      else g_smem_attr.push_back({d, kernel, smem});
+    }
   }
   int n = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (n < 1) return fail(QMV_ERR_UNSUPPORTED, "kernel with %d threads and %zu B shared memory does not fit an SM", threads, smem);
-  std::lock_guard<std::mutex> lk(g_mu);
   g_fit.push_back({d, kernel, threads, smem, n});
   *per_sm = n;
   return QMV_OK;
@@ -162,9 +175,18 @@ int build_task(const qmv_desc* d, int format, const void* w, const void* x, int6
 
 namespace {
 
-// Launch `n` tasks with M activation rows, splitting M into launches of <= 8 rows.
-int run_tasks(int format, GemvTask* tasks, int n, int M, cudaStream_t s) {
+// Launch `n` tasks with M activation rows: one tensor-core launch, or
+// fp16-FMA launches of <= 8 rows each. `flags` holds the QMV_FLAG_PATH_* bits
+// of the tasks' descriptors.
+int run_tasks(int format, GemvTask* tasks, int n, int M, uint64_t flags, cudaStream_t s) {
   static thread_local GemvBatch b;
+  const uint64_t path = flags & (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA);
+  if (path == (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA)) return fail(QMV_ERR_ARG, "both QMV_FLAG_PATH_FMA and _MMA set");
+  if (path == QMV_FLAG_PATH_MMA || (path == 0 && M >= kMmaMinM)) {
+    for (int i = 0; i < n; ++i) b.t[i] = tasks[i];
+    b.n_tasks = n;
+    return launch_gemv_mma(format, b, M, s);
+  }
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mt = M - m0 < 8 ? M - m0 : 8;
     for (int i = 0; i < n; ++i) {
@@ -186,7 +208,7 @@ int run_one(int format, const qmv_desc* d, const void* w, const void* x, int M, 
   GemvTask t;
   int rc = build_task(d, format, w, x, ldx, y, ldy, &t);
   if (rc) return rc;
-  return run_tasks(format, &t, 1, M, static_cast<cudaStream_t>(stream));
+  return run_tasks(format, &t, 1, M, d->flags, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -233,13 +255,15 @@ int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* s
   if (M < 1 || M > QMV_MAX_M) return fail(QMV_ERR_ARG, "M=%d outside 1..%d", M, QMV_MAX_M);
   static thread_local GemvTask t[QMV_MAX_BATCH];
   int64_t tiles = 0;
+  uint64_t flags = 0;
   for (int i = 0; i < n_tasks; ++i) {
     int rc = build_task(tasks[i].desc, format, tasks[i].w, tasks[i].x, tasks[i].ldx, tasks[i].y, tasks[i].ldy, &t[i]);
     if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
     tiles += (t[i].N + 3) / 4;
+    flags |= tasks[i].desc->flags;
   }
   if (tiles > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
-  return run_tasks(format, t, n_tasks, M, static_cast<cudaStream_t>(stream));
+  return run_tasks(format, t, n_tasks, M, flags, static_cast<cudaStream_t>(stream));
 }
 
 int qmv_check_status(void* stream, int32_t* device_code) {

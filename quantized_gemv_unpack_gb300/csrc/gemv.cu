@@ -12,9 +12,9 @@
 // one step, so a warp's rows of a step are one contiguous range: lane 0 of the
 // warp fills a slot with a single 1D bulk copy (cp.async.bulk) that completes
 // on the slot's mbarrier, two steps ahead of the step being decoded, walking
-// the same (tile, chunk, step) sequence as the decode loop. Every wait polls a
-// bounded number of times and then records QMV_ERR_TIMEOUT in the device
-// error word instead of spinning on.
+// the same (tile, chunk, step) sequence as the decode loop. Every wait gives
+// up after 2 s and records QMV_ERR_TIMEOUT in the device error word instead of
+// spinning on.
 //
 // Inside a decode warp, lane = 8*g + p: lane p (0..7) owns one 128-column
 // block of the step and lane group g (0..3) one row of each row quad, so the
@@ -46,9 +46,6 @@
 // Two fp16 pair accumulators per block (first and second half of the words)
 // are added, widened to fp32 and scaled by the block's fp16 scale; three warp
 // shuffles reduce the eight lanes of a row at the end of the tile.
-#include <algorithm>
-#include <cstdlib>
-
 #include <algorithm>
 #include <cstdlib>
 

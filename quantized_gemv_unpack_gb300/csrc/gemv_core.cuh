@@ -35,7 +35,7 @@ constexpr int kBlocksPerStep = 8;     // lanes per row
 constexpr int kStep = kBlocksPerStep * 128;
 constexpr int kSlots = 2;             // ring slots per decode warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr uint32_t kWaitLimit = 1u << 26;  // polls before a wait is declared lost
+constexpr uint64_t kWaitNs = 2000000000ull;  // a wait not done after 2 s is declared lost
 
 // (a & b) ^ c as one logic op
 __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
@@ -116,10 +116,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// bounded wait: false (and the device error word set) if the phase never completes
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false (and QMV_ERR_TIMEOUT in the device error word) if the
+// phase does not complete within kWaitNs. Once the error word holds a timeout,
+// later waits give up after a few hundred polls, so a launch that lost a
+// barrier ends quickly instead of timing out wait after wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t polls = 0; polls < kWaitLimit; ++polls)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t polls = 1;; ++polls) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((polls & 255u) == 0u &&
+        (global_ns() - t0 > kWaitNs || *reinterpret_cast<volatile int*>(err) == (int)QMV_ERR_TIMEOUT))
+      break;
+  }
   atomicCAS(err, 0, (int)QMV_ERR_TIMEOUT);
   return false;
 }

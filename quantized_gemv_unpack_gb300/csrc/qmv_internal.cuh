@@ -67,8 +67,13 @@ struct GemvBatch {
   GemvTask t[kMaxTasks];
 };
 
-// Launch the persistent matvec kernel for `format` (QMV_TERNARY2 / QMV_INT4)
-// over b.t[0 .. b.n_tasks); fills the tiling fields of b. M in 1..8.
+// Launch the persistent fp16-FMA matvec kernel for `format` (QMV_TERNARY2 /
+// QMV_INT4) over b.t[0 .. b.n_tasks); fills the tiling fields of b. M in 1..8.
 int launch_gemv(int format, GemvBatch& b, int M, cudaStream_t s);
+// The tensor-core matvec kernel (gemv_mma.cu), same contract, M in 1..16.
+int launch_gemv_mma(int format, GemvBatch& b, int M, cudaStream_t s);
+// From this many activation rows on, the entry points use the tensor-core
+// kernel (unless qmv_desc.flags forces one of the two).
+constexpr int kMmaMinM = 4;
 
 }  // namespace qmv

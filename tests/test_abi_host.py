@@ -27,6 +27,21 @@ def _declared_functions():
     return sorted(set(names))
 
 
+def test_header_constants_match_the_binding():
+    src = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    defines = re.findall(r"^#define\s+(QMV_[A-Z0-9_]+)\s+([0-9u*()\s]+?)\s*(?:/\*.*)?$", src, flags=re.M)
+    assert len(defines) >= 8
+    for name, expr in defines:
+        value = 1
+        for factor in re.findall(r"[0-9]+", expr):   # a number or a product of numbers
+            value *= int(factor)
+        assert getattr(q, name) == value, name
+    enums = re.findall(r"(QMV_[A-Z0-9_]+)\s*=\s*(-?[0-9]+)", src)
+    assert len(enums) >= 10
+    for name, value in enums:
+        assert getattr(q, name) == int(value), name
+
+
 def test_every_declared_symbol_is_exported(L):
     declared = _declared_functions()
     assert len(declared) >= 14
@@ -78,6 +93,9 @@ def test_run_rejects_bad_arguments_on_the_host(L):
     bad.abi_version = 99
     assert L.qmv_run_ternary(ctypes.byref(bad), 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
     assert L.qmv_run_batch(q.QMV_TERNARY2, None, 0, 1, None) == q.QMV_ERR_ARG
+    both = q.qmv_pack_desc(q.QMV_TERNARY2, 64, 256)
+    both.flags = q.QMV_FLAG_PATH_FMA | q.QMV_FLAG_PATH_MMA          # contradictory kernel choice
+    assert L.qmv_run_ternary(ctypes.byref(both), 256, 256, 4, 256, 256, 64, None) == q.QMV_ERR_ARG
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

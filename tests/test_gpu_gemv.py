@@ -1,7 +1,9 @@
 """GPU parity of the ternary and INT4 paths against the float64 oracle (through the C ABI).
 
 Packed bytes and decoded codes must be bit-identical to the oracle's; matvec
-outputs must satisfy |y - y_ref| <= 2e-3 * sum_k |w_hat_k x_k| for every row.
+outputs of both kernels (fp16-FMA and tensor-core, forced through
+qmv_desc.flags) must satisfy |y - y_ref| <= 2e-3 * sum_k |w_hat_k x_k| for every
+row.
 """
 import numpy as np
 import pytest
@@ -36,10 +38,14 @@ def _to_dev_bf16(torch, bits, dev):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
-def _pack(q, torch, dev, name, w):
+PATHS = {"fma": 1, "mma": 2}   # QMV_FLAG_PATH_FMA / QMV_FLAG_PATH_MMA
+
+
+def _pack(q, torch, dev, name, w, path=None):
     fmt, ref, pack, run = _fmt(q, name)
     N, K = w.shape
     d = q.qmv_pack_desc(fmt, N, K)
+    d.flags = PATHS[path] if path else 0
     packed = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
     pack(d, torch.from_numpy(w).to(dev), packed)
     return d, packed
@@ -87,7 +93,8 @@ def test_unpack_flags_invalid_ternary_code(env):
 @pytest.mark.parametrize("name", ["ternary", "int4"])
 @pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (33, 256), (200, 1152), (96, 5120), (40, 13824)])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 16])
-def test_matvec_matches_oracle(env, name, N, K, M):
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_matvec_matches_oracle(env, name, N, K, M, path):
     q, torch, dev = env
     from oracle.matvec import matvec_bf16x
     from quantized_gemv_unpack_gb300 import synth
@@ -95,33 +102,38 @@ def test_matvec_matches_oracle(env, name, N, K, M):
     g = synth.rng(1000 * M + N + K)
     w = synth.student_t4(g, (N, K))
     xb = synth.activations_bf16(g, (M, K))
-    d, packed = _pack(q, torch, dev, name, w)
+    d, packed = _pack(q, torch, dev, name, w, path)
     y = torch.full((M, N), float("nan"), device=dev)
     run(d, packed, _to_dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
     qq, _, s16 = ref.quantize(w)
     yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
-    _check_bound(y.cpu().numpy(), yr, B, f"{name} N={N} K={K} M={M}")
+    _check_bound(y.cpu().numpy(), yr, B, f"{name} N={N} K={K} M={M} {path}")
 
 
 @pytest.mark.parametrize("name", ["ternary", "int4"])
-def test_cfg_ternary_4096_square_full(env, name):
-    """The single-matrix workload (4096 x 4096, batch 1), every row against the oracle."""
+@pytest.mark.parametrize("M", [1, 8])
+def test_cfg_ternary_4096_square_full(env, name, M):
+    """The single-matrix workload (4096 x 4096) at batch 1 and as a verification of
+    1 + 7 draft tokens (M = 8, tensor-core kernel), every row against the oracle."""
     q, torch, dev = env
     from oracle.matvec import matvec_bf16x
     from quantized_gemv_unpack_gb300 import synth
     fmt, ref, _, run = _fmt(q, name)
     g = synth.rng(0)
     w = synth.student_t4(g, (4096, 4096))
-    xb = synth.activations_bf16(g, (1, 4096))
+    xb = synth.activations_bf16(g, (M, 4096))
     d, packed = _pack(q, torch, dev, name, w)
-    y = torch.empty((1, 4096), device=dev)
+    y = torch.empty((M, 4096), device=dev)
     run(d, packed, _to_dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
     qq, _, s16 = ref.quantize(w)
     yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
-    _check_bound(y.cpu().numpy(), yr, B, f"{name} 4096x4096")
+    _check_bound(y.cpu().numpy(), yr, B, f"{name} 4096x4096 M={M}")
 
 
-def test_activation_range_is_handled(env):
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_activation_range_is_handled(env, path):
     """Tiny and huge activations (bf16 range far outside fp16's) stay within the bound."""
     q, torch, dev = env
     from oracle.matvec import matvec_bf16x
@@ -129,7 +141,7 @@ def test_activation_range_is_handled(env):
     from quantized_gemv_unpack_gb300 import synth
     g = synth.rng(77)
     w = synth.student_t4(g, (64, 1024))
-    d, packed = _pack(q, torch, dev, "ternary", w)
+    d, packed = _pack(q, torch, dev, "ternary", w, path)
     qq, _, s16 = ternary.quantize(w)
     for scale in [1e-30, 1e-6, 1e4, 1e30]:
         x = synth.to_bf16_bits(g.standard_normal((2, 1024)).astype(np.float32) * np.float32(scale))
@@ -139,7 +151,8 @@ def test_activation_range_is_handled(env):
         _check_bound(y.cpu().numpy(), yr, B, f"x scale {scale}")
 
 
-def test_strided_activations_and_outputs(env):
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_strided_activations_and_outputs(env, path):
     q, torch, dev = env
     from oracle.matvec import matvec_bf16x
     from oracle import int4
@@ -148,7 +161,7 @@ def test_strided_activations_and_outputs(env):
     N, K, M = 48, 640, 3
     w = synth.student_t4(g, (N, K))
     xb = synth.activations_bf16(g, (M, K))
-    d, packed = _pack(q, torch, dev, "int4", w)
+    d, packed = _pack(q, torch, dev, "int4", w, path)
     xbig = torch.zeros((M, K + 64), dtype=torch.bfloat16, device=dev)
     xbig[:, :K] = _to_dev_bf16(torch, xb, dev)
     ybig = torch.full((M, N + 12), 7.0, device=dev)
@@ -161,27 +174,40 @@ def test_strided_activations_and_outputs(env):
 
 
 @pytest.mark.parametrize("name", ["ternary", "int4"])
-def test_batch_equals_separate_calls(env, name):
-    """q|k|v sharing one x in a single launch give the same bits as three launches."""
+@pytest.mark.parametrize("M", [2, 6])
+def test_batch_equals_separate_calls(env, name, M):
+    """q|k|v sharing one x in a single launch: the fp16-FMA kernel (M = 2) gives the
+    same bits as separate launches; the tensor-core kernel (M = 6), whose warps add
+    partial sums with shared-memory atomics in no fixed order, stays within the bound
+    in both forms."""
     q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
     from quantized_gemv_unpack_gb300 import synth
     fmt, ref, _, run = _fmt(q, name)
     g = synth.rng(90)
     K = 1280
     shapes = [(320, K), (64, K), (64, K), (96, 2560)]
-    mats = [_pack(q, torch, dev, name, synth.student_t4(g, s)) for s in shapes]
-    x1 = _to_dev_bf16(torch, synth.activations_bf16(g, (2, K)), dev)
-    x2 = _to_dev_bf16(torch, synth.activations_bf16(g, (2, 2560)), dev)
-    xs = [x1, x1, x1, x2]
-    ys_b = [torch.empty((2, s[0]), device=dev) for s in shapes]
-    q.qmv_run_batch(fmt, [(d, p, x, y) for (d, p), x, y in zip(mats, xs, ys_b)], 2)
-    for (d, p), x, yb in zip(mats, xs, ys_b):
+    ws = [synth.student_t4(g, s) for s in shapes]
+    mats = [_pack(q, torch, dev, name, w) for w in ws]
+    xb1 = synth.activations_bf16(g, (M, K))
+    xb2 = synth.activations_bf16(g, (M, 2560))
+    x1, x2 = _to_dev_bf16(torch, xb1, dev), _to_dev_bf16(torch, xb2, dev)
+    xs, xbs = [x1, x1, x1, x2], [xb1, xb1, xb1, xb2]
+    ys_b = [torch.empty((M, s[0]), device=dev) for s in shapes]
+    q.qmv_run_batch(fmt, [(d, p, x, y) for (d, p), x, y in zip(mats, xs, ys_b)], M)
+    for (d, p), x, xb, w, yb in zip(mats, xs, xbs, ws, ys_b):
         y = torch.empty_like(yb)
         run(d, p, x, y)
-        assert torch.equal(y, yb)
+        if M < 4:
+            assert torch.equal(y, yb)
+        else:
+            qq, _, s16 = ref.quantize(w)
+            yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
+            _check_bound(yb.cpu().numpy(), yr, B, "batched")
+            _check_bound(y.cpu().numpy(), yr, B, "separate")
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_int4_gqa_layer_set_sampled(env, M):
     """The INT4 GQA layer set (hidden 5120, 40/8 heads of 128, SwiGLU 13824) at full size, one batched
     launch as the benchmark runs it; sampled rows of every matrix against the oracle."""
@@ -218,3 +244,28 @@ def test_int4_gqa_layer_set_sampled(env, M):
         xb = xs[K].view(torch.int16).cpu().numpy().view(np.uint16)
         yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
         _check_bound(y[:, torch.from_numpy(rows).to(dev)].cpu().numpy(), yr, B, f"{name} M={M}")
+
+
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_smaller_launch_does_not_break_a_larger_one(env, path):
+    """A launch needing less shared memory between two larger ones of the same kernel
+    (the per-kernel shared-memory limit must only ever grow)."""
+    q, torch, dev = env
+    from oracle.matvec import matvec_bf16x
+    from oracle import int4
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(91)
+    M = 4
+    runs = []
+    for K in (13824, 384, 13824):
+        w = synth.student_t4(g, (24, K))
+        xb = synth.activations_bf16(g, (M, K))
+        d, packed = _pack(q, torch, dev, "int4", w, path)
+        y = torch.empty((M, 24), device=dev)
+        q.qmv_run_int4(d, packed, _to_dev_bf16(torch, xb, dev), y)
+        runs.append((w, xb, y))
+    assert q.qmv_check_status() == 0
+    for w, xb, y in runs:
+        qq, _, s16 = int4.quantize(w)
+        yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+        _check_bound(y.cpu().numpy(), yr, B, f"K={w.shape[1]}")
