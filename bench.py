@@ -57,6 +57,18 @@ def copies_for(nbytes: int) -> int:
     return max(1, -(-3 * L2_BYTES // nbytes))
 
 
+PATH_FLAGS = {"auto": 0, "fma": 1, "mma": 2}   # qmv_desc.flags: QMV_FLAG_PATH_FMA / QMV_FLAG_PATH_MMA
+MMA_MIN_M = {"int4": 1, "ternary": 3}          # the library's automatic choice of the tensor-core kernel
+
+
+def matvec_kernel(fmt: str, M: int, path: str) -> str:
+    """Name of the matvec kernel the library runs for this M and kernel choice."""
+    mma = path == "mma" or (path == "auto" and M >= MMA_MIN_M[fmt])
+    if mma:
+        return f"gemv_mma_kernel<{fmt}, n-tiles={1 if M <= 8 else 2}> (mma.sync m16n8k16)"
+    return f"gemv_kernel<{fmt}, M={min(M, 8)}> (fp16 FMA)"
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -187,8 +199,9 @@ class Stack(Workload):
     kernel = "gemv_kernel<ternary, M=1>"
     tok_s = True
 
-    def __init__(self, q, torch, dev, layers=LAYERS, seed=4):
+    def __init__(self, q, torch, dev, layers=LAYERS, seed=4, path="auto"):
         from quantized_gemv_unpack_gb300 import synth
+        self.kernel = matvec_kernel("ternary", 1, path)
         gen = synth.torch_generator(seed, dev)
         shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
         tasks, xs = [], []
@@ -198,13 +211,14 @@ class Stack(Workload):
             x_i = synth.activations_bf16_torch(gen, (1, INTER), device=dev)
             for _, N, K in shapes:
                 d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+                d.flags = PATH_FLAGS[path]
                 p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
                 w = synth.student_t4_torch(gen, (N, K), device=dev)
                 q.qmv_pack_ternary(d, w, p)
                 del w
                 y = torch.empty((1, N), dtype=torch.float32, device=dev)
                 tasks.append((d, p, x_i if K == INTER else x_h, y))
-                nbytes += d.bytes[0] + d.bytes[1] + N * 4
+                nbytes += d.bytes[0] + N * (K // 128) * 2 + N * 4
             nbytes += (HIDDEN + INTER) * 2
             xs += [x_h, x_i]
         torch.cuda.synchronize()
@@ -236,18 +250,20 @@ class Ternary4096(Workload):
     name = "ternary-4096"
     kernel = "gemv_kernel<ternary, M=1>"
 
-    def __init__(self, q, torch, dev, M=1):
+    def __init__(self, q, torch, dev, M=1, path="auto"):
         from quantized_gemv_unpack_gb300 import synth
+        self.kernel = matvec_kernel("ternary", M, path)
         gen = synth.torch_generator(0, dev)
         N = K = 4096
         self.d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+        self.d.flags = PATH_FLAGS[path]
         one = torch.empty(self.d.total_bytes, dtype=torch.uint8, device=dev)
         q.qmv_pack_ternary(self.d, synth.student_t4_torch(gen, (N, K), device=dev), one)
         self.copies = copies_for(self.d.total_bytes)
         self.ps = [one.clone() for _ in range(self.copies)]
         self.x = synth.activations_bf16_torch(gen, (M, K), device=dev)
         self.y = torch.empty((M, N), device=dev)
-        self.nbytes = self.d.bytes[0] + self.d.bytes[1] + M * K * 2 + M * N * 4
+        self.nbytes = self.d.bytes[0] + N * (K // 128) * 2 + M * K * 2 + M * N * 4
         self.M = M
         self.q = q
 
@@ -266,13 +282,15 @@ class Int4Layer(Workload):
     name = "int4-layer"
     kernel = "gemv_kernel<int4, M>"
 
-    def __init__(self, q, torch, dev, M=1):
+    def __init__(self, q, torch, dev, M=1, path="auto"):
         from quantized_gemv_unpack_gb300 import synth
+        self.kernel = matvec_kernel("int4", M, path)
         gen = synth.torch_generator(1, dev)
         shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824)
         one = []
         for _, N, K in shapes:
             d = q.qmv_pack_desc(q.QMV_INT4, N, K)
+            d.flags = PATH_FLAGS[path]
             p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
             q.qmv_pack_int4(d, synth.student_t4_torch(gen, (N, K), device=dev), p)
             one.append((d, p, N, K))
@@ -284,7 +302,7 @@ class Int4Layer(Workload):
         for c in range(self.copies):
             tasks = [(d, p if c == 0 else p.clone(), self.xs[K], y) for (d, p, N, K), y in zip(one, self.ys)]
             self.batches.append(q.Batch(q.QMV_INT4, tasks, M))
-        self.nbytes = sum(d.bytes[0] + d.bytes[1] + M * N * 4 for d, _, N, _ in one) + M * (5120 + 13824) * 2
+        self.nbytes = sum(d.bytes[0] + N * (K // 128) * 2 + M * N * 4 for d, _, N, K in one) + M * (5120 + 13824) * 2
         self.M = M
 
     def config(self):
@@ -381,11 +399,11 @@ class Moe(Workload):
 
 def make_workload(name, q, torch, dev, a):
     if name == "stack":
-        return Stack(q, torch, dev, a.layers)
+        return Stack(q, torch, dev, a.layers, path=a.path)
     if name == "ternary-4096":
-        return Ternary4096(q, torch, dev, a.M or 1)
+        return Ternary4096(q, torch, dev, a.M or 1, path=a.path)
     if name == "int4-layer":
-        return Int4Layer(q, torch, dev, a.M or 1)
+        return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
     if name == "cass-draft":
         return Cassandra(q, torch, dev, target=False)
     if name == "cass-target":
@@ -406,6 +424,8 @@ def main():
     ap.add_argument("--workload", default="stack",
                     choices=["stack", "ternary-4096", "int4-layer", "cass-draft", "cass-target", "moe"])
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
+    ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
+                    help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
@@ -514,14 +534,15 @@ def main():
         return
     peak, peak_kind = peaks()
     per_gpu = nbytes / (ms * 1e-3) / 1e9
-    launches = {"stack": 1, "ternary-4096": 1, "int4-layer": 1 if (a.M or 1) <= 8 else 2, "cass-draft": 1,
+    fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
+    launches = {"stack": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
                 "cass-target": 1, "moe": 3}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp16x2-f32" if a.workload in ("stack", "ternary-4096", "int4-layer", "moe") else "f32",
         "data": DATA,
-        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU"),
+        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU", kernel_choice=a.path),
         "pct_of_peak": 100.0 * per_gpu / peak,
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,

@@ -101,11 +101,12 @@ typedef struct {
 
 /*
  * Kernel choice of the ternary/INT4 matvec entry points (qmv_desc.flags; the
- * packers leave it 0). With 0 the library picks by M: the fp16-FMA kernel,
- * whose cost grows with M, below 4 activation rows, and the tensor-core kernel
- * (mma.sync m16n8k16, decode cost independent of M) from 4 on. Setting one bit
- * forces a kernel, for testing and tuning; both bits set is QMV_ERR_ARG.
- * Results of both kernels satisfy the same error bound.
+ * packers leave it 0). With 0 the library picks: the tensor-core kernel
+ * (mma.sync m16n8k16, decode cost independent of M) for INT4 and for ternary
+ * from M = 3, the fp16-FMA kernel (cost grows with M) for ternary at M <= 2.
+ * Setting one bit forces a kernel, for testing and tuning; both bits set is
+ * QMV_ERR_ARG. Results of both kernels satisfy the same error bound; the
+ * tensor-core kernel's are also reproducible bit for bit.
  */
 #define QMV_FLAG_PATH_FMA 1u
 #define QMV_FLAG_PATH_MMA 2u
@@ -152,7 +153,7 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
  * M in 1..QMV_MAX_M, ldx >= K, ldy >= N. Activations are rounded to fp16 after
  * a power-of-two scaling per row and chunk of K; the fp16-FMA kernel sums
  * products in fp16 pairs over 16-32 columns and in fp32 beyond, the
- * tensor-core kernel (M >= 4, see QMV_FLAG_PATH_*) in fp32 from the start. Each
+ * tensor-core kernel (see QMV_FLAG_PATH_*) in fp32 from the start. Each
  * row's error stays within the library's documented bound
  * |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|.
  */

@@ -45,7 +45,7 @@ def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
     buf = bytearray(total)
     rec = layout.records_from_rows(words, 16)
     buf[offs[0]:offs[0] + rec.nbytes] = rec.astype("<u4").tobytes()
-    s = np.asarray(s16, dtype="<u2")
+    s = layout.scale_records_from_rows(np.asarray(s16, dtype=np.uint16), K).astype("<u2")
     buf[offs[1]:offs[1] + s.nbytes] = s.tobytes()
     return bytes(buf)
 
@@ -59,7 +59,8 @@ def unpack(buf: bytes, N: int, K: int):
     for r in range(8):
         nib = ((words >> np.uint32(layout.int4_bit_pos(r))) & 0xF).astype(np.int32)
         q[:, :, r] = np.where(nib >= 8, nib - 16, nib)
-    s16 = np.frombuffer(buf, dtype="<u2", count=N * (K // 128), offset=offs[1]).reshape(N, K // 128)
+    flat_s = np.frombuffer(buf, dtype="<u2", count=layout.scale_section_bytes(N, K) // 2, offset=offs[1])
+    s16 = layout.rows_from_scale_records(flat_s, N, K)
     return q.reshape(N, K), s16.copy()
 
 

@@ -22,7 +22,12 @@ two's complement, values -7 .. 7) share one arrangement:
                       2 bits each, code bit 0 first;
                     * INT4 word of columns k0..k0+7: column r = k % 8 at bit
                       2r (r even) or 14 + 2r (r odd), 4 bits each.
-  section 1 scales: N x K/128 fp16 bit patterns, row-major.
+  section 1 scales: fp16 bit patterns in the same record order as the codes:
+                    the record of (group g, step s) is 16 rows x 8 scales
+                    (256 bytes; rows past N and blocks past K/128 hold 0), so
+                    the scale of (row n, block b) is element
+                    ((n // 16) * S + b // 8) * 128 + (n % 16) * 8 + b % 8,
+                    with S = ceil(K / 1024) steps per row.
 
 Cassandra split (see ``oracle.cassandra`` for the contents):
   0 bitmap    : N x K/32 uint32, bit (j % 32) of word j // 32 = kept(n, j)
@@ -64,12 +69,52 @@ def padded_rows(N: int) -> int:
     return (N + ROW_GROUP - 1) // ROW_GROUP * ROW_GROUP
 
 
+def steps(K: int) -> int:
+    """Steps of 1024 columns per row (the last one may hold fewer blocks)."""
+    return (K // 128 + STEP_BLOCKS - 1) // STEP_BLOCKS
+
+
+def scale_section_bytes(N: int, K: int) -> int:
+    return padded_rows(N) // ROW_GROUP * steps(K) * ROW_GROUP * STEP_BLOCKS * 2
+
+
 def ternary_sizes(N: int, K: int):
-    return [padded_rows(N) * K // 4, N * (K // 128) * 2]
+    return [padded_rows(N) * K // 4, scale_section_bytes(N, K)]
 
 
 def int4_sizes(N: int, K: int):
-    return [padded_rows(N) * K // 2, N * (K // 128) * 2]
+    return [padded_rows(N) * K // 2, scale_section_bytes(N, K)]
+
+
+def payload_bytes(N: int, K: int, bits: int) -> int:
+    """Bytes of information in a block-128 matrix: the codes and one fp16 scale per block."""
+    return N * K * bits // 8 + N * (K // 128) * 2
+
+
+def scale_index(n: int, b: int, K: int) -> int:
+    """Element index of the scale of (row n, block b) in section 1."""
+    return ((n // ROW_GROUP) * steps(K) + b // STEP_BLOCKS) * (ROW_GROUP * STEP_BLOCKS) + \
+        (n % ROW_GROUP) * STEP_BLOCKS + b % STEP_BLOCKS
+
+
+def scale_indices(N: int, K: int):
+    """scale_index for every (row, block) of an N x K matrix, as an [N][K/128] array."""
+    n = np.arange(N)[:, None]
+    b = np.arange(K // 128)[None, :]
+    return scale_index(n, b, K)
+
+
+def scale_records_from_rows(s16, K: int):
+    """fp16 scale bits [N][K/128] -> section 1 (uint16, record order, zero padded)."""
+    N = s16.shape[0]
+    out = np.zeros(scale_section_bytes(N, K) // 2, dtype=np.uint16)
+    out[scale_indices(N, K)] = s16
+    return out
+
+
+def rows_from_scale_records(flat, N: int, K: int):
+    """Inverse of scale_records_from_rows."""
+    return np.asarray(flat)[scale_indices(N, K)].astype(np.uint16)
 
 
 def records_from_rows(words, block_words: int):

@@ -55,7 +55,7 @@ def pack(q: np.ndarray, s16: np.ndarray) -> bytes:
     buf = bytearray(total)
     rec = layout.records_from_rows(words, 8)
     buf[offs[0]:offs[0] + rec.nbytes] = rec.astype("<u4").tobytes()
-    s = np.asarray(s16, dtype="<u2")
+    s = layout.scale_records_from_rows(np.asarray(s16, dtype=np.uint16), K).astype("<u2")
     buf[offs[1]:offs[1] + s.nbytes] = s.tobytes()
     return bytes(buf)
 
@@ -72,7 +72,8 @@ def unpack(buf: bytes, N: int, K: int):
     if np.any(c == 3):
         raise ValueError("invalid ternary code 11")
     q = np.where(c == 1, 1, np.where(c == 2, -1, 0)).astype(np.int8).reshape(N, K)
-    s16 = np.frombuffer(buf, dtype="<u2", count=N * (K // 128), offset=offs[1]).reshape(N, K // 128)
+    flat_s = np.frombuffer(buf, dtype="<u2", count=layout.scale_section_bytes(N, K) // 2, offset=offs[1])
+    s16 = layout.rows_from_scale_records(flat_s, N, K)
     return q, s16.copy()
 
 

@@ -182,7 +182,7 @@ int run_tasks(int format, GemvTask* tasks, int n, int M, uint64_t flags, cudaStr
   static thread_local GemvBatch b;
   const uint64_t path = flags & (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA);
   if (path == (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA)) return fail(QMV_ERR_ARG, "both QMV_FLAG_PATH_FMA and _MMA set");
-  if (path == QMV_FLAG_PATH_MMA || (path == 0 && M >= kMmaMinM)) {
+  if (path == QMV_FLAG_PATH_MMA || (path == 0 && M >= mma_min_m(format))) {
     for (int i = 0; i < n; ++i) b.t[i] = tasks[i];
     b.n_tasks = n;
     return launch_gemv_mma(format, b, M, s);
@@ -234,7 +234,7 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
   out->group = group;
   const int64_t padded = (N + 15) / 16 * 16;   // row groups of 16
   const int64_t codes = format == QMV_TERNARY2 ? padded * K / 4 : padded * K / 2;
-  const int64_t sizes[2] = {codes, N * (K / QMV_GROUP) * 2};
+  const int64_t sizes[2] = {codes, padded / 16 * scale_steps(K) * 256};
   fill_sections(out, sizes, 2);
   return QMV_OK;
 }

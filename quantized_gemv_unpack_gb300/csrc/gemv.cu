@@ -176,11 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
 
       // ---- decode this warp's rows over the chunk, one ring slot per step
+      // scales of (row, block p of each step): record order, one 128-entry record per step
       const unsigned short* sp[RQ];
+      const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;
 #pragma unroll
       for (int r = 0; r < RQ; ++r) {
         const int row = min(wrow0 + r * kGroups + g, N - 1);  // rows past N read the last row, never stored
-        sp[r] = scales + (size_t)row * KB + kc0 / 128 + p;
+        sp[r] = scales + ((size_t)(row / 16) * SS + kc0 / kStep) * 128 + (row % 16) * kBlocksPerStep + p;
       }
       float accc[RQ][MT];
 #pragma unroll
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
         for (int r = 0; r < RQ; ++r) {
           sc[r] = scn[r];
-          if ((s + 1) * kBlocksPerStep + p < nb) scn[r] = __ldg(sp[r] + (s + 1) * kBlocksPerStep);
+          if ((s + 1) * kBlocksPerStep + p < nb) scn[r] = __ldg(sp[r] + (s + 1) * 128);
         }
         const int slot = it % kSlots;
         mbar_wait(&wfull[slot], (it / kSlots) & 1u, b.err);

@@ -10,35 +10,43 @@
 //
 // Work split. Tiles are 16 rows (one row group of the packed record layout),
 // numbered across the tasks of a batch; each CTA takes a contiguous range of
-// about equal bytes. Within a CTA all 16 consumer warps work on every step
-// (1024 columns) of a tile: warp w takes 64 columns (half of block w/2), so
-// each warp issues 4 MMAs per step and n-tile, and the CTA never waits on a
-// ragged split of steps between warps. Partial sums of the 16 warps meet in
-// shared memory (fp32 atomics); the last warp to add writes y.
+// about equal bytes. A CTA runs four independent pipelines ("quads" of 4
+// warps, one warp per SM sub-partition): per task segment and activation chunk,
+// quad q takes every 4th tile from the q-th, and its warp w takes blocks 2w and
+// 2w + 1 of every 1024-column step of those tiles (16 MMAs per step and n-tile).
+// At the end of a tile's chunk the quad's four partial sums meet in shared
+// memory behind a 128-thread barrier and are added in a fixed order, so results
+// are reproducible bit for bit. The whole CTA synchronises only to restage
+// activations.
 //
-// Streaming. A producer warp copies each step of a tile into a ring slot:
-// one 1D bulk copy per row (16 per slot) into rows padded to 272 B (ternary)
-// or 544 B (INT4), so that the 8 rows one load instruction touches fall on
-// distinct shared-memory banks. Full barriers complete on the copies' byte
-// count, empty barriers on one arrival per consumer warp. All waits are
+// Streaming. Each step of a tile is one contiguous code record of the packed
+// layout (16 rows x 1024 columns, 4 KB ternary / 8 KB INT4) plus its 256-byte
+// scale record; both land in a slot of the quad's ring (4 slots ternary, 3
+// INT4) with one 1D bulk copy each. The copy duty rotates over the quad's warps:
+// after step i, warp i % 4 refills the slot of step i - 1 with step i + RING - 1
+// once the quad is done with step i - 1. Full barriers complete on the copies'
+// byte count, empty barriers on one arrival per warp of the quad. All waits are
 // bounded and record QMV_ERR_TIMEOUT in the device error word.
 //
 // MMA operand mapping. Lane (g, t) = (lane / 4, lane % 4) holds A rows g and
 // g + 8 and B column n = g. Any bijection between the MMA's k index and the
-// columns works as long as A and B agree; here lane t's A entries of the four
-// k-slices of a warp's 64 columns are the 16 columns 16t..16t+15 (pair i =
-// columns 2i, 2i+1 of that run): k-slice j takes pair 2j at k = 2t, 2t+1 and
-// pair 2j+1 at k = 2t+8, 2t+9. These 16 columns are one ternary code word (or
-// two INT4 words) of a row, decoded with the fixed shifts of gemv_core.cuh, and
-// the lane's B registers are the activation pairs of the same columns, i.e.
-// 32 contiguous bytes of staged x.
+// columns works as long as A and B agree; here lane t's A entries of the eight
+// k-slices of a 128-column block are the 32 columns 32t..32t+31 (pair p =
+// columns 32t + 2p, +1): k-slice j takes pair 2j at k = 2t, 2t+1 and pair
+// 2j+1 at k = 2t+8, 2t+9. These 32 columns are two ternary code words (or four
+// INT4 words) of a row, decoded with the fixed shifts of gemv_core.cuh, and the
+// lane's B registers are the activation pairs of the same columns, i.e. 64
+// contiguous bytes of staged x. The 8 rows one code load touches share banks
+// (rows are 256 or 512 B apart in a slot); those loads stay well below the
+// shared-memory bandwidth.
 //
-// Block scales. Each k-slice lies inside one 128-column block, so the warp's
-// four MMAs accumulate one block-half; the fp32 result is scaled by the
-// block's fp16 scale of row g / g + 8 and added to the running sum. Ternary
-// codes decode to v = 1 + q/2 (see gemv.cu); the accumulator starts at
-// -sum(x) of the block-half, leaving (1/2) sum q x, and the factor 2 is applied
-// when y is written. INT4 decodes to q exactly.
+// Block scales. Each k-slice lies inside one 128-column block, so a warp's
+// eight MMAs of a block accumulate that block; the fp32 result is scaled by
+// the block's fp16 scale of row g / g + 8 (from the scale record in the slot)
+// and added to the running sum. Ternary codes decode to v = 1 + q/2 (see
+// gemv.cu); the accumulator starts at -sum(x) of the block, leaving
+// (1/2) sum q x, and the factor 2 is applied when y is written. INT4 decodes
+// to q exactly.
 //
 // Activations are staged per chunk of K as fp16, scaled per row by a power of
 // two (largest magnitude in [2^9, 2^10) for ternary, [2^8, 2^9) for INT4), in
@@ -53,8 +61,9 @@ namespace {
 
 using namespace core;
 
-constexpr int kMmaWarps = 16;                        // consumer warps
-constexpr int kMmaThreads = (kMmaWarps + 1) * 32;    // + one producer warp
+constexpr int kMmaWarps = 16;                        // warps per CTA
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kQuads = 4;                            // independent 4-warp pipelines per CTA
 constexpr int kTileRows = 16;
 
 template <int FMT>
@@ -62,10 +71,8 @@ struct MmaGeo {
   static constexpr int WPB = Fmt<FMT>::WPB;
   static constexpr int BLOCK_BYTES = WPB * 4;
   static constexpr int ROW_STEP = kBlocksPerStep * BLOCK_BYTES;       // 256 / 512
-  static constexpr int PITCH = ROW_STEP + (FMT == QMV_TERNARY2 ? 16 : 32);  // row pitch in the ring
-  static constexpr int SLOT = kTileRows * PITCH;
-  static constexpr int RING = FMT == QMV_TERNARY2 ? 8 : 5;            // slots
-  static constexpr int NBUF = RING + 2;                               // reduction buffers
+  static constexpr int SLOT = kTileRows * ROW_STEP;                   // one record: 4 / 8 KB
+  static constexpr int RING = FMT == QMV_TERNARY2 ? 4 : 3;            // slots per quad (64 / 96 KB per CTA)
 };
 
 __device__ __forceinline__ void bar_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(kMmaWarps * 32) : "memory"); }
@@ -92,49 +99,56 @@ __device__ __forceinline__ int find_task_mma(const GemvBatch& b, int tile) {
   return lo;
 }
 
-// Walks a CTA's (tile, chunk, step) sequence in the order both the producer and
-// the consumers use: per task segment of the tile range, chunk by chunk, every
-// tile of the segment, every step of the chunk.
-struct Walk {
-  int tile, seg_begin, seg_end, ti, kc0, s, N, K, nb, nsteps;
-  __device__ bool start(const GemvBatch& b, int tile_begin, int tile_end, int KC) {
-    tile = seg_begin = tile_begin;
-    if (tile >= tile_end) return false;
+// Walks one quad's (tile, chunk, step) sequence: per task segment of the CTA's
+// tile range, chunk by chunk, the quad's tiles of the segment (every 4th, from
+// the quad's index), every step of the chunk.
+struct QuadWalk {
+  int seg_begin, seg_end, ti, K, kc0, nb, nsteps, tile, s, q;
+  __device__ bool start(const GemvBatch& b, int tile_begin, int tile_end, int KC, int quad) {
+    q = quad;
+    seg_begin = tile_begin;
+    if (seg_begin >= tile_end) return false;
     begin_segment(b, tile_end, KC);
-    return true;
+    return settle(b, tile_end, KC);
   }
   __device__ void begin_segment(const GemvBatch& b, int tile_end, int KC) {
     ti = find_task_mma(b, seg_begin);
-    N = b.t[ti].N;
     K = b.t[ti].K;
-    seg_end = min(tile_end, b.t[ti].tile0 + (N + kTileRows - 1) / kTileRows);
-    tile = seg_begin;
+    seg_end = min(tile_end, b.t[ti].tile0 + (b.t[ti].N + kTileRows - 1) / kTileRows);
     kc0 = 0;
-    s = 0;
-    nb = min(KC, K) / 128;
-    nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
+    begin_chunk(KC);
   }
-  // advance one step; returns false at the end of the CTA's range
+  __device__ void begin_chunk(int KC) {
+    nb = min(KC, K - kc0) / 128;
+    nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
+    tile = seg_begin + q;
+    s = 0;
+  }
+  // move past segment-chunks in which this quad has no tile; false at the end
+  __device__ bool settle(const GemvBatch& b, int tile_end, int KC) {
+    while (tile >= seg_end) {
+      kc0 += KC;
+      if (kc0 < K) {
+        begin_chunk(KC);
+        continue;
+      }
+      seg_begin = seg_end;
+      if (seg_begin >= tile_end) return false;
+      begin_segment(b, tile_end, KC);
+    }
+    return true;
+  }
   __device__ bool next(const GemvBatch& b, int tile_end, int KC) {
     if (++s < nsteps) return true;
     s = 0;
-    if (++tile < seg_end) return true;
-    tile = seg_begin;
-    kc0 += KC;
-    if (kc0 < K) {
-      nb = min(KC, K - kc0) / 128;
-      nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
-      return true;
-    }
-    seg_begin = seg_end;
-    if (seg_begin >= tile_end) return false;
-    begin_segment(b, tile_end, KC);
-    return true;
+    tile += kQuads;
+    return settle(b, tile_end, KC);
   }
 };
 
-// Stage columns [kc0, kc0 + kcn) of the M activation rows (MT >= M slots; the
-// rest zero) and, for ternary, -sum(x) of every 64-column half-block.
+// Stage columns [kc0, kc0 + kcn) of the M activation rows (only rows < M are
+// stored; lanes of rows past M read row 0 of their n-tile) and, for ternary,
+// -sum(x) of every 128-column block for rows < MT (0 past M).
 template <int FMT, int MT>
 __device__ void stage_mma(const uint16_t* __restrict__ x, int ldx, int kc0, int kcn, int M, int KCU, uint4* xs,
                           float* xneg, float (*s_red)[MT], float* s_xinv) {
@@ -176,31 +190,28 @@ __device__ void stage_mma(const uint16_t* __restrict__ x, int ldx, int kc0, int 
     s_xinv[tid] = exp2i(-e);
   }
   bar_consumers();
-  for (int q = tid; q < MT * nu; q += NT) {
+  for (int q = tid; q < M * nu; q += NT) {
     const int m = q / nu, u = q - m * nu;
-    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M) {
-      const float sc = s_xscale[m];
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + kc0 + u * 8);
-      uint32_t hv[4];
+    const float sc = s_xscale[m];
+    const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + kc0 + u * 8);
+    uint32_t hv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t w = word_of(raw, e);
-        hv[e] = h2u(__floats2half2_rn(bf16_to_f32(w & 0xFFFFu) * sc, bf16_to_f32(w >> 16) * sc));
-      }
-      out = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t w = word_of(raw, e);
+      hv[e] = h2u(__floats2half2_rn(bf16_to_f32(w & 0xFFFFu) * sc, bf16_to_f32(w >> 16) * sc));
     }
-    xs[(size_t)m * KCU + (u ^ (m & 7))] = out;
+    xs[(size_t)m * KCU + (u ^ (m & 7))] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
   }
   if constexpr (FMT == QMV_TERNARY2) {
     bar_consumers();
-    const int nh = kcn / 64;
-    for (int q = tid; q < nh * MT; q += NT) {
-      const int hb = q / MT, m = q - hb * MT;
+    const int nblk = kcn / 128;
+    for (int q = tid; q < nblk * MT; q += NT) {
+      const int blk = q / MT, m = q - blk * MT;
       float sum = 0.f;
+      if (m < M)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 v = xs[(size_t)m * KCU + ((hb * 8 + u) ^ (m & 7))];
+      for (int u = 0; u < 16; ++u) {
+        const uint4 v = xs[(size_t)m * KCU + ((blk * 16 + u) ^ (m & 7))];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(as_h2(word_of(v, e)));
@@ -219,205 +230,200 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
   using G = MmaGeo<FMT>;
   constexpr int MT = 8 * NT;
   constexpr bool TERN = FMT == QMV_TERNARY2;
-  constexpr int R = G::RING;
+  constexpr int R = G::RING;  // slots per quad
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* ring = smem_raw;                                              // [R][16][PITCH]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R * G::SLOT);       // [R]
-  uint64_t* empty = full + R;                                                  // [R]
-  float* red = reinterpret_cast<float*>(empty + R);                            // [NBUF][16][MT]
-  int* cnt = reinterpret_cast<int*>(red + G::NBUF * kTileRows * MT);           // [NBUF] (+pad)
+  unsigned char* ring = smem_raw;                                                          // [4][R][SLOT]
+  unsigned short* sring = reinterpret_cast<unsigned short*>(smem_raw + kQuads * R * G::SLOT);  // [4][R][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sring + kQuads * R * 128);                  // [4][R]
+  uint64_t* empty = full + kQuads * R;                                                     // [4][R]
+  float* red = reinterpret_cast<float*>(empty + kQuads * R);                               // [4][2][4][16][MT]
   const int KC = b.kc;
   const int KCU = KC / 8;
-  uint4* xs = reinterpret_cast<uint4*>(cnt + 32);                              // [MT][KCU]
-  float* xneg = reinterpret_cast<float*>(xs + (size_t)MT * KCU);               // [KC/64][MT]
+  uint4* xs = reinterpret_cast<uint4*>(red + kQuads * 2 * 4 * kTileRows * MT);             // [M][KCU]
+  float* xneg = reinterpret_cast<float*>(xs + (size_t)M * KCU);                            // [KC/128][MT]
   __shared__ float s_red[kMmaWarps][MT];
   __shared__ float s_xinv[MT];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int quad = warp >> 2, wq = warp & 3;  // quad, and position in it
   const int tile_begin = b.cta_tile[blockIdx.x];
   const int tile_end = b.cta_tile[blockIdx.x + 1];
+  unsigned char* qring = ring + (size_t)quad * R * G::SLOT;
+  unsigned short* qsring = sring + (size_t)quad * R * 128;
+  uint64_t* qfull = full + quad * R;
+  uint64_t* qempty = empty + quad * R;
+  float* qred = red + (size_t)quad * 2 * 4 * kTileRows * MT;
 
-  if (tid == 0) {
-    for (int i = 0; i < R; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kMmaWarps);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (tid < kQuads * R) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 4);
   }
-  for (int i = tid; i < G::NBUF * kTileRows * MT; i += kMmaThreads) red[i] = 0.f;
-  if (tid < G::NBUF) cnt[tid] = 0;
+  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
+  if (tile_begin >= tile_end) return;
 
-  if (warp == kMmaWarps) {
-    // ===================== producer warp: one bulk copy per row of each step
-    Walk wk;
-    if (!wk.start(b, tile_begin, tile_end, KC)) return;
-    uint32_t it = 0;
-    do {
-      const int slot = it % R;
-      if (it >= (uint32_t)R) mbar_wait(&empty[slot], ((it / R) - 1) & 1u, b.err);
-      const GemvTask& T = b.t[wk.ti];
-      const int nbk = min(kBlocksPerStep, wk.nb - wk.s * kBlocksPerStep);
-      const uint32_t row_bytes = (uint32_t)nbk * G::BLOCK_BYTES;
-      const int group = wk.tile - T.tile0;  // 16-row group within the matrix
-      const unsigned char* src = reinterpret_cast<const unsigned char*>(T.codes) +
-                                 (size_t)group * kTileRows * (T.K / F::CPW) * 4 +
-                                 (size_t)(wk.kc0 / kStep + wk.s) * kTileRows * G::ROW_STEP;
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&full[slot], kTileRows * row_bytes);
-      }
-      __syncwarp();
-      if (lane < kTileRows)
-        bulk_g2s(ring + (size_t)slot * G::SLOT + lane * G::PITCH, src + (size_t)lane * row_bytes, row_bytes,
-                 &full[slot]);
-      __syncwarp();
-      ++it;
-    } while (wk.next(b, tile_end, KC));
-    return;
+  // ---- streaming: step i of this quad's sequence lands in slot i % R of the
+  // quad's ring as two bulk copies, its code record and its scale record. The
+  // copies of step i + R - 1 are issued by warp i % 4 of the quad right after it
+  // finished step i, once the quad is done with step i - 1 (whose slot they
+  // reuse); steps 0 .. R-2 are issued up front.
+  auto issue_step = [&](const QuadWalk& w, uint32_t step) {
+    const GemvTask& T = b.t[w.ti];
+    const int nbk = min(kBlocksPerStep, w.nb - w.s * kBlocksPerStep);
+    const uint32_t bytes = (uint32_t)(kTileRows * nbk * G::BLOCK_BYTES);
+    const size_t grp = (size_t)(w.tile - T.tile0);
+    const size_t st = (size_t)(w.kc0 / kStep + w.s);
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(T.codes) + grp * kTileRows * (T.K / F::CPW) * 4 +
+                               st * kTileRows * G::ROW_STEP;
+    const int slot = step % R;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the slot precede the copy
+    mbar_arrive_expect_tx(&qfull[slot], bytes + 256u);
+    bulk_g2s(qring + (size_t)slot * G::SLOT, src, bytes, &qfull[slot]);
+    bulk_g2s(qsring + (size_t)slot * 128, T.scales + (grp * scale_steps(T.K) + st) * 128, 256u, &qfull[slot]);
+  };
+  QuadWalk pw;  // position of step it + R - 1 of this quad
+  bool pw_live = pw.start(b, tile_begin, tile_end, KC, quad);
+  for (int i = 0; i < R - 1 && pw_live; ++i) {
+    if (wq == 0 && lane == 0) issue_step(pw, i);
+    pw_live = pw.next(b, tile_end, KC);
   }
 
-  // ===================== consumer warps
   const int g = lane >> 2, t = lane & 3;
-  const int bw = warp >> 1, hw = warp & 1;  // block of the step, half of the block
   const DecodeK dk = load_decode_k(b.magic);
-  Walk wk;
-  if (!wk.start(b, tile_begin, tile_end, KC)) return;
-  uint32_t it = 0, unit = 0;
   const uint16_t* staged_x = nullptr;
   int staged_kc0 = -1, staged_K = -1;
-  float tot[NT][4];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) tot[n][e] = 0.f;
+  uint32_t it = 0, tile_no = 0;
 
-  do {
-    const GemvTask& T = b.t[wk.ti];
-    if (wk.tile == wk.seg_begin && wk.s == 0) {
-      // first step of a chunk for this segment: stage its activations
-      if (T.x != staged_x || wk.kc0 != staged_kc0 || wk.K != staged_K) {
-        stage_mma<FMT, MT>(T.x, T.ldx, wk.kc0, min(KC, wk.K - wk.kc0), M, KCU, xs, xneg, s_red, s_xinv);
+  // segment-chunks in CTA order: every warp stages each one (the barrier inside
+  // needs all 16), then the quad works through its tiles of it
+  int seg_begin = tile_begin;
+  while (seg_begin < tile_end) {
+    const int ti = find_task_mma(b, seg_begin);
+    const GemvTask& T = b.t[ti];
+    const int N = T.N, K = T.K;
+    const int seg_end = min(tile_end, T.tile0 + (N + kTileRows - 1) / kTileRows);
+    for (int kc0 = 0; kc0 < K; kc0 += KC) {
+      const int kcn = min(KC, K - kc0);
+      if (T.x != staged_x || kc0 != staged_kc0 || K != staged_K) {
+        stage_mma<FMT, MT>(T.x, T.ldx, kc0, kcn, M, KCU, xs, xneg, s_red, s_xinv);
         staged_x = T.x;
-        staged_kc0 = wk.kc0;
-        staged_K = wk.K;
+        staged_kc0 = kc0;
+        staged_K = K;
       }
-    }
-    const int nbk = min(kBlocksPerStep, wk.nb - wk.s * kBlocksPerStep);
-    const int row0 = (wk.tile - T.tile0) * kTileRows;
-    const int slot = it % R;
-    // scales of rows g, g+8 for this warp's block (rows past N read the last row; never stored)
-    unsigned short sg = 0, sg8 = 0;
-    const bool active = bw < nbk;
-    const int blk = wk.kc0 / 128 + wk.s * kBlocksPerStep + bw;
-    if (active) {
-      const int KB = wk.K / 128;
-      sg = __ldg(reinterpret_cast<const unsigned short*>(T.scales) + (size_t)min(row0 + g, wk.N - 1) * KB + blk);
-      sg8 = __ldg(reinterpret_cast<const unsigned short*>(T.scales) + (size_t)min(row0 + g + 8, wk.N - 1) * KB + blk);
-    }
-    mbar_wait(&full[slot], (it / R) & 1u, b.err);
-    if (active) {
-      const unsigned char* rows = ring + (size_t)slot * G::SLOT;
-      // this lane's 16 columns of rows g and g+8
-      uint32_t wg[TERN ? 1 : 2], wg8[TERN ? 1 : 2];
-      if constexpr (TERN) {
-        const int wo = (bw * 8 + hw * 4 + t) * 4;
-        wg[0] = *reinterpret_cast<const uint32_t*>(rows + g * G::PITCH + wo);
-        wg8[0] = *reinterpret_cast<const uint32_t*>(rows + (g + 8) * G::PITCH + wo);
-      } else {
-        const int wo = (bw * 16 + hw * 8 + 2 * t) * 4;
-        const uint2 a = *reinterpret_cast<const uint2*>(rows + g * G::PITCH + wo);
-        const uint2 c = *reinterpret_cast<const uint2*>(rows + (g + 8) * G::PITCH + wo);
-        wg[0] = a.x; wg[1] = a.y;
-        wg8[0] = c.x; wg8[1] = c.y;
-      }
-      // decode: pair p (columns 2p, 2p+1 of the lane's 16) of rows g / g+8
-      uint32_t ag[8], ag8[8];
+      const int nb = kcn / 128;
+      const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
+      for (int tile = seg_begin + quad; tile < seg_end; tile += kQuads, ++tile_no) {
+        float tot[NT][4];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        if constexpr (TERN) {
-          ag[p] = h2u(decode_pair<FMT>(wg[0], p, dk));
-          ag8[p] = h2u(decode_pair<FMT>(wg8[0], p, dk));
-        } else {
-          ag[p] = h2u(decode_pair<FMT>(wg[p >> 2], p & 3, dk));
-          ag8[p] = h2u(decode_pair<FMT>(wg8[p >> 2], p & 3, dk));
-        }
-      }
-      const float fg = __half2float(__ushort_as_half(sg));
-      const float fg8 = __half2float(__ushort_as_half(sg8));
-      const int u0 = wk.s * 128 + bw * 16 + hw * 8 + 2 * t;  // staged 16-byte unit of the lane's first 8 columns
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const int m = n * 8 + g;
-        const uint4 x0 = xs[(size_t)m * KCU + (u0 ^ g)];
-        const uint4 x1 = xs[(size_t)m * KCU + ((u0 + 1) ^ g)];
-        const uint32_t xp[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        float d[4];
-        if constexpr (TERN) {
-          const float2 xn = *reinterpret_cast<const float2*>(xneg + (size_t)(wk.s * 16 + bw * 2 + hw) * MT + n * 8 + 2 * t);
-          d[0] = xn.x; d[1] = xn.y; d[2] = xn.x; d[3] = xn.y;
-        } else {
-          d[0] = d[1] = d[2] = d[3] = 0.f;
-        }
+          for (int e = 0; e < 4; ++e) tot[n][e] = 0.f;
+        for (int s = 0; s < nsteps; ++s, ++it) {
+          const int nbk = min(kBlocksPerStep, nb - s * kBlocksPerStep);
+          const int slot = it % R;
+          mbar_wait(&qfull[slot], (it / R) & 1u, b.err);
+          const unsigned char* rows = qring + (size_t)slot * G::SLOT;
+          const int row_bytes = nbk * G::BLOCK_BYTES;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t a[4] = {ag[2 * j], ag8[2 * j], ag[2 * j + 1], ag8[2 * j + 1]};
-          mma16816(d, a, xp[2 * j], xp[2 * j + 1]);
-        }
-        tot[n][0] = fmaf(d[0], fg, tot[n][0]);
-        tot[n][1] = fmaf(d[1], fg, tot[n][1]);
-        tot[n][2] = fmaf(d[2], fg8, tot[n][2]);
-        tot[n][3] = fmaf(d[3], fg8, tot[n][3]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-    ++it;
-
-    if (wk.s == wk.nsteps - 1) {
-      // ---- end of this tile's chunk: combine the 16 warps' partial sums
-      float* buf = red + (size_t)(unit % G::NBUF) * kTileRows * MT;
+          for (int j = 0; j < 2; ++j) {
+            const int bk = wq * 2 + j;  // block of the step
+            if (bk >= nbk) break;
+            // this lane's 32 columns (32t .. 32t+31 of the block) of rows g and g+8
+            uint32_t wg[TERN ? 2 : 4], wg8[TERN ? 2 : 4];
+            if constexpr (TERN) {
+              const int wo = bk * G::BLOCK_BYTES + t * 8;
+              const uint2 a = *reinterpret_cast<const uint2*>(rows + g * row_bytes + wo);
+              const uint2 c = *reinterpret_cast<const uint2*>(rows + (g + 8) * row_bytes + wo);
+              wg[0] = a.x; wg[1] = a.y;
+              wg8[0] = c.x; wg8[1] = c.y;
+            } else {
+              const int wo = bk * G::BLOCK_BYTES + t * 16;
+              const uint4 a = *reinterpret_cast<const uint4*>(rows + g * row_bytes + wo);
+              const uint4 c = *reinterpret_cast<const uint4*>(rows + (g + 8) * row_bytes + wo);
+              wg[0] = a.x; wg[1] = a.y; wg[2] = a.z; wg[3] = a.w;
+              wg8[0] = c.x; wg8[1] = c.y; wg8[2] = c.z; wg8[3] = c.w;
+            }
+            const float fg = __half2float(__ushort_as_half(qsring[(size_t)slot * 128 + g * 8 + bk]));
+            const float fg8 = __half2float(__ushort_as_half(qsring[(size_t)slot * 128 + (g + 8) * 8 + bk]));
+            const int u0 = s * 128 + bk * 16 + 4 * t;  // staged 16-byte unit of the lane's first 8 columns
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const int c0 = n * 8 + 2 * t;
-        atomicAdd(&buf[g * MT + c0], tot[n][0]);
-        atomicAdd(&buf[g * MT + c0 + 1], tot[n][1]);
-        atomicAdd(&buf[(g + 8) * MT + c0], tot[n][2]);
-        atomicAdd(&buf[(g + 8) * MT + c0 + 1], tot[n][3]);
+            for (int n = 0; n < NT; ++n) {
+              // lanes of activation rows past M load row n*8 instead (the same address as
+              // a live lane, so no extra shared-memory traffic); their output columns are
+              // never stored
+              const int m = n * 8 + g < M ? n * 8 + g : n * 8;
+              uint32_t xp[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tot[n][e] = 0.f;
-      }
-      __syncwarp();
-      int old = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        old = atomicAdd(&cnt[unit % G::NBUF], 1);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == kMmaWarps - 1) {
-        __threadfence_block();
-        constexpr float kFactor = TERN ? 2.f : 1.f;
-        const bool first = wk.kc0 == 0;
-        for (int e = lane; e < kTileRows * MT; e += 32) {
-          const int r = e / MT, m = e - r * MT;
-          const float v = buf[e];
-          buf[e] = 0.f;
-          const int row = row0 + r;
-          if (row < wk.N && m < M) {
-            float* yp = T.y + (size_t)m * T.ldy + row;
-            const float val = kFactor * v * s_xinv[m];
-            *yp = first ? val : *yp + val;
+              for (int v = 0; v < 4; ++v) {
+                const uint4 xv = xs[(size_t)m * KCU + ((u0 + v) ^ (m & 7))];
+                xp[4 * v] = xv.x; xp[4 * v + 1] = xv.y; xp[4 * v + 2] = xv.z; xp[4 * v + 3] = xv.w;
+              }
+              float d[4];
+              if constexpr (TERN) {
+                // -sum x over the block
+                const float2 xn = *reinterpret_cast<const float2*>(xneg + (size_t)(s * 8 + bk) * MT + n * 8 + 2 * t);
+                d[0] = xn.x; d[1] = xn.y; d[2] = xn.x; d[3] = xn.y;
+              } else {
+                d[0] = d[1] = d[2] = d[3] = 0.f;
+              }
+              // k-slice kk: pairs 2kk and 2kk+1 (columns 32t + 4kk .. +3) of rows g and g+8
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                constexpr int PPW = F::PPW;
+                const int p0 = 2 * kk, p1 = 2 * kk + 1;
+                const uint32_t a[4] = {h2u(decode_pair<FMT>(wg[p0 / PPW], p0 % PPW, dk)),
+                                       h2u(decode_pair<FMT>(wg8[p0 / PPW], p0 % PPW, dk)),
+                                       h2u(decode_pair<FMT>(wg[p1 / PPW], p1 % PPW, dk)),
+                                       h2u(decode_pair<FMT>(wg8[p1 / PPW], p1 % PPW, dk))};
+                mma16816(d, a, xp[2 * kk], xp[2 * kk + 1]);
+              }
+              tot[n][0] = fmaf(d[0], fg, tot[n][0]);
+              tot[n][1] = fmaf(d[1], fg, tot[n][1]);
+              tot[n][2] = fmaf(d[2], fg8, tot[n][2]);
+              tot[n][3] = fmaf(d[3], fg8, tot[n][3]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qempty[slot]);
+          // refill: step it + R - 1 of the quad goes to the slot of step it - 1, issued by warp it % 4
+          if (pw_live) {
+            if (wq == (int)(it % 4)) {
+              if (it >= 1) mbar_wait(&qempty[(it - 1) % R], ((it - 1) / R) & 1u, b.err);
+              if (lane == 0) issue_step(pw, it + R - 1);
+            }
+            pw_live = pw.next(b, tile_end, KC);
           }
         }
-        __syncwarp();
-        if (lane == 0) cnt[unit % G::NBUF] = 0;
-        __syncwarp();
+        // ---- end of this tile's chunk: the quad's 4 partial sums, added in a fixed order
+        float* buf = qred + (size_t)(tile_no & 1) * 4 * kTileRows * MT;
+        float* mine = buf + (size_t)wq * kTileRows * MT;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int c0 = n * 8 + 2 * t;
+          *reinterpret_cast<float2*>(&mine[g * MT + c0]) = make_float2(tot[n][0], tot[n][1]);
+          *reinterpret_cast<float2*>(&mine[(g + 8) * MT + c0]) = make_float2(tot[n][2], tot[n][3]);
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(2 + quad) : "memory");
+        if (wq == (int)(tile_no & 3)) {  // the writing warp rotates
+          constexpr float kFactor = TERN ? 2.f : 1.f;
+          const int row0 = (tile - T.tile0) * kTileRows;
+          for (int e = lane; e < kTileRows * MT; e += 32) {
+            const int r = e / MT, m = e - r * MT;
+            const float v = ((buf[e] + buf[kTileRows * MT + e]) + buf[2 * kTileRows * MT + e]) + buf[3 * kTileRows * MT + e];
+            const int row = row0 + r;
+            if (row < N && m < M) {
+              float* yp = T.y + (size_t)m * T.ldy + row;
+              const float val = kFactor * v * s_xinv[m];
+              *yp = kc0 == 0 ? val : *yp + val;
+            }
+          }
+        }
       }
-      ++unit;
     }
-  } while (wk.next(b, tile_end, KC));
+    seg_begin = seg_end;
+  }
 }
 
 template <int FMT, int NT>
@@ -433,16 +439,16 @@ int launch_mma_t(GemvBatch& b, int M, cudaStream_t s) {
   }
   b.n_tiles = tiles;
   b.rows_per_tile = kTileRows;
-  const size_t ring = (size_t)G::RING * G::SLOT + 2 * G::RING * 8 + (size_t)G::NBUF * kTileRows * MT * 4 + 32 * 4;
+  const size_t ring = (size_t)kQuads * G::RING * (G::SLOT + 256 + 16) + (size_t)kQuads * 2 * 4 * kTileRows * MT * 4;
   const size_t budget = kSmemMax - ring - 2048;  // static shared memory (s_red, s_xinv, s_xscale) < 2 KB
-  // per staged column: MT fp16 values, and for ternary MT floats per 64 columns
-  const size_t per_col = (size_t)MT * 2 + (FMT == QMV_TERNARY2 ? ((size_t)MT * 4 + 63) / 64 : 0);
+  // per staged column: M fp16 values, and for ternary MT floats per 128 columns
+  const size_t per_col = (size_t)M * 2 + (FMT == QMV_TERNARY2 ? ((size_t)MT * 4 + 127) / 128 : 0);
   int kc = (int)(budget / per_col) / kStep * kStep;
   const int need = (max_K + kStep - 1) / kStep * kStep;
   if (kc > need) kc = need;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", M);
   b.kc = kc;
-  const size_t smem = ring + (size_t)MT * kc * 2 + (FMT == QMV_TERNARY2 ? (size_t)(kc / 64) * MT * 4 : 0);
+  const size_t smem = ring + (size_t)M * kc * 2 + (FMT == QMV_TERNARY2 ? (size_t)(kc / 128) * MT * 4 : 0);
   fill_magic<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");

@@ -241,12 +241,16 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
 
   stage_chunk<FMT, MT, kThreads>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
 
+  const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;  // scale records per 16-row group
   for (; u < u_end; ++u) {
     const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
     const unsigned short* sp[RQ];
 #pragma unroll
-    for (int r = 0; r < RQ; ++r)
-      sp[r] = reinterpret_cast<const unsigned short*>(scales) + (size_t)min(wrow0 + r * kGroups + g, N - 1) * KB + p;
+    for (int r = 0; r < RQ; ++r) {
+      const int row = min(wrow0 + r * kGroups + g, N - 1);
+      sp[r] = reinterpret_cast<const unsigned short*>(scales) + (size_t)(row / 16) * SS * 128 +
+              (row % 16) * kBlocksPerStep + p;
+    }
     float accc[RQ][MT];
 #pragma unroll
     for (int r = 0; r < RQ; ++r)
@@ -256,7 +260,7 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
       const bool active = s * kBlocksPerStep + p < nb;
       unsigned short sc[RQ];
 #pragma unroll
-      for (int r = 0; r < RQ; ++r) sc[r] = active ? __ldg(sp[r] + s * kBlocksPerStep) : (unsigned short)0;
+      for (int r = 0; r < RQ; ++r) sc[r] = active ? __ldg(sp[r] + s * 128) : (unsigned short)0;
       const int slot = it % kSlots;
       mbar_wait(&prod.wfull[slot], (it / kSlots) & 1u, err);
       if (active) {

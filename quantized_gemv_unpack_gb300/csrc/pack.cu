@@ -75,7 +75,7 @@ __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int6
   uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 8));
   dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
   dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-  scales[n * nb + b] = f64_to_f16_rne(s);
+  scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
 }
 
 __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
@@ -113,12 +113,14 @@ __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t
   uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 16));
 #pragma unroll
   for (int j = 0; j < 4; ++j) dst[j] = make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
-  scales[n * nb + b] = f64_to_f16_rne(s);
+  scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
 }
 
-// One thread per (row, block): decodes the block's columns to int8.
-__global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, int64_t N, int64_t K,
-                              int8_t* __restrict__ q, int* err) {
+// One thread per (row, block): decodes the block's columns to int8 and copies
+// its scale to row-major order.
+__global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                              int64_t N, int64_t K, int8_t* __restrict__ q, uint16_t* __restrict__ scales_out,
+                              int* err) {
   const int64_t KB = K / 128;
   const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= N * KB) return;
@@ -145,6 +147,7 @@ __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, in
     }
   }
   if (bad) atomicCAS(err, 0, QMV_ERR_CORRUPT);
+  if (scales_out) scales_out[n * KB + b] = scales[scale_index(n, b, scale_steps(K))];
 }
 
 int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, void* stream) {
@@ -160,11 +163,16 @@ int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, 
   const int64_t grid = (blocks + threads - 1) / threads;
   if (grid > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "matrix too large for one pack launch");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // zero the padding rows of the last row group and the alignment padding after
-  // each section, so every byte is determined
+  // zero the padding rows of the last row group, the padding scales (rows past
+  // N, blocks past K/128) and the alignment padding after each section, so
+  // every byte is determined
   if (desc->N % 16) {
     cudaError_t e = cudaMemsetAsync(base + desc->off[0], 0, (size_t)desc->bytes[0], s);
     if (e != cudaSuccess) return cuda_fail(e, "zero padding rows");
+  }
+  if (desc->N % 16 || (desc->K / 128) % 8) {
+    cudaError_t e = cudaMemsetAsync(base + desc->off[1], 0, (size_t)desc->bytes[1], s);
+    if (e != cudaSuccess) return cuda_fail(e, "zero padding scales");
   }
   const int64_t gaps[2][2] = {{desc->off[0] + desc->bytes[0], desc->off[1]},
                               {desc->off[1] + desc->bytes[1], desc->total_bytes}};
@@ -214,13 +222,10 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
   const int64_t nblk = desc->N * (desc->K / 128);
   const int threads = 128;
   unpack_kernel<<<(unsigned)((nblk + threads - 1) / threads), threads, 0, s>>>(
-      format, reinterpret_cast<const uint32_t*>(base + desc->off[0]), desc->N, desc->K, q, err);
+      format, reinterpret_cast<const uint32_t*>(base + desc->off[0]),
+      reinterpret_cast<const uint16_t*>(base + desc->off[1]), desc->N, desc->K, q, scales, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
-  if (scales) {
-    e = cudaMemcpyAsync(scales, base + desc->off[1], desc->bytes[1], cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "copy scales");
-  }
   return QMV_OK;
 }
 

@@ -23,6 +23,14 @@ int sm_count();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Ternary/INT4 scale section: fp16 scales in the record order of the codes, one
+// record of 16 rows x 8 blocks (256 bytes) per (16-row group, 1024-column step),
+// rows past N and blocks past K/128 zero. scale_steps(K) steps per row.
+__host__ __device__ __forceinline__ int64_t scale_steps(int64_t K) { return (K / 128 + 7) / 8; }
+__host__ __device__ __forceinline__ int64_t scale_index(int64_t n, int64_t b, int64_t steps) {
+  return ((n / 16) * steps + b / 8) * 128 + (n % 16) * 8 + b % 8;
+}
+
 int check_desc(const qmv_desc* d, int format);
 // Raise the kernel's dynamic shared memory limit when needed and return how
 // many CTAs of `threads` threads fit on one SM (cached per kernel and size).
@@ -73,7 +81,10 @@ int launch_gemv(int format, GemvBatch& b, int M, cudaStream_t s);
 // The tensor-core matvec kernel (gemv_mma.cu), same contract, M in 1..16.
 int launch_gemv_mma(int format, GemvBatch& b, int M, cudaStream_t s);
 // From this many activation rows on, the entry points use the tensor-core
-// kernel (unless qmv_desc.flags forces one of the two).
-constexpr int kMmaMinM = 4;
+// kernel (unless qmv_desc.flags forces one of the two): the fp16-FMA kernel's
+// cost grows with M; measured on the INT4 layer set and the ternary stack it is
+// ahead only for ternary at M <= 2 (INT4 decodes more words per weight byte, so
+// the tensor-core kernel wins there from M = 1).
+inline int mma_min_m(int format) { return format == QMV_INT4 ? 1 : 3; }
 
 }  // namespace qmv

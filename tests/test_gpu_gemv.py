@@ -176,10 +176,8 @@ def test_strided_activations_and_outputs(env, path):
 @pytest.mark.parametrize("name", ["ternary", "int4"])
 @pytest.mark.parametrize("M", [2, 6])
 def test_batch_equals_separate_calls(env, name, M):
-    """q|k|v sharing one x in a single launch: the fp16-FMA kernel (M = 2) gives the
-    same bits as separate launches; the tensor-core kernel (M = 6), whose warps add
-    partial sums with shared-memory atomics in no fixed order, stays within the bound
-    in both forms."""
+    """q|k|v sharing one x in a single launch give the same bits as separate launches,
+    on the fp16-FMA kernel (ternary, M = 2) and the tensor-core kernel (INT4, and M = 6)."""
     q, torch, dev = env
     from oracle.matvec import matvec_bf16x
     from quantized_gemv_unpack_gb300 import synth
@@ -198,13 +196,10 @@ def test_batch_equals_separate_calls(env, name, M):
     for (d, p), x, xb, w, yb in zip(mats, xs, xbs, ws, ys_b):
         y = torch.empty_like(yb)
         run(d, p, x, y)
-        if M < 4:
-            assert torch.equal(y, yb)
-        else:
-            qq, _, s16 = ref.quantize(w)
-            yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
-            _check_bound(yb.cpu().numpy(), yr, B, "batched")
-            _check_bound(y.cpu().numpy(), yr, B, "separate")
+        assert torch.equal(y, yb)   # both kernels add partial sums in a fixed order
+        qq, _, s16 = ref.quantize(w)
+        yr, B = matvec_bf16x(ref.dequant(qq, s16), xb)
+        _check_bound(yb.cpu().numpy(), yr, B, "batched")
 
 
 @pytest.mark.parametrize("M", [1, 4, 8])

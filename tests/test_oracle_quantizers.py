@@ -164,9 +164,28 @@ def test_ternary_pack_roundtrip_and_size():
     iq = bpw["iq2_xxs"]
     assert iq["data_bits"] + iq["scale_bits"] / iq["block"] == iq["bits_per_weight"]
     t = bpw["this_library"]["ternary_block128_fp16"]
-    assert sum(layout.ternary_sizes(32, 384)) * 8 / (32 * 384) == t["bits_per_weight"]
+    assert layout.payload_bytes(32, 384, 2) * 8 / (32 * 384) == t["bits_per_weight"]
     t = bpw["this_library"]["int4_group128_fp16"]
-    assert sum(layout.int4_sizes(32, 384)) * 8 / (32 * 384) == t["bits_per_weight"]
+    assert layout.payload_bytes(32, 384, 4) * 8 / (32 * 384) == t["bits_per_weight"]
+    # the stored sections add nothing to that payload when rows come in groups of 16 and K in steps of 1024
+    assert sum(layout.ternary_sizes(32, 2048)) == layout.payload_bytes(32, 2048, 2)
+    assert sum(layout.int4_sizes(48, 5120)) == layout.payload_bytes(48, 5120, 4)
+
+
+def test_scale_records_hand_placed():
+    """Section 1 stores scales in the order of the code records: (row 17, block 9) of a
+    20 x 1280 matrix is row 1 of group 1, block 1 of step 1; with 2 steps per row that is
+    element ((1 * 2 + 1) * 128) + 1 * 8 + 1 = 393."""
+    assert layout.scale_index(17, 9, 1280) == 393
+    s16 = np.zeros((20, 10), np.uint16)
+    s16[17, 9] = 0x3C00
+    flat = layout.scale_records_from_rows(s16, 1280)
+    assert flat.size == 2 * 2 * 128 and np.flatnonzero(flat).tolist() == [393]
+    assert np.array_equal(layout.rows_from_scale_records(flat, 20, 1280), s16)
+    q = np.zeros((20, 1280), np.int8)
+    buf = ternary.pack(q, s16)
+    offs, _ = layout.sections(layout.ternary_sizes(20, 1280))
+    assert buf[offs[1] + 2 * 393:offs[1] + 2 * 393 + 2] == bytes([0x00, 0x3C])
 
 
 def test_ternary_unpack_rejects_code_11():
