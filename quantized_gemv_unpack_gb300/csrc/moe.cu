@@ -4,9 +4,9 @@
 // Three launches on the caller's stream, all state in the caller's workspace:
 //  1. route: one warp per token takes the top-k of its E logits (equal logits:
 //     lower expert first) by k rounds of a warp arg-max, softmax over the k
-//     selected logits in fp32; one thread then orders the (token, expert)
-//     pairs by expert and token and lists each active expert once (a slot),
-//     and the CTA zeroes y.
+//     selected logits in fp32; then one thread per expert counts its
+//     (token, expert) pairs, a block scan orders the pairs by expert and token
+//     and lists each active expert once (a slot), and the CTA zeroes y.
 //  2. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
 //     tile of 64 rows of the [gate; up] matrix) into equal contiguous ranges;
 //     a CTA stages the slot's token rows of x (gathered) once per slot and
@@ -129,27 +129,50 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const MoeArgs a) {
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // pairs ordered by expert, then token: one slot per active expert
-    int ns = 0, np = 0;
-    for (int e = 0; e < a.E; ++e) {
-      int first = np;
-      for (int t = 0; t < a.M; ++t)
-        for (int r = 0; r < a.topk; ++r)
-          if (s_exp[t][r] == e) {
-            pair_token[np] = t;
-            pair_prob[np] = s_prob[t][r];
-            ++np;
-          }
-      if (np > first) {
-        slot_expert[ns] = e;
-        slot_first[ns] = first;
-        slot_count[ns] = np - first;
-        ++ns;
-      }
+  // pairs ordered by expert, then token: thread e counts expert e's pairs, a
+  // block-wide exclusive scan of (pairs, active) gives its first pair and its
+  // slot, and it writes its pairs in token order
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < a.E)
+    for (int t = 0; t < a.M; ++t)
+      for (int r = 0; r < a.topk; ++r) cnt += s_exp[t][r] == e;
+  const int act = cnt > 0;
+  int pc = cnt, sc = act;  // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int up = __shfl_up_sync(0xffffffffu, pc, o), us = __shfl_up_sync(0xffffffffu, sc, o);
+    if (lane >= o) {
+      pc += up;
+      sc += us;
     }
-    *n_slots = ns;
   }
+  __shared__ int s_wp[8], s_ws[8];
+  if (lane == 31) {
+    s_wp[warp] = pc;
+    s_ws[warp] = sc;
+  }
+  __syncthreads();
+  int base_p = 0, base_s = 0;
+  for (int w = 0; w < warp; ++w) {
+    base_p += s_wp[w];
+    base_s += s_ws[w];
+  }
+  if (act) {
+    int np = base_p + pc - cnt;
+    const int slot = base_s + sc - 1;
+    slot_expert[slot] = e;
+    slot_first[slot] = np;
+    slot_count[slot] = cnt;
+    for (int t = 0; t < a.M; ++t)
+      for (int r = 0; r < a.topk; ++r)
+        if (s_exp[t][r] == e) {
+          pair_token[np] = t;
+          pair_prob[np] = s_prob[t][r];
+          ++np;
+        }
+  }
+  if (threadIdx.x == 255) *n_slots = base_s + sc;
   for (int i = threadIdx.x; i < a.M * a.H; i += blockDim.x) a.y[(size_t)(i / a.H) * a.ldy + i % a.H] = 0.f;
 }
 
