@@ -52,6 +52,26 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def captured_traffic(key: str, scale: float = 1.0):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu captures
+    (profiles/traffic.json), or None when there is no capture for this workload or the
+    kernel's source files have changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    entry = json.load(open(p))["workloads"].get(key)
+    if entry is None:
+        return None
+    h = hashlib.sha256()
+    for f in entry["sources"]:
+        h.update(os.path.basename(f).encode())
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if h.hexdigest() != entry["sources_sha256"]:
+        return None
+    return entry["bytes"] * scale
+
+
 def copies_for(nbytes: int) -> int:
     """Rotation depth so consecutive steps never find their weights in L2."""
     return max(1, -(-3 * L2_BYTES // nbytes))
@@ -193,6 +213,10 @@ class Workload:
         """(device inputs, device outputs) that an end-to-end step copies from / to pinned host memory."""
         raise NotImplementedError
 
+    def traffic(self):
+        """Captured DRAM bytes per launch of the dominant kernel (None if not captured or stale)."""
+        return None
+
 
 class Stack(Workload):
     name = "stack"
@@ -204,11 +228,18 @@ class Stack(Workload):
         self.kernel = matvec_kernel("ternary", 1, path)
         gen = synth.torch_generator(seed, dev)
         shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
-        tasks, xs = [], []
+        # all activations in one buffer and all outputs in another, so an end-to-end
+        # step is one host-to-device and one device-to-host copy
+        self.x_all = torch.empty((layers, HIDDEN + INTER), dtype=torch.bfloat16, device=dev)
+        self.y_all = torch.empty(layers * sum(N for _, N, _ in shapes), dtype=torch.float32, device=dev)
+        tasks = []
         nbytes = 0
-        for _ in range(layers):
-            x_h = synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)
-            x_i = synth.activations_bf16_torch(gen, (1, INTER), device=dev)
+        y_off = 0
+        for layer in range(layers):
+            x_h = self.x_all[layer, :HIDDEN]
+            x_i = self.x_all[layer, HIDDEN:]
+            x_h.copy_(synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)[0])
+            x_i.copy_(synth.activations_bf16_torch(gen, (1, INTER), device=dev)[0])
             for _, N, K in shapes:
                 d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
                 d.flags = PATH_FLAGS[path]
@@ -216,16 +247,16 @@ class Stack(Workload):
                 w = synth.student_t4_torch(gen, (N, K), device=dev)
                 q.qmv_pack_ternary(d, w, p)
                 del w
-                y = torch.empty((1, N), dtype=torch.float32, device=dev)
-                tasks.append((d, p, x_i if K == INTER else x_h, y))
+                y = self.y_all[y_off:y_off + N].view(1, N)
+                y_off += N
+                tasks.append((d, p, (x_i if K == INTER else x_h).view(1, K), y))
                 nbytes += d.bytes[0] + N * (K // 128) * 2 + N * 4
             nbytes += (HIDDEN + INTER) * 2
-            xs += [x_h, x_i]
         torch.cuda.synchronize()
         self.batch = q.Batch(q.QMV_TERNARY2, tasks, 1)
-        self.xs, self.ys = xs, [t[3] for t in tasks]
         self.nbytes = nbytes
         self.layers = layers
+        self.path = path
 
     @staticmethod
     def stack_config(layers):
@@ -243,7 +274,11 @@ class Stack(Workload):
         self.batch.run(stream)
 
     def host_io(self):
-        return self.xs, self.ys
+        return [self.x_all], [self.y_all]
+
+    def traffic(self):
+        # the capture is of 3 layers, scaled to 60 there; traffic grows with the layer count
+        return captured_traffic("stack", self.layers / LAYERS) if self.path == "auto" else None
 
 
 class Ternary4096(Workload):
@@ -266,6 +301,7 @@ class Ternary4096(Workload):
         self.nbytes = self.d.bytes[0] + N * (K // 128) * 2 + M * K * 2 + M * N * 4
         self.M = M
         self.q = q
+        self.path = path
 
     def config(self):
         return {"workload": f"ternary GEMV 4096 x 4096, block-128 absmean + fp16 scales, M={self.M}", "M": self.M,
@@ -276,6 +312,9 @@ class Ternary4096(Workload):
 
     def host_io(self):
         return [self.x], [self.y]
+
+    def traffic(self):
+        return captured_traffic(f"ternary-4096 M={self.M}") if self.path == "auto" else None
 
 
 class Int4Layer(Workload):
@@ -304,6 +343,7 @@ class Int4Layer(Workload):
             self.batches.append(q.Batch(q.QMV_INT4, tasks, M))
         self.nbytes = sum(d.bytes[0] + N * (K // 128) * 2 + M * N * 4 for d, _, N, K in one) + M * (5120 + 13824) * 2
         self.M = M
+        self.path = path
 
     def config(self):
         return {"workload": f"INT4 GQA layer set (hidden 5120, 40/8 heads x 128, SwiGLU 13824), group-128 absmax/7, "
@@ -315,6 +355,9 @@ class Int4Layer(Workload):
 
     def host_io(self):
         return list(self.xs.values()), self.ys
+
+    def traffic(self):
+        return captured_traffic(f"int4-layer M={self.M}") if self.path == "auto" else None
 
 
 class Cassandra(Workload):
@@ -353,10 +396,13 @@ class Cassandra(Workload):
     def host_io(self):
         return [self.x], [self.y]
 
+    def traffic(self):
+        return captured_traffic(f"{self.name} M={self.M}")
+
 
 class Moe(Workload):
     name = "moe"
-    kernel = "moe_expert_kernel"
+    kernel = "moe_route_kernel + moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
 
     def __init__(self, q, torch, dev, M=1, n_logits=64):
         from quantized_gemv_unpack_gb300 import synth
@@ -395,6 +441,11 @@ class Moe(Workload):
 
     def host_io(self):
         return [self.x], [self.y]
+
+    def traffic(self):
+        # the capture is of the first timed step (logits draw 0): scale to the mean active expert count
+        t = captured_traffic(f"moe M={self.M}")
+        return None if t is None else t * (sum(self.active) / len(self.active)) / self.active[0]
 
 
 def make_workload(name, q, torch, dev, a):
@@ -546,7 +597,7 @@ def main():
         "pct_of_peak": 100.0 * per_gpu / peak,
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
-                     "traffic": None, "kernel": wl.kernel, "peak_kind": f"copy bandwidth, {peak_kind}"},
+                     "traffic": wl.traffic(), "kernel": wl.kernel, "peak_kind": f"copy bandwidth, {peak_kind}"},
         "e2e": {"value": e2e_bytes / (ms_e2e * 1e-3) / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": launches * a.steps,
