@@ -363,31 +363,42 @@ class Int4Layer(Workload):
 class Cassandra(Workload):
     kernel = "cass_kernel"
 
-    def __init__(self, q, torch, dev, target=False):
+    def __init__(self, q, torch, dev, target=False, mx=False):
         from quantized_gemv_unpack_gb300 import synth
         g = synth.rng(2)
         N, K = 14336, 4096
         W = synth.to_bf16_bits(synth.student_t4(g, (N, K)))
         X, _ = synth.calibration_bf16(g, 128, K)
-        self.d, buf = q.cass_pack_host(W, X)
+        self.d, buf = (q.cass_mx_pack_host if mx else q.cass_pack_host)(W, X)
+        self.mx = mx
+        if mx:
+            self.kernel = "cassmx_kernel"
         one = torch.from_numpy(buf).to(dev)
         self.copies = copies_for(self.d.total_bytes)
         self.ps = [one] + [one.clone() for _ in range(self.copies - 1)]
         self.M = 5 if target else 1
         self.x = torch.from_numpy(synth.activations_bf16(g, (self.M, K)).view("int16")).to(dev).view(torch.bfloat16)
         self.y = torch.empty((self.M, N), device=dev)
-        spec = sum(self.d.bytes[i] for i in range(5))
-        verif = self.d.bytes[5] + self.d.bytes[6]
+        n_spec = 4 if mx else 5
+        spec = sum(self.d.bytes[i] for i in range(n_spec))
+        verif = sum(self.d.bytes[i] for i in range(n_spec, 7 if not mx else 6))
         self.nbytes = (spec + (verif if target else 0)) + self.M * K * 2 + self.M * N * 4
         self.target = target
         self.fn = q.cass_reconstruct if target else q.cass_decode_draft
-        self.name = "cass-target" if target else "cass-draft"
+        self.name = ("cass-mx-" if mx else "cass-") + ("target" if target else "draft")
         self.dense = N * K * 2
+        self.spec_bytes, self.verif_bytes = spec, verif
 
     def config(self):
-        path = "target (speculation + verification, bit-exact rebuild)" if self.target else "draft (speculation only)"
-        return {"workload": f"Cassandra split 14336 x 4096 MLP matrix, {path}, M={self.M}", "M": self.M, "seed": 2,
-                "dense_bf16_bytes": self.dense, "n_symbols": self.d.n_symbols,
+        if self.mx:
+            path = ("target (speculation + verification, MX values)" if self.target else "draft (speculation only)")
+            name = "Cassandra-2 (MX shared exponent, groups of 32)"
+        else:
+            path = "target (speculation + verification, bit-exact rebuild)" if self.target else "draft (speculation only)"
+            name = "Cassandra split"
+        return {"workload": f"{name} 14336 x 4096 MLP matrix, {path}, M={self.M}", "M": self.M, "seed": 2,
+                "dense_bf16_bytes": self.dense, "speculation_bytes": self.spec_bytes,
+                "verification_bytes": self.verif_bytes, "n_symbols": self.d.n_symbols,
                 "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
 
     def step(self, i, stream):
@@ -455,10 +466,8 @@ def make_workload(name, q, torch, dev, a):
         return Ternary4096(q, torch, dev, a.M or 1, path=a.path)
     if name == "int4-layer":
         return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
-    if name == "cass-draft":
-        return Cassandra(q, torch, dev, target=False)
-    if name == "cass-target":
-        return Cassandra(q, torch, dev, target=True)
+    if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
+        return Cassandra(q, torch, dev, target=name.endswith("target"), mx="-mx-" in name)
     if name == "moe":
         return Moe(q, torch, dev, a.M or 1)
     raise SystemExit(f"unknown workload {name}")
@@ -473,7 +482,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
     ap.add_argument("--workload", default="stack",
-                    choices=["stack", "ternary-4096", "int4-layer", "cass-draft", "cass-target", "moe"])
+                    choices=["stack", "ternary-4096", "int4-layer", "cass-draft", "cass-target", "cass-mx-draft",
+                             "cass-mx-target", "moe"])
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
@@ -586,8 +596,8 @@ def main():
     peak, peak_kind = peaks()
     per_gpu = nbytes / (ms * 1e-3) / 1e9
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
-    launches = {"stack": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
-                "cass-target": 1, "moe": 3}[a.workload]
+    launches = {"stack": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1, "cass-target": 1,
+                "cass-mx-draft": 1, "cass-mx-target": 1, "moe": 3}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

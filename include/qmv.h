@@ -54,7 +54,8 @@ typedef enum {
 typedef enum {
   QMV_TERNARY2 = 1,          /* block-128 absmean ternary, 2 bits + fp16 scale per block */
   QMV_INT4 = 2,              /* group-128 absmax/7 INT4, 4 bits + fp16 scale per group */
-  QMV_CASS = 3               /* Cassandra lossless bf16 split (speculation + verification) */
+  QMV_CASS = 3,              /* Cassandra lossless bf16 split (speculation + verification) */
+  QMV_CASS_MX = 4            /* Cassandra-2: the split with MX shared exponents (slightly lossy) */
 } qmv_format;
 
 /*
@@ -74,8 +75,11 @@ typedef enum {
  *             01 = +1, 10 = -1 (11 is invalid). INT4 word of columns
  *             k0..k0+7: column r = k%8 at bit 2r (r even) or 14+2r (r odd);
  *             4-bit two's complement, -7..7.
- *   1 scales: N x K/128 fp16, row-major: ternary fp16(mean|w| + 1e-8), INT4
- *             fp16(max|w| / 7) of each block/group.
+ *   1 scales: fp16 scales (ternary fp16(mean|w| + 1e-8), INT4 fp16(max|w| / 7)
+ *             of each block/group) in the record order of the codes: record
+ *             (group g, step s) is 16 rows x 8 scales, 256 bytes, so the scale
+ *             of (row n, block b) is element ((n/16)*S + b/8)*128 + (n%16)*8 + b%8
+ *             with S = ceil(K/1024); rows past N and blocks past K/128 hold 0.
  * QMV_CASS ("Cassandra", sections 3.1-3.3):
  *   0 bitmap : N x K/32 uint32, bit j%32 of word j/32 set = value (n, j) kept
  *   1 signmant: N x K/16 uint32, nibble i = S<<3 | (M>>4) of the i-th kept value
@@ -86,12 +90,27 @@ typedef enum {
  *   5 pruned : N x K/2 uint16, raw bf16 bits of the pruned values
  *   6 mlo    : N x K/16 uint32, nibble i = M & 0xF of the i-th kept value
  *   Sections 0-4 are the speculation data, 5-6 the verification data.
+ * QMV_CASS_MX ("Cassandra", section 3.3, the MX route of Cassandra-2): the
+ * same Wanda bitmap and raw pruned values; the kept values of a row, in column
+ * order, form groups of 32 that share their largest exponent g (e = max(E, 1)
+ * per value); each value's 8-bit significand (128 + M, or M when E = 0) is
+ * shifted right by g - e (truncated), giving A. Draft value (-1)^S * (A >> 4)
+ * * 2^(g - 130), target value (-1)^S * A * 2^(g - 134): exact where e = g,
+ * below the original by less than 2^(g - 134) elsewhere. K % 64 == 0.
+ *   0 bitmap : N x K/32 uint32 (as QMV_CASS)
+ *   1 gexp   : N x K/64 uint8, shared exponent of each group
+ *   2 signs  : N x K/64 uint32, bit i%32 of word i/32 = S of kept value i
+ *   3 dnib   : N x K/16 uint32, nibble i = A >> 4 of kept value i
+ *   4 lnib   : N x K/16 uint32, nibble i = A & 15 of kept value i
+ *   5 pruned : N x K/2 uint16, raw bf16 bits of the pruned values
+ *   Sections 0-3 are the speculation data (3.625 bits per weight), 4-5 the
+ *   verification data. group = 32.
  */
 typedef struct {
   uint32_t abi_version;      /* QMV_ABI_VERSION */
   uint32_t format;           /* qmv_format */
   int64_t N, K;
-  int32_t group;             /* 128 for ternary/INT4, 0 for Cassandra */
+  int32_t group;             /* 128 for ternary/INT4, 0 for Cassandra, 32 for Cassandra-2 (MX) */
   int32_t n_symbols;         /* Cassandra: number of codebook entries in use */
   int64_t off[QMV_MAX_SECTIONS];
   int64_t bytes[QMV_MAX_SECTIONS];
@@ -123,8 +142,9 @@ typedef struct {
 /*
  * Layout math only (host, no GPU needed): fill `out` for a ternary or INT4
  * matrix of N x K with the given group (must be 128). K must be a positive
- * multiple of 128 and N positive. Returns QMV_ERR_UNSUPPORTED for QMV_CASS,
- * whose stream length depends on the data (use cass_pack_host).
+ * multiple of 128 and N positive; for QMV_CASS_MX (group 32) K must be a
+ * multiple of 64. Returns QMV_ERR_UNSUPPORTED for QMV_CASS, whose stream
+ * length depends on the data (use cass_pack_host).
  */
 int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out);
 
@@ -186,9 +206,21 @@ int cass_pack_host(const uint16_t* w_bf16, int64_t N, int64_t K, const uint16_t*
                    int64_t R, qmv_desc* desc, void* out, int64_t out_capacity);
 
 /*
+ * Cassandra-2 offline transform on the host ("Cassandra", 3.3, MX route): the
+ * same Wanda selection as cass_pack_host, then the QMV_CASS_MX layout (see
+ * qmv_desc). K must be a positive multiple of 64, N, R > 0. The layout depends
+ * only on N and K (desc equals qmv_pack_desc(QMV_CASS_MX, N, K, 32)). With out
+ * == NULL only `desc` is filled; otherwise out_capacity >= desc->total_bytes.
+ * out is host memory.
+ */
+int cass_mx_pack_host(const uint16_t* w_bf16, int64_t N, int64_t K, const uint16_t* calib_bf16,
+                      int64_t R, qmv_desc* desc, void* out, int64_t out_capacity);
+
+/*
  * Draft path ("Cassandra", 3.2 figure b): reads only the speculation sections
- * (0-4) of the packed buffer. Draft weight = S<<15 | E<<7 | m_hi<<4 for kept
- * values (low mantissa bits zero-filled), +0 for pruned values.
+ * of the packed buffer (QMV_CASS: 0-4, QMV_CASS_MX: 0-3). Draft weight = S<<15 |
+ * E<<7 | m_hi<<4 for kept values (low mantissa bits zero-filled; QMV_CASS_MX:
+ * the sign and A >> 4 at the group exponent), +0 for pruned values.
  * y: device fp32 [M][ldy] or NULL; w_draft: device bf16 bits [N][K] or NULL
  * (materialised draft weights, for bit-exact checks). M in 1..8.
  * A unary rank beyond the codebook or a bitmap row without exactly K/2 kept
@@ -199,8 +231,9 @@ int cass_decode_draft(const qmv_desc* desc, const void* packed, const void* x_bf
 
 /*
  * Target path ("Cassandra", 3.2 figure c): reads speculation and verification
- * data and rebuilds every original bf16 bit before the matvec. Same argument
- * rules as cass_decode_draft; w_out receives the reconstructed bf16 bits.
+ * data and rebuilds every original bf16 bit before the matvec (QMV_CASS_MX:
+ * the MX target values, see qmv_desc). Same argument rules as
+ * cass_decode_draft; w_out receives the reconstructed bf16 bits.
  */
 int cass_reconstruct(const qmv_desc* desc, const void* packed, const void* x_bf16, int M,
                      int64_t ldx, float* y, int64_t ldy, uint16_t* w_out, void* stream);

@@ -22,12 +22,12 @@ QMV_MAX_BATCH = 448
 
 QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
 QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
-QMV_TERNARY2, QMV_INT4, QMV_CASS = 1, 2, 3
+QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX = 1, 2, 3, 4
 QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-FMA or the tensor-core matvec kernel
 
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
-           "qmv_run_int4", "qmv_run_batch", "cass_pack_host", "cass_decode_draft", "cass_reconstruct",
+           "qmv_run_int4", "qmv_run_batch", "cass_pack_host", "cass_mx_pack_host", "cass_decode_draft", "cass_reconstruct",
            "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
 
 
@@ -68,6 +68,7 @@ _SIGS = {
     "qmv_run_int4": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P]),
     "qmv_run_batch": (_I32, [_I32, ctypes.POINTER(qmv_task), _I32, _I32, _P]),
     "cass_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
+    "cass_mx_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
     "cass_decode_draft": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "cass_reconstruct": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
@@ -191,19 +192,27 @@ def qmv_run_batch(format: int, tasks, M: int, stream=None):
 
 # ----------------------------------------------------------------------------- Cassandra
 
-def cass_pack_host(w_bf16_bits, calib_bf16_bits):
-    """Host packer: NumPy uint16 [N][K] weights and [R][K] calibration rows -> (desc, uint8 buffer)."""
+def _host_pack(fn, w_bf16_bits, calib_bf16_bits):
     import numpy as np
     w = np.ascontiguousarray(w_bf16_bits, dtype=np.uint16)
     c = np.ascontiguousarray(calib_bf16_bits, dtype=np.uint16)
     N, K = w.shape
     R = c.shape[0]
     d = qmv_desc()
-    _check(lib().cass_pack_host(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), None, 0))
+    _check(fn(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), None, 0))
     out = np.zeros(d.total_bytes, dtype=np.uint8)
-    _check(lib().cass_pack_host(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), out.ctypes.data,
-                                out.nbytes))
+    _check(fn(w.ctypes.data, N, K, c.ctypes.data, R, ctypes.byref(d), out.ctypes.data, out.nbytes))
     return d, out
+
+
+def cass_pack_host(w_bf16_bits, calib_bf16_bits):
+    """Host packer: NumPy uint16 [N][K] weights and [R][K] calibration rows -> (desc, uint8 buffer)."""
+    return _host_pack(lib().cass_pack_host, w_bf16_bits, calib_bf16_bits)
+
+
+def cass_mx_pack_host(w_bf16_bits, calib_bf16_bits):
+    """Cassandra-2 (MX) host packer, same arguments and result as cass_pack_host."""
+    return _host_pack(lib().cass_mx_pack_host, w_bf16_bits, calib_bf16_bits)
 
 
 def cass_decode_draft(desc: qmv_desc, packed, x, y=None, w_draft=None, stream=None):

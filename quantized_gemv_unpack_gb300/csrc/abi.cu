@@ -223,6 +223,20 @@ const char* qmv_last_error(void) { return g_msg; }
 int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out) {
   if (!out) return fail(QMV_ERR_ARG, "out is NULL");
   if (format == QMV_CASS) return fail(QMV_ERR_UNSUPPORTED, "Cassandra layouts depend on the data; use cass_pack_host");
+  if (format == QMV_CASS_MX) {
+    // Cassandra-2 (MX): fixed layout, see qmv.h
+    if (group != 32) return fail(QMV_ERR_ARG, "group must be 32 for QMV_CASS_MX");
+    if (N <= 0 || K <= 0 || K % 64) return fail(QMV_ERR_ARG, "N=%lld K=%lld (K must be a positive multiple of 64)", (long long)N, (long long)K);
+    memset(out, 0, sizeof(*out));
+    out->abi_version = QMV_ABI_VERSION;
+    out->format = (uint32_t)format;
+    out->N = N;
+    out->K = K;
+    out->group = group;
+    const int64_t sizes[6] = {N * K / 8, N * K / 64, N * K / 16, N * K / 4, N * K / 4, N * K};
+    fill_sections(out, sizes, 6);
+    return QMV_OK;
+  }
   if (format != QMV_TERNARY2 && format != QMV_INT4) return fail(QMV_ERR_ARG, "unknown format %d", format);
   if (group != QMV_GROUP) return fail(QMV_ERR_ARG, "group must be 128");
   if (N <= 0 || K <= 0 || K % QMV_GROUP) return fail(QMV_ERR_ARG, "N=%lld K=%lld (K must be a positive multiple of 128)", (long long)N, (long long)K);

@@ -221,6 +221,144 @@ __global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs
   }
 }
 
+// ----------------------------------------------------------------------------- Cassandra-2 (MX)
+
+struct CassMxArgs {
+  const uint32_t* bitmap;    // [N][K/32]
+  const uint8_t* gexp;       // [N][K/64]
+  const uint32_t* signs;     // [N][K/64]
+  const uint32_t* dnib;      // [N][K/16]
+  const uint32_t* lnib;      // [N][K/16]
+  const uint16_t* pruned;    // [N][K/2]
+  const uint16_t* x;         // bf16 [M][ldx]
+  float* y;                  // [M][ldy] or null
+  uint16_t* w_out;           // [N][K] or null
+  int N, K, ldx, ldy;
+  int* err;
+};
+
+__host__ __device__ inline size_t cassmx_per_warp(size_t K, bool target) {
+  // bitmap, signs, dnib, group scales (+ target: lnib, pruned)
+  return (K / 8 + K / 16 + K / 4 + K / 16 + (target ? K / 4 + K : 0) + 15) / 16 * 16;
+}
+
+// One warp per row, rows strided over a persistent grid. The row's sections are
+// staged in shared memory together with one fp32 scale per group of 32 kept
+// values (2^(g - 134) for the target, 2^(g - 130) for the draft), so a kept
+// column's value is one nibble lookup times its group's scale: no per-value
+// exponent decode. Lane l owns column 32*i + l of each bitmap word, as in the
+// Cassandra-1 kernel; values are exact in fp32 and in bf16.
+template <int MT, bool TARGET>
+__global__ void __launch_bounds__(kCassWarpsMax * 32) cassmx_kernel(const CassMxArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int K = a.K;
+  const int K2 = K / 2;
+  const int KG = K / 64;
+  const int nwarps = blockDim.x / 32;
+  float* xs = reinterpret_cast<float*>(smem);  // [MT][K] fp32
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  unsigned char* wb = smem + (size_t)MT * K * 4 + (size_t)warp * cassmx_per_warp(K, TARGET);
+  uint32_t* bm_s = reinterpret_cast<uint32_t*>(wb);
+  uint32_t* sg_s = bm_s + K / 32;
+  uint32_t* dn_s = sg_s + K / 64;
+  float* sc_s = reinterpret_cast<float*>(dn_s + K / 16);
+  uint32_t* ln_s = reinterpret_cast<uint32_t*>(sc_s + KG);
+  uint16_t* pr_s = reinterpret_cast<uint16_t*>(ln_s + (TARGET ? K / 16 : 0));
+
+  for (int m = 0; m < MT; ++m)
+    for (int j = threadIdx.x; j < K; j += blockDim.x)
+      xs[(size_t)m * K + j] = __uint_as_float((uint32_t)a.x[(size_t)m * a.ldx + j] << 16);
+  __syncthreads();
+
+  const uint32_t below = lanemask_lt();
+  const int gw = blockIdx.x * nwarps + warp;
+  const int stride = gridDim.x * nwarps;
+  for (int n = gw; n < a.N; n += stride) {
+    for (int i = lane; i < K / 32; i += 32) bm_s[i] = __ldg(a.bitmap + (size_t)n * (K / 32) + i);
+    for (int i = lane; i < K / 64; i += 32) sg_s[i] = __ldg(a.signs + (size_t)n * (K / 64) + i);
+    for (int i = lane; i < K / 16; i += 32) dn_s[i] = __ldg(a.dnib + (size_t)n * (K / 16) + i);
+    for (int i = lane; i < KG; i += 32)
+      sc_s[i] = ldexpf(1.f, (int)__ldg(a.gexp + (size_t)n * KG + i) - (TARGET ? 134 : 130));
+    if (TARGET) {
+      for (int i = lane; i < K / 16; i += 32) ln_s[i] = __ldg(a.lnib + (size_t)n * (K / 16) + i);
+      for (int i = lane; i < K2; i += 32) pr_s[i] = __ldg(a.pruned + (size_t)n * K2 + i);
+    }
+    __syncwarp();
+
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    uint16_t* wrow = a.w_out ? a.w_out + (size_t)n * K : nullptr;
+    int kbase = 0;
+    bool bad = false;
+    for (int it = 0; it < K / 32; ++it) {
+      const uint32_t word = bm_s[it];
+      const int j = it * 32 + lane;
+      const int kidx = kbase + __popc(word & below);
+      float v = 0.f;
+      if ((word >> lane) & 1u) {
+        if (kidx < K2) {
+          const uint32_t sh = (kidx & 7) * 4;
+          uint32_t mag = (dn_s[kidx >> 3] >> sh) & 0xFu;
+          if (TARGET) mag = (mag << 4) | ((ln_s[kidx >> 3] >> sh) & 0xFu);
+          v = (float)mag * sc_s[kidx >> 5];
+          if ((sg_s[kidx >> 5] >> (kidx & 31)) & 1u) v = -v;
+        } else {
+          bad = true;
+        }
+      } else if (TARGET) {
+        const int pidx = j - kidx;
+        if (pidx < K2) v = __uint_as_float((uint32_t)pr_s[pidx] << 16);
+        else bad = true;
+      }
+      if (wrow) wrow[j] = (uint16_t)(__float_as_uint(v) >> 16);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[m] = fmaf(v, xs[(size_t)m * K + j], acc[m]);
+      kbase += __popc(word);
+    }
+    if (bad || (kbase != K2 && lane == 0)) flag(a.err);
+    if (a.y) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float t = acc[m];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) a.y[(size_t)m * a.ldy + n] = t;
+      }
+    }
+    __syncwarp();  // the staged row buffers are reused by the next row
+  }
+}
+
+template <bool TARGET>
+int launch_cassmx(const CassMxArgs& a, int M, cudaStream_t s) {
+  const size_t K = a.K;
+  const size_t per_warp = cassmx_per_warp(K, TARGET);
+  const size_t fixed = (size_t)M * K * 4;
+  const size_t cap = 227 * 1024 - 1024;
+  if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%zu with M=%d does not fit shared memory", K, M);
+  const int warps = (int)std::min<size_t>(kCassWarpsMax, (cap - fixed) / per_warp);
+  const size_t smem = fixed + per_warp * warps;
+  const void* kern = nullptr;
+  switch (M) {
+#define QMV_CASSMX_CASE(m) \
+  case m: kern = (const void*)cassmx_kernel<m, TARGET>; break;
+    QMV_CASSMX_CASE(1) QMV_CASSMX_CASE(2) QMV_CASSMX_CASE(3) QMV_CASSMX_CASE(4)
+    QMV_CASSMX_CASE(5) QMV_CASSMX_CASE(6) QMV_CASSMX_CASE(7) QMV_CASSMX_CASE(8)
+#undef QMV_CASSMX_CASE
+    default: return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
+  }
+  int per_sm = 0;
+  int rc = kernel_fit(kern, warps * 32, smem, &per_sm);
+  if (rc) return rc;
+  const int grid = std::max(1, std::min(sm_count() * per_sm, (a.N + warps - 1) / warps));
+  void* args[] = {const_cast<CassMxArgs*>(&a)};
+  cudaError_t e = cudaLaunchKernel(kern, grid, warps * 32, args, smem, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cassandra-2 launch");
+  return QMV_OK;
+}
+
 template <bool TARGET>
 int launch_cass(const CassArgs& a, int M, cudaStream_t s) {
   const size_t K = a.K;
@@ -265,9 +403,25 @@ int check_cass_desc(const qmv_desc* d) {
   return QMV_OK;
 }
 
+int check_cassmx_desc(const qmv_desc* d) {
+  if (d->N <= 0 || d->K <= 0 || d->K % 64 || d->group != 32)
+    return fail(QMV_ERR_ARG, "N=%lld K=%lld group=%d (K must be a multiple of 64, group 32)", (long long)d->N,
+                (long long)d->K, d->group);
+  if (d->N > INT32_MAX / 2 || d->K > (1 << 20)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
+  qmv_desc ref;
+  qmv_pack_desc(QMV_CASS_MX, d->N, d->K, 32, &ref);
+  for (int i = 0; i < 6; ++i)
+    if (ref.off[i] != d->off[i] || ref.bytes[i] != d->bytes[i])
+      return fail(QMV_ERR_ARG, "Cassandra-2 section %d does not match the layout of a %lld x %lld matrix", i,
+                  (long long)d->N, (long long)d->K);
+  return QMV_OK;
+}
+
 int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, int M, int64_t ldx, float* y,
              int64_t ldy, uint16_t* w_out, void* stream) {
-  int rc = check_cass_desc(d);
+  if (!d) return fail(QMV_ERR_ARG, "desc is NULL");
+  const bool mx = d->abi_version == QMV_ABI_VERSION && d->format == QMV_CASS_MX;
+  int rc = mx ? check_cassmx_desc(d) : check_cass_desc(d);
   if (rc) return rc;
   if (M < 1 || M > 8) return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
   if (!packed || !x) return fail(QMV_ERR_ARG, "NULL packed or x");
@@ -278,6 +432,25 @@ int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, 
   int* err = device_error_word();
   if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   const char* b = static_cast<const char*>(packed);
+  if (mx) {
+    CassMxArgs m;
+    m.bitmap = reinterpret_cast<const uint32_t*>(b + d->off[0]);
+    m.gexp = reinterpret_cast<const uint8_t*>(b + d->off[1]);
+    m.signs = reinterpret_cast<const uint32_t*>(b + d->off[2]);
+    m.dnib = reinterpret_cast<const uint32_t*>(b + d->off[3]);
+    m.lnib = reinterpret_cast<const uint32_t*>(b + d->off[4]);
+    m.pruned = reinterpret_cast<const uint16_t*>(b + d->off[5]);
+    m.x = static_cast<const uint16_t*>(x);
+    m.y = y;
+    m.w_out = w_out;
+    m.N = (int)d->N;
+    m.K = (int)d->K;
+    m.ldx = (int)ldx;
+    m.ldy = (int)(y ? ldy : 0);
+    m.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return target ? launch_cassmx<true>(m, M, s) : launch_cassmx<false>(m, M, s);
+  }
   CassArgs a;
   a.bitmap = reinterpret_cast<const uint32_t*>(b + d->off[0]);
   a.signmant = reinterpret_cast<const uint32_t*>(b + d->off[1]);
@@ -300,9 +473,45 @@ int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, 
   return target ? launch_cass<true>(a, M, s) : launch_cass<false>(a, M, s);
 }
 
-// ----------------------------------------------------------------------------- host packer
+// ----------------------------------------------------------------------------- host packers
 
 int64_t align256(int64_t n) { return (n + 255) / 256 * 256; }
+
+double bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// Wanda value pruning ("Cassandra", 3.2 step 1): keep[n*K + j] = 1 for the K/2
+// largest |w| * ||X[:,j]||_2 of each row (float64; column norms summed over the
+// calibration rows in order; equal scores keep the lower column; NaN scores as
+// +inf).
+void wanda_select(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X, int64_t R, std::vector<uint8_t>& keep) {
+  const int64_t K2 = K / 2;
+  std::vector<double> c(K, 0.0);
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t j = 0; j < K; ++j) {
+      const double v = bf16_value(X[r * K + j]);
+      c[j] += v * v;
+    }
+  for (int64_t j = 0; j < K; ++j) c[j] = std::sqrt(c[j]);
+  keep.assign((size_t)(N * K), 0);
+  std::vector<double> score(K);
+  std::vector<int32_t> idx(K);
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = w + n * K;
+    for (int64_t j = 0; j < K; ++j) {
+      const double s = std::fabs(bf16_value(row[j])) * c[j];
+      score[j] = std::isnan(s) ? HUGE_VAL : s;
+      idx[j] = (int32_t)j;
+    }
+    auto before = [&](int32_t a2, int32_t b2) { return score[a2] > score[b2] || (score[a2] == score[b2] && a2 < b2); };
+    std::nth_element(idx.begin(), idx.begin() + K2, idx.end(), before);
+    for (int64_t i = 0; i < K2; ++i) keep[n * K + idx[i]] = 1;
+  }
+}
 
 }  // namespace
 }  // namespace qmv
@@ -317,37 +526,13 @@ int cass_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X, i
   if (N <= 0 || K <= 0 || K % 32 || R <= 0) return fail(QMV_ERR_ARG, "N=%lld K=%lld R=%lld (K must be a positive multiple of 32)", (long long)N, (long long)K, (long long)R);
   if (N > INT32_MAX / 2 || K > (1 << 20)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
   const int64_t K2 = K / 2;
-  auto value = [](uint16_t b) {
-    uint32_t u = (uint32_t)b << 16;
-    float f;
-    memcpy(&f, &u, 4);
-    return (double)f;
-  };
-  // 1. calibration column norms, rows summed in order
-  std::vector<double> c(K, 0.0);
-  for (int64_t r = 0; r < R; ++r)
-    for (int64_t j = 0; j < K; ++j) {
-      const double v = value(X[r * K + j]);
-      c[j] += v * v;
-    }
-  for (int64_t j = 0; j < K; ++j) c[j] = std::sqrt(c[j]);
-
-  // 2. Wanda selection per row + 3. split of the kept values
-  std::vector<uint8_t> keep((size_t)(N * K), 0);
+  // 1.-2. Wanda selection per row, then 3. the exponents of the kept values
+  std::vector<uint8_t> keep;
+  wanda_select(w, N, K, X, R, keep);
   std::vector<uint8_t> ek((size_t)(N * K2));
   std::vector<int64_t> hist(256, 0);
-  std::vector<double> score(K);
-  std::vector<int32_t> idx(K);
   for (int64_t n = 0; n < N; ++n) {
     const uint16_t* row = w + n * K;
-    for (int64_t j = 0; j < K; ++j) {
-      const double s = std::fabs(value(row[j])) * c[j];
-      score[j] = std::isnan(s) ? HUGE_VAL : s;
-      idx[j] = (int32_t)j;
-    }
-    auto before = [&](int32_t a2, int32_t b2) { return score[a2] > score[b2] || (score[a2] == score[b2] && a2 < b2); };
-    std::nth_element(idx.begin(), idx.begin() + K2, idx.end(), before);
-    for (int64_t i = 0; i < K2; ++i) keep[n * K + idx[i]] = 1;
     int64_t k = 0;
     for (int64_t j = 0; j < K; ++j)
       if (keep[n * K + j]) {
@@ -420,6 +605,60 @@ int cass_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X, i
         ++k;
       } else {
         pruned[n * K2 + p++] = v;
+      }
+    }
+  }
+  return QMV_OK;
+}
+
+int cass_mx_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X, int64_t R, qmv_desc* desc,
+                      void* out, int64_t out_capacity) {
+  if (!w || !X || !desc) return fail(QMV_ERR_ARG, "NULL w, calibration or desc");
+  if (N <= 0 || K <= 0 || K % 64 || R <= 0)
+    return fail(QMV_ERR_ARG, "N=%lld K=%lld R=%lld (K must be a positive multiple of 64)", (long long)N, (long long)K, (long long)R);
+  if (N > INT32_MAX / 2 || K > (1 << 20)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
+  int rc = qmv_pack_desc(QMV_CASS_MX, N, K, 32, desc);
+  if (rc) return rc;
+  if (!out) return QMV_OK;
+  if (out_capacity < desc->total_bytes) return fail(QMV_ERR_ARG, "out_capacity %lld < %lld", (long long)out_capacity, (long long)desc->total_bytes);
+  std::vector<uint8_t> keep;
+  wanda_select(w, N, K, X, R, keep);
+  unsigned char* o = static_cast<unsigned char*>(out);
+  memset(o, 0, (size_t)desc->total_bytes);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(o + desc->off[0]);
+  uint8_t* gexp = o + desc->off[1];
+  uint32_t* signs = reinterpret_cast<uint32_t*>(o + desc->off[2]);
+  uint32_t* dnib = reinterpret_cast<uint32_t*>(o + desc->off[3]);
+  uint32_t* lnib = reinterpret_cast<uint32_t*>(o + desc->off[4]);
+  uint16_t* pruned = reinterpret_cast<uint16_t*>(o + desc->off[5]);
+  const int64_t K2 = K / 2;
+  std::vector<uint16_t> kept((size_t)K2);
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t* row = w + n * K;
+    int64_t k = 0, p = 0;
+    for (int64_t j = 0; j < K; ++j) {
+      if (keep[n * K + j]) {
+        bitmap[n * (K / 32) + j / 32] |= 1u << (j % 32);
+        kept[k++] = row[j];
+      } else {
+        pruned[n * K2 + p++] = row[j];
+      }
+    }
+    // groups of 32 kept values share their largest exponent e = max(E, 1)
+    for (int64_t g0 = 0; g0 < K2; g0 += 32) {
+      int gmax = 1;
+      for (int64_t i = g0; i < g0 + 32; ++i) gmax = std::max(gmax, std::max((int)((kept[i] >> 7) & 0xFF), 1));
+      gexp[n * (K2 / 32) + g0 / 32] = (uint8_t)gmax;
+      for (int64_t i = g0; i < g0 + 32; ++i) {
+        const uint32_t v = kept[i], E = (v >> 7) & 0xFF, Mt = v & 0x7F;
+        const int e = std::max((int)E, 1);
+        const uint32_t sig = (E ? 128u : 0u) + Mt;
+        const int sh = gmax - e;
+        const uint32_t A = sh < 8 ? sig >> sh : 0u;
+        const int64_t ki = n * K2 + i;
+        signs[ki / 32] |= (v >> 15) << (ki % 32);
+        dnib[ki / 8] |= (A >> 4) << ((ki % 8) * 4);
+        lnib[ki / 8] |= (A & 15u) << ((ki % 8) * 4);
       }
     }
   }
