@@ -281,6 +281,74 @@ class Stack(Workload):
         return captured_traffic("stack", self.layers / LAYERS) if self.path == "auto" else None
 
 
+class SparseStack(Workload):
+    """The 27B-shaped stack with a seeded 16.5 % of its 16 x 128 tiles zero, in the flagged
+    sparse ternary format (about 1.78 bits per weight)."""
+    name = "stack-sparse"
+    kernel = "sparse_kernel<M=1> (fp16 FMA over stored tiles)"
+    tok_s = True
+    ZERO = 0.165
+
+    def __init__(self, q, torch, dev, layers=LAYERS, seed=4):
+        from quantized_gemv_unpack_gb300 import synth
+        gen = synth.torch_generator(seed, dev)
+        shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
+        self.x_all = torch.empty((layers, HIDDEN + INTER), dtype=torch.bfloat16, device=dev)
+        self.y_all = torch.empty(layers * sum(N for _, N, _ in shapes), dtype=torch.float32, device=dev)
+        tasks, self.bufs = [], []
+        nbytes = dense_bytes = 0
+        y_off = 0
+        for layer in range(layers):
+            x_h, x_i = self.x_all[layer, :HIDDEN], self.x_all[layer, HIDDEN:]
+            x_h.copy_(synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)[0])
+            x_i.copy_(synth.activations_bf16_torch(gen, (1, INTER), device=dev)[0])
+            for _, N, K in shapes:
+                w = synth.student_t4_torch(gen, (N, K), device=dev)
+                zero = torch.rand((N // 16, K // 128), generator=gen, device=dev) < self.ZERO
+                w.view(N // 16, 16, K // 128, 128).mul_((~zero).to(w.dtype)[:, None, :, None])
+                dense = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
+                p = torch.empty(dense.total_bytes, dtype=torch.uint8, device=dev)
+                q.qmv_pack_ternary(dense, w, p)
+                del w
+                d, host = q.qmv_sparse_pack_host(dense, p.cpu().numpy())
+                del p
+                sp = torch.from_numpy(host).to(dev)
+                self.bufs.append((d, sp))
+                y = self.y_all[y_off:y_off + N].view(1, N)
+                y_off += N
+                tasks.append((d, sp, (x_i if K == INTER else x_h).view(1, K), y))
+                nbytes += d.total_bytes + N * 4
+                dense_bytes += dense.bytes[0] + N * (K // 128) * 2
+            nbytes += (HIDDEN + INTER) * 2
+        torch.cuda.synchronize()
+        self.batch = q.Batch(q.QMV_TERNARY2_SPARSE, tasks, 1)
+        self.nbytes = nbytes
+        self.dense_bytes = dense_bytes
+        self.layers = layers
+
+    def config(self):
+        c = Stack.stack_config(self.layers)
+        c["workload"] = c["workload"].replace("block-128 absmean ternary", "flagged sparse block-128 ternary "
+                                              f"({100 * self.ZERO:.1f} % of 16 x 128 tiles zero)")
+        c["zero_tile_fraction"] = self.ZERO
+        c["bits_per_weight"] = 8 * (self.nbytes - self.layers * (HIDDEN + INTER) * 2) / sum(
+            N * K for _, N, K in synth_shapes()) / self.layers
+        c["dense_ternary_bytes"] = self.dense_bytes
+        c["l2"] = "inputs larger than L2 (about 6.1 GB of packed weights per step; no flush needed)"
+        return c
+
+    def step(self, i, stream):
+        self.batch.run(stream)
+
+    def host_io(self):
+        return [self.x_all], [self.y_all]
+
+
+def synth_shapes():
+    from quantized_gemv_unpack_gb300 import synth
+    return synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
+
+
 class Ternary4096(Workload):
     name = "ternary-4096"
     kernel = "gemv_kernel<ternary, M=1>"
@@ -462,6 +530,8 @@ class Moe(Workload):
 def make_workload(name, q, torch, dev, a):
     if name == "stack":
         return Stack(q, torch, dev, a.layers, path=a.path)
+    if name == "stack-sparse":
+        return SparseStack(q, torch, dev, a.layers)
     if name == "ternary-4096":
         return Ternary4096(q, torch, dev, a.M or 1, path=a.path)
     if name == "int4-layer":
@@ -482,8 +552,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
     ap.add_argument("--workload", default="stack",
-                    choices=["stack", "ternary-4096", "int4-layer", "cass-draft", "cass-target", "cass-mx-draft",
-                             "cass-mx-target", "moe"])
+                    choices=["stack", "stack-sparse", "ternary-4096", "int4-layer", "cass-draft", "cass-target",
+                             "cass-mx-draft", "cass-mx-target", "moe"])
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
@@ -596,12 +666,12 @@ def main():
     peak, peak_kind = peaks()
     per_gpu = nbytes / (ms * 1e-3) / 1e9
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
-    launches = {"stack": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1, "cass-target": 1,
-                "cass-mx-draft": 1, "cass-mx-target": 1, "moe": 3}[a.workload]
+    launches = {"stack": 1, "stack-sparse": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
+                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "moe": 3}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp16x2-f32" if a.workload in ("stack", "ternary-4096", "int4-layer", "moe") else "f32",
+        "dtype": "fp16x2-f32" if a.workload in ("stack", "stack-sparse", "ternary-4096", "int4-layer", "moe") else "f32",
         "data": DATA,
         "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU", kernel_choice=a.path),
         "pct_of_peak": 100.0 * per_gpu / peak,

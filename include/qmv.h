@@ -55,7 +55,8 @@ typedef enum {
   QMV_TERNARY2 = 1,          /* block-128 absmean ternary, 2 bits + fp16 scale per block */
   QMV_INT4 = 2,              /* group-128 absmax/7 INT4, 4 bits + fp16 scale per group */
   QMV_CASS = 3,              /* Cassandra lossless bf16 split (speculation + verification) */
-  QMV_CASS_MX = 4            /* Cassandra-2: the split with MX shared exponents (slightly lossy) */
+  QMV_CASS_MX = 4,           /* Cassandra-2: the split with MX shared exponents (slightly lossy) */
+  QMV_TERNARY2_SPARSE = 5    /* ternary with flagged all-zero tiles left out */
 } qmv_format;
 
 /*
@@ -105,6 +106,18 @@ typedef enum {
  *   5 pruned : N x K/2 uint16, raw bf16 bits of the pruned values
  *   Sections 0-3 are the speculation data (3.625 bits per weight), 4-5 the
  *   verification data. group = 32.
+ * QMV_TERNARY2_SPARSE ("Ternary Bonsai 2", 1.1, 3.3-3.4, 5.5: all-zero blocks
+ * flagged with scale 1, structured block sparsity with a sparse index): the
+ * codes of QMV_TERNARY2, in which every tile of 16 rows (one row group) x 128
+ * columns whose codes are all zero is flagged and left out. n_symbols holds T,
+ * the number of stored tiles; G = ceil(N/16), KB = K/128.
+ *   0 tilemap  : G x ceil(KB/32) uint32, bit b%32 of word b/32 = tile (g, b) stored
+ *   1 tilestart: G+1 uint32, stored tiles before group g (last = T)
+ *   2 tileblock: T uint16, block index of each stored tile, group by group
+ *   3 codes    : per group, records of up to 8 stored tiles in column order; a
+ *                record is the 16 rows' code blocks of its tiles, row after row
+ *   4 scales   : T x 16 fp16, the 16 rows' scales of each stored tile (1.0 for
+ *                an all-zero block of a real row, 0 for padding rows)
  */
 typedef struct {
   uint32_t abi_version;      /* QMV_ABI_VERSION */
@@ -161,6 +174,16 @@ int qmv_pack_ternary(const qmv_desc* desc, const float* w, void* packed, void* s
 int qmv_pack_int4(const qmv_desc* desc, const float* w, void* packed, void* stream);
 
 /*
+ * Flagged sparse ternary packer (host): dense_packed is a host copy of a
+ * QMV_TERNARY2 buffer described by `dense`; desc receives the
+ * QMV_TERNARY2_SPARSE layout (out == NULL: size query only) and out (host,
+ * out_capacity >= desc->total_bytes) the buffer: tiles whose 16 x 128 codes are
+ * all zero are left out, an all-zero block of a stored tile gets the scale 1.0.
+ */
+int qmv_sparse_pack_host(const qmv_desc* dense, const void* dense_packed, qmv_desc* desc, void* out,
+                         int64_t out_capacity);
+
+/*
  * Decode a packed ternary or INT4 matrix to int8 q [N][K] (device) and its
  * fp16 scales [N][K/128] (device, nullable) for bit-exact checks. A ternary
  * code 11 writes 0 to q and sets QMV_ERR_CORRUPT in the device error word.
@@ -170,7 +193,9 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
 /*
  * y[m][n] = sum_k W_hat[n][k] * x[m][k] for m < M, n < N, where W_hat = q * scale
  * of the packed ternary (qmv_run_ternary) or INT4 (qmv_run_int4) matrix.
- * M in 1..QMV_MAX_M, ldx >= K, ldy >= N. Activations are rounded to fp16 after
+ * M in 1..QMV_MAX_M, ldx >= K, ldy >= N (a QMV_TERNARY2_SPARSE desc in
+ * qmv_run_ternary or qmv_run_batch: M in 1..8, the fp16-FMA kernel, and K must
+ * fit shared memory in one piece). Activations are rounded to fp16 after
  * a power-of-two scaling per row and chunk of K; the fp16-FMA kernel sums
  * products in fp16 pairs over 16-32 columns and in fp32 beyond, the
  * tensor-core kernel (see QMV_FLAG_PATH_*) in fp32 from the start. Each

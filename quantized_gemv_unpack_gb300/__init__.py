@@ -22,12 +22,12 @@ QMV_MAX_BATCH = 448
 
 QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
 QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
-QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX = 1, 2, 3, 4
+QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX, QMV_TERNARY2_SPARSE = 1, 2, 3, 4, 5
 QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-FMA or the tensor-core matvec kernel
 
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
-           "qmv_run_int4", "qmv_run_batch", "cass_pack_host", "cass_mx_pack_host", "cass_decode_draft", "cass_reconstruct",
+           "qmv_run_int4", "qmv_run_batch", "qmv_sparse_pack_host", "cass_pack_host", "cass_mx_pack_host", "cass_decode_draft", "cass_reconstruct",
            "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
 
 
@@ -69,6 +69,7 @@ _SIGS = {
     "qmv_run_batch": (_I32, [_I32, ctypes.POINTER(qmv_task), _I32, _I32, _P]),
     "cass_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
     "cass_mx_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
+    "qmv_sparse_pack_host": (_I32, [_DESC, _P, _DESC, _P, _I64]),
     "cass_decode_draft": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "cass_reconstruct": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
@@ -208,6 +209,19 @@ def _host_pack(fn, w_bf16_bits, calib_bf16_bits):
 def cass_pack_host(w_bf16_bits, calib_bf16_bits):
     """Host packer: NumPy uint16 [N][K] weights and [R][K] calibration rows -> (desc, uint8 buffer)."""
     return _host_pack(lib().cass_pack_host, w_bf16_bits, calib_bf16_bits)
+
+
+def qmv_sparse_pack_host(dense_desc: qmv_desc, dense_packed_host):
+    """Flagged sparse ternary packer: a host copy (NumPy uint8) of a dense ternary buffer ->
+    (desc, uint8 buffer) with all-zero 16 x 128 tiles left out."""
+    import numpy as np
+    src = np.ascontiguousarray(dense_packed_host, dtype=np.uint8)
+    d = qmv_desc()
+    _check(lib().qmv_sparse_pack_host(ctypes.byref(dense_desc), src.ctypes.data, ctypes.byref(d), None, 0))
+    out = np.zeros(d.total_bytes, dtype=np.uint8)
+    _check(lib().qmv_sparse_pack_host(ctypes.byref(dense_desc), src.ctypes.data, ctypes.byref(d), out.ctypes.data,
+                                      out.nbytes))
+    return d, out
 
 
 def cass_mx_pack_host(w_bf16_bits, calib_bf16_bits):

@@ -255,6 +255,10 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
 
 int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx, float* y,
                     int64_t ldy, void* stream) {
+  if (desc && desc->format == QMV_TERNARY2_SPARSE) {
+    qmv_task t{desc, w, x_bf16, y, ldx, ldy};
+    return qmv_run_batch(QMV_TERNARY2_SPARSE, &t, 1, M, stream);
+  }
   return run_one(QMV_TERNARY2, desc, w, x_bf16, M, ldx, y, ldy, stream);
 }
 
@@ -264,6 +268,31 @@ int qmv_run_int4(const qmv_desc* desc, const void* w, const void* x_bf16, int M,
 }
 
 int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* stream) {
+  if (format == QMV_TERNARY2_SPARSE) {
+    if (!tasks || n_tasks < 1 || n_tasks > QMV_MAX_BATCH) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n_tasks, QMV_MAX_BATCH);
+    if (M < 1 || M > 8) return fail(QMV_ERR_ARG, "sparse ternary: M=%d outside 1..8", M);
+    static thread_local const qmv_desc* ds[QMV_MAX_BATCH];
+    static thread_local const void* ws[QMV_MAX_BATCH];
+    static thread_local const void* xs[QMV_MAX_BATCH];
+    static thread_local float* ys[QMV_MAX_BATCH];
+    static thread_local int64_t lx[QMV_MAX_BATCH], ly[QMV_MAX_BATCH];
+    for (int i = 0; i < n_tasks; ++i) {
+      const qmv_task& t = tasks[i];
+      int rc = check_sparse_desc(t.desc);
+      if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
+      if (!t.w || !t.x || !t.y) return fail(QMV_ERR_ARG, "task %d: NULL w, x or y", i);
+      if (!aligned16(t.w) || !aligned16(t.x) || !aligned16(t.y)) return fail(QMV_ERR_ALIGN, "task %d: w, x and y must be 16-byte aligned", i);
+      if (t.ldx < t.desc->K || t.ldy < t.desc->N || t.ldx % 8 || t.ldx > INT32_MAX || t.ldy > INT32_MAX)
+        return fail(QMV_ERR_ARG, "task %d: ldx=%lld ldy=%lld", i, (long long)t.ldx, (long long)t.ldy);
+      ds[i] = t.desc;
+      ws[i] = t.w;
+      xs[i] = t.x;
+      ys[i] = t.y;
+      lx[i] = t.ldx;
+      ly[i] = t.ldy;
+    }
+    return run_sparse(ds, ws, xs, lx, ys, ly, n_tasks, M, static_cast<cudaStream_t>(stream));
+  }
   if (format != QMV_TERNARY2 && format != QMV_INT4) return fail(QMV_ERR_UNSUPPORTED, "qmv_run_batch serves ternary and INT4");
   if (!tasks || n_tasks < 1 || n_tasks > QMV_MAX_BATCH) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n_tasks, QMV_MAX_BATCH);
   if (M < 1 || M > QMV_MAX_M) return fail(QMV_ERR_ARG, "M=%d outside 1..%d", M, QMV_MAX_M);

@@ -80,6 +80,12 @@ struct GemvBatch {
 int launch_gemv(int format, GemvBatch& b, int M, cudaStream_t s);
 // The tensor-core matvec kernel (gemv_mma.cu), same contract, M in 1..16.
 int launch_gemv_mma(int format, GemvBatch& b, int M, cudaStream_t s);
+// Flagged sparse ternary (sparse.cu): descriptor check, and n matvecs with M
+// activation rows in one launch (descriptors already checked).
+int check_sparse_desc(const qmv_desc* d);
+int run_sparse(const qmv_desc* const* descs, const void* const* ws, const void* const* xs, const int64_t* ldx,
+               float* const* ys, const int64_t* ldy, int n, int M, cudaStream_t s);
+
 // From this many activation rows on, the entry points use the tensor-core
 // kernel (unless qmv_desc.flags forces one of the two): the fp16-FMA kernel's
 // cost grows with M; measured on the INT4 layer set and the ternary stack it is
