@@ -479,6 +479,47 @@ class Cassandra(Workload):
         return captured_traffic(f"{self.name} M={self.M}")
 
 
+class KvEncode(Workload):
+    """Online KV encoder: one decode step's new K and V for the 27B-shaped stack at batch 128
+    (60 layers x 2 x 128 token rows of 8 KV heads x 128 = 1024 values), encoded into the
+    Cassandra-1 layout with a fixed exponent codebook."""
+    name = "kv-encode"
+    kernel = "kv_encode_kernel"
+
+    def __init__(self, q, torch, dev, batch=128):
+        import numpy as np
+        from quantized_gemv_unpack_gb300 import synth
+        gen = synth.torch_generator(5, dev)
+        self.T, self.D = LAYERS * 2 * batch, NKV * HD
+        v = torch.randn((self.T, self.D), generator=gen, device=dev) * 0.5
+        v[:, ::64] *= 20                                            # channel outliers, as keys have
+        one = v.to(torch.bfloat16)
+        E = ((one[:64].view(torch.int16).to(torch.int32) >> 7) & 0xFF).cpu().numpy()
+        counts = np.bincount(E.ravel(), minlength=256)
+        present = sorted((e for e in range(256) if counts[e]), key=lambda e: (-counts[e], e))
+        self.codebook = np.array(present + [e for e in range(256) if not counts[e]], dtype=np.uint8)
+        self.slot = self.D * 3 // 32 // 4 * 4                       # 3 bits per kept value on average
+        self.copies = copies_for(self.T * self.D * 2)
+        self.xs = [one.view(torch.int16)] + [one.view(torch.int16).clone() for _ in range(self.copies - 1)]
+        self.d = q.cass_kv_encode(self.xs[0], self.codebook, self.slot)
+        self.out = torch.empty(self.d.total_bytes, dtype=torch.uint8, device=dev)
+        self.nbytes = self.T * self.D * 2 + self.d.total_bytes
+        self.batch, self.q = batch, q
+
+    def config(self):
+        return {"workload": f"online KV-cache encoder (Cassandra-1 layout): one decode step's new K and V of the "
+                            f"27B-shaped stack at batch {self.batch}: {self.T} token rows x {self.D} bf16",
+                "tokens": self.T, "values_per_token": self.D, "slot_words": self.slot, "seed": 5,
+                "encoded_bytes": self.d.total_bytes, "input_bytes": self.T * self.D * 2,
+                "l2": f"rotating {self.copies} copies of the input (>= 3x L2)"}
+
+    def step(self, i, stream):
+        self.q.cass_kv_encode(self.xs[i % self.copies], self.codebook, self.slot, self.out, stream)
+
+    def host_io(self):
+        return [self.xs[0]], [self.out]
+
+
 class Moe(Workload):
     name = "moe"
     kernel = "moe_route_kernel + moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
@@ -532,6 +573,8 @@ def make_workload(name, q, torch, dev, a):
         return Stack(q, torch, dev, a.layers, path=a.path)
     if name == "stack-sparse":
         return SparseStack(q, torch, dev, a.layers)
+    if name == "kv-encode":
+        return KvEncode(q, torch, dev)
     if name == "ternary-4096":
         return Ternary4096(q, torch, dev, a.M or 1, path=a.path)
     if name == "int4-layer":
@@ -553,7 +596,7 @@ def main():
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
     ap.add_argument("--workload", default="stack",
                     choices=["stack", "stack-sparse", "ternary-4096", "int4-layer", "cass-draft", "cass-target",
-                             "cass-mx-draft", "cass-mx-target", "moe"])
+                             "cass-mx-draft", "cass-mx-target", "kv-encode", "moe"])
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
@@ -667,7 +710,7 @@ def main():
     per_gpu = nbytes / (ms * 1e-3) / 1e9
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
     launches = {"stack": 1, "stack-sparse": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
-                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "moe": 3}[a.workload]
+                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "kv-encode": 1, "moe": 3}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -242,6 +242,25 @@ int cass_mx_pack_host(const uint16_t* w_bf16, int64_t N, int64_t K, const uint16
                       int64_t R, qmv_desc* desc, void* out, int64_t out_capacity);
 
 /*
+ * Online KV-cache encoder on the GPU ("Cassandra", 3.5: new K/V are pruned,
+ * truncated and encoded as they are produced; 3.2: the KV cache is pruned by
+ * per-token magnitude). kv: device bf16 [T][ld], one token's D values per row.
+ * Keeps the D/2 largest |v| of each row (equal magnitudes: lower index first;
+ * NaN as +inf), splits the kept values as cass_pack_host does, and writes each
+ * exponent as a unary code of its rank in `codebook` (host, the 256 exponent
+ * values in rank order, each once) into a fixed slot of slot_words 32-bit words
+ * per row (rowstart[n] = n * slot_words, zero-filled after the codes). The
+ * result is a QMV_CASS buffer (n_symbols 256) that cass_decode_draft and
+ * cass_reconstruct read. D % 32 == 0, D <= 16384, slot_words a positive
+ * multiple of 4. desc is filled on the host; with packed == NULL nothing runs
+ * (size query), otherwise packed (device, capacity >= desc->total_bytes) is
+ * written on `stream`. A row whose codes exceed its slot keeps the codes that
+ * fit and records QMV_ERR_UNSUPPORTED in the device error word.
+ */
+int cass_kv_encode(const uint16_t* kv, int64_t T, int64_t D, int64_t ld, const uint8_t* codebook,
+                   int64_t slot_words, qmv_desc* desc, void* packed, int64_t capacity, void* stream);
+
+/*
  * Draft path ("Cassandra", 3.2 figure b): reads only the speculation sections
  * of the packed buffer (QMV_CASS: 0-4, QMV_CASS_MX: 0-3). Draft weight = S<<15 |
  * E<<7 | m_hi<<4 for kept values (low mantissa bits zero-filled; QMV_CASS_MX:

@@ -27,7 +27,7 @@ QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-F
 
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
-           "qmv_run_int4", "qmv_run_batch", "qmv_sparse_pack_host", "cass_pack_host", "cass_mx_pack_host", "cass_decode_draft", "cass_reconstruct",
+           "qmv_run_int4", "qmv_run_batch", "qmv_sparse_pack_host", "cass_pack_host", "cass_mx_pack_host", "cass_kv_encode", "cass_decode_draft", "cass_reconstruct",
            "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
 
 
@@ -70,6 +70,7 @@ _SIGS = {
     "cass_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
     "cass_mx_pack_host": (_I32, [_P, _I64, _I64, _P, _I64, _DESC, _P, _I64]),
     "qmv_sparse_pack_host": (_I32, [_DESC, _P, _DESC, _P, _I64]),
+    "cass_kv_encode": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _DESC, _P, _I64, _P]),
     "cass_decode_draft": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "cass_reconstruct": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
@@ -222,6 +223,21 @@ def qmv_sparse_pack_host(dense_desc: qmv_desc, dense_packed_host):
     _check(lib().qmv_sparse_pack_host(ctypes.byref(dense_desc), src.ctypes.data, ctypes.byref(d), out.ctypes.data,
                                       out.nbytes))
     return d, out
+
+
+def cass_kv_encode(kv, codebook, slot_words: int, packed=None, stream=None) -> qmv_desc:
+    """Online KV encoder: kv device bf16 [T][ld] (one token per row), codebook NumPy uint8 [256]
+    (the exponents in rank order). Returns the QMV_CASS descriptor; with packed (device uint8 of
+    at least desc.total_bytes) also encodes into it. packed=None is a size query."""
+    import numpy as np
+    cb = np.ascontiguousarray(codebook, dtype=np.uint8)
+    T, ld = _rows(kv)
+    D = kv.shape[1]
+    d = qmv_desc()
+    _check(lib().cass_kv_encode(_ptr(kv), T, D, ld, cb.ctypes.data, slot_words, ctypes.byref(d),
+                                _ptr(packed) if packed is not None else None,
+                                packed.numel() if packed is not None else 0, _stream(stream)))
+    return d
 
 
 def cass_mx_pack_host(w_bf16_bits, calib_bf16_bits):

@@ -359,6 +359,167 @@ int launch_cassmx(const CassMxArgs& a, int M, cudaStream_t s) {
   return QMV_OK;
 }
 
+// ----------------------------------------------------------------------------- online KV encoder
+
+struct KvEncArgs {
+  const uint16_t* v;         // bf16 [T][ld]
+  int64_t ld;
+  int T, D, slot_words;
+  uint32_t* bitmap;          // the Cassandra-1 sections of the output buffer
+  uint32_t* signmant;
+  uint32_t* stream;
+  uint32_t* rowstart;
+  uint8_t* codebook;
+  uint16_t* pruned;
+  uint32_t* mlo;
+  unsigned char* base;       // the output buffer, for its section gaps
+  int64_t gap_begin[7], gap_end[7];
+  uint32_t cb_words[64];     // codebook bytes in rank order
+  int* err;
+};
+
+constexpr int kEncWarps = 4;
+
+__device__ __forceinline__ uint32_t magnitude_key(uint32_t b) {
+  // |v| ordering of bf16 bits; Inf and NaN both as +inf
+  return ((b >> 7) & 0xFFu) == 0xFFu ? 0x7F80u : (b & 0x7FFFu);
+}
+
+// Among the 256 bins of hist (one digit of the key), the digit d at which the
+// count of keys with digit > d stays below `need` and with digit >= d reaches
+// it; returns d and sets *above to the count with digit > d. Warp-collective.
+__device__ int select_digit(const int* hist, int need, int* above) {
+  const int lane = threadIdx.x & 31;
+  // lane l holds bins 255 - 8l .. 248 - 8l (descending)
+  int h[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = hist[255 - 8 * lane - i];
+    sum += h[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int run = incl - sum, found = -1, before = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (found < 0 && run + h[i] >= need) {
+      found = 255 - 8 * lane - i;
+      before = run;
+    }
+    run += h[i];
+  }
+  const uint32_t who = __ballot_sync(0xffffffffu, found >= 0 && (incl - sum) < need);
+  const int src = who ? __ffs(who) - 1 : 0;
+  *above = __shfl_sync(0xffffffffu, before, src);
+  return __shfl_sync(0xffffffffu, found, src);
+}
+
+// One warp per token row: magnitude pruning (radix select of the D/2-th largest
+// |v| on 16-bit keys, equal keys kept in index order), bitmap by ballot, kept
+// values' sign/high-mantissa and low-mantissa nibbles and pruned raw values in
+// order, unary exponent codes at offsets from a warp scan of the code lengths.
+__global__ void __launch_bounds__(kEncWarps * 32) kv_encode_kernel(const __grid_constant__ KvEncArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ uint8_t rank_of[256];
+  const int D = a.D, K2 = D / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t per_warp = ((size_t)D * 2 + 1024 + (size_t)D / 16 * 8 + (size_t)a.slot_words * 4 + 15) / 16 * 16;
+  unsigned char* wb = smem + (size_t)warp * per_warp;
+  uint16_t* vals = reinterpret_cast<uint16_t*>(wb);
+  int* hist = reinterpret_cast<int*>(wb + (size_t)D * 2);
+  uint32_t* sm_w = reinterpret_cast<uint32_t*>(hist + 256);
+  uint32_t* lo_w = sm_w + D / 16;
+  uint32_t* slot = lo_w + D / 16;
+  const uint32_t below = lanemask_lt();
+
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    rank_of[(a.cb_words[i >> 2] >> ((i & 3) * 8)) & 0xFFu] = (uint8_t)i;
+  if (blockIdx.x == 0 && warp == 0) {
+    for (int i = lane; i < 256; i += 32) a.codebook[i] = (uint8_t)((a.cb_words[i >> 2] >> ((i & 3) * 8)) & 0xFFu);
+    for (int gi = 0; gi < 7; ++gi)
+      for (int64_t q = a.gap_begin[gi] + lane; q < a.gap_end[gi]; q += 32) a.base[q] = 0;
+    if (lane == 0) a.rowstart[a.T] = (uint32_t)a.T * (uint32_t)a.slot_words;
+  }
+  __syncthreads();
+
+  for (int n = blockIdx.x * kEncWarps + warp; n < a.T; n += gridDim.x * kEncWarps) {
+    const uint16_t* row = a.v + (size_t)n * a.ld;
+    for (int j = lane; j < D; j += 32) vals[j] = row[j];
+    for (int i = lane; i < D / 16; i += 32) sm_w[i] = lo_w[i] = 0u;
+    for (int i = lane; i < a.slot_words; i += 32) slot[i] = 0u;
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    // ---- radix select: high byte, then low byte among keys with that high byte
+    for (int j = lane; j < D; j += 32) atomicAdd(&hist[magnitude_key(vals[j]) >> 8], 1);
+    __syncwarp();
+    int above1, above0;
+    const int d1 = select_digit(hist, K2, &above1);
+    __syncwarp();
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int j = lane; j < D; j += 32) {
+      const uint32_t k = magnitude_key(vals[j]);
+      if ((int)(k >> 8) == d1) atomicAdd(&hist[k & 0xFFu], 1);
+    }
+    __syncwarp();
+    const int d0 = select_digit(hist, K2 - above1, &above0);
+    const uint32_t thr = ((uint32_t)d1 << 8) | (uint32_t)d0;
+    const int ties_kept = K2 - above1 - above0;  // how many keys equal to thr are kept
+    // ---- bitmap, kept nibbles, pruned values and unary codes, 32 columns at a time
+    int kb = 0, tb = 0;
+    uint32_t bitoff = 0;
+    bool overflow = false;
+    for (int w = 0; w < D / 32; ++w) {
+      const int j = w * 32 + lane;
+      const uint32_t b = vals[j];
+      const uint32_t k = magnitude_key(b);
+      const bool tie = k == thr;
+      const uint32_t tball = __ballot_sync(0xffffffffu, tie);
+      const bool kept = k > thr || (tie && tb + __popc(tball & below) < ties_kept);
+      const uint32_t km = __ballot_sync(0xffffffffu, kept);
+      if (lane == 0) a.bitmap[(size_t)n * (D / 32) + w] = km;
+      const int kidx = kb + __popc(km & below);
+      uint32_t len = 0, r = 0;
+      if (kept) {
+        const uint32_t sh = (kidx & 7) * 4;
+        atomicOr(&sm_w[kidx >> 3], (((b >> 15) << 3) | ((b >> 4) & 7u)) << sh);
+        atomicOr(&lo_w[kidx >> 3], (b & 15u) << sh);
+        r = rank_of[(b >> 7) & 0xFFu];
+        len = r + 1;
+      } else {
+        a.pruned[(size_t)n * K2 + (j - kidx)] = (uint16_t)b;
+      }
+      uint32_t incl = len;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (kept) {
+        const uint32_t pos = bitoff + incl - len + r;
+        if (pos < (uint32_t)a.slot_words * 32u) atomicOr(&slot[pos >> 5], 1u << (pos & 31u));
+        else overflow = true;
+      }
+      bitoff += __shfl_sync(0xffffffffu, incl, 31);
+      kb += __popc(km);
+      tb += __popc(tball);
+    }
+    if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicCAS(a.err, 0, (int)QMV_ERR_UNSUPPORTED);
+    __syncwarp();
+    for (int i = lane; i < D / 16; i += 32) {
+      a.signmant[(size_t)n * (D / 16) + i] = sm_w[i];
+      a.mlo[(size_t)n * (D / 16) + i] = lo_w[i];
+    }
+    for (int i = lane; i < a.slot_words; i += 32) a.stream[(size_t)n * a.slot_words + i] = slot[i];
+    if (lane == 0) a.rowstart[n] = (uint32_t)n * (uint32_t)a.slot_words;
+    __syncwarp();  // the warp's buffers are reused by its next row
+  }
+}
+
 template <bool TARGET>
 int launch_cass(const CassArgs& a, int M, cudaStream_t s) {
   const size_t K = a.K;
@@ -662,6 +823,75 @@ int cass_mx_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint16_t* X
       }
     }
   }
+  return QMV_OK;
+}
+
+int cass_kv_encode(const uint16_t* kv, int64_t T, int64_t D, int64_t ld, const uint8_t* codebook, int64_t slot_words,
+                   qmv_desc* desc, void* packed, int64_t capacity, void* stream) {
+  if (!codebook || !desc) return fail(QMV_ERR_ARG, "NULL codebook or desc");
+  if (T <= 0 || D <= 0 || D % 32 || D > 16384) return fail(QMV_ERR_ARG, "T=%lld D=%lld (D a multiple of 32, at most 16384)", (long long)T, (long long)D);
+  if (slot_words <= 0 || slot_words % 4 || slot_words > (int64_t)D * 8) return fail(QMV_ERR_ARG, "slot_words=%lld must be a positive multiple of 4", (long long)slot_words);
+  if (T > INT32_MAX / 2 || T * slot_words > (int64_t)UINT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "too many tokens");
+  bool seen[256] = {false};
+  for (int i = 0; i < 256; ++i) {
+    if (seen[codebook[i]]) return fail(QMV_ERR_ARG, "codebook must list each of the 256 exponents once");
+    seen[codebook[i]] = true;
+  }
+  const int64_t sizes[7] = {T * D / 8, T * D / 4, T * slot_words * 4, (T + 1) * 4, 256, T * D, T * D / 4};
+  memset(desc, 0, sizeof(*desc));
+  desc->abi_version = QMV_ABI_VERSION;
+  desc->format = QMV_CASS;
+  desc->N = T;
+  desc->K = D;
+  desc->group = 0;
+  desc->n_symbols = 256;
+  int64_t pos = 0;
+  for (int i = 0; i < 7; ++i) {
+    desc->off[i] = pos;
+    desc->bytes[i] = sizes[i];
+    pos = align256(pos + sizes[i]);
+  }
+  desc->total_bytes = pos;
+  if (!packed) return QMV_OK;
+  if (!kv) return fail(QMV_ERR_ARG, "NULL kv");
+  if (capacity < desc->total_bytes) return fail(QMV_ERR_ARG, "capacity %lld < %lld", (long long)capacity, (long long)desc->total_bytes);
+  if (!aligned16(kv) || !aligned16(packed)) return fail(QMV_ERR_ALIGN, "kv and packed must be 16-byte aligned");
+  if (ld < D || ld % 8) return fail(QMV_ERR_ARG, "ld=%lld must be >= D and a multiple of 8", (long long)ld);
+  int* err = device_error_word();
+  if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+  unsigned char* b = static_cast<unsigned char*>(packed);
+  KvEncArgs a;
+  a.v = kv;
+  a.ld = ld;
+  a.T = (int)T;
+  a.D = (int)D;
+  a.slot_words = (int)slot_words;
+  a.bitmap = reinterpret_cast<uint32_t*>(b + desc->off[0]);
+  a.signmant = reinterpret_cast<uint32_t*>(b + desc->off[1]);
+  a.stream = reinterpret_cast<uint32_t*>(b + desc->off[2]);
+  a.rowstart = reinterpret_cast<uint32_t*>(b + desc->off[3]);
+  a.codebook = b + desc->off[4];
+  a.pruned = reinterpret_cast<uint16_t*>(b + desc->off[5]);
+  a.mlo = reinterpret_cast<uint32_t*>(b + desc->off[6]);
+  a.base = b;
+  for (int i = 0; i < 7; ++i) {
+    a.gap_begin[i] = desc->off[i] + desc->bytes[i];
+    a.gap_end[i] = i + 1 < 7 ? desc->off[i + 1] : desc->total_bytes;
+  }
+  for (int i = 0; i < 64; ++i)
+    a.cb_words[i] = (uint32_t)codebook[4 * i] | ((uint32_t)codebook[4 * i + 1] << 8) | ((uint32_t)codebook[4 * i + 2] << 16) |
+                    ((uint32_t)codebook[4 * i + 3] << 24);
+  a.err = err;
+  const size_t per_warp = ((size_t)D * 2 + 1024 + (size_t)D / 16 * 8 + (size_t)slot_words * 4 + 15) / 16 * 16;
+  const size_t smem = per_warp * kEncWarps;
+  if (smem > 227 * 1024 - 1024) return fail(QMV_ERR_UNSUPPORTED, "D=%lld with slot_words=%lld does not fit shared memory", (long long)D, (long long)slot_words);
+  int per_sm = 0;
+  int rc = kernel_fit((const void*)kv_encode_kernel, kEncWarps * 32, smem, &per_sm);
+  if (rc) return rc;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sm_count() * per_sm, (T + kEncWarps - 1) / kEncWarps));
+  kv_encode_kernel<<<grid, kEncWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kv encode launch");
   return QMV_OK;
 }
 
