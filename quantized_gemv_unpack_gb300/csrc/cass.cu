@@ -1,5 +1,6 @@
-// Cassandra lossless bf16 split ("Cassandra", sections 3.1-3.3): the host-side
-// offline transform and the GPU draft / target paths.
+// Cassandra lossless bf16 split ("Cassandra", sections 3.1-3.3) and its
+// shared-exponent variant (Cassandra-2): the host-side offline transforms and
+// the GPU draft / target paths.
 //
 // Offline (host): Wanda value pruning keeps the K/2 largest |w| * ||X[:,j]||_2
 // of every row (bitmap), kept values keep sign + 3 high mantissa bits in the
@@ -8,20 +9,26 @@
 // codes (rank r = r zeros then a one), pruned values go to the verification
 // data as raw bf16.
 //
-// GPU: one warp per row, rows strided over a persistent grid. Phase A decodes
-// the row's unary exponent stream: each lane takes one 32-bit word, counts the
-// codewords ending in it (__popc), an inclusive warp scan turns the counts into
-// codeword indices, and an exclusive warp max-scan of each word's last one bit
-// (carried across 32-word chunks) gives every codeword's start, so a lane can
-// turn each set bit into a rank = zeros since the previous one and look the
-// exponent up in the codebook. Exponents land in shared memory in kept-value
-// order. Phase B walks the bitmap 32 columns at a time: lane l owns column
-// 32*i + l, its kept index is the number of kept columns before it
-// (__popc(word & lanemask_lt) plus the running count), its pruned index is
-// column - kept index. The draft value is S<<15 | E<<7 | m_hi<<4 (pruned: +0),
-// the target value adds m_lo (pruned: the raw verification bits); either is
-// widened to fp32 (exact) and multiplied into fp32 accumulators per activation
-// row. Every loop is bounded by the row's sizes; inconsistent streams set
+// GPU: one warp per row, rows strided over a persistent grid. A row keeps
+// exactly K/2 values and prunes K/2, so lane l takes the kept values of rank
+// k in [l*K2/32, (l+1)*K2/32) and the pruned values of the same ranks: every
+// lane has the same work whatever the bitmap looks like, and no lane works
+// per column. Each lane walks its ranks in order with bit cursors: over the
+// exponent stream (the k-th one ends the k-th codeword; the zeros since the
+// previous one are its rank), over the bitmap's ones (the column of the k-th
+// kept value) and over its zeros (the column of the p-th pruned value). The
+// cursors start from warp-wide selects: the row's words are scanned 128 at a
+// time (four per lane, warp prefix sum of their bit counts) and each lane
+// finds the word holding the one or zero of its first rank by a binary search
+// over the lanes' prefix sums. Nibbles, sign bits and pruned halves are read
+// in rank order from skewed shared-memory copies (one pad word per 8 or 32
+// words, so that the 32 lanes' reads fall in distinct banks). Activations are
+// staged per CTA as bf16 with all M rows of a column side by side (padded to
+// 1, 2, 4 or 8), so one shared load gathers a column's activations; column j
+// sits at unit j + (j >> sk), 2^sk being about the columns one lane covers,
+// again to spread the lanes over the banks. Each product is exact in fp32
+// (bf16 x bf16) and summed in fp32; the lanes' partial sums are reduced by
+// shuffles. Every loop is bounded by the row's sizes; inconsistent streams set
 // QMV_ERR_CORRUPT in the device error word.
 #include <algorithm>
 #include <cmath>
@@ -36,6 +43,276 @@ namespace {
 
 constexpr int kCassWarpsMax = 16;
 
+__device__ __forceinline__ void flag(int* err) { atomicCAS(err, 0, (int)QMV_ERR_CORRUPT); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ----------------------------------------------------------------------------- rank walks
+
+// Words of a skewed copy of n words with one pad word after every 2^SH.
+__host__ __device__ constexpr size_t skewed_words(size_t n, int sh) { return n + (n >> sh) + 1; }
+template <int SH>
+__device__ __forceinline__ int skew(int w) { return w + (w >> SH); }
+
+// Activation staging: unit j + (j >> sk) holds the M rows of column j, as
+// P bf16 (one fp32 when M = 1, which saves the widening in the walk).
+template <int MT>
+struct XPad {
+  static constexpr int P = MT == 1 ? 1 : MT == 2 ? 2 : MT <= 4 ? 4 : 8;
+};
+__host__ __device__ inline size_t xs_bytes(size_t K, int sk, int P) {
+  return ((K + (K >> sk) + 1) * (size_t)(P == 1 ? 4 : P * 2) + 15) / 16 * 16;
+}
+
+template <int MT>
+__device__ void stage_x(uint16_t* xs, const uint16_t* x, int ldx, int K, int sk) {
+  constexpr int P = XPad<MT>::P;
+  if constexpr (P == 1) {
+    float* xf = reinterpret_cast<float*>(xs);
+    for (int j = threadIdx.x; j < K; j += blockDim.x) xf[j + (j >> sk)] = __uint_as_float((uint32_t)x[j] << 16);
+  } else {
+    for (int i = threadIdx.x; i < K * P; i += blockDim.x) {
+      const int j = i / P, m = i % P;
+      xs[(size_t)(j + (j >> sk)) * P + m] = m < MT ? x[(size_t)m * ldx + j] : (uint16_t)0;
+    }
+  }
+}
+
+template <int MT>
+__device__ __forceinline__ void x_gather(const uint16_t* xs, int j, int sk, float (&xv)[MT]) {
+  constexpr int P = XPad<MT>::P;
+  const int u = j + (j >> sk);
+  uint32_t w[P == 1 ? 1 : P / 2];
+  if constexpr (P == 1) {
+    xv[0] = reinterpret_cast<const float*>(xs)[u];
+    return;
+  } else if constexpr (P == 2) {
+    w[0] = reinterpret_cast<const uint32_t*>(xs)[u];
+  } else if constexpr (P == 4) {
+    const uint2 v = reinterpret_cast<const uint2*>(xs)[u];
+    w[0] = v.x, w[1] = v.y;
+  } else {
+    const uint4 v = reinterpret_cast<const uint4*>(xs)[u];
+    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+  }
+  if constexpr (P > 1) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      xv[m] = __uint_as_float(m & 1 ? w[m >> 1] & 0xffff0000u : w[m >> 1] << 16);
+  }
+}
+
+// Copies n words to dst[skew<SH>(w)]; 16-byte loads when the source allows.
+template <int SH>
+__device__ __forceinline__ void stage_words(uint32_t* dst, const uint32_t* src, int n) {
+  const int lane = threadIdx.x & 31;
+  if ((n & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int i = lane; i < n / 4; i += 32) {
+      const uint4 v = __ldg(s4 + i);
+      uint32_t* d = dst + skew<SH>(4 * i);  // 4 words never straddle a pad (SH >= 2)
+      d[0] = v.x, d[1] = v.y, d[2] = v.z, d[3] = v.w;
+    }
+  } else {
+    for (int w = lane; w < n; w += 32) dst[skew<SH>(w)] = __ldg(src + w);
+  }
+}
+
+// Position (0..31) of the r-th set bit of x (r < popc(x)).
+__device__ __forceinline__ int select_in_word(uint32_t x, int r) {
+  int p = 0, c;
+  c = __popc(x & 0xFFFFu);
+  if (r >= c) r -= c, x >>= 16, p += 16;
+  c = __popc(x & 0xFFu);
+  if (r >= c) r -= c, x >>= 8, p += 8;
+  c = __popc(x & 0xFu);
+  if (r >= c) r -= c, x >>= 4, p += 4;
+  c = __popc(x & 0x3u);
+  if (r >= c) r -= c, x >>= 2, p += 2;
+  if (r >= (int)(x & 1u)) p += 1;
+  return p;
+}
+
+struct Hit {
+  uint32_t w;  // the word holding the target bit
+  int r;       // the target's rank among the word's set bits
+  int wi;      // the word's index (past the end: not found)
+};
+__device__ __forceinline__ int hit_pos(const Hit& h) { return h.wi * 32 + select_in_word(h.w, h.r); }
+
+// One warp-collective step of a select: q holds words c + 4*lane + 0..3 of an
+// array (0 past its end) and `carry` counts the set bits before word c. If the
+// lane's target rank t falls in these 128 words, h records where. Returns the
+// set bits in the 128 words.
+__device__ __forceinline__ int select_chunk(const uint32_t (&q)[4], int c, int t, int carry, Hit& h) {
+  const int lane = threadIdx.x & 31;
+  const int v = __popc(q[0]) + __popc(q[1]) + __popc(q[2]) + __popc(q[3]);
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  const int excl = incl - v;
+  const int tot = __shfl_sync(0xffffffffu, incl, 31);
+  const int tt = t - carry;
+  int j = 0;  // the last lane whose words start at or before rank tt
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const int e = __shfl_sync(0xffffffffu, excl, j + s);
+    if (e <= tt) j += s;
+  }
+  const int ej = __shfl_sync(0xffffffffu, excl, j);
+  const uint32_t a0 = __shfl_sync(0xffffffffu, q[0], j), a1 = __shfl_sync(0xffffffffu, q[1], j);
+  const uint32_t a2 = __shfl_sync(0xffffffffu, q[2], j), a3 = __shfl_sync(0xffffffffu, q[3], j);
+  if (tt >= 0 && tt < tot) {
+    int r = tt - ej, sel = 0;
+    uint32_t x = a0;
+    if (r >= __popc(a0)) {
+      r -= __popc(a0), x = a1, sel = 1;
+      if (r >= __popc(a1)) {
+        r -= __popc(a1), x = a2, sel = 2;
+        if (r >= __popc(a2)) r -= __popc(a2), x = a3, sel = 3;
+      }
+    }
+    h.w = x, h.r = r, h.wi = c + 4 * j + sel;
+  }
+  return tot;
+}
+
+// Loads words c + 4*lane + 0..3 of a row (0 past n), 16 bytes at a time when aligned.
+__device__ __forceinline__ void load_quad(const uint32_t* src, int n, int c, bool vec, uint32_t (&q)[4]) {
+  const int w0 = c + 4 * (threadIdx.x & 31);
+  if (vec) {
+    const uint4 v = w0 < n ? __ldg(reinterpret_cast<const uint4*>(src + w0)) : make_uint4(0, 0, 0, 0);
+    q[0] = v.x, q[1] = v.y, q[2] = v.z, q[3] = v.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = w0 + i < n ? __ldg(src + w0 + i) : 0u;
+  }
+}
+
+// Stages a row's bitmap (KW words) and finds the column of the lane's first
+// kept value (rank k0 among the ones) and first pruned value (rank k0 among
+// the zeros). Returns the number of ones; `clean` (warp-uniform) says that no
+// word is all zeros or all ones, so the cursors never skip a whole word.
+__device__ __forceinline__ int bitmap_selects(const uint32_t* src, uint32_t* bm_s, int KW, int k0, Hit& h1, Hit& h0,
+                                              bool& clean) {
+  const bool vec = (KW & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+  int ones = 0, zeros = 0;
+  h1.wi = h0.wi = KW;
+  h1.w = h0.w = 0u;
+  h1.r = h0.r = 0;
+  bool flat = false;
+  for (int c = 0; c < KW; c += 128) {
+    uint32_t q[4], z[4];
+    load_quad(src, KW, c, vec, q);
+    const int w0 = c + 4 * (threadIdx.x & 31);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (w0 + i < KW) {
+        bm_s[w0 + i] = q[i];
+        flat |= q[i] == 0u || q[i] == 0xffffffffu;
+      }
+      z[i] = w0 + i < KW ? ~q[i] : 0u;
+    }
+    ones += select_chunk(q, c, k0, ones, h1);
+    zeros += select_chunk(z, c, k0, zeros, h0);
+  }
+  clean = !__any_sync(0xffffffffu, flat);
+  return ones;
+}
+
+// A forward cursor over the set bits (INV: the clear bits) of a word array,
+// with the next word preloaded.
+struct Cursor {
+  uint32_t w;   // the unread bits of word wi
+  uint32_t nx;  // word wi + 1
+  int wi;
+};
+
+template <bool INV>
+__device__ __forceinline__ uint32_t cursor_word(const uint32_t* s, int nw, int i) {
+  const uint32_t raw = i < nw ? s[i] : (INV ? 0xffffffffu : 0u);
+  return INV ? ~raw : raw;
+}
+
+template <bool INV>
+__device__ __forceinline__ Cursor cursor_at(const uint32_t* s, int nw, int pos) {
+  Cursor c;
+  c.wi = pos >> 5;
+  c.w = cursor_word<INV>(s, nw, c.wi) & (0xffffffffu << (pos & 31));
+  c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+  return c;
+}
+
+// The next bit at or after the cursor (its position); the cursor moves past
+// it. Without SAFE the caller guarantees that no word before the last bit it
+// asks for is empty, so one step to the preloaded word always finds a bit.
+// With SAFE empty words are skipped, and running off the end sets `bad`.
+template <bool INV, bool SAFE>
+__device__ __forceinline__ int cursor_next(Cursor& c, const uint32_t* s, int nw, bool& bad) {
+  if (c.w == 0) {
+    c.w = c.nx;
+    ++c.wi;
+    c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+  }
+  if (SAFE) {
+    while (c.w == 0) {
+      if (c.wi >= nw) {
+        bad = true;
+        return 0;
+      }
+      c.w = c.nx;
+      ++c.wi;
+      c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+    }
+  }
+  const int b = __ffs(c.w) - 1;
+  c.w &= c.w - 1;
+  return c.wi * 32 + b;
+}
+
+// The fast-walk step: the caller guarantees that the bit exists and that no
+// word before it is empty, and pads the array so that word wi + 1 can always
+// be read; the refill is then branch-free.
+template <bool INV>
+__device__ __forceinline__ int cursor_step(Cursor& c, const uint32_t* s) {
+  const bool e = c.w == 0;
+  c.w = e ? c.nx : c.w;
+  c.wi += e ? 1 : 0;
+  const uint32_t raw = s[c.wi + 1];  // unchanged when e is false
+  c.nx = INV ? ~raw : raw;
+  const int b = __ffs(c.w) - 1;
+  c.w &= c.w - 1;
+  return c.wi * 32 + b;
+}
+
+template <int MT>
+__device__ __forceinline__ void accumulate(const uint16_t* xs, int j, int sk, float w, float (&acc)[MT]) {
+  float xv[MT];
+  x_gather<MT>(xs, j, sk, xv);
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m] = fmaf(w, xv[m], acc[m]);
+}
+
+template <int MT>
+__device__ __forceinline__ void store_row(float (&acc)[MT], float* y, int ldy, int n) {
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    float v = acc[m];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) y[(size_t)m * ldy + n] = v;
+  }
+}
+
+// ----------------------------------------------------------------------------- Cassandra-1
+
 struct CassArgs {
   const uint32_t* bitmap;    // [N][K/32]
   const uint32_t* signmant;  // [N][K/16]
@@ -46,177 +323,203 @@ struct CassArgs {
   const uint32_t* mlo;       // [N][K/16]
   const uint16_t* x;         // bf16 [M][ldx]
   float* y;                  // [M][ldy] or null
-  uint16_t* w_out;           // [N][K] or null
+  uint16_t* w_out;           // [N][K] or null (written by the WOUT kernels only)
   int64_t stream_words;
   int N, K, ldx, ldy, n_symbols;
+  int sk;                    // activation unit skew shift
+  int scap;                  // stream words a warp stages (longer rows are read in place)
   int* err;
 };
 
-__device__ __forceinline__ void flag(int* err) { atomicCAS(err, 0, (int)QMV_ERR_CORRUPT); }
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
+// Shared memory of one warp: bitmap, nibbles (+ target: low nibbles, pruned
+// halves), staged stream; the bitmap and the stream carry two pad words for
+// the fast walk's read-ahead.
+__host__ __device__ inline size_t cass_per_warp(size_t K, size_t scap, bool target) {
+  const size_t w = K / 32 + 2 + skewed_words(K / 16, 3) + (target ? skewed_words(K / 16, 3) + skewed_words(K / 4, 5) : 0) +
+                   scap + 2;
+  return (w * 4 + 15) / 16 * 16;
 }
 
+// Bytes of the (rank, nibble) -> draft bits table: bf16 bits S<<15 | E<<7 |
+// m_hi<<4 for every codebook rank and sign/high-mantissa nibble.
+__host__ __device__ inline size_t cass_tab_bytes(int n_symbols) { return ((size_t)n_symbols * 32 + 15) / 16 * 16; }
+
+// The staged row one lane walks.
+struct CassRow {
+  const uint32_t *bm, *sm, *lo, *pr, *st;
+  const uint16_t* tab;
+  const uint16_t* xs;
+  uint16_t* wrow;
+  int KW, nsw, nsym, sk;
+  int k0, cnt;
+  int send;            // where codeword k0 starts in the stream
+  int kpos, zpos;      // columns of kept value k0 and pruned value k0
+};
+
+// Kept value k and pruned value k for k in [k0, k0 + cnt): see the file comment.
+template <int MT, bool TARGET, bool WOUT, bool SAFE>
+__device__ __forceinline__ void cass_walk(const CassRow& r, float (&acc)[MT], bool& bad) {
+  Cursor cs = cursor_at<false>(r.st, r.nsw, r.send);
+  Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
+  Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  int send = r.send;
+  uint32_t smw = r.sm[skew<3>(r.k0 >> 3)];
+  uint32_t low = TARGET ? r.lo[skew<3>(r.k0 >> 3)] : 0u;
+  uint32_t prw = TARGET ? r.pr[skew<5>(r.k0 >> 1)] : 0u;
+  for (int k = r.k0; k < r.k0 + r.cnt; ++k) {
+    const int sp = cursor_next<false, SAFE>(cs, r.st, r.nsw, bad);
+    int rank = sp - send;
+    send = sp + 1;
+    if ((unsigned)rank >= (unsigned)r.nsym) bad = true, rank = 0;
+    const int j = cursor_next<false, SAFE>(ck, r.bm, r.KW, bad);
+    if ((k & 7) == 0) {
+      smw = r.sm[skew<3>(k >> 3)];
+      if (TARGET) low = r.lo[skew<3>(k >> 3)];
+    }
+    const int sh = (k & 7) * 4;
+    uint32_t v = r.tab[rank * 16 + ((smw >> sh) & 0xFu)];
+    if (TARGET) v |= (low >> sh) & 0xFu;
+    if (WOUT) r.wrow[j] = (uint16_t)v;
+    accumulate<MT>(r.xs, j, r.sk, __uint_as_float(v << 16), acc);
+    if (TARGET || WOUT) {
+      const int jz = cursor_next<true, SAFE>(cz, r.bm, r.KW, bad);
+      uint32_t pv = 0;
+      if (TARGET) {
+        if ((k & 1) == 0) prw = r.pr[skew<5>(k >> 1)];
+        pv = k & 1 ? prw >> 16 : prw & 0xFFFFu;
+        accumulate<MT>(r.xs, jz, r.sk, __uint_as_float(pv << 16), acc);
+      }
+      if (WOUT) r.wrow[jz] = (uint16_t)pv;
+    }
+  }
+}
+
+// The same walk for rows with no empty word in the way and K a multiple of
+// 512 (every lane's ranks start at a multiple of 8 and come in blocks of 8):
+// unrolled by 8, nibble shifts constant, cursors branch-free.
 template <int MT, bool TARGET>
+__device__ __forceinline__ void cass_walk8(const CassRow& r, float (&acc)[MT], bool& bad) {
+  Cursor cs = cursor_at<false>(r.st, r.nsw, r.send);
+  Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
+  Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  int send = r.send;
+  for (int k = r.k0; k < r.k0 + r.cnt; k += 8) {
+    const uint32_t smw = r.sm[skew<3>(k >> 3)];
+    const uint32_t low = TARGET ? r.lo[skew<3>(k >> 3)] : 0u;
+    uint32_t prw[4];
+    if (TARGET) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) prw[i] = r.pr[skew<5>((k >> 1) + i)];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sp = cursor_step<false>(cs, r.st);
+      int rank = sp - send;
+      send = sp + 1;
+      if ((unsigned)rank >= (unsigned)r.nsym) bad = true, rank = 0;
+      uint32_t v = r.tab[rank * 16 + ((smw >> (4 * u)) & 0xFu)];
+      if (TARGET) v |= (low >> (4 * u)) & 0xFu;
+      accumulate<MT>(r.xs, cursor_step<false>(ck, r.bm), r.sk, __uint_as_float(v << 16), acc);
+      if (TARGET) {
+        const uint32_t pv = u & 1 ? prw[u >> 1] >> 16 : prw[u >> 1] & 0xFFFFu;
+        accumulate<MT>(r.xs, cursor_step<true>(cz, r.bm), r.sk, __uint_as_float(pv << 16), acc);
+      }
+    }
+  }
+}
+
+template <int MT, bool TARGET, bool WOUT>
 __global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int K = a.K;
-  const int K2 = K / 2;
-  const int nwarps = blockDim.x / 32;
-  float* xs = reinterpret_cast<float*>(smem);                       // [MT][K] fp32
-  uint8_t* cb = smem + (size_t)MT * K * 4;                           // [256]
-  // per-warp buffers: bitmap[K/32] words, signmant[K/16] words, (target: mlo[K/16] words,
-  // pruned[K/2] halves), exps[K/2] bytes
-  const size_t per_warp = ((size_t)K2 + (size_t)K / 8 + (size_t)K / 4 + (TARGET ? (size_t)K / 4 + (size_t)K : 0) + 15) / 16 * 16;
+  constexpr int P = XPad<MT>::P;
+  const int K = a.K, K2 = K / 2, KW = K / 32;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  unsigned char* wb = smem + (size_t)MT * K * 4 + 256 + (size_t)warp * per_warp;
-  uint32_t* bm_s = reinterpret_cast<uint32_t*>(wb);
-  uint32_t* sm_s = bm_s + K / 32;
-  uint32_t* lo_s = sm_s + K / 16;
-  uint16_t* pr_s = reinterpret_cast<uint16_t*>(lo_s + (TARGET ? K / 16 : 0));
-  uint8_t* exps = reinterpret_cast<uint8_t*>(pr_s + (TARGET ? K2 : 0));
+  const int nwarps = blockDim.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  const size_t xb = xs_bytes(K, a.sk, P);
+  uint16_t* tab = reinterpret_cast<uint16_t*>(smem + xb);
+  uint32_t* bm_s = reinterpret_cast<uint32_t*>(smem + xb + cass_tab_bytes(a.n_symbols) +
+                                               (size_t)warp * cass_per_warp(K, a.scap, TARGET));
+  uint32_t* sm_s = bm_s + KW + 2;
+  uint32_t* lo_s = sm_s + skewed_words(K / 16, 3);
+  uint32_t* pr_s = lo_s + (TARGET ? skewed_words(K / 16, 3) : 0);
+  uint32_t* st_s = pr_s + (TARGET ? skewed_words(K / 4, 5) : 0);
 
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) cb[i] = a.codebook[i];
-  for (int m = 0; m < MT; ++m)
-    for (int j = threadIdx.x; j < K; j += blockDim.x)
-      xs[(size_t)m * K + j] = __uint_as_float((uint32_t)a.x[(size_t)m * a.ldx + j] << 16);
+  for (int i = threadIdx.x; i < a.n_symbols * 16; i += blockDim.x) {
+    const uint32_t nib = i & 15;
+    tab[i] = (uint16_t)(((nib & 8u) << 12) | ((uint32_t)a.codebook[i >> 4] << 7) | ((nib & 7u) << 4));
+  }
+  stage_x<MT>(xs, a.x, a.ldx, K, a.sk);
   __syncthreads();
 
-  const uint32_t below = lanemask_lt();
-  const int gw = blockIdx.x * nwarps + warp;
-  const int stride = gridDim.x * nwarps;
-  for (int n = gw; n < a.N; n += stride) {
-    // ---- stage the row's fixed-size sections (all loads in flight together);
-    // rows are 16-byte aligned in global memory when K is a multiple of 128
-    if (K % 128 == 0) {
-      const uint4* bm = reinterpret_cast<const uint4*>(a.bitmap + (size_t)n * (K / 32));
-      const uint4* sm = reinterpret_cast<const uint4*>(a.signmant + (size_t)n * (K / 16));
-      for (int i = lane; i < K / 128; i += 32) reinterpret_cast<uint4*>(bm_s)[i] = __ldg(bm + i);
-      for (int i = lane; i < K / 64; i += 32) reinterpret_cast<uint4*>(sm_s)[i] = __ldg(sm + i);
-      if (TARGET) {
-        const uint4* lo = reinterpret_cast<const uint4*>(a.mlo + (size_t)n * (K / 16));
-        const uint4* pr = reinterpret_cast<const uint4*>(a.pruned + (size_t)n * K2);
-        for (int i = lane; i < K / 64; i += 32) reinterpret_cast<uint4*>(lo_s)[i] = __ldg(lo + i);
-        for (int i = lane; i < K / 16; i += 32) reinterpret_cast<uint4*>(pr_s)[i] = __ldg(pr + i);
-      }
-    } else {
-      const uint32_t* bm = a.bitmap + (size_t)n * (K / 32);
-      const uint32_t* sm = a.signmant + (size_t)n * (K / 16);
-      for (int i = lane; i < K / 32; i += 32) bm_s[i] = __ldg(bm + i);
-      for (int i = lane; i < K / 16; i += 32) sm_s[i] = __ldg(sm + i);
-      if (TARGET) {
-        const uint32_t* lo = a.mlo + (size_t)n * (K / 16);
-        const uint16_t* pr = a.pruned + (size_t)n * K2;
-        for (int i = lane; i < K / 16; i += 32) lo_s[i] = __ldg(lo + i);
-        for (int i = lane; i < K2; i += 32) pr_s[i] = __ldg(pr + i);
-      }
+  CassRow r;
+  r.bm = bm_s, r.sm = sm_s, r.lo = lo_s, r.pr = pr_s, r.tab = tab, r.xs = xs;
+  r.KW = KW, r.nsym = a.n_symbols, r.sk = a.sk;
+  r.k0 = (int)(((int64_t)lane * K2) >> 5);
+  r.cnt = (int)(((int64_t)(lane + 1) * K2) >> 5) - r.k0;
+  for (int n = blockIdx.x * nwarps + warp; n < a.N; n += gridDim.x * nwarps) {
+    // ---- stage the row: nibbles (skewed), bitmap with the two selects, stream with one
+    stage_words<3>(sm_s, a.signmant + (size_t)n * (K / 16), K / 16);
+    if (TARGET) {
+      stage_words<3>(lo_s, a.mlo + (size_t)n * (K / 16), K / 16);
+      stage_words<5>(pr_s, reinterpret_cast<const uint32_t*>(a.pruned + (size_t)n * K2), K / 4);
     }
-
-    // ---- phase A: unary exponent codes -> exps[kept index]
+    Hit h1, h0;
+    bool clean;
+    const int ones = bitmap_selects(a.bitmap + (size_t)n * KW, bm_s, KW, r.k0, h1, h0, clean);
     uint32_t s0 = __ldg(a.rowstart + n), s1 = __ldg(a.rowstart + n + 1);
-    if (s1 < s0 || (int64_t)s1 > a.stream_words) {
-      if (lane == 0) flag(a.err);
-      s1 = s0;
-    }
-    const int nwords = (int)(s1 - s0);
-    int count = 0;       // codewords so far (warp-uniform)
-    int carry = -1;      // row-relative bit position of the last one so far
-    for (int c = 0; c < nwords; c += 32) {
-      const int wi = c + lane;
-      const uint32_t w = wi < nwords ? __ldg(a.stream + s0 + wi) : 0u;
-      const int cnt = __popc(w);
-      int incl = cnt;
+    bool bad = ones != K2;
+    if (s1 < s0 || (int64_t)s1 > a.stream_words) bad = true, s1 = s0;
+    const int nsw = (int)(s1 - s0);
+    const uint32_t* sg = a.stream + s0;
+    const bool fits = nsw <= a.scap;
+    Hit hs;
+    hs.w = 0u, hs.r = 0, hs.wi = nsw;
+    int codes = 0;
+    int first_zero = nsw, last_set = -1;  // an empty word before the last one needs the safe walk
+    for (int c = 0; c < nsw; c += 128) {
+      uint32_t q[4];
+      load_quad(sg, nsw, c, false, q);
+      const int w0 = c + 4 * lane;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+      for (int i = 0; i < 4; ++i) {
+        if (w0 + i < nsw) {
+          if (fits) st_s[w0 + i] = q[i];
+          if (q[i]) last_set = w0 + i;
+          else first_zero = min(first_zero, w0 + i);
+        }
       }
-      const int lastpos = w ? wi * 32 + 31 - __clz(w) : -1;
-      int mx = lastpos;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, mx, o);
-        if (lane >= o) mx = max(mx, t);
-      }
-      int prev = __shfl_up_sync(0xffffffffu, mx, 1);
-      prev = lane == 0 ? carry : max(prev, carry);
-      int k = count + incl - cnt;
-      uint32_t bits = w;
-      bool bad = false;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int pos = wi * 32 + b;
-        const int rank = pos - prev - 1;
-        prev = pos;
-        uint8_t e = 0;
-        if (rank < a.n_symbols) e = cb[rank]; else bad = true;
-        if (k < K2) exps[k] = e; else bad = true;
-        ++k;
-      }
-      if (bad) flag(a.err);
-      count += __shfl_sync(0xffffffffu, incl, 31);
-      carry = max(carry, __shfl_sync(0xffffffffu, mx, 31));
+      codes += select_chunk(q, c, r.k0 - 1, codes, hs);
     }
-    if (count != K2 && lane == 0) flag(a.err);
+    first_zero = __reduce_min_sync(0xffffffffu, first_zero);
+    last_set = __reduce_max_sync(0xffffffffu, last_set);
+    if (codes != K2) bad = true;
     __syncwarp();
 
-    // ---- phase B: rebuild each column's bf16 value and accumulate w * x,
-    // four bitmap words per iteration (their kept counts prefix-summed first)
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    int kbase = 0;
-    uint16_t* wrow = a.w_out ? a.w_out + (size_t)n * K : nullptr;
-    auto column = [&](uint32_t word, int it, int kb) {
-      const int j = it * 32 + lane;
-      const bool kept = (word >> lane) & 1u;
-      const int kidx = kb + __popc(word & below);
-      uint32_t v = 0;
-      if (kept) {
-        if (kidx < K2) {
-          const uint32_t nib = (sm_s[kidx >> 3] >> ((kidx & 7) * 4)) & 0xFu;
-          v = ((nib >> 3) << 15) | ((uint32_t)exps[kidx] << 7) | ((nib & 7u) << 4);
-          if (TARGET) v |= (lo_s[kidx >> 3] >> ((kidx & 7) * 4)) & 0xFu;
-        }
-      } else if (TARGET) {
-        const int pidx = j - kidx;
-        if (pidx < K2) v = pr_s[pidx];
-      }
-      if (wrow) wrow[j] = (uint16_t)v;
-      const float wf = __uint_as_float(v << 16);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = fmaf(wf, xs[(size_t)m * K + j], acc[m]);
-    };
-    int it = 0;
-    for (; it + 4 <= K / 32; it += 4) {
-      const uint4 w4 = reinterpret_cast<const uint4*>(bm_s)[it >> 2];
-      const int k1 = kbase + __popc(w4.x), k2 = k1 + __popc(w4.y), k3 = k2 + __popc(w4.z);
-      column(w4.x, it, kbase);
-      column(w4.y, it + 1, k1);
-      column(w4.z, it + 2, k2);
-      column(w4.w, it + 3, k3);
-      kbase = k3 + __popc(w4.w);
-    }
-    for (; it < K / 32; ++it) {
-      const uint32_t word = bm_s[it];
-      column(word, it, kbase);
-      kbase += __popc(word);
-    }
-    if (kbase != K2 && lane == 0) flag(a.err);
-    if (a.y) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        float v = acc[m];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) a.y[(size_t)m * a.ldy + n] = v;
+    bool lbad = false;
+    if (!bad && r.cnt > 0) {
+      r.nsw = nsw;
+      r.send = r.k0 == 0 ? 0 : hit_pos(hs) + 1;
+      r.kpos = hit_pos(h1);
+      r.zpos = hit_pos(h0);
+      r.wrow = WOUT ? a.w_out + (size_t)n * K : nullptr;
+      if (!WOUT && (K & 511) == 0 && fits && clean && first_zero > last_set) {
+        r.st = st_s;
+        cass_walk8<MT, TARGET>(r, acc, lbad);
+      } else if (fits && clean && first_zero > last_set) {
+        r.st = st_s;
+        cass_walk<MT, TARGET, WOUT, false>(r, acc, lbad);
+      } else {
+        r.st = fits ? st_s : sg;
+        cass_walk<MT, TARGET, WOUT, true>(r, acc, lbad);
       }
     }
+    if ((__any_sync(0xffffffffu, lbad) || bad) && lane == 0) flag(a.err);
+    if (a.y) store_row<MT>(acc, a.y, a.ldy, n);
     __syncwarp();  // the staged row buffers are reused by the next row
   }
 }
@@ -232,131 +535,221 @@ struct CassMxArgs {
   const uint16_t* pruned;    // [N][K/2]
   const uint16_t* x;         // bf16 [M][ldx]
   float* y;                  // [M][ldy] or null
-  uint16_t* w_out;           // [N][K] or null
+  uint16_t* w_out;           // [N][K] or null (written by the WOUT kernels only)
   int N, K, ldx, ldy;
+  int sk;                    // activation unit skew shift
   int* err;
 };
 
 __host__ __device__ inline size_t cassmx_per_warp(size_t K, bool target) {
-  // bitmap, signs, dnib, group scales (+ target: lnib, pruned)
-  return (K / 8 + K / 16 + K / 4 + K / 16 + (target ? K / 4 + K : 0) + 15) / 16 * 16;
+  // bitmap, signs, draft nibbles, group scales (+ target: low nibbles, pruned halves)
+  const size_t w = K / 32 + 2 + K / 64 + skewed_words(K / 16, 3) + K / 64 +
+                   (target ? skewed_words(K / 16, 3) + skewed_words(K / 4, 5) : 0);
+  return (w * 4 + 15) / 16 * 16;
 }
 
-// One warp per row, rows strided over a persistent grid. The row's sections are
-// staged in shared memory together with one fp32 scale per group of 32 kept
-// values (2^(g - 134) for the target, 2^(g - 130) for the draft), so a kept
-// column's value is one nibble lookup times its group's scale: no per-value
-// exponent decode. Lane l owns column 32*i + l of each bitmap word, as in the
-// Cassandra-1 kernel; values are exact in fp32 and in bf16.
+struct MxRow {
+  const uint32_t *bm, *sg, *dn, *ln, *pr;
+  const float* sc;
+  const uint16_t* xs;
+  uint16_t* wrow;
+  int KW, sk, k0, cnt, kpos, zpos;
+};
+
+// The rank walk with no exponent stream: the kept value of rank k is its
+// nibble(s) times the fp32 scale of its group of 32 (2^(g - 134) for the
+// target, 2^(g - 130) for the draft), sign from the sign bits; exact in fp32
+// and in bf16.
+template <int MT, bool TARGET, bool WOUT, bool SAFE>
+__device__ __forceinline__ void cassmx_walk(const MxRow& r, float (&acc)[MT], bool& bad) {
+  Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
+  Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  uint32_t dw = r.dn[skew<3>(r.k0 >> 3)];
+  uint32_t lw = TARGET ? r.ln[skew<3>(r.k0 >> 3)] : 0u;
+  uint32_t sgw = r.sg[r.k0 >> 5];
+  float scl = r.sc[r.k0 >> 5];
+  uint32_t prw = TARGET ? r.pr[skew<5>(r.k0 >> 1)] : 0u;
+  for (int k = r.k0; k < r.k0 + r.cnt; ++k) {
+    const int j = cursor_next<false, SAFE>(ck, r.bm, r.KW, bad);
+    if ((k & 7) == 0) {
+      dw = r.dn[skew<3>(k >> 3)];
+      if (TARGET) lw = r.ln[skew<3>(k >> 3)];
+    }
+    if ((k & 31) == 0) sgw = r.sg[k >> 5], scl = r.sc[k >> 5];
+    const int sh = (k & 7) * 4;
+    uint32_t mag = (dw >> sh) & 0xFu;
+    if (TARGET) mag = (mag << 4) | ((lw >> sh) & 0xFu);
+    float v = (float)mag * scl;
+    if ((sgw >> (k & 31)) & 1u) v = -v;
+    if (WOUT) r.wrow[j] = (uint16_t)(__float_as_uint(v) >> 16);
+    accumulate<MT>(r.xs, j, r.sk, v, acc);
+    if (TARGET || WOUT) {
+      const int jz = cursor_next<true, SAFE>(cz, r.bm, r.KW, bad);
+      uint32_t pv = 0;
+      if (TARGET) {
+        if ((k & 1) == 0) prw = r.pr[skew<5>(k >> 1)];
+        pv = k & 1 ? prw >> 16 : prw & 0xFFFFu;
+        accumulate<MT>(r.xs, jz, r.sk, __uint_as_float(pv << 16), acc);
+      }
+      if (WOUT) r.wrow[jz] = (uint16_t)pv;
+    }
+  }
+}
+
+// Unrolled by 8 for clean rows and K a multiple of 512, as cass_walk8.
 template <int MT, bool TARGET>
+__device__ __forceinline__ void cassmx_walk8(const MxRow& r, float (&acc)[MT]) {
+  Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
+  Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  for (int k = r.k0; k < r.k0 + r.cnt; k += 8) {
+    const uint32_t dw = r.dn[skew<3>(k >> 3)];
+    const uint32_t lw = TARGET ? r.ln[skew<3>(k >> 3)] : 0u;
+    const uint32_t sgb = r.sg[k >> 5] >> (k & 24);
+    const float scl = r.sc[k >> 5];
+    uint32_t prw[4];
+    if (TARGET) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) prw[i] = r.pr[skew<5>((k >> 1) + i)];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t mag = (dw >> (4 * u)) & 0xFu;
+      if (TARGET) mag = (mag << 4) | ((lw >> (4 * u)) & 0xFu);
+      const float v = __uint_as_float(__float_as_uint((float)mag * scl) ^ (((sgb >> u) & 1u) << 31));
+      accumulate<MT>(r.xs, cursor_step<false>(ck, r.bm), r.sk, v, acc);
+      if (TARGET) {
+        const uint32_t pv = u & 1 ? prw[u >> 1] >> 16 : prw[u >> 1] & 0xFFFFu;
+        accumulate<MT>(r.xs, cursor_step<true>(cz, r.bm), r.sk, __uint_as_float(pv << 16), acc);
+      }
+    }
+  }
+}
+
+template <int MT, bool TARGET, bool WOUT>
 __global__ void __launch_bounds__(kCassWarpsMax * 32) cassmx_kernel(const CassMxArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int K = a.K;
-  const int K2 = K / 2;
-  const int KG = K / 64;
-  const int nwarps = blockDim.x / 32;
-  float* xs = reinterpret_cast<float*>(smem);  // [MT][K] fp32
+  constexpr int P = XPad<MT>::P;
+  const int K = a.K, K2 = K / 2, KW = K / 32, KG = K / 64;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  unsigned char* wb = smem + (size_t)MT * K * 4 + (size_t)warp * cassmx_per_warp(K, TARGET);
-  uint32_t* bm_s = reinterpret_cast<uint32_t*>(wb);
-  uint32_t* sg_s = bm_s + K / 32;
-  uint32_t* dn_s = sg_s + K / 64;
-  float* sc_s = reinterpret_cast<float*>(dn_s + K / 16);
+  const int nwarps = blockDim.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  const size_t xb = xs_bytes(K, a.sk, P);
+  uint32_t* bm_s = reinterpret_cast<uint32_t*>(smem + xb + (size_t)warp * cassmx_per_warp(K, TARGET));
+  uint32_t* sg_s = bm_s + KW + 2;
+  uint32_t* dn_s = sg_s + KG;
+  float* sc_s = reinterpret_cast<float*>(dn_s + skewed_words(K / 16, 3));
   uint32_t* ln_s = reinterpret_cast<uint32_t*>(sc_s + KG);
-  uint16_t* pr_s = reinterpret_cast<uint16_t*>(ln_s + (TARGET ? K / 16 : 0));
+  uint32_t* pr_s = ln_s + (TARGET ? skewed_words(K / 16, 3) : 0);
 
-  for (int m = 0; m < MT; ++m)
-    for (int j = threadIdx.x; j < K; j += blockDim.x)
-      xs[(size_t)m * K + j] = __uint_as_float((uint32_t)a.x[(size_t)m * a.ldx + j] << 16);
+  stage_x<MT>(xs, a.x, a.ldx, K, a.sk);
   __syncthreads();
 
-  const uint32_t below = lanemask_lt();
-  const int gw = blockIdx.x * nwarps + warp;
-  const int stride = gridDim.x * nwarps;
-  for (int n = gw; n < a.N; n += stride) {
-    for (int i = lane; i < K / 32; i += 32) bm_s[i] = __ldg(a.bitmap + (size_t)n * (K / 32) + i);
-    for (int i = lane; i < K / 64; i += 32) sg_s[i] = __ldg(a.signs + (size_t)n * (K / 64) + i);
-    for (int i = lane; i < K / 16; i += 32) dn_s[i] = __ldg(a.dnib + (size_t)n * (K / 16) + i);
-    for (int i = lane; i < KG; i += 32)
+  MxRow r;
+  r.bm = bm_s, r.sg = sg_s, r.dn = dn_s, r.ln = ln_s, r.pr = pr_s, r.sc = sc_s, r.xs = xs;
+  r.KW = KW, r.sk = a.sk;
+  r.k0 = (int)(((int64_t)lane * K2) >> 5);
+  r.cnt = (int)(((int64_t)(lane + 1) * K2) >> 5) - r.k0;
+  for (int n = blockIdx.x * nwarps + warp; n < a.N; n += gridDim.x * nwarps) {
+    for (int i = lane; i < KG; i += 32) {
+      sg_s[i] = __ldg(a.signs + (size_t)n * KG + i);
       sc_s[i] = ldexpf(1.f, (int)__ldg(a.gexp + (size_t)n * KG + i) - (TARGET ? 134 : 130));
-    if (TARGET) {
-      for (int i = lane; i < K / 16; i += 32) ln_s[i] = __ldg(a.lnib + (size_t)n * (K / 16) + i);
-      for (int i = lane; i < K2; i += 32) pr_s[i] = __ldg(a.pruned + (size_t)n * K2 + i);
     }
+    stage_words<3>(dn_s, a.dnib + (size_t)n * (K / 16), K / 16);
+    if (TARGET) {
+      stage_words<3>(ln_s, a.lnib + (size_t)n * (K / 16), K / 16);
+      stage_words<5>(pr_s, reinterpret_cast<const uint32_t*>(a.pruned + (size_t)n * K2), K / 4);
+    }
+    Hit h1, h0;
+    bool clean;
+    const bool bad = bitmap_selects(a.bitmap + (size_t)n * KW, bm_s, KW, r.k0, h1, h0, clean) != K2;
     __syncwarp();
 
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    uint16_t* wrow = a.w_out ? a.w_out + (size_t)n * K : nullptr;
-    int kbase = 0;
-    bool bad = false;
-    for (int it = 0; it < K / 32; ++it) {
-      const uint32_t word = bm_s[it];
-      const int j = it * 32 + lane;
-      const int kidx = kbase + __popc(word & below);
-      float v = 0.f;
-      if ((word >> lane) & 1u) {
-        if (kidx < K2) {
-          const uint32_t sh = (kidx & 7) * 4;
-          uint32_t mag = (dn_s[kidx >> 3] >> sh) & 0xFu;
-          if (TARGET) mag = (mag << 4) | ((ln_s[kidx >> 3] >> sh) & 0xFu);
-          v = (float)mag * sc_s[kidx >> 5];
-          if ((sg_s[kidx >> 5] >> (kidx & 31)) & 1u) v = -v;
-        } else {
-          bad = true;
-        }
-      } else if (TARGET) {
-        const int pidx = j - kidx;
-        if (pidx < K2) v = __uint_as_float((uint32_t)pr_s[pidx] << 16);
-        else bad = true;
-      }
-      if (wrow) wrow[j] = (uint16_t)(__float_as_uint(v) >> 16);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = fmaf(v, xs[(size_t)m * K + j], acc[m]);
-      kbase += __popc(word);
+    bool lbad = false;
+    if (!bad && r.cnt > 0) {
+      r.kpos = hit_pos(h1);
+      r.zpos = hit_pos(h0);
+      r.wrow = WOUT ? a.w_out + (size_t)n * K : nullptr;
+      if (!WOUT && (K & 511) == 0 && clean) cassmx_walk8<MT, TARGET>(r, acc);
+      else if (clean) cassmx_walk<MT, TARGET, WOUT, false>(r, acc, lbad);
+      else cassmx_walk<MT, TARGET, WOUT, true>(r, acc, lbad);
     }
-    if (bad || (kbase != K2 && lane == 0)) flag(a.err);
-    if (a.y) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        float t = acc[m];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) a.y[(size_t)m * a.ldy + n] = t;
-      }
-    }
+    if ((__any_sync(0xffffffffu, lbad) || bad) && lane == 0) flag(a.err);
+    if (a.y) store_row<MT>(acc, a.y, a.ldy, n);
     __syncwarp();  // the staged row buffers are reused by the next row
   }
 }
 
-template <bool TARGET>
-int launch_cassmx(const CassMxArgs& a, int M, cudaStream_t s) {
-  const size_t K = a.K;
-  const size_t per_warp = cassmx_per_warp(K, TARGET);
-  const size_t fixed = (size_t)M * K * 4;
+// Activation unit skew: 2^sk about the K/32 columns one lane covers.
+inline int x_skew(int K) {
+  int sk = 0;
+  while ((2 << sk) <= K / 32) ++sk;
+  return sk;
+}
+
+template <class Args>
+int launch_rows(const void* kern, const Args& a, size_t fixed, size_t per_warp, const char* what, cudaStream_t s) {
   const size_t cap = 227 * 1024 - 1024;
-  if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%zu with M=%d does not fit shared memory", K, M);
+  if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%d does not fit shared memory", a.K);
   const int warps = (int)std::min<size_t>(kCassWarpsMax, (cap - fixed) / per_warp);
   const size_t smem = fixed + per_warp * warps;
-  const void* kern = nullptr;
-  switch (M) {
-#define QMV_CASSMX_CASE(m) \
-  case m: kern = (const void*)cassmx_kernel<m, TARGET>; break;
-    QMV_CASSMX_CASE(1) QMV_CASSMX_CASE(2) QMV_CASSMX_CASE(3) QMV_CASSMX_CASE(4)
-    QMV_CASSMX_CASE(5) QMV_CASSMX_CASE(6) QMV_CASSMX_CASE(7) QMV_CASSMX_CASE(8)
-#undef QMV_CASSMX_CASE
-    default: return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
-  }
   int per_sm = 0;
   int rc = kernel_fit(kern, warps * 32, smem, &per_sm);
   if (rc) return rc;
   const int grid = std::max(1, std::min(sm_count() * per_sm, (a.N + warps - 1) / warps));
-  void* args[] = {const_cast<CassMxArgs*>(&a)};
+  void* args[] = {const_cast<Args*>(&a)};
   cudaError_t e = cudaLaunchKernel(kern, grid, warps * 32, args, smem, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cassandra-2 launch");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   return QMV_OK;
+}
+
+// Kernels with M = 1..8 activation rows; a dense w_out is written by the
+// M = 1 WOUT variant (which then also serves y when M = 1), so the matvec
+// kernels carry no per-value stores.
+template <template <int, bool, bool> class Pick, class Args, bool TARGET>
+int launch_pair(Args& a, int M, size_t fixed_extra, size_t per_warp, const char* what, cudaStream_t s) {
+  if (M < 1 || M > 8) return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
+  const int P = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+  int rc = QMV_OK;
+  if (a.w_out) {
+    Args b = a;
+    if (M != 1) b.y = nullptr;
+    rc = launch_rows(Pick<1, TARGET, true>::get(), b, xs_bytes(a.K, a.sk, 1) + fixed_extra, per_warp, what, s);
+    if (rc || M == 1 || !a.y) return rc;
+  }
+  if (!a.y) return rc;
+  Args b = a;
+  b.w_out = nullptr;
+  const void* kern = nullptr;
+  switch (M) {
+    case 1: kern = Pick<1, TARGET, false>::get(); break;
+    case 2: kern = Pick<2, TARGET, false>::get(); break;
+    case 3: kern = Pick<3, TARGET, false>::get(); break;
+    case 4: kern = Pick<4, TARGET, false>::get(); break;
+    case 5: kern = Pick<5, TARGET, false>::get(); break;
+    case 6: kern = Pick<6, TARGET, false>::get(); break;
+    case 7: kern = Pick<7, TARGET, false>::get(); break;
+    default: kern = Pick<8, TARGET, false>::get(); break;
+  }
+  return launch_rows(kern, b, xs_bytes(a.K, a.sk, P) + fixed_extra, per_warp, what, s);
+}
+
+template <int MT, bool TARGET, bool WOUT>
+struct PickCass {
+  static const void* get() { return (const void*)cass_kernel<MT, TARGET, WOUT>; }
+};
+template <int MT, bool TARGET, bool WOUT>
+struct PickCassMx {
+  static const void* get() { return (const void*)cassmx_kernel<MT, TARGET, WOUT>; }
+};
+
+template <bool TARGET>
+int launch_cassmx(CassMxArgs& a, int M, cudaStream_t s) {
+  a.sk = x_skew(a.K);
+  return launch_pair<PickCassMx, CassMxArgs, TARGET>(a, M, 0, cassmx_per_warp(a.K, TARGET), "cassandra-2 launch", s);
 }
 
 // ----------------------------------------------------------------------------- online KV encoder
@@ -521,31 +914,11 @@ __global__ void __launch_bounds__(kEncWarps * 32) kv_encode_kernel(const __grid_
 }
 
 template <bool TARGET>
-int launch_cass(const CassArgs& a, int M, cudaStream_t s) {
-  const size_t K = a.K;
-  const size_t per_warp = (K / 2 + K / 8 + K / 4 + (TARGET ? K / 4 + K : 0) + 15) / 16 * 16;
-  const size_t fixed = (size_t)M * K * 4 + 256;
-  const size_t cap = 227 * 1024 - 1024;
-  if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%zu with M=%d does not fit shared memory", K, M);
-  const int warps = (int)std::min<size_t>(kCassWarpsMax, (cap - fixed) / per_warp);
-  const size_t smem = fixed + per_warp * warps;
-  const void* kern = nullptr;
-  switch (M) {
-#define QMV_CASS_CASE(m) \
-  case m: kern = (const void*)cass_kernel<m, TARGET>; break;
-    QMV_CASS_CASE(1) QMV_CASS_CASE(2) QMV_CASS_CASE(3) QMV_CASS_CASE(4)
-    QMV_CASS_CASE(5) QMV_CASS_CASE(6) QMV_CASS_CASE(7) QMV_CASS_CASE(8)
-#undef QMV_CASS_CASE
-    default: return fail(QMV_ERR_ARG, "M=%d outside 1..8", M);
-  }
-  int per_sm = 0;
-  int rc = kernel_fit(kern, warps * 32, smem, &per_sm);
-  if (rc) return rc;
-  const int grid = std::max(1, std::min(sm_count() * per_sm, (a.N + warps - 1) / warps));
-  void* args[] = {const_cast<CassArgs*>(&a)};
-  cudaError_t e = cudaLaunchKernel(kern, grid, warps * 32, args, smem, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cassandra launch");
-  return QMV_OK;
+int launch_cass(CassArgs& a, int M, cudaStream_t s) {
+  a.sk = x_skew(a.K);
+  a.scap = std::max(4, a.K / 8);  // 4 bits per kept value; longer rows are read in place
+  return launch_pair<PickCass, CassArgs, TARGET>(a, M, cass_tab_bytes(a.n_symbols), cass_per_warp(a.K, a.scap, TARGET),
+                                                "cassandra launch", s);
 }
 
 int check_cass_desc(const qmv_desc* d) {

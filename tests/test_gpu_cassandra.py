@@ -92,6 +92,42 @@ def test_special_values_roundtrip(env):
     assert np.array_equal(_u16(wd), cs.draft(ref, meta))
 
 
+def _edge_rows(K, seed):
+    """Rows that defeat a one-word cursor step: row 0 prunes a whole 32-column word, row 1 keeps
+    one, row 2 keeps values of 40 distinct exponents once each (unary codes of rank >= 32, so
+    empty stream words), the other rows are ordinary."""
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(seed)
+    w = synth.student_t4(g, (24, K))
+    w[0, 0:32] = 1e-7
+    w[1, 32:64] = 1.0
+    w[2, :] = 1e-30
+    w[2, 0:40] = [2.0 ** -e for e in range(1, 41)]
+    w[2, 40:K // 2] = 0.75
+    return synth.to_bf16_bits(w)
+
+
+@pytest.mark.parametrize("K", [256, 512])
+@pytest.mark.parametrize("M", [1, 3])
+def test_rows_with_empty_words(env, M, K):
+    """Full-word runs in the bitmap and empty exponent-stream words: bit-exact weights, y in tolerance."""
+    q, torch, dev = env
+    from oracle import cassandra as cs
+    from oracle.matvec import matvec_bf16x
+    from oracle.numerics import bf16_bits_to_f64
+    from quantized_gemv_unpack_gb300 import synth
+    W = _edge_rows(K, 41)
+    X, _ = synth.calibration_bf16(synth.rng(42), 8, K)
+    X[:] = synth.to_bf16_bits(np.ones(X.shape, np.float32))
+    ref, meta = cs.pack(W, X)
+    assert not meta["keep"][0, :32].any() and meta["keep"][1, 32:64].all()
+    d, packed, xb, yd, yt, wd, wt = _run(q, torch, dev, W, X, M, 43)
+    assert np.array_equal(wt, W) and np.array_equal(wd, cs.draft(ref, meta))
+    for y, Wr in ((yd, cs.draft(ref, meta)), (yt, W)):
+        yr, B = matvec_bf16x(bf16_bits_to_f64(Wr), xb)
+        assert np.all(np.abs(y - yr) <= RTOL * B)
+
+
 def test_mlp_matrix_full_size_sampled(env):
     """The 14336 x 4096 MLP matrix with 128 calibration rows (1% outlier channels x20): draft at M=1,
     target at M=5; reconstruction checked on every weight, draft weights and outputs on sampled rows."""

@@ -90,6 +90,41 @@ def test_mx_special_values(env):
     assert np.array_equal(wt.cpu().numpy().view(np.uint16), mx.reconstruct(ref, meta))
 
 
+@pytest.mark.parametrize("K", [256, 512])
+@pytest.mark.parametrize("M", [1, 3])
+def test_mx_rows_with_full_bitmap_words(env, M, K):
+    """A row pruning a whole 32-column word and one keeping one: bit-exact weights, y in tolerance."""
+    q, torch, dev = env
+    from oracle import cassandra_mx as mx
+    from oracle.matvec import matvec_bf16x
+    from oracle.numerics import bf16_bits_to_f64
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(44)
+    w = synth.student_t4(g, (24, K))
+    w[0, 0:32] = 1e-7
+    w[1, 32:64] = 1.0
+    W = synth.to_bf16_bits(w)
+    X = synth.to_bf16_bits(np.ones((8, K), np.float32))
+    ref, meta = mx.pack(W, X)
+    d, buf = q.cass_mx_pack_host(W, X)
+    packed = torch.from_numpy(buf).to(dev)
+    xb = synth.activations_bf16(synth.rng(45), (M, K))
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    yd = torch.empty((M, 24), device=dev)
+    yt = torch.empty((M, 24), device=dev)
+    wd = torch.empty((24, K), dtype=torch.int16, device=dev)
+    wt = torch.empty((24, K), dtype=torch.int16, device=dev)
+    q.cass_decode_draft(d, packed, x, yd, wd)
+    q.cass_reconstruct(d, packed, x, yt, wt)
+    assert q.qmv_check_status() == 0
+    draft, target = mx.draft(ref, meta), mx.reconstruct(ref, meta)
+    assert np.array_equal(wd.cpu().numpy().view(np.uint16), draft)
+    assert np.array_equal(wt.cpu().numpy().view(np.uint16), target)
+    for y, Wr in ((yd, draft), (yt, target)):
+        yr, B = matvec_bf16x(bf16_bits_to_f64(Wr), xb)
+        assert np.all(np.abs(y.cpu().numpy() - yr) <= RTOL * B)
+
+
 def test_mx_full_mlp_matrix_sampled(env):
     """The 14336 x 4096 MLP matrix of the Cassandra workload: target weights of sampled rows
     bit-exact, matvec of sampled rows within the bound."""
