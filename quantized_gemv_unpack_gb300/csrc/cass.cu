@@ -41,7 +41,12 @@
 namespace qmv {
 namespace {
 
-constexpr int kCassWarpsMax = 16;
+// Warps per CTA: 32 where the kernel fits 64 registers a thread, else 16.
+template <int MT, bool TARGET>
+struct CassWarps {
+  static constexpr int value = TARGET && MT > 5 ? 16 : 32;
+};
+inline int cass_warps(int M, bool target) { return target && M > 5 ? 16 : 32; }
 
 __device__ __forceinline__ void flag(int* err) { atomicCAS(err, 0, (int)QMV_ERR_CORRUPT); }
 
@@ -230,23 +235,23 @@ __device__ __forceinline__ int bitmap_selects(const uint32_t* src, uint32_t* bm_
 // A forward cursor over the set bits (INV: the clear bits) of a word array,
 // with the next word preloaded.
 struct Cursor {
-  uint32_t w;   // the unread bits of word wi
-  uint32_t nx;  // word wi + 1
+  uint32_t w;   // the unread bits of word wi (inverted for INV)
+  uint32_t nx;  // word wi + 1 as stored
   int wi;
 };
 
 template <bool INV>
-__device__ __forceinline__ uint32_t cursor_word(const uint32_t* s, int nw, int i) {
-  const uint32_t raw = i < nw ? s[i] : (INV ? 0xffffffffu : 0u);
-  return INV ? ~raw : raw;
+__device__ __forceinline__ uint32_t cursor_raw(const uint32_t* s, int nw, int i) {
+  return i < nw ? s[i] : (INV ? 0xffffffffu : 0u);
 }
 
 template <bool INV>
 __device__ __forceinline__ Cursor cursor_at(const uint32_t* s, int nw, int pos) {
   Cursor c;
   c.wi = pos >> 5;
-  c.w = cursor_word<INV>(s, nw, c.wi) & (0xffffffffu << (pos & 31));
-  c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+  const uint32_t raw = cursor_raw<INV>(s, nw, c.wi);
+  c.w = (INV ? ~raw : raw) & (0xffffffffu << (pos & 31));
+  c.nx = cursor_raw<INV>(s, nw, c.wi + 1);
   return c;
 }
 
@@ -257,9 +262,9 @@ __device__ __forceinline__ Cursor cursor_at(const uint32_t* s, int nw, int pos) 
 template <bool INV, bool SAFE>
 __device__ __forceinline__ int cursor_next(Cursor& c, const uint32_t* s, int nw, bool& bad) {
   if (c.w == 0) {
-    c.w = c.nx;
+    c.w = INV ? ~c.nx : c.nx;
     ++c.wi;
-    c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+    c.nx = cursor_raw<INV>(s, nw, c.wi + 1);
   }
   if (SAFE) {
     while (c.w == 0) {
@@ -267,9 +272,9 @@ __device__ __forceinline__ int cursor_next(Cursor& c, const uint32_t* s, int nw,
         bad = true;
         return 0;
       }
-      c.w = c.nx;
+      c.w = INV ? ~c.nx : c.nx;
       ++c.wi;
-      c.nx = cursor_word<INV>(s, nw, c.wi + 1);
+      c.nx = cursor_raw<INV>(s, nw, c.wi + 1);
     }
   }
   const int b = __ffs(c.w) - 1;
@@ -277,20 +282,26 @@ __device__ __forceinline__ int cursor_next(Cursor& c, const uint32_t* s, int nw,
   return c.wi * 32 + b;
 }
 
-// The fast-walk step: the caller guarantees that the bit exists and that no
-// word before it is empty, and pads the array so that word wi + 1 can always
-// be read; the refill is then branch-free.
+// The fast-walk step over a shared-memory array (`base` its shared address):
+// the caller guarantees that the bit exists and that no word before it is
+// empty, and pads the array so that word wi + 1 can be read. The refill is
+// branch-free and only the lanes that refill load (a predicated load), which
+// keeps the cursors off the shared-memory banks most steps.
 template <bool INV>
-__device__ __forceinline__ int cursor_step(Cursor& c, const uint32_t* s) {
-  const bool e = c.w == 0;
-  c.w = e ? c.nx : c.w;
-  c.wi += e ? 1 : 0;
-  const uint32_t raw = s[c.wi + 1];  // unchanged when e is false
-  c.nx = INV ? ~raw : raw;
+__device__ __forceinline__ int cursor_step(Cursor& c, uint32_t base) {
+  const uint32_t e = c.w == 0;
+  c.w = e ? (INV ? ~c.nx : c.nx) : c.w;
+  c.wi += e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p ld.shared.u32 %0, [%2];\n\t}"
+      : "+r"(c.nx)
+      : "r"(e), "r"(base + 4u * (uint32_t)(c.wi + 1)));
   const int b = __ffs(c.w) - 1;
   c.w &= c.w - 1;
   return c.wi * 32 + b;
 }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 template <int MT>
 __device__ __forceinline__ void accumulate(const uint16_t* xs, int j, int sk, float w, float (&acc)[MT]) {
@@ -331,12 +342,12 @@ struct CassArgs {
   int* err;
 };
 
-// Shared memory of one warp: bitmap, nibbles (+ target: low nibbles, pruned
-// halves), staged stream; the bitmap and the stream carry two pad words for
-// the fast walk's read-ahead.
+// Shared memory of one warp: bitmap, nibbles (+ target: low nibbles), staged
+// stream; the bitmap and the stream carry two pad words for the fast walk's
+// read-ahead. Pruned halves are read from global memory, each lane's run
+// being contiguous.
 __host__ __device__ inline size_t cass_per_warp(size_t K, size_t scap, bool target) {
-  const size_t w = K / 32 + 2 + skewed_words(K / 16, 3) + (target ? skewed_words(K / 16, 3) + skewed_words(K / 4, 5) : 0) +
-                   scap + 2;
+  const size_t w = K / 32 + 2 + skewed_words(K / 16, 3) + (target ? skewed_words(K / 16, 3) : 0) + scap + 2;
   return (w * 4 + 15) / 16 * 16;
 }
 
@@ -346,7 +357,8 @@ __host__ __device__ inline size_t cass_tab_bytes(int n_symbols) { return ((size_
 
 // The staged row one lane walks.
 struct CassRow {
-  const uint32_t *bm, *sm, *lo, *pr, *st;
+  const uint32_t *bm, *sm, *lo, *st;
+  const uint16_t* prg;  // the row's pruned halves (global)
   const uint16_t* tab;
   const uint16_t* xs;
   uint16_t* wrow;
@@ -365,7 +377,6 @@ __device__ __forceinline__ void cass_walk(const CassRow& r, float (&acc)[MT], bo
   int send = r.send;
   uint32_t smw = r.sm[skew<3>(r.k0 >> 3)];
   uint32_t low = TARGET ? r.lo[skew<3>(r.k0 >> 3)] : 0u;
-  uint32_t prw = TARGET ? r.pr[skew<5>(r.k0 >> 1)] : 0u;
   for (int k = r.k0; k < r.k0 + r.cnt; ++k) {
     const int sp = cursor_next<false, SAFE>(cs, r.st, r.nsw, bad);
     int rank = sp - send;
@@ -385,13 +396,21 @@ __device__ __forceinline__ void cass_walk(const CassRow& r, float (&acc)[MT], bo
       const int jz = cursor_next<true, SAFE>(cz, r.bm, r.KW, bad);
       uint32_t pv = 0;
       if (TARGET) {
-        if ((k & 1) == 0) prw = r.pr[skew<5>(k >> 1)];
-        pv = k & 1 ? prw >> 16 : prw & 0xFFFFu;
+        pv = __ldg(r.prg + k);
         accumulate<MT>(r.xs, jz, r.sk, __uint_as_float(pv << 16), acc);
       }
       if (WOUT) r.wrow[jz] = (uint16_t)pv;
     }
   }
+}
+
+// Pruned halves of ranks k .. k + 7 (16-byte aligned: k is a multiple of 8).
+__device__ __forceinline__ uint4 pruned_block(const uint16_t* prg, int k) {
+  return __ldg(reinterpret_cast<const uint4*>(prg + k));
+}
+__device__ __forceinline__ uint32_t block_half(const uint4& v, int u) {
+  const uint32_t w = u < 2 ? v.x : u < 4 ? v.y : u < 6 ? v.z : v.w;
+  return u & 1 ? w >> 16 : w & 0xFFFFu;
 }
 
 // The same walk for rows with no empty word in the way and K a multiple of
@@ -402,34 +421,31 @@ __device__ __forceinline__ void cass_walk8(const CassRow& r, float (&acc)[MT], b
   Cursor cs = cursor_at<false>(r.st, r.nsw, r.send);
   Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
   Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  const uint32_t st_base = smem_u32(r.st), bm_base = smem_u32(r.bm);
   int send = r.send;
+  uint4 pnext = TARGET ? pruned_block(r.prg, r.k0) : make_uint4(0, 0, 0, 0);
   for (int k = r.k0; k < r.k0 + r.cnt; k += 8) {
     const uint32_t smw = r.sm[skew<3>(k >> 3)];
     const uint32_t low = TARGET ? r.lo[skew<3>(k >> 3)] : 0u;
-    uint32_t prw[4];
-    if (TARGET) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) prw[i] = r.pr[skew<5>((k >> 1) + i)];
-    }
+    const uint4 pcur = pnext;
+    if (TARGET && k + 8 < r.k0 + r.cnt) pnext = pruned_block(r.prg, k + 8);  // one block ahead
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int sp = cursor_step<false>(cs, r.st);
+      const int sp = cursor_step<false>(cs, st_base);
       int rank = sp - send;
       send = sp + 1;
       if ((unsigned)rank >= (unsigned)r.nsym) bad = true, rank = 0;
       uint32_t v = r.tab[rank * 16 + ((smw >> (4 * u)) & 0xFu)];
       if (TARGET) v |= (low >> (4 * u)) & 0xFu;
-      accumulate<MT>(r.xs, cursor_step<false>(ck, r.bm), r.sk, __uint_as_float(v << 16), acc);
-      if (TARGET) {
-        const uint32_t pv = u & 1 ? prw[u >> 1] >> 16 : prw[u >> 1] & 0xFFFFu;
-        accumulate<MT>(r.xs, cursor_step<true>(cz, r.bm), r.sk, __uint_as_float(pv << 16), acc);
-      }
+      accumulate<MT>(r.xs, cursor_step<false>(ck, bm_base), r.sk, __uint_as_float(v << 16), acc);
+      if (TARGET)
+        accumulate<MT>(r.xs, cursor_step<true>(cz, bm_base), r.sk, __uint_as_float(block_half(pcur, u) << 16), acc);
     }
   }
 }
 
 template <int MT, bool TARGET, bool WOUT>
-__global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs a) {
+__global__ void __launch_bounds__(CassWarps<MT, TARGET>::value * 32) cass_kernel(const CassArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int P = XPad<MT>::P;
   const int K = a.K, K2 = K / 2, KW = K / 32;
@@ -443,8 +459,7 @@ __global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs
                                                (size_t)warp * cass_per_warp(K, a.scap, TARGET));
   uint32_t* sm_s = bm_s + KW + 2;
   uint32_t* lo_s = sm_s + skewed_words(K / 16, 3);
-  uint32_t* pr_s = lo_s + (TARGET ? skewed_words(K / 16, 3) : 0);
-  uint32_t* st_s = pr_s + (TARGET ? skewed_words(K / 4, 5) : 0);
+  uint32_t* st_s = lo_s + (TARGET ? skewed_words(K / 16, 3) : 0);
 
   for (int i = threadIdx.x; i < a.n_symbols * 16; i += blockDim.x) {
     const uint32_t nib = i & 15;
@@ -454,17 +469,15 @@ __global__ void __launch_bounds__(kCassWarpsMax * 32) cass_kernel(const CassArgs
   __syncthreads();
 
   CassRow r;
-  r.bm = bm_s, r.sm = sm_s, r.lo = lo_s, r.pr = pr_s, r.tab = tab, r.xs = xs;
+  r.bm = bm_s, r.sm = sm_s, r.lo = lo_s, r.tab = tab, r.xs = xs;
   r.KW = KW, r.nsym = a.n_symbols, r.sk = a.sk;
   r.k0 = (int)(((int64_t)lane * K2) >> 5);
   r.cnt = (int)(((int64_t)(lane + 1) * K2) >> 5) - r.k0;
   for (int n = blockIdx.x * nwarps + warp; n < a.N; n += gridDim.x * nwarps) {
     // ---- stage the row: nibbles (skewed), bitmap with the two selects, stream with one
     stage_words<3>(sm_s, a.signmant + (size_t)n * (K / 16), K / 16);
-    if (TARGET) {
-      stage_words<3>(lo_s, a.mlo + (size_t)n * (K / 16), K / 16);
-      stage_words<5>(pr_s, reinterpret_cast<const uint32_t*>(a.pruned + (size_t)n * K2), K / 4);
-    }
+    if (TARGET) stage_words<3>(lo_s, a.mlo + (size_t)n * (K / 16), K / 16);
+    r.prg = a.pruned + (size_t)n * K2;
     Hit h1, h0;
     bool clean;
     const int ones = bitmap_selects(a.bitmap + (size_t)n * KW, bm_s, KW, r.k0, h1, h0, clean);
@@ -542,14 +555,14 @@ struct CassMxArgs {
 };
 
 __host__ __device__ inline size_t cassmx_per_warp(size_t K, bool target) {
-  // bitmap, signs, draft nibbles, group scales (+ target: low nibbles, pruned halves)
-  const size_t w = K / 32 + 2 + K / 64 + skewed_words(K / 16, 3) + K / 64 +
-                   (target ? skewed_words(K / 16, 3) + skewed_words(K / 4, 5) : 0);
+  // bitmap, signs, draft nibbles, group scales (+ target: low nibbles); pruned halves stay in global memory
+  const size_t w = K / 32 + 2 + K / 64 + skewed_words(K / 16, 3) + K / 64 + (target ? skewed_words(K / 16, 3) : 0);
   return (w * 4 + 15) / 16 * 16;
 }
 
 struct MxRow {
-  const uint32_t *bm, *sg, *dn, *ln, *pr;
+  const uint32_t *bm, *sg, *dn, *ln;
+  const uint16_t* prg;  // the row's pruned halves (global)
   const float* sc;
   const uint16_t* xs;
   uint16_t* wrow;
@@ -568,7 +581,6 @@ __device__ __forceinline__ void cassmx_walk(const MxRow& r, float (&acc)[MT], bo
   uint32_t lw = TARGET ? r.ln[skew<3>(r.k0 >> 3)] : 0u;
   uint32_t sgw = r.sg[r.k0 >> 5];
   float scl = r.sc[r.k0 >> 5];
-  uint32_t prw = TARGET ? r.pr[skew<5>(r.k0 >> 1)] : 0u;
   for (int k = r.k0; k < r.k0 + r.cnt; ++k) {
     const int j = cursor_next<false, SAFE>(ck, r.bm, r.KW, bad);
     if ((k & 7) == 0) {
@@ -587,8 +599,7 @@ __device__ __forceinline__ void cassmx_walk(const MxRow& r, float (&acc)[MT], bo
       const int jz = cursor_next<true, SAFE>(cz, r.bm, r.KW, bad);
       uint32_t pv = 0;
       if (TARGET) {
-        if ((k & 1) == 0) prw = r.pr[skew<5>(k >> 1)];
-        pv = k & 1 ? prw >> 16 : prw & 0xFFFFu;
+        pv = __ldg(r.prg + k);
         accumulate<MT>(r.xs, jz, r.sk, __uint_as_float(pv << 16), acc);
       }
       if (WOUT) r.wrow[jz] = (uint16_t)pv;
@@ -601,32 +612,29 @@ template <int MT, bool TARGET>
 __device__ __forceinline__ void cassmx_walk8(const MxRow& r, float (&acc)[MT]) {
   Cursor ck = cursor_at<false>(r.bm, r.KW, r.kpos);
   Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
+  const uint32_t bm_base = smem_u32(r.bm);
+  uint4 pnext = TARGET ? pruned_block(r.prg, r.k0) : make_uint4(0, 0, 0, 0);
   for (int k = r.k0; k < r.k0 + r.cnt; k += 8) {
     const uint32_t dw = r.dn[skew<3>(k >> 3)];
     const uint32_t lw = TARGET ? r.ln[skew<3>(k >> 3)] : 0u;
     const uint32_t sgb = r.sg[k >> 5] >> (k & 24);
     const float scl = r.sc[k >> 5];
-    uint32_t prw[4];
-    if (TARGET) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) prw[i] = r.pr[skew<5>((k >> 1) + i)];
-    }
+    const uint4 pcur = pnext;
+    if (TARGET && k + 8 < r.k0 + r.cnt) pnext = pruned_block(r.prg, k + 8);  // one block ahead
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       uint32_t mag = (dw >> (4 * u)) & 0xFu;
       if (TARGET) mag = (mag << 4) | ((lw >> (4 * u)) & 0xFu);
       const float v = __uint_as_float(__float_as_uint((float)mag * scl) ^ (((sgb >> u) & 1u) << 31));
-      accumulate<MT>(r.xs, cursor_step<false>(ck, r.bm), r.sk, v, acc);
-      if (TARGET) {
-        const uint32_t pv = u & 1 ? prw[u >> 1] >> 16 : prw[u >> 1] & 0xFFFFu;
-        accumulate<MT>(r.xs, cursor_step<true>(cz, r.bm), r.sk, __uint_as_float(pv << 16), acc);
-      }
+      accumulate<MT>(r.xs, cursor_step<false>(ck, bm_base), r.sk, v, acc);
+      if (TARGET)
+        accumulate<MT>(r.xs, cursor_step<true>(cz, bm_base), r.sk, __uint_as_float(block_half(pcur, u) << 16), acc);
     }
   }
 }
 
 template <int MT, bool TARGET, bool WOUT>
-__global__ void __launch_bounds__(kCassWarpsMax * 32) cassmx_kernel(const CassMxArgs a) {
+__global__ void __launch_bounds__(CassWarps<MT, TARGET>::value * 32) cassmx_kernel(const CassMxArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int P = XPad<MT>::P;
   const int K = a.K, K2 = K / 2, KW = K / 32, KG = K / 64;
@@ -640,13 +648,12 @@ __global__ void __launch_bounds__(kCassWarpsMax * 32) cassmx_kernel(const CassMx
   uint32_t* dn_s = sg_s + KG;
   float* sc_s = reinterpret_cast<float*>(dn_s + skewed_words(K / 16, 3));
   uint32_t* ln_s = reinterpret_cast<uint32_t*>(sc_s + KG);
-  uint32_t* pr_s = ln_s + (TARGET ? skewed_words(K / 16, 3) : 0);
 
   stage_x<MT>(xs, a.x, a.ldx, K, a.sk);
   __syncthreads();
 
   MxRow r;
-  r.bm = bm_s, r.sg = sg_s, r.dn = dn_s, r.ln = ln_s, r.pr = pr_s, r.sc = sc_s, r.xs = xs;
+  r.bm = bm_s, r.sg = sg_s, r.dn = dn_s, r.ln = ln_s, r.sc = sc_s, r.xs = xs;
   r.KW = KW, r.sk = a.sk;
   r.k0 = (int)(((int64_t)lane * K2) >> 5);
   r.cnt = (int)(((int64_t)(lane + 1) * K2) >> 5) - r.k0;
@@ -656,10 +663,8 @@ __global__ void __launch_bounds__(kCassWarpsMax * 32) cassmx_kernel(const CassMx
       sc_s[i] = ldexpf(1.f, (int)__ldg(a.gexp + (size_t)n * KG + i) - (TARGET ? 134 : 130));
     }
     stage_words<3>(dn_s, a.dnib + (size_t)n * (K / 16), K / 16);
-    if (TARGET) {
-      stage_words<3>(ln_s, a.lnib + (size_t)n * (K / 16), K / 16);
-      stage_words<5>(pr_s, reinterpret_cast<const uint32_t*>(a.pruned + (size_t)n * K2), K / 4);
-    }
+    if (TARGET) stage_words<3>(ln_s, a.lnib + (size_t)n * (K / 16), K / 16);
+    r.prg = a.pruned + (size_t)n * K2;
     Hit h1, h0;
     bool clean;
     const bool bad = bitmap_selects(a.bitmap + (size_t)n * KW, bm_s, KW, r.k0, h1, h0, clean) != K2;
@@ -691,10 +696,11 @@ inline int x_skew(int K) {
 }
 
 template <class Args>
-int launch_rows(const void* kern, const Args& a, size_t fixed, size_t per_warp, const char* what, cudaStream_t s) {
+int launch_rows(const void* kern, const Args& a, int max_warps, size_t fixed, size_t per_warp, const char* what,
+                cudaStream_t s) {
   const size_t cap = 227 * 1024 - 1024;
   if (fixed + per_warp > cap) return fail(QMV_ERR_UNSUPPORTED, "K=%d does not fit shared memory", a.K);
-  const int warps = (int)std::min<size_t>(kCassWarpsMax, (cap - fixed) / per_warp);
+  const int warps = (int)std::min<size_t>(max_warps, (cap - fixed) / per_warp);
   const size_t smem = fixed + per_warp * warps;
   int per_sm = 0;
   int rc = kernel_fit(kern, warps * 32, smem, &per_sm);
@@ -717,7 +723,8 @@ int launch_pair(Args& a, int M, size_t fixed_extra, size_t per_warp, const char*
   if (a.w_out) {
     Args b = a;
     if (M != 1) b.y = nullptr;
-    rc = launch_rows(Pick<1, TARGET, true>::get(), b, xs_bytes(a.K, a.sk, 1) + fixed_extra, per_warp, what, s);
+    rc = launch_rows(Pick<1, TARGET, true>::get(), b, cass_warps(1, TARGET), xs_bytes(a.K, a.sk, 1) + fixed_extra,
+                     per_warp, what, s);
     if (rc || M == 1 || !a.y) return rc;
   }
   if (!a.y) return rc;
@@ -734,7 +741,7 @@ int launch_pair(Args& a, int M, size_t fixed_extra, size_t per_warp, const char*
     case 7: kern = Pick<7, TARGET, false>::get(); break;
     default: kern = Pick<8, TARGET, false>::get(); break;
   }
-  return launch_rows(kern, b, xs_bytes(a.K, a.sk, P) + fixed_extra, per_warp, what, s);
+  return launch_rows(kern, b, cass_warps(M, TARGET), xs_bytes(a.K, a.sk, P) + fixed_extra, per_warp, what, s);
 }
 
 template <int MT, bool TARGET, bool WOUT>
