@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int KC = b.kc;
   const int S = KC / kStep;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);        // [MT][S][WPB][JW][8]
-  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8]
+  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8][seeds per block]
   __shared__ float s_red[kConsumerWarps][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
@@ -263,16 +263,16 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   b.n_tiles = tiles;
   b.rows_per_tile = G::TILE_ROWS;
   // activation chunk: as much of K as fits next to the ring, in whole steps;
-  // per staged column: MT fp16 values, plus one fp16 pair per 128 columns and row
+  // per staged column: MT fp16 values, plus the seeds (fp16 pairs per 128 columns and row)
   const size_t fixed = G::RING + G::BARS;
   const size_t budget = kSmemMax - fixed - 1024;
-  int kc_cap = (int)(budget / ((size_t)MT * 2 + ((size_t)MT * 4 + 127) / 128)) / kStep * kStep;
+  int kc_cap = (int)(budget / ((size_t)MT * 2 + ((size_t)MT * 4 * Chain<FMT>::SEEDS + 127) / 128)) / kStep * kStep;
   int kc = ((max_K + kStep - 1) / kStep) * kStep;
   if (kc > kc_cap) kc = kc_cap;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", MT);
   b.kc = kc;
   const size_t S = kc / kStep;
-  const size_t smem = fixed + (size_t)MT * kc * 2 + (size_t)MT * S * kBlocksPerStep * 4;
+  const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<FMT>(MT, S);
   fill_magic<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");

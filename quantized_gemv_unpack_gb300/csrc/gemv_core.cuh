@@ -9,6 +9,8 @@
 namespace qmv {
 namespace core {
 
+constexpr int kBlocksPerStepHost = 8;  // 128-column blocks per 1024-column step (kBlocksPerStep)
+
 template <int FMT>
 struct Fmt;
 template <>
@@ -26,12 +28,29 @@ struct Fmt<QMV_INT4> {
   static constexpr int PPW = 4;
   static constexpr int CPW = 8;
   static constexpr int JW = 1;
-  static constexpr int XLOG2 = 8;
+  // staged |x| max in [2^5, 2^6): a block half sums 64 products |q x| <= 8 * 64, so no
+  // fp16 partial sum can overflow (65504)
+  static constexpr int XLOG2 = 5;
   static constexpr uint32_t MASK = 0x000F000Fu, BASE = 0x64086408u;
 };
 
+// fp16 accumulation chains of four code words: two per ternary block, each
+// seeded with -sum x over its own 64 columns (so that its partial sums stay
+// near the chain's own result), four per INT4 block. Chains are added into the
+// block's pair sum, which is widened to fp32 once per block.
+template <int FMT>
+struct Chain {
+  static constexpr int WORDS = 4;
+  static constexpr int SEEDS = FMT == QMV_TERNARY2 ? Fmt<FMT>::WPB / WORDS : 1;  // staged seeds per block
+};
+// Shared-memory bytes of the staged seeds for MT rows and S steps.
+template <int FMT>
+inline size_t seed_bytes(size_t MT, size_t S) {
+  return MT * S * kBlocksPerStepHost * Chain<FMT>::SEEDS * 4;
+}
+
 constexpr int kGroups = 4;            // lane groups (rows of a row quad)
-constexpr int kBlocksPerStep = 8;     // lanes per row
+constexpr int kBlocksPerStep = kBlocksPerStepHost;  // lanes per row
 constexpr int kStep = kBlocksPerStep * 128;
 constexpr int kSlots = 2;             // ring slots per decode warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
@@ -174,7 +193,8 @@ struct Bf16Rows {  // x[m][ldx], bf16
 // Stage columns [kc0, kc0 + kcn) of MT activation rows into shared memory: fp16
 // pairs in the order a lane consumes them, scaled by a power of two per row so
 // the largest magnitude lands in [2^XLOG2, 2^(XLOG2+1)); for ternary also the
-// negated per-block sums that seed the accumulators. Called by every thread of
+// negated per-chain sums (even and odd columns) that seed the accumulation
+// chains. Called by every thread of
 // the CTA (NT threads); begins and ends with a CTA barrier.
 template <int FMT, int MT, int NT, class Src>
 __device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, __half2* negs, float (*s_red)[MT],
@@ -238,13 +258,18 @@ __device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, __half2* 
   }
   if constexpr (FMT == QMV_TERNARY2) {
     __syncthreads();
-    for (int q = tid; q < MT * S * kBlocksPerStep; q += NT) {
-      const int m = q / (S * kBlocksPerStep);
-      const int blk = q % (S * kBlocksPerStep);
+    // seed q = ((m * S + s) * 8 + block) * (WPB / CW) + chain
+    constexpr int CW = Chain<FMT>::WORDS;
+    constexpr int NCH = WPB / CW;
+    for (int q = tid; q < MT * S * kBlocksPerStep * NCH; q += NT) {
+      const int c = q % NCH;
+      const int m = q / (S * kBlocksPerStep * NCH);
+      const int blk = (q / NCH) % (S * kBlocksPerStep);
       const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
       float se = 0.f, so = 0.f;
       if (blk < nb) {
-        for (int h = 0; h < WPB; ++h)
+#pragma unroll
+        for (int h = c * CW; h < (c + 1) * CW; ++h)
 #pragma unroll
           for (int j = 0; j < JW; ++j) {
             const uint4 pc = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp];
@@ -280,35 +305,55 @@ __device__ __forceinline__ void decode_step(const unsigned char* sb, int row_byt
 #pragma unroll
     for (int u = 0; u < WPB / 4; ++u)
       cw[r][u] = *reinterpret_cast<const uint4*>(sb + (r * kGroups + g) * row_bytes + u * 16);
-  __half2 a0[RQ][MT], a1[RQ][MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    const __half2 init = TERN ? negs[((size_t)m * S + s) * kBlocksPerStep + p] : __floats2half2_rn(0.f, 0.f);
-#pragma unroll
-    for (int r = 0; r < RQ; ++r) {
-      a0[r][m] = init;
-      a1[r][m] = __floats2half2_rn(0.f, 0.f);
-    }
-  }
+  constexpr int CW = Chain<FMT>::WORDS;
+  __half2 blk[RQ][MT], ch[RQ][MT];
+  auto seed_of = [&](int m, int h) {
+    return TERN ? negs[(((size_t)m * S + s) * kBlocksPerStep + p) * (WPB / CW) + h / CW] : __floats2half2_rn(0.f, 0.f);
+  };
+  auto xload = [&](int m, int h, int j) { return xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + p]; };
 #pragma unroll
   for (int h = 0; h < WPB; ++h) {
-    uint4 xw[MT][JW];
+    if constexpr (RQ == 1) {
+      // one row: decode the word once, then stream each activation row through it
+      const uint32_t w = word_of(cw[0][h / 4], h % 4);
+      __half2 v[F::PPW];
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+      for (int i = 0; i < F::PPW; ++i) v[i] = decode_pair<FMT>(w, i, dk);
 #pragma unroll
-      for (int j = 0; j < JW; ++j) xw[m][j] = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + p];
+      for (int m = 0; m < MT; ++m) {
+        uint4 xw[JW];
 #pragma unroll
-    for (int r = 0; r < RQ; ++r) {
-      const uint32_t w = word_of(cw[r][h / 4], h % 4);
+        for (int j = 0; j < JW; ++j) xw[j] = xload(m, h, j);
+        if (h % CW == 0) ch[0][m] = seed_of(m, h);
 #pragma unroll
-      for (int i = 0; i < F::PPW; ++i) {
-        const __half2 v = decode_pair<FMT>(w, i, dk);
+        for (int i = 0; i < F::PPW; ++i) ch[0][m] = __hfma2(v[i], as_h2(word_of(xw[i / 4], i % 4)), ch[0][m]);
+        if (h % CW == CW - 1) blk[0][m] = h == CW - 1 ? ch[0][m] : __hadd2(blk[0][m], ch[0][m]);
+      }
+    } else {
+      // several rows share each activation load
+      uint4 xw[MT][JW];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const __half2 xv = as_h2(word_of(xw[m][i / 4], i % 4));
-          if (h < WPB / 2) a0[r][m] = __hfma2(v, xv, a0[r][m]);
-          else a1[r][m] = __hfma2(v, xv, a1[r][m]);
+      for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int j = 0; j < JW; ++j) xw[m][j] = xload(m, h, j);
+        if (h % CW == 0) {
+          const __half2 seed = seed_of(m, h);
+#pragma unroll
+          for (int r = 0; r < RQ; ++r) ch[r][m] = seed;
         }
+      }
+#pragma unroll
+      for (int r = 0; r < RQ; ++r) {
+        const uint32_t w = word_of(cw[r][h / 4], h % 4);
+#pragma unroll
+        for (int i = 0; i < F::PPW; ++i) {
+          const __half2 v = decode_pair<FMT>(w, i, dk);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) ch[r][m] = __hfma2(v, as_h2(word_of(xw[m][i / 4], i % 4)), ch[r][m]);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (h % CW == CW - 1) blk[r][m] = h == CW - 1 ? ch[r][m] : __hadd2(blk[r][m], ch[r][m]);
       }
     }
   }
@@ -316,10 +361,7 @@ __device__ __forceinline__ void decode_step(const unsigned char* sb, int row_byt
   for (int r = 0; r < RQ; ++r) {
     const float scf = __half2float(__ushort_as_half(sc[r]));
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const __half2 t = __hadd2(a0[r][m], a1[r][m]);
-      accc[r][m] = fmaf(__low2float(t) + __high2float(t), scf, accc[r][m]);
-    }
+    for (int m = 0; m < MT; ++m) accc[r][m] = fmaf(__low2float(blk[r][m]) + __high2float(blk[r][m]), scf, accc[r][m]);
   }
 }
 

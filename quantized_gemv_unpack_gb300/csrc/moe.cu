@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a
 size_t expert_smem(int64_t K) {
   using G = Geometry<QMV_TERNARY2, kMoeRPW>;
   const int64_t S = (K + kStep - 1) / kStep;
-  return G::RING + G::BARS + (size_t)kMaxTokens * S * kStep * 2 + (size_t)kMaxTokens * S * kBlocksPerStep * 4;
+  return G::RING + G::BARS + (size_t)kMaxTokens * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(kMaxTokens, S);
 }
 
 // Scratch for moe_qmv_run_static: one fixed array per device, in the module's

@@ -7,7 +7,8 @@
 //
 // Matvec. One persistent launch (one CTA of 16 warps per SM) over a table of
 // matvecs; rows are cut into tiles of 16 warps x RPW rows. A warp owns RPW rows
-// of one 16-row group (the whole group at RPW = 16, one half at RPW = 8) and
+// of one 16-row group (the whole group at RPW = 16, a half at RPW = 8, a quarter
+// at RPW = 4, which M >= 5 uses to stay within 128 registers) and
 // walks the group's records (up to 8 stored tiles each, its rows contiguous in
 // the record): lane 0 copies the warp's rows of a record into a two-slot ring
 // with one bulk copy, two records ahead; lane 8g + p decodes stored tile p of
@@ -233,7 +234,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   const size_t fixed = G::RING + G::BARS;
   const int kc = (max_K + kStep - 1) / kStep * kStep;
   const size_t S = kc / kStep;
-  const size_t smem = fixed + (size_t)MT * kc * 2 + (size_t)MT * S * kBlocksPerStep * 4;
+  const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<QMV_TERNARY2>(MT, S);
   if (smem > kSmemMax - 1024)
     return fail(QMV_ERR_UNSUPPORTED, "sparse ternary: K=%d with M=%d does not fit shared memory in one piece", max_K, MT);
   b.kc = kc;
@@ -259,10 +260,10 @@ int launch_sparse(SparseBatch& b, int M, cudaStream_t s) {
     case 2: return launch_sparse_t<2, 8>(b, s);
     case 3: return launch_sparse_t<3, 8>(b, s);
     case 4: return launch_sparse_t<4, 8>(b, s);
-    case 5: return launch_sparse_t<5, 8>(b, s);
-    case 6: return launch_sparse_t<6, 8>(b, s);
-    case 7: return launch_sparse_t<7, 8>(b, s);
-    case 8: return launch_sparse_t<8, 8>(b, s);
+    case 5: return launch_sparse_t<5, 4>(b, s);
+    case 6: return launch_sparse_t<6, 4>(b, s);
+    case 7: return launch_sparse_t<7, 4>(b, s);
+    case 8: return launch_sparse_t<8, 4>(b, s);
     default: return fail(QMV_ERR_ARG, "sparse ternary: M=%d outside 1..8", M);
   }
 }
