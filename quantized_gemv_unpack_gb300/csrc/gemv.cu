@@ -66,21 +66,31 @@ __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
 }
 
 
+// A ring slot holds the warp's rows of one step, then the step's 256-byte
+// scale record (16 rows x 8 blocks of fp16), both copied on the slot's barrier.
+template <int FMT, int RPW>
+struct FmaRing {
+  using G = Geometry<FMT, RPW>;
+  static constexpr int SLOT = G::SLOT + 256;
+  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
+};
+
 template <int FMT, int MT, int RPW>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvBatch b) {
   using F = Fmt<FMT>;
   using G = Geometry<FMT, RPW>;
+  using R = FmaRing<FMT, RPW>;
   constexpr int WPB = F::WPB;
   constexpr int JW = F::JW;
   constexpr int RQ = RPW / kGroups;          // row quads per decode warp
   constexpr bool TERN = FMT == QMV_TERNARY2;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* ring = smem_raw;                                             // [warp][slot][RPW rows of a step]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + G::RING);          // [warp][slot]
+  unsigned char* ring = smem_raw;                                             // [warp][slot][RPW rows of a step | scales]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R::RING);          // [warp][slot]
   const int KC = b.kc;
   const int S = KC / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);        // [MT][S][WPB][JW][8]
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + G::BARS);        // [MT][S][WPB][JW][8]
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8][seeds per block]
   __shared__ float s_red[kConsumerWarps][MT];
   __shared__ float s_xinv[MT];
@@ -91,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int lane = tid & 31;
   const int tile_begin = b.cta_tile[blockIdx.x];
   const int tile_end = b.cta_tile[blockIdx.x + 1];
-  unsigned char* wring = ring + (size_t)warp * kSlots * G::SLOT;
+  unsigned char* wring = ring + (size_t)warp * kSlots * R::SLOT;
   uint64_t* wfull = full + warp * kSlots;
 
   if (lane == 0) {
@@ -100,41 +110,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   }
   __syncthreads();
 
-  // ---- producer side of this warp: copy the warp's rows of one step into a slot
+  // ---- producer side of this warp: copy the warp's rows of one step and the
+  // step's scale record into a slot. The source of the next step is one record
+  // further on, except at a chunk's last (possibly partial) step or a new tile,
+  // where it is located from scratch.
   constexpr int kStepWords = kBlocksPerStep * WPB;
-  int p_tile = tile_begin, p_ti = 0, p_kc0 = 0, p_s = 0;
-  if (p_tile < tile_end) p_ti = find_task(b, p_tile);
-  uint32_t n_issued = 0;
-  auto issue_one = [&]() {
-    if (p_tile >= tile_end) return;
+  int p_tile = tile_begin, p_ti = 0, p_kc0 = 0, p_s = 0, p_nb = 0, p_K = 0;
+  const uint32_t* p_src = nullptr;
+  const uint16_t* p_ssrc = nullptr;
+  uint32_t p_bytes = 0;
+  auto p_locate = [&]() {
     const GemvTask& T = b.t[p_ti];
-    const int K = T.K;
-    const int nb = min(KC, K - p_kc0) / 128;
-    const int nbk = min(kBlocksPerStep, nb - p_s * kBlocksPerStep);
+    p_K = T.K;
+    p_nb = min(KC, p_K - p_kc0) / 128;
+    const int nbk = min(kBlocksPerStep, p_nb - p_s * kBlocksPerStep);
     const int blk0 = p_kc0 / 128 + p_s * kBlocksPerStep;
     const int wrow0 = (p_tile - T.tile0) * G::TILE_ROWS + warp * RPW;
     const int N16 = (T.N + 15) / 16 * 16;
     // the warp's RPW rows lie inside one 16-row group: one contiguous piece of
     // the (group, step) record; rows past the padded end are not copied
-    const uint32_t bytes = wrow0 < N16 ? (uint32_t)(RPW * nbk * G::BLOCK_BYTES) : 0u;
+    p_bytes = wrow0 < N16 ? (uint32_t)(RPW * nbk * G::BLOCK_BYTES) : 0u;
+    p_src = T.codes + (size_t)(wrow0 / 16) * 16 * (p_K / F::CPW) + (size_t)(blk0 / kBlocksPerStep) * 16 * kStepWords +
+            (size_t)(wrow0 % 16) * nbk * WPB;
+    p_ssrc = T.scales + ((size_t)(wrow0 / 16) * scale_steps(p_K) + blk0 / kBlocksPerStep) * 128;
+  };
+  if (p_tile < tile_end) {
+    p_ti = find_task(b, p_tile);
+    p_locate();
+  }
+  uint32_t n_issued = 0;
+  auto issue_one = [&]() {
+    if (p_tile >= tile_end) return;
     const int slot = n_issued % kSlots;
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the slot precede the copy
-      mbar_arrive_expect_tx(&wfull[slot], bytes);
-      if (bytes) {
-        const size_t off = (size_t)(wrow0 / 16) * 16 * (K / F::CPW) + (size_t)(blk0 / kBlocksPerStep) * 16 * kStepWords +
-                           (size_t)(wrow0 % 16) * nbk * WPB;
-        bulk_g2s(wring + (size_t)slot * G::SLOT, T.codes + off, bytes, &wfull[slot]);
+      mbar_arrive_expect_tx(&wfull[slot], p_bytes ? p_bytes + 256u : 0u);
+      if (p_bytes) {
+        bulk_g2s(wring + (size_t)slot * R::SLOT, p_src, p_bytes, &wfull[slot]);
+        bulk_g2s(wring + (size_t)slot * R::SLOT + G::SLOT, p_ssrc, 256u, &wfull[slot]);
       }
     }
     ++n_issued;
-    if (++p_s * kBlocksPerStep >= nb) {
-      p_s = 0;
-      p_kc0 += KC;
-      if (p_kc0 >= K) {
-        p_kc0 = 0;
-        if (++p_tile < tile_end) p_ti = find_task(b, p_tile);
+    if ((++p_s + 1) * kBlocksPerStep <= p_nb) {  // another full step of this chunk
+      p_src += 16 * kStepWords;
+      p_ssrc += 128;
+    } else {
+      if (p_s * kBlocksPerStep >= p_nb) {
+        p_s = 0;
+        p_kc0 += KC;
+        if (p_kc0 >= p_K) {
+          p_kc0 = 0;
+          if (++p_tile < tile_end) p_ti = find_task(b, p_tile);
+        }
       }
+      if (p_tile < tile_end) p_locate();
     }
   };
   for (int i = 0; i < kSlots; ++i) issue_one();
@@ -150,12 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   for (int tile = tile_begin; tile < tile_end; ++tile) {
     const int ti = find_task(b, tile);
-    const unsigned short* __restrict__ scales = reinterpret_cast<const unsigned short*>(b.t[ti].scales);
     const uint16_t* __restrict__ x = b.t[ti].x;
     float* __restrict__ y = b.t[ti].y;
     const int N = b.t[ti].N, K = b.t[ti].K, ldx = b.t[ti].ldx, ldy = b.t[ti].ldy;
-    const int KB = K / 128;
     const int wrow0 = (tile - b.t[ti].tile0) * G::TILE_ROWS + warp * RPW;
+    const int srow = wrow0 % 16 + g;  // this lane's first row in the scale record
 
     float acc[RQ][MT];
 #pragma unroll
@@ -176,39 +204,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
 
       // ---- decode this warp's rows over the chunk, one ring slot per step
-      // scales of (row, block p of each step): record order, one 128-entry record per step
-      const unsigned short* sp[RQ];
-      const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;
-#pragma unroll
-      for (int r = 0; r < RQ; ++r) {
-        const int row = min(wrow0 + r * kGroups + g, N - 1);  // rows past N read the last row, never stored
-        sp[r] = scales + ((size_t)(row / 16) * SS + kc0 / kStep) * 128 + (row % 16) * kBlocksPerStep + p;
-      }
       float accc[RQ][MT];
 #pragma unroll
       for (int r = 0; r < RQ; ++r)
 #pragma unroll
         for (int m = 0; m < MT; ++m) accc[r][m] = 0.f;
       const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
-      unsigned short scn[RQ];
-#pragma unroll
-      for (int r = 0; r < RQ; ++r) scn[r] = p < nb ? __ldg(sp[r]) : (unsigned short)0;
 
       for (int s = 0; s < nsteps; ++s, ++it) {
-        const bool active = s * kBlocksPerStep + p < nb;
-        unsigned short sc[RQ];
-#pragma unroll
-        for (int r = 0; r < RQ; ++r) {
-          sc[r] = scn[r];
-          if ((s + 1) * kBlocksPerStep + p < nb) scn[r] = __ldg(sp[r] + (s + 1) * 128);
-        }
         const int slot = it % kSlots;
         mbar_wait(&wfull[slot], (it / kSlots) & 1u, b.err);
-        if (active) {
+        if (s * kBlocksPerStep + p < nb) {
+          const unsigned char* sb = wring + (size_t)slot * R::SLOT;
+          // scales of (row, block p): entry row * 8 + p of the step's record
+          const unsigned short* srec = reinterpret_cast<const unsigned short*>(sb + G::SLOT);
+          unsigned short sc[RQ];
+#pragma unroll
+          for (int r = 0; r < RQ; ++r) sc[r] = srec[(srow + r * kGroups) * kBlocksPerStep + p];
           // rows of the step are nbk blocks apart in the slot
           const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
-          decode_step<FMT, MT, RQ>(wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, negs, S, s, g,
-                                   p, dk, sc, accc);
+          decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, row_bytes, xs, negs, S, s, g, p, dk, sc, accc);
         }
         __syncwarp();  // every lane is done with the slot before it is refilled
         issue_one();
@@ -264,7 +279,7 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   b.rows_per_tile = G::TILE_ROWS;
   // activation chunk: as much of K as fits next to the ring, in whole steps;
   // per staged column: MT fp16 values, plus the seeds (fp16 pairs per 128 columns and row)
-  const size_t fixed = G::RING + G::BARS;
+  const size_t fixed = FmaRing<FMT, RPW>::RING + G::BARS;
   const size_t budget = kSmemMax - fixed - 1024;
   int kc_cap = (int)(budget / ((size_t)MT * 2 + ((size_t)MT * 4 * Chain<FMT>::SEEDS + 127) / 128)) / kStep * kStep;
   int kc = ((max_K + kStep - 1) / kStep) * kStep;
