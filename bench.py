@@ -348,6 +348,11 @@ def synth_shapes():
     from quantized_gemv_unpack_gb300 import synth
     return synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
 
+    def traffic(self):
+        # captured on 3 layers; every layer's stored tiles are read once, so traffic grows with the layer count
+        return captured_traffic("stack-sparse", self.layers / LAYERS)
+
+
 
 class Ternary4096(Workload):
     name = "ternary-4096"
@@ -518,6 +523,10 @@ class KvEncode(Workload):
 
     def host_io(self):
         return [self.xs[0]], [self.out]
+
+    def traffic(self):
+        return captured_traffic("kv-encode")
+
 
 
 class Moe(Workload):
