@@ -531,7 +531,7 @@ class KvEncode(Workload):
 
 class Moe(Workload):
     name = "moe"
-    kernel = "moe_route_kernel + moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
+    kernel = "moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
 
     def __init__(self, q, torch, dev, M=1, n_logits=64):
         from quantized_gemv_unpack_gb300 import synth
@@ -719,7 +719,7 @@ def main():
     per_gpu = nbytes / (ms * 1e-3) / 1e9
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
     launches = {"stack": 1, "stack-sparse": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
-                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "kv-encode": 1, "moe": 3}[a.workload]
+                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "kv-encode": 1, "moe": 2}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -1,19 +1,21 @@
 // Mixture-of-experts decode over ternary SwiGLU experts ("Nemotron 3.5 Bolt",
 // expert top-K routing): only the experts the router selects are read.
 //
-// Three launches on the caller's stream, all state in the caller's workspace:
-//  1. route: one warp per token takes the top-k of its E logits (equal logits:
-//     lower expert first) by k rounds of a warp arg-max, softmax over the k
-//     selected logits in fp32; then one thread per expert counts its
-//     (token, expert) pairs, a block scan orders the pairs by expert and token
-//     and lists each active expert once (a slot), and the CTA zeroes y.
-//  2. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
+// Two launches on the caller's stream; g and u pass between them in the
+// caller's workspace. Each CTA of both starts by routing in shared memory (the
+// same inputs and code give every CTA the same result): one warp per token takes
+// the top-k of its E logits (equal logits: lower expert first) by k rounds of a
+// warp arg-max, softmax over the k selected logits in fp32; then one thread per
+// expert counts its (token, expert) pairs, a block scan orders the pairs by
+// expert and token and lists each active expert once (a slot).
+//  1. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
 //     tile of 64 rows of the [gate; up] matrix) into equal contiguous ranges;
 //     a CTA stages the slot's token rows of x (gathered) once per slot and
-//     decodes its rows with the same per-warp TMA ring and decode step as the
-//     matvec batch (prefetching across unit boundaries), writing g and u per
-//     (token, expert) pair to the workspace in fp32.
-//  3. down: the same over the down matrices; staging computes h = silu(g) * u
+//     decodes its rows with the same per-warp bulk-copy ring and decode step as
+//     the matvec batch, prefetching across unit boundaries, and writes g and u
+//     per (token, expert) pair to the workspace in fp32. The CTAs also zero y,
+//     and CTA 0 leaves the routing (slots and pairs) in the workspace.
+//  2. down: the same over the down matrices; staging computes h = silu(g) * u
 //     (fp32) per pair, and the decoded rows are added into y[token] with
 //     weight p by fp32 atomics (their order varies between runs; the sum stays
 //     within the documented bound).
@@ -33,6 +35,17 @@ constexpr int kMoeTileRows = kConsumerWarps * kMoeRPW;  // 64
 constexpr int kMaxTopk = 8;
 constexpr int kMaxTokens = 8;
 constexpr int kMaxExperts = 256;
+constexpr int kMaxPairs = kMaxTokens * kMaxTopk;
+constexpr int kMoeSlots = 2;                            // ring slots per decode warp
+
+// The expert kernels' ring: per warp kMoeSlots slots of one step of 4 rows (a
+// deeper ring measured slower at M = 1).
+struct MoeRing {
+  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+  static constexpr int SLOT = G::SLOT;
+  static constexpr int RING = kConsumerWarps * kMoeSlots * SLOT;
+  static constexpr int BARS = kConsumerWarps * kMoeSlots * 8;
+};
 
 // Workspace layout (all offsets in bytes from the workspace base).
 struct MoeLayout {
@@ -69,63 +82,61 @@ struct MoeArgs {
   int* err;
 };
 
-__global__ void __launch_bounds__(256) moe_route_kernel(const MoeArgs a) {
-  __shared__ int s_exp[kMaxTokens][kMaxTopk];
-  __shared__ float s_prob[kMaxTokens][kMaxTopk];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* slot_expert = reinterpret_cast<int*>(a.ws + a.off_slot_expert);
-  int* slot_first = reinterpret_cast<int*>(a.ws + a.off_slot_first);
-  int* slot_count = reinterpret_cast<int*>(a.ws + a.off_slot_count);
-  int* pair_token = reinterpret_cast<int*>(a.ws + a.off_pair_token);
-  float* pair_prob = reinterpret_cast<float*>(a.ws + a.off_pair_prob);
-  int* n_slots = reinterpret_cast<int*>(a.ws);
+// Routing of the M tokens, in shared memory.
+struct MoeRoute {
+  int n_slots;
+  int slot_expert[kMaxPairs], slot_first[kMaxPairs], slot_count[kMaxPairs];
+  int pair_token[kMaxPairs];
+  float pair_prob[kMaxPairs];
+  int exp[kMaxTokens][kMaxTopk];
+  float prob[kMaxTokens][kMaxTopk];
+  int wp[kThreads / 32], ws[kThreads / 32];
+};
 
+// Called by all threads of the CTA (blockDim.x >= E); ends with a CTA barrier.
+__device__ void route(const MoeArgs& a, MoeRoute& R) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < a.M) {
+    // the lane's logits in registers and a bit mask of the entries taken (or past
+    // E), so that nothing is indexed at run time
     const float* lg = a.logits + (size_t)warp * a.E;
     float v[kMaxExperts / 32];
-    bool used[kMaxExperts / 32];
+    uint32_t taken = 0u;
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = i * 32 + lane;
       v[i] = e < a.E ? lg[e] : -INFINITY;
-      used[i] = e >= a.E;
+      if (e >= a.E) taken |= 1u << i;
     }
     for (int r = 0; r < a.topk; ++r) {
-      // best remaining (value, index) of this lane, then across the warp
+      // best remaining (value, index) of this lane, then across the warp; equal
+      // values keep the lower index
       float bv = -INFINITY;
       int bi = 1 << 30;
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = i * 32 + lane;
-        if (!used[i] && (v[i] > bv || (v[i] == bv && e < bi) || bi == (1 << 30))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
+      for (int i = 0; i < kMaxExperts / 32; ++i)
+        if (!((taken >> i) & 1u) && (bi == (1 << 30) || v[i] > bv)) bv = v[i], bi = i * 32 + lane;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
+        if (ov > bv || (ov == bv && oi < bi)) bv = ov, bi = oi;
       }
-      if (bi < a.E && (bi & 31) == lane) used[bi >> 5] = true;
+      if (bi < a.E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
       if (lane == 0) {
-        s_exp[warp][r] = bi < a.E ? bi : 0;
-        s_prob[warp][r] = bv;
+        R.exp[warp][r] = bi < a.E ? bi : 0;
+        R.prob[warp][r] = bv;
       }
     }
     __syncwarp();
     if (lane == 0) {
-      const float mx = s_prob[warp][0];
+      const float mx = R.prob[warp][0];
       float z = 0.f;
       for (int r = 0; r < a.topk; ++r) {
-        s_prob[warp][r] = expf(s_prob[warp][r] - mx);
-        z += s_prob[warp][r];
+        R.prob[warp][r] = expf(R.prob[warp][r] - mx);
+        z += R.prob[warp][r];
       }
-      for (int r = 0; r < a.topk; ++r) s_prob[warp][r] /= z;
+      for (int r = 0; r < a.topk; ++r) R.prob[warp][r] /= z;
     }
   }
   __syncthreads();
@@ -136,7 +147,7 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const MoeArgs a) {
   int cnt = 0;
   if (e < a.E)
     for (int t = 0; t < a.M; ++t)
-      for (int r = 0; r < a.topk; ++r) cnt += s_exp[t][r] == e;
+      for (int r = 0; r < a.topk; ++r) cnt += R.exp[t][r] == e;
   const int act = cnt > 0;
   int pc = cnt, sc = act;  // inclusive scans within the warp
 #pragma unroll
@@ -147,33 +158,32 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const MoeArgs a) {
       sc += us;
     }
   }
-  __shared__ int s_wp[8], s_ws[8];
   if (lane == 31) {
-    s_wp[warp] = pc;
-    s_ws[warp] = sc;
+    R.wp[warp] = pc;
+    R.ws[warp] = sc;
   }
   __syncthreads();
   int base_p = 0, base_s = 0;
   for (int w = 0; w < warp; ++w) {
-    base_p += s_wp[w];
-    base_s += s_ws[w];
+    base_p += R.wp[w];
+    base_s += R.ws[w];
   }
   if (act) {
     int np = base_p + pc - cnt;
     const int slot = base_s + sc - 1;
-    slot_expert[slot] = e;
-    slot_first[slot] = np;
-    slot_count[slot] = cnt;
+    R.slot_expert[slot] = e;
+    R.slot_first[slot] = np;
+    R.slot_count[slot] = cnt;
     for (int t = 0; t < a.M; ++t)
       for (int r = 0; r < a.topk; ++r)
-        if (s_exp[t][r] == e) {
-          pair_token[np] = t;
-          pair_prob[np] = s_prob[t][r];
+        if (R.exp[t][r] == e) {
+          R.pair_token[np] = t;
+          R.pair_prob[np] = R.prob[t][r];
           ++np;
         }
   }
-  if (threadIdx.x == 255) *n_slots = base_s + sc;
-  for (int i = threadIdx.x; i < a.M * a.H; i += blockDim.x) a.y[(size_t)(i / a.H) * a.ldy + i % a.H] = 0.f;
+  if (threadIdx.x == blockDim.x - 1) R.n_slots = base_s + sc;
+  __syncthreads();
 }
 
 // activation sources of the two expert phases
@@ -206,7 +216,7 @@ struct SwiGlu {  // h = silu(g) * u from the workspace, pair rows [first + m]
 struct UnitProducer {
   const uint32_t* codes0;   // expert 0's codes; expert e at + e * stride_words
   int64_t stride_words;
-  const int* slot_expert;
+  const int* slot_expert;   // shared memory
   int N, K, tiles, u, u_end, s, nsteps, warp, lane;
   uint32_t n_issued;
   unsigned char* wring;
@@ -221,7 +231,7 @@ struct UnitProducer {
     const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
     const int N16 = (N + 15) / 16 * 16;
     const uint32_t bytes = wrow0 < N16 ? (uint32_t)(kMoeRPW * nbk * G::BLOCK_BYTES) : 0u;
-    const int slot = n_issued % kSlots;
+    const int slot = n_issued % kMoeSlots;
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive_expect_tx(&wfull[slot], bytes);
@@ -254,7 +264,7 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
   const int S = (K + kStep - 1) / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + MoeRing::RING + MoeRing::BARS);
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 3, p = lane & 7;
@@ -284,8 +294,8 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
       unsigned short sc[RQ];
 #pragma unroll
       for (int r = 0; r < RQ; ++r) sc[r] = active ? __ldg(sp[r] + s * 128) : (unsigned short)0;
-      const int slot = it % kSlots;
-      mbar_wait(&prod.wfull[slot], (it / kSlots) & 1u, err);
+      const int slot = it % kMoeSlots;
+      mbar_wait(&prod.wfull[slot], (it / kMoeSlots) & 1u, err);
       if (active) {
         const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
         decode_step<FMT, MT, RQ>(prod.wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, negs, S,
@@ -334,10 +344,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int s_tok[kMaxTokens];
   __shared__ float s_prob[kMaxTokens];
-  const int ns = *reinterpret_cast<const int*>(a.ws);
-  const int* slot_expert = reinterpret_cast<const int*>(a.ws + a.off_slot_expert);
-  const int* slot_first = reinterpret_cast<const int*>(a.ws + a.off_slot_first);
-  const int* slot_count = reinterpret_cast<const int*>(a.ws + a.off_slot_count);
+  __shared__ MoeRoute R;
+  route(a, R);
+  if (PHASE == 0) {
+    // y is accumulated by the down phase's atomics
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.M * a.H; i += gridDim.x * blockDim.x)
+      a.y[(size_t)(i / a.H) * a.ldy + i % a.H] = 0.f;
+    if (blockIdx.x == 0) {  // the routing, for inspection: slots and pairs in the workspace layout
+      const int np = a.M * a.topk;
+      for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        reinterpret_cast<int*>(a.ws + a.off_pair_token)[i] = R.pair_token[i];
+        reinterpret_cast<float*>(a.ws + a.off_pair_prob)[i] = R.pair_prob[i];
+      }
+      for (int i = threadIdx.x; i < R.n_slots; i += blockDim.x) {
+        reinterpret_cast<int*>(a.ws + a.off_slot_expert)[i] = R.slot_expert[i];
+        reinterpret_cast<int*>(a.ws + a.off_slot_first)[i] = R.slot_first[i];
+        reinterpret_cast<int*>(a.ws + a.off_slot_count)[i] = R.slot_count[i];
+      }
+      if (threadIdx.x == 0) *reinterpret_cast<int*>(a.ws) = R.n_slots;
+    }
+  }
+  const int ns = R.n_slots;
+  const int* slot_expert = R.slot_expert;
+  const int* slot_first = R.slot_first;
+  const int* slot_count = R.slot_count;
   const int N = PHASE == 0 ? 2 * a.I : a.H;
   const int K = PHASE == 0 ? a.H : a.I;
   const int tiles = (N + kMoeTileRows - 1) / kMoeTileRows;
@@ -360,14 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a
   prod.warp = warp;
   prod.lane = lane;
   prod.n_issued = 0;
-  prod.wring = smem_raw + (size_t)warp * kSlots * G::SLOT;
-  prod.wfull = reinterpret_cast<uint64_t*>(smem_raw + G::RING) + warp * kSlots;
+  prod.wring = smem_raw + (size_t)warp * kMoeSlots * MoeRing::SLOT;
+  prod.wfull = reinterpret_cast<uint64_t*>(smem_raw + MoeRing::RING) + warp * kMoeSlots;
   if (lane == 0) {
-    for (int i = 0; i < kSlots; ++i) mbar_init(&prod.wfull[i], 1);
+    for (int i = 0; i < kMoeSlots; ++i) mbar_init(&prod.wfull[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  for (int i = 0; i < kSlots; ++i) prod.issue();
+  for (int i = 0; i < kMoeSlots; ++i) prod.issue();
 
   const DecodeK dk = load_decode_k(a.magic);
   float* gu = reinterpret_cast<float*>(a.ws + a.off_gu);
@@ -381,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a
     const int cnt = slot_count[slot];
     __syncthreads();  // the previous slot's token table is no longer read
     if (threadIdx.x < cnt) {
-      s_tok[threadIdx.x] = reinterpret_cast<const int*>(a.ws + a.off_pair_token)[first + threadIdx.x];
-      s_prob[threadIdx.x] = reinterpret_cast<const float*>(a.ws + a.off_pair_prob)[first + threadIdx.x];
+      s_tok[threadIdx.x] = R.pair_token[first + threadIdx.x];
+      s_prob[threadIdx.x] = R.pair_prob[first + threadIdx.x];
     }
     __syncthreads();
     const uint16_t* scales = scales0 + (size_t)e * a.stride_halves;
@@ -416,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a
 size_t expert_smem(int64_t K) {
   using G = Geometry<QMV_TERNARY2, kMoeRPW>;
   const int64_t S = (K + kStep - 1) / kStep;
-  return G::RING + G::BARS + (size_t)kMaxTokens * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(kMaxTokens, S);
+  return MoeRing::RING + MoeRing::BARS + (size_t)kMaxTokens * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(kMaxTokens, S);
 }
 
 // Scratch for moe_qmv_run_static: one fixed array per device, in the module's
@@ -515,9 +545,7 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   a.err = err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  moe_route_kernel<<<1, 256, 0, s>>>(a);
-  cudaError_t ce = cudaGetLastError();
-  if (ce != cudaSuccess) return cuda_fail(ce, "moe route launch");
+  cudaError_t ce;
   int per_sm = 0;
   rc = kernel_fit((const void*)moe_expert_kernel<0>, kThreads, smem_gu, &per_sm);
   if (rc) return rc;
