@@ -245,9 +245,28 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   int per_sm = 0;
   int rc = kernel_fit((const void*)kern, kThreads, smem, &per_sm);
   if (rc) return rc;
+  // persistent grid, one CTA per SM; contiguous tile ranges of about equal work,
+  // a tile weighing rows x K x the matrix's stored fraction of 16 x 128 tiles
   const int grid = std::min(std::min(sm_count(), kMaxCtas), tiles);
   b.n_ctas = grid;
-  for (int c = 0; c <= grid; ++c) b.cta_tile[c] = (int)((int64_t)tiles * c / grid);
+  std::vector<double> w(b.n_tasks);
+  double total = 0;
+  for (int i = 0; i < b.n_tasks; ++i) {
+    const double groups = (double)((b.t[i].N + 15) / 16), blocks = (double)(b.t[i].K / 128);
+    w[i] = (double)b.t[i].K * ((double)b.t[i].T / (groups * blocks));
+    total += w[i] * b.t[i].N;
+  }
+  b.cta_tile[0] = 0;
+  int c = 1;
+  double done = 0;
+  for (int i = 0; i < b.n_tasks && c < grid; ++i) {
+    const int nt = (b.t[i].N + TILE_ROWS - 1) / TILE_ROWS;
+    for (int j = 0; j < nt && c < grid; ++j) {
+      done += w[i] * std::min(TILE_ROWS, (int)b.t[i].N - j * TILE_ROWS);
+      while (c < grid && done >= total * c / grid) b.cta_tile[c++] = b.t[i].tile0 + j + 1;
+    }
+  }
+  for (; c <= grid; ++c) b.cta_tile[c] = tiles;
   kern<<<grid, kThreads, smem, s>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse ternary launch");
