@@ -56,19 +56,30 @@ __device__ __forceinline__ int find_sparse_task(const SparseBatch& b, int tile) 
   return lo;
 }
 
+// A ring slot holds the warp's rows of one record, then the record's tile
+// scales (16 rows x up to 8 tiles of fp16, 32 bytes a tile), both copied on the
+// slot's barrier.
+template <int RPW>
+struct SparseRing {
+  using G = Geometry<QMV_TERNARY2, RPW>;
+  static constexpr int SLOT = G::SLOT + 256;
+  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
+};
+
 template <int MT, int RPW>
 __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_constant__ SparseBatch b) {
   constexpr int FMT = QMV_TERNARY2;
   using F = Fmt<FMT>;
   using G = Geometry<FMT, RPW>;
+  using R = SparseRing<RPW>;
   constexpr int RQ = RPW / kGroups;
   constexpr int TILE_ROWS = kConsumerWarps * RPW;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + G::RING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R::RING);
   const int S = b.kc / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + G::RING + G::BARS);
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + G::BARS);
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
   __shared__ float s_red[kConsumerWarps][MT];
   __shared__ float s_xinv[MT];
@@ -79,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
   const int lane = tid & 31;
   const int tile_begin = b.cta_tile[blockIdx.x];
   const int tile_end = b.cta_tile[blockIdx.x + 1];
-  unsigned char* wring = ring + (size_t)warp * kSlots * G::SLOT;
+  unsigned char* wring = ring + (size_t)warp * kSlots * R::SLOT;
   uint64_t* wfull = full + warp * kSlots;
 
   if (lane == 0) {
@@ -107,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
     }
   };
 
-  // ---- producer side of this warp: one bulk copy per record, two records ahead
+  // ---- producer side of this warp: the warp's rows of a record and the record's
+  // scales, two records ahead
   int p_tile = tile_begin, p_ti = 0, p_r = 0, p_cnt = 0, p_g = 0, p_half = 0;
   uint32_t p_t0 = 0, n_issued = 0;
   auto settle = [&]() {  // move to the next tile with records
@@ -127,10 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
     const int slot = n_issued % kSlots;
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&wfull[slot], bytes);
-      const unsigned char* src = T.w + T.off_codes + ((size_t)p_t0 + (size_t)p_r * kBlocksPerStep) * 16 * G::BLOCK_BYTES +
-                                 (size_t)p_half * RPW * nbk * G::BLOCK_BYTES;
-      bulk_g2s(wring + (size_t)slot * G::SLOT, src, bytes, &wfull[slot]);
+      const size_t tt = (size_t)p_t0 + (size_t)p_r * kBlocksPerStep;  // the record's first stored tile
+      mbar_arrive_expect_tx(&wfull[slot], bytes + 32u * nbk);
+      const unsigned char* src = T.w + T.off_codes + tt * 16 * G::BLOCK_BYTES + (size_t)p_half * RPW * nbk * G::BLOCK_BYTES;
+      bulk_g2s(wring + (size_t)slot * R::SLOT, src, bytes, &wfull[slot]);
+      bulk_g2s(wring + (size_t)slot * R::SLOT + G::SLOT, T.w + T.off_scales + tt * 32, 32u * nbk, &wfull[slot]);
     }
     ++n_issued;
     if (++p_r * kBlocksPerStep >= p_cnt) {
@@ -161,43 +174,39 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
     uint32_t t0;
     rows_of(T, tile, grp, half, t0, cnt);
     const uint16_t* tblock = reinterpret_cast<const uint16_t*>(T.w + T.off_block);
-    const unsigned short* tscale = reinterpret_cast<const unsigned short*>(T.w + T.off_scales);
     float accc[RQ][MT];
 #pragma unroll
     for (int r = 0; r < RQ; ++r)
 #pragma unroll
       for (int m = 0; m < MT; ++m) accc[r][m] = 0.f;
     const int nrec = (cnt + kBlocksPerStep - 1) / kBlocksPerStep;
-    // block index and row scales of this lane's tile in a record, loaded one record ahead
-    auto tile_info = [&](int rec, int& blk, unsigned short (&sc)[RQ]) {
-      blk = 0;
-      if (rec < nrec && rec * kBlocksPerStep + p < cnt) {
-        const uint32_t tt = t0 + (uint32_t)(rec * kBlocksPerStep + p);
-        blk = __ldg(tblock + tt);
-#pragma unroll
-        for (int r = 0; r < RQ; ++r) sc[r] = __ldg(tscale + (size_t)tt * 16 + half * RPW + r * kGroups + g);
-      }
+    // block index of this lane's tile in a record, loaded one record ahead
+    auto tile_block = [&](int rec) {
+      return rec < nrec && rec * kBlocksPerStep + p < cnt ? (int)__ldg(tblock + t0 + (uint32_t)(rec * kBlocksPerStep + p))
+                                                          : 0;
     };
-    int blk_next;
-    unsigned short sc_next[RQ];
-    tile_info(0, blk_next, sc_next);
+    int blk_next = tile_block(0);
     for (int rec = 0; rec < nrec; ++rec, ++it) {
       const int nbk = min(kBlocksPerStep, cnt - rec * kBlocksPerStep);
       const bool active = p < nbk;
       int blk = blk_next;
-      unsigned short sc[RQ];
-#pragma unroll
-      for (int r = 0; r < RQ; ++r) sc[r] = sc_next[r];
-      tile_info(rec + 1, blk_next, sc_next);
+      blk_next = tile_block(rec + 1);
       if (active && blk >= T.K / 128) {
         atomicCAS(b.err, 0, (int)QMV_ERR_CORRUPT);
         blk = 0;
       }
       const int slot = it % kSlots;
       mbar_wait(&wfull[slot], (it / kSlots) & 1u, b.err);
-      if (active)
-        decode_step<FMT, MT, RQ>(wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, nbk * G::BLOCK_BYTES, xs, negs,
-                                 S, blk / kBlocksPerStep, g, blk % kBlocksPerStep, dk, sc, accc);
+      if (active) {
+        const unsigned char* sb = wring + (size_t)slot * R::SLOT;
+        // the rows' scales of stored tile p: entries p * 16 + row of the record's scales
+        const unsigned short* srec = reinterpret_cast<const unsigned short*>(sb + G::SLOT);
+        unsigned short sc[RQ];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) sc[r] = srec[p * 16 + half * RPW + r * kGroups + g];
+        decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, nbk * G::BLOCK_BYTES, xs, negs, S, blk / kBlocksPerStep, g,
+                                 blk % kBlocksPerStep, dk, sc, accc);
+      }
       __syncwarp();
       issue_one();
     }
@@ -231,7 +240,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   }
   b.n_tiles = tiles;
   b.rows_per_tile = TILE_ROWS;
-  const size_t fixed = G::RING + G::BARS;
+  const size_t fixed = SparseRing<RPW>::RING + G::BARS;
   const int kc = (max_K + kStep - 1) / kStep * kStep;
   const size_t S = kc / kStep;
   const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<QMV_TERNARY2>(MT, S);
