@@ -281,7 +281,7 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   // per staged column: MT fp16 values, plus the seeds (fp16 pairs per 128 columns and row)
   const size_t fixed = FmaRing<FMT, RPW>::RING + G::BARS;
   const size_t budget = kSmemMax - fixed - 1024;
-  int kc_cap = (int)(budget / ((size_t)MT * 2 + ((size_t)MT * 4 * Chain<FMT>::SEEDS + 127) / 128)) / kStep * kStep;
+  int kc_cap = (int)(budget / ((size_t)MT * kStep * 2 + seed_bytes<FMT>(MT, 1))) * kStep;
   int kc = ((max_K + kStep - 1) / kStep) * kStep;
   if (kc > kc_cap) kc = kc_cap;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", MT);

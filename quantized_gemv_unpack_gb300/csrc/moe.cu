@@ -9,7 +9,7 @@
 // expert counts its (token, expert) pairs, a block scan orders the pairs by
 // expert and token and lists each active expert once (a slot).
 //  1. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
-//     tile of 64 rows of the [gate; up] matrix) into equal contiguous ranges;
+//     tile of 80 rows of the [gate; up] matrix) into equal contiguous ranges;
 //     a CTA stages the slot's token rows of x (gathered) once per slot and
 //     decodes its rows with the same per-warp bulk-copy ring and decode step as
 //     the matvec batch, prefetching across unit boundaries, and writes g and u
@@ -30,8 +30,10 @@ namespace {
 
 using namespace core;
 
+constexpr int kMoeWarps = 20;                           // decode warps per CTA: 4-row warps fit 102
+constexpr int kMoeThreads = kMoeWarps * 32;             // registers, and the extra warps hide latency
 constexpr int kMoeRPW = 4;                              // rows per decode warp
-constexpr int kMoeTileRows = kConsumerWarps * kMoeRPW;  // 64
+constexpr int kMoeTileRows = kMoeWarps * kMoeRPW;       // 80
 constexpr int kMaxTopk = 8;
 constexpr int kMaxTokens = 8;
 constexpr int kMaxExperts = 256;
@@ -43,8 +45,8 @@ constexpr int kMoeSlots = 2;                            // ring slots per decode
 struct MoeRing {
   using G = Geometry<QMV_TERNARY2, kMoeRPW>;
   static constexpr int SLOT = G::SLOT;
-  static constexpr int RING = kConsumerWarps * kMoeSlots * SLOT;
-  static constexpr int BARS = kConsumerWarps * kMoeSlots * 8;
+  static constexpr int RING = kMoeWarps * kMoeSlots * SLOT;
+  static constexpr int BARS = kMoeWarps * kMoeSlots * 8;
 };
 
 // Workspace layout (all offsets in bytes from the workspace base).
@@ -90,7 +92,7 @@ struct MoeRoute {
   float pair_prob[kMaxPairs];
   int exp[kMaxTokens][kMaxTopk];
   float prob[kMaxTokens][kMaxTopk];
-  int wp[kThreads / 32], ws[kThreads / 32];
+  int wp[kMoeWarps], ws[kMoeWarps];
 };
 
 // Called by all threads of the CTA (blockDim.x >= E); ends with a CTA barrier.
@@ -260,7 +262,7 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
   using F = Fmt<FMT>;
   using G = Geometry<FMT, kMoeRPW>;
   constexpr int RQ = kMoeRPW / kGroups;
-  __shared__ float s_red[kConsumerWarps][MT];
+  __shared__ float s_red[kMoeWarps][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
   const int S = (K + kStep - 1) / kStep;
@@ -272,7 +274,7 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
   const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
   const int KB = K / 128;
 
-  stage_chunk<FMT, MT, kThreads>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
+  stage_chunk<FMT, MT, kMoeThreads>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
 
   const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;  // scale records per 16-row group
   for (; u < u_end; ++u) {
@@ -339,7 +341,7 @@ struct DownOut {  // y[token] += p * value
 // Persistent: CTA c takes the contiguous unit range [c*U/G, (c+1)*U/G) of the
 // U = n_slots * tiles units of this phase (all units are the same size).
 template <int PHASE>
-__global__ void __launch_bounds__(kThreads, 1) moe_expert_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArgs a) {
   using G = Geometry<QMV_TERNARY2, kMoeRPW>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int s_tok[kMaxTokens];
@@ -547,17 +549,17 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t ce;
   int per_sm = 0;
-  rc = kernel_fit((const void*)moe_expert_kernel<0>, kThreads, smem_gu, &per_sm);
+  rc = kernel_fit((const void*)moe_expert_kernel<0>, kMoeThreads, smem_gu, &per_sm);
   if (rc) return rc;
-  rc = kernel_fit((const void*)moe_expert_kernel<1>, kThreads, smem_dn, &per_sm);
+  rc = kernel_fit((const void*)moe_expert_kernel<1>, kMoeThreads, smem_dn, &per_sm);
   if (rc) return rc;
   // persistent grids: one CTA per SM, capped by the largest possible unit count
   const int units_gu = a.max_slots * (int)((I2 + kMoeTileRows - 1) / kMoeTileRows);
   const int units_dn = a.max_slots * (int)((H + kMoeTileRows - 1) / kMoeTileRows);
-  moe_expert_kernel<0><<<std::min(sm_count(), units_gu), kThreads, smem_gu, s>>>(a);
+  moe_expert_kernel<0><<<std::min(sm_count(), units_gu), kMoeThreads, smem_gu, s>>>(a);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return cuda_fail(ce, "moe gate|up launch");
-  moe_expert_kernel<1><<<std::min(sm_count(), units_dn), kThreads, smem_dn, s>>>(a);
+  moe_expert_kernel<1><<<std::min(sm_count(), units_dn), kMoeThreads, smem_dn, s>>>(a);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
   return QMV_OK;
