@@ -5,8 +5,8 @@
 // buffer; the matvec is the fp16-FMA kernel of gemv.cu walking each row group's
 // stored tiles.
 //
-// Matvec. One persistent launch (one CTA of 16 warps per SM) over a table of
-// matvecs; rows are cut into tiles of 16 warps x RPW rows. A warp owns RPW rows
+// Matvec. One persistent launch (one CTA of W warps per SM: 20 up to M = 4, 16
+// above) over a table of matvecs; rows are cut into tiles of W warps x RPW rows. A warp owns RPW rows
 // of one 16-row group (the whole group at RPW = 16, a half at RPW = 8, a quarter
 // at RPW = 4, which M >= 5 uses to stay within 128 registers) and
 // walks the group's records (up to 8 stored tiles each, its rows contiguous in
@@ -29,6 +29,12 @@ namespace {
 using namespace core;
 
 constexpr int kMaxSparseTasks = QMV_MAX_BATCH;
+// Decode warps per CTA: 20 up to M = 4 (the kernel then fits 102 registers and
+// the extra warps hide latency), 16 above.
+template <int MT>
+struct SparseWarps {
+  static constexpr int value = MT <= 4 ? 20 : 16;
+};
 
 // one matvec; the sections are located by byte offsets from the packed buffer
 struct SparseTask {
@@ -59,29 +65,32 @@ __device__ __forceinline__ int find_sparse_task(const SparseBatch& b, int tile) 
 // A ring slot holds the warp's rows of one record, then the record's tile
 // scales (16 rows x up to 8 tiles of fp16, 32 bytes a tile), both copied on the
 // slot's barrier.
-template <int RPW>
+template <int RPW, int W>
 struct SparseRing {
   using G = Geometry<QMV_TERNARY2, RPW>;
   static constexpr int SLOT = G::SLOT + 256;
-  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
+  static constexpr int RING = W * kSlots * SLOT;
+  static constexpr int BARS = W * kSlots * 8;
 };
 
 template <int MT, int RPW>
-__global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_constant__ SparseBatch b) {
+__global__ void __launch_bounds__(SparseWarps<MT>::value * 32, 1)
+    sparse_kernel(const __grid_constant__ SparseBatch b) {
   constexpr int FMT = QMV_TERNARY2;
+  constexpr int W = SparseWarps<MT>::value;
   using F = Fmt<FMT>;
   using G = Geometry<FMT, RPW>;
-  using R = SparseRing<RPW>;
+  using R = SparseRing<RPW, W>;
   constexpr int RQ = RPW / kGroups;
-  constexpr int TILE_ROWS = kConsumerWarps * RPW;
+  constexpr int TILE_ROWS = W * RPW;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R::RING);
   const int S = b.kc / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + G::BARS);
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + R::BARS);
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
-  __shared__ float s_red[kConsumerWarps][MT];
+  __shared__ float s_red[W][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
 
@@ -166,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
     const int ti = find_sparse_task(b, tile);
     const SparseTask& T = b.t[ti];
     if (T.x != staged_x || T.K != staged_K) {
-      stage_chunk<FMT, MT, kThreads>(Bf16Rows{T.x, T.ldx, 0}, T.K, S, xs, negs, s_red, s_xscale, s_xinv);
+      stage_chunk<FMT, MT, W * 32>(Bf16Rows{T.x, T.ldx, 0}, T.K, S, xs, negs, s_red, s_xscale, s_xinv);
       staged_x = T.x;
       staged_K = T.K;
     }
@@ -230,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_kernel(const __grid_consta
 template <int MT, int RPW>
 int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   using G = Geometry<QMV_TERNARY2, RPW>;
-  constexpr int TILE_ROWS = kConsumerWarps * RPW;
+  constexpr int W = SparseWarps<MT>::value;
+  constexpr int TILE_ROWS = W * RPW;
   constexpr size_t kSmemMax = 227 * 1024;
   int tiles = 0, max_K = 0;
   for (int i = 0; i < b.n_tasks; ++i) {
@@ -240,7 +250,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   }
   b.n_tiles = tiles;
   b.rows_per_tile = TILE_ROWS;
-  const size_t fixed = SparseRing<RPW>::RING + G::BARS;
+  const size_t fixed = SparseRing<RPW, W>::RING + SparseRing<RPW, W>::BARS;
   const int kc = (max_K + kStep - 1) / kStep * kStep;
   const size_t S = kc / kStep;
   const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<QMV_TERNARY2>(MT, S);
@@ -252,7 +262,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   auto kern = sparse_kernel<MT, RPW>;
   int per_sm = 0;
-  int rc = kernel_fit((const void*)kern, kThreads, smem, &per_sm);
+  int rc = kernel_fit((const void*)kern, W * 32, smem, &per_sm);
   if (rc) return rc;
   // persistent grid, one CTA per SM; contiguous tile ranges of about equal work,
   // a tile weighing rows x K x the matrix's stored fraction of 16 x 128 tiles
@@ -276,7 +286,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
     }
   }
   for (; c <= grid; ++c) b.cta_tile[c] = tiles;
-  kern<<<grid, kThreads, smem, s>>>(b);
+  kern<<<grid, W * 32, smem, s>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse ternary launch");
   return QMV_OK;
