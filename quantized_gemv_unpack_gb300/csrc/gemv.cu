@@ -2,11 +2,13 @@
 //
 // One persistent launch (one CTA per SM) walks a table of matvecs: one GEMV,
 // the q|k|v group of a layer, or a whole decode stack. Rows are cut into tiles
-// of kConsumerWarps * RPW rows; the host gives every CTA a contiguous range of
-// tiles holding about the same number of bytes, so a CTA re-stages its
-// activations only when its range crosses into the next matvec.
+// of W * RPW rows; the host gives every CTA a contiguous range of tiles holding
+// about the same number of bytes, so a CTA re-stages its activations only when
+// its range crosses into the next matvec. W = 16 decode warps per CTA; a launch
+// too small to give every SM a 64-row tile uses 4-warp CTAs of 16 rows instead,
+// several per SM.
 //
-// Streaming. A CTA has 16 decode warps. Each warp owns RPW consecutive rows of
+// Streaming. Each warp owns RPW consecutive rows of
 // the tile and a two-slot ring in shared memory; a slot holds one step (1024
 // columns) of its rows. The packed codes are stored in records of 16 rows x
 // one step, so a warp's rows of a step are one contiguous range: lane 0 of the
@@ -68,18 +70,22 @@ __device__ __forceinline__ int find_task(const GemvBatch& b, int tile) {
 
 // A ring slot holds the warp's rows of one step, then the step's 256-byte
 // scale record (16 rows x 8 blocks of fp16), both copied on the slot's barrier.
-template <int FMT, int RPW>
+// W decode warps per CTA: 16 (one persistent CTA per SM) or, for launches too
+// small to give every SM a 64-row tile, 4 (16-row tiles, several CTAs per SM).
+template <int FMT, int RPW, int W>
 struct FmaRing {
   using G = Geometry<FMT, RPW>;
   static constexpr int SLOT = G::SLOT + 256;
-  static constexpr int RING = kConsumerWarps * kSlots * SLOT;
+  static constexpr int RING = W * kSlots * SLOT;
+  static constexpr int BARS = W * kSlots * 8;
+  static constexpr int TILE_ROWS = W * RPW;
 };
 
-template <int FMT, int MT, int RPW>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvBatch b) {
+template <int FMT, int MT, int RPW, int W>
+__global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__ GemvBatch b) {
   using F = Fmt<FMT>;
   using G = Geometry<FMT, RPW>;
-  using R = FmaRing<FMT, RPW>;
+  using R = FmaRing<FMT, RPW, W>;
   constexpr int WPB = F::WPB;
   constexpr int JW = F::JW;
   constexpr int RQ = RPW / kGroups;          // row quads per decode warp
@@ -90,9 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R::RING);          // [warp][slot]
   const int KC = b.kc;
   const int S = KC / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + G::BARS);        // [MT][S][WPB][JW][8]
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + R::BARS);        // [MT][S][WPB][JW][8]
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8][seeds per block]
-  __shared__ float s_red[kConsumerWarps][MT];
+  __shared__ float s_red[W][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
 
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     p_nb = min(KC, p_K - p_kc0) / 128;
     const int nbk = min(kBlocksPerStep, p_nb - p_s * kBlocksPerStep);
     const int blk0 = p_kc0 / 128 + p_s * kBlocksPerStep;
-    const int wrow0 = (p_tile - T.tile0) * G::TILE_ROWS + warp * RPW;
+    const int wrow0 = (p_tile - T.tile0) * R::TILE_ROWS + warp * RPW;
     const int N16 = (T.N + 15) / 16 * 16;
     // the warp's RPW rows lie inside one 16-row group: one contiguous piece of
     // the (group, step) record; rows past the padded end are not copied
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const uint16_t* __restrict__ x = b.t[ti].x;
     float* __restrict__ y = b.t[ti].y;
     const int N = b.t[ti].N, K = b.t[ti].K, ldx = b.t[ti].ldx, ldy = b.t[ti].ldy;
-    const int wrow0 = (tile - b.t[ti].tile0) * G::TILE_ROWS + warp * RPW;
+    const int wrow0 = (tile - b.t[ti].tile0) * R::TILE_ROWS + warp * RPW;
     const int srow = wrow0 % 16 + g;  // this lane's first row in the scale record
 
     float acc[RQ][MT];
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
       if (x != staged_x || kc0 != staged_kc0 || K != staged_K) {
         // ---- stage the activations of this chunk
-        stage_chunk<FMT, MT, kThreads>(Bf16Rows{x, ldx, kc0}, kcn, S, xs, negs, s_red, s_xscale, s_xinv);
+        stage_chunk<FMT, MT, W * 32>(Bf16Rows{x, ldx, kc0}, kcn, S, xs, negs, s_red, s_xscale, s_xinv);
         staged_x = x;
         staged_kc0 = kc0;
         staged_K = K;
@@ -262,24 +268,24 @@ int pick_rpw(int M, int64_t total_rows) {
   return big;
 }
 
-template <int FMT, int MT, int RPW>
+template <int FMT, int MT, int RPW, int W = kConsumerWarps>
 int launch_t(GemvBatch& b, cudaStream_t s) {
   using F = Fmt<FMT>;
-  using G = Geometry<FMT, RPW>;
+  using R = FmaRing<FMT, RPW, W>;
   constexpr size_t kSmemMax = 227 * 1024;
   // tiles, numbered across tasks
   int tiles = 0;
   int max_K = 0;
   for (int i = 0; i < b.n_tasks; ++i) {
     b.t[i].tile0 = tiles;
-    tiles += (b.t[i].N + G::TILE_ROWS - 1) / G::TILE_ROWS;
+    tiles += (b.t[i].N + R::TILE_ROWS - 1) / R::TILE_ROWS;
     max_K = std::max(max_K, (int)b.t[i].K);
   }
   b.n_tiles = tiles;
-  b.rows_per_tile = G::TILE_ROWS;
+  b.rows_per_tile = R::TILE_ROWS;
   // activation chunk: as much of K as fits next to the ring, in whole steps;
   // per staged column: MT fp16 values, plus the seeds (fp16 pairs per 128 columns and row)
-  const size_t fixed = FmaRing<FMT, RPW>::RING + G::BARS;
+  const size_t fixed = R::RING + R::BARS;
   const size_t budget = kSmemMax - fixed - 1024;
   int kc_cap = (int)(budget / ((size_t)MT * kStep * 2 + seed_bytes<FMT>(MT, 1))) * kStep;
   int kc = ((max_K + kStep - 1) / kStep) * kStep;
@@ -291,12 +297,13 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   fill_magic<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
-  auto kern = gemv_kernel<FMT, MT, RPW>;
+  auto kern = gemv_kernel<FMT, MT, RPW, W>;
   int per_sm = 0;
-  int rc = kernel_fit((const void*)kern, kThreads, smem, &per_sm);
+  int rc = kernel_fit((const void*)kern, W * 32, smem, &per_sm);
   if (rc != QMV_OK) return rc;
-  // persistent grid, one CTA per SM; contiguous tile ranges of about equal bytes
-  const int grid = std::min(std::min(sm_count(), kMaxCtas), tiles);
+  // persistent grid (16-warp CTAs: one per SM; smaller CTAs: as many as fit);
+  // contiguous tile ranges of about equal bytes
+  const int grid = std::min(std::min(sm_count() * (W == kConsumerWarps ? 1 : per_sm), kMaxCtas), tiles);
   double total = 0;
   for (int i = 0; i < b.n_tasks; ++i) total += (double)b.t[i].N * b.t[i].K;
   b.n_ctas = grid;
@@ -304,14 +311,14 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   int c = 1;
   double done = 0;
   for (int i = 0; i < b.n_tasks && c < grid; ++i) {
-    const int nt = (b.t[i].N + G::TILE_ROWS - 1) / G::TILE_ROWS;
+    const int nt = (b.t[i].N + R::TILE_ROWS - 1) / R::TILE_ROWS;
     for (int j = 0; j < nt && c < grid; ++j) {
-      done += (double)std::min(G::TILE_ROWS, (int)b.t[i].N - j * G::TILE_ROWS) * b.t[i].K;
+      done += (double)std::min(R::TILE_ROWS, (int)b.t[i].N - j * R::TILE_ROWS) * b.t[i].K;
       while (c < grid && done >= total * c / grid) b.cta_tile[c++] = b.t[i].tile0 + j + 1;
     }
   }
   for (; c <= grid; ++c) b.cta_tile[c] = tiles;
-  kern<<<grid, kThreads, smem, s>>>(b);
+  kern<<<grid, W * 32, smem, s>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
   return QMV_OK;
@@ -322,10 +329,14 @@ int launch_fmt(GemvBatch& b, int M, cudaStream_t s) {
   int64_t rows = 0;
   for (int i = 0; i < b.n_tasks; ++i) rows += b.t[i].N;
   const int rpw = pick_rpw<FMT>(M, rows);
+  // fewer 64-row tiles than SMs: 4-warp CTAs of 16 rows instead
+  const bool small = rpw == 4 && rows / ((int64_t)kConsumerWarps * 4) < sm_count();
   constexpr int BIG1 = FMT == QMV_TERNARY2 ? 16 : 8;
   switch (M) {
-    case 1: return rpw == 4 ? launch_t<FMT, 1, 4>(b, s) : launch_t<FMT, 1, BIG1>(b, s);
-    case 2: return rpw == 4 ? launch_t<FMT, 2, 4>(b, s) : launch_t<FMT, 2, 8>(b, s);
+    case 1:
+      return small ? launch_t<FMT, 1, 4, 4>(b, s) : rpw == 4 ? launch_t<FMT, 1, 4>(b, s) : launch_t<FMT, 1, BIG1>(b, s);
+    case 2:
+      return small ? launch_t<FMT, 2, 4, 4>(b, s) : rpw == 4 ? launch_t<FMT, 2, 4>(b, s) : launch_t<FMT, 2, 8>(b, s);
     case 3: return launch_t<FMT, 3, 4>(b, s);
     case 4: return launch_t<FMT, 4, 4>(b, s);
     case 5: return launch_t<FMT, 5, 4>(b, s);
