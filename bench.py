@@ -81,8 +81,13 @@ PATH_FLAGS = {"auto": 0, "fma": 1, "mma": 2}   # qmv_desc.flags: QMV_FLAG_PATH_F
 MMA_MIN_M = {"int4": 1, "ternary": 3}          # the library's automatic choice of the tensor-core kernel
 
 
-def matvec_kernel(fmt: str, M: int, path: str) -> str:
-    """Name of the matvec kernel the library runs for this M and kernel choice."""
+LUT_KERNEL = "lut_kernel (byte-lookup tables, fp32)"
+
+
+def matvec_kernel(fmt: str, M: int, path: str, layout: str = "record") -> str:
+    """Name of the matvec kernel the library runs for this M, layout and kernel choice."""
+    if fmt == "ternary" and layout == "lut":
+        return LUT_KERNEL
     mma = path == "mma" or (path == "auto" and M >= MMA_MIN_M[fmt])
     if mma:
         return f"gemv_mma_kernel<{fmt}, n-tiles={1 if M <= 8 else 2}> (mma.sync m16n8k16)"
@@ -223,9 +228,10 @@ class Stack(Workload):
     kernel = "gemv_kernel<ternary, M=1>"
     tok_s = True
 
-    def __init__(self, q, torch, dev, layers=LAYERS, seed=4, path="auto"):
+    def __init__(self, q, torch, dev, layers=LAYERS, seed=4, path="auto", layout="lut"):
         from quantized_gemv_unpack_gb300 import synth
-        self.kernel = matvec_kernel("ternary", 1, path)
+        self.kernel = matvec_kernel("ternary", 1, path, layout)
+        fmt = q.QMV_TERNARY2_LUT if layout == "lut" else q.QMV_TERNARY2
         gen = synth.torch_generator(seed, dev)
         shapes = synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
         # all activations in one buffer and all outputs in another, so an end-to-end
@@ -241,8 +247,8 @@ class Stack(Workload):
             x_h.copy_(synth.activations_bf16_torch(gen, (1, HIDDEN), device=dev)[0])
             x_i.copy_(synth.activations_bf16_torch(gen, (1, INTER), device=dev)[0])
             for _, N, K in shapes:
-                d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
-                d.flags = PATH_FLAGS[path]
+                d = q.qmv_pack_desc(fmt, N, K)
+                d.flags = PATH_FLAGS[path] if layout == "record" else 0
                 p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
                 w = synth.student_t4_torch(gen, (N, K), device=dev)
                 q.qmv_pack_ternary(d, w, p)
@@ -250,25 +256,27 @@ class Stack(Workload):
                 y = self.y_all[y_off:y_off + N].view(1, N)
                 y_off += N
                 tasks.append((d, p, (x_i if K == INTER else x_h).view(1, K), y))
-                nbytes += d.bytes[0] + N * (K // 128) * 2 + N * 4
+                nbytes += N * K // 4 + N * (K // 128) * 2 + N * 4
             nbytes += (HIDDEN + INTER) * 2
         torch.cuda.synchronize()
-        self.batch = q.Batch(q.QMV_TERNARY2, tasks, 1)
+        self.batch = q.Batch(fmt, tasks, 1)
         self.nbytes = nbytes
         self.layers = layers
         self.path = path
+        self.layout = layout
 
     @staticmethod
-    def stack_config(layers):
+    def stack_config(layers, layout="lut"):
         return {"workload": f"27B-shaped ternary decode stack: {layers} layers x {{q,k,v,o,gate,up,down}}, "
                             "hidden 5120, 40/8 heads x 128, SwiGLU 25600, block-128 absmean ternary + fp16 scales, "
                             "batch 1",
+                "layout": {"lut": "byte-lookup (QMV_TERNARY2_LUT)", "record": "row-group records (QMV_TERNARY2)"}[layout],
                 "layers": layers, "hidden": HIDDEN, "heads": [NQ, NKV, HD], "intermediate": INTER,
                 "batch": 1, "matvecs_per_step": 7 * layers, "seed": 4,
                 "l2": "inputs larger than L2 (7.27 GB of packed weights per step; no flush needed)"}
 
     def config(self):
-        return self.stack_config(self.layers)
+        return self.stack_config(self.layers, self.layout)
 
     def step(self, i, stream):
         self.batch.run(stream)
@@ -278,7 +286,8 @@ class Stack(Workload):
 
     def traffic(self):
         # the capture is of 3 layers, scaled to 60 there; traffic grows with the layer count
-        return captured_traffic("stack", self.layers / LAYERS) if self.path == "auto" else None
+        key = "stack" if self.layout == "lut" else "stack-record"
+        return captured_traffic(key, self.layers / LAYERS) if self.path == "auto" else None
 
 
 class SparseStack(Workload):
@@ -358,13 +367,13 @@ class Ternary4096(Workload):
     name = "ternary-4096"
     kernel = "gemv_kernel<ternary, M=1>"
 
-    def __init__(self, q, torch, dev, M=1, path="auto"):
+    def __init__(self, q, torch, dev, M=1, path="auto", layout="record"):
         from quantized_gemv_unpack_gb300 import synth
-        self.kernel = matvec_kernel("ternary", M, path)
+        self.kernel = matvec_kernel("ternary", M, path, layout)
         gen = synth.torch_generator(0, dev)
         N = K = 4096
-        self.d = q.qmv_pack_desc(q.QMV_TERNARY2, N, K)
-        self.d.flags = PATH_FLAGS[path]
+        self.d = q.qmv_pack_desc(q.QMV_TERNARY2_LUT if layout == "lut" else q.QMV_TERNARY2, N, K)
+        self.d.flags = PATH_FLAGS[path] if layout == "record" else 0
         one = torch.empty(self.d.total_bytes, dtype=torch.uint8, device=dev)
         q.qmv_pack_ternary(self.d, synth.student_t4_torch(gen, (N, K), device=dev), one)
         self.copies = copies_for(self.d.total_bytes)
@@ -375,10 +384,11 @@ class Ternary4096(Workload):
         self.M = M
         self.q = q
         self.path = path
+        self.layout = layout
 
     def config(self):
         return {"workload": f"ternary GEMV 4096 x 4096, block-128 absmean + fp16 scales, M={self.M}", "M": self.M,
-                "seed": 0, "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
+                "layout": self.layout, "seed": 0, "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
 
     def step(self, i, stream):
         self.q.qmv_run_ternary(self.d, self.ps[i % self.copies], self.x, self.y, stream)
@@ -387,7 +397,8 @@ class Ternary4096(Workload):
         return [self.x], [self.y]
 
     def traffic(self):
-        return captured_traffic(f"ternary-4096 M={self.M}") if self.path == "auto" else None
+        key = f"ternary-4096 M={self.M}" + (" lut" if self.layout == "lut" else "")
+        return captured_traffic(key) if self.path == "auto" else None
 
 
 class Int4Layer(Workload):
@@ -579,13 +590,13 @@ class Moe(Workload):
 
 def make_workload(name, q, torch, dev, a):
     if name == "stack":
-        return Stack(q, torch, dev, a.layers, path=a.path)
+        return Stack(q, torch, dev, a.layers, path=a.path, layout=a.layout)
     if name == "stack-sparse":
         return SparseStack(q, torch, dev, a.layers)
     if name == "kv-encode":
         return KvEncode(q, torch, dev)
     if name == "ternary-4096":
-        return Ternary4096(q, torch, dev, a.M or 1, path=a.path)
+        return Ternary4096(q, torch, dev, a.M or 1, path=a.path, layout=a.layout if (a.M or 1) == 1 else "record")
     if name == "int4-layer":
         return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
@@ -609,6 +620,8 @@ def main():
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
+    ap.add_argument("--layout", default="lut", choices=["lut", "record"],
+                    help="ternary at M = 1 (stack, ternary-4096): byte-lookup layout or row-group records")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
@@ -631,7 +644,7 @@ def main():
         line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": base["seconds_per_pass"] * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-                "config": Stack.stack_config(LAYERS), "impl": "reference",
+                "config": Stack.stack_config(LAYERS, a.layout), "impl": "reference",
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
                                  "unit": UNIT},
                 "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -723,7 +736,8 @@ def main():
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp16x2-f32" if a.workload in ("stack", "stack-sparse", "ternary-4096", "int4-layer", "moe") else "f32",
+        "dtype": "f32" if "lut_kernel" in wl.kernel else (
+            "fp16x2-f32" if a.workload in ("stack", "stack-sparse", "ternary-4096", "int4-layer", "moe") else "f32"),
         "data": DATA,
         "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU", kernel_choice=a.path),
         "pct_of_peak": 100.0 * per_gpu / peak,

@@ -56,7 +56,8 @@ typedef enum {
   QMV_INT4 = 2,              /* group-128 absmax/7 INT4, 4 bits + fp16 scale per group */
   QMV_CASS = 3,              /* Cassandra lossless bf16 split (speculation + verification) */
   QMV_CASS_MX = 4,           /* Cassandra-2: the split with MX shared exponents (slightly lossy) */
-  QMV_TERNARY2_SPARSE = 5    /* ternary with flagged all-zero tiles left out */
+  QMV_TERNARY2_SPARSE = 5,   /* ternary with flagged all-zero tiles left out */
+  QMV_TERNARY2_LUT = 6       /* QMV_TERNARY2's codes and scales in the byte-lookup layout (M = 1) */
 } qmv_format;
 
 /*
@@ -118,6 +119,20 @@ typedef enum {
  *                record is the 16 rows' code blocks of its tiles, row after row
  *   4 scales   : T x 16 fp16, the 16 rows' scales of each stored tile (1.0 for
  *                an all-zero block of a real row, 0 for padding rows)
+ * QMV_TERNARY2_LUT ("Ternary Bonsai 2", section 1.2, block_ternary: the same
+ * codes and fp16 scales as QMV_TERNARY2, arranged for the byte-lookup matvec
+ * at one activation row). Rows go in NG = ceil(N/32) groups of 32 (the last
+ * padded with zero codes and zero scales); KB = K/128 blocks.
+ *   0 codes : NG * KB * 1024 bytes. A code byte holds the codes of four
+ *             consecutive columns 4c..4c+3 of a block, column 4c + i at bits
+ *             2i..2i+1 (00 = 0, 01 = +1, 10 = -1; 11 is invalid). The 32 bytes
+ *             of (row n, block b) are rotated by n % 32: byte t holds column
+ *             group c = (t + n) % 32. They lie in the 1024-byte record of
+ *             (block b, row group n / 32), which starts at (b * NG + n / 32) *
+ *             1024; inside it byte t of row n is at (t / 16) * 512 + (n % 32)
+ *             * 16 + t % 16.
+ *   1 scales: fp16 [KB][NG * 32]; the scale of (row n, block b) is element
+ *             b * NG * 32 + n.
  */
 typedef struct {
   uint32_t abi_version;      /* QMV_ABI_VERSION */
@@ -153,8 +168,8 @@ typedef struct {
 } qmv_task;
 
 /*
- * Layout math only (host, no GPU needed): fill `out` for a ternary or INT4
- * matrix of N x K with the given group (must be 128). K must be a positive
+ * Layout math only (host, no GPU needed): fill `out` for a ternary (either
+ * layout) or INT4 matrix of N x K with the given group (must be 128). K must be a positive
  * multiple of 128 and N positive; for QMV_CASS_MX (group 32) K must be a
  * multiple of 64. Returns QMV_ERR_UNSUPPORTED for QMV_CASS, whose stream
  * length depends on the data (use cass_pack_host).
@@ -163,6 +178,7 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
 
 /*
  * Quantize and pack on the GPU (offline step). w: device fp32 [N][K] row-major.
+ * qmv_pack_ternary writes QMV_TERNARY2 or QMV_TERNARY2_LUT, after desc->format.
  * packed: device buffer of desc->total_bytes. Ternary follows block_ternary
  * ("Ternary Bonsai 2", 1.2): scale* = (sum_k |w_k|)/128 + 1e-8 summed in float64
  * in column order, q = clamp(rint(w/scale*), -1, 1) in float64, stored scale =
@@ -184,9 +200,10 @@ int qmv_sparse_pack_host(const qmv_desc* dense, const void* dense_packed, qmv_de
                          int64_t out_capacity);
 
 /*
- * Decode a packed ternary or INT4 matrix to int8 q [N][K] (device) and its
- * fp16 scales [N][K/128] (device, nullable) for bit-exact checks. A ternary
- * code 11 writes 0 to q and sets QMV_ERR_CORRUPT in the device error word.
+ * Decode a packed ternary (QMV_TERNARY2 or QMV_TERNARY2_LUT) or INT4 matrix
+ * to int8 q [N][K] (device) and its fp16 scales [N][K/128] (device, nullable)
+ * for bit-exact checks. A ternary code 11 writes 0 to q and sets
+ * QMV_ERR_CORRUPT in the device error word.
  */
 int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* scales, void* stream);
 
@@ -204,6 +221,16 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
  */
 int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
                     float* y, int64_t ldy, void* stream);
+/*
+ * A QMV_TERNARY2_LUT desc in qmv_run_ternary or qmv_run_batch serves M = 1
+ * only (QMV_ERR_UNSUPPORTED otherwise; ldx and ldy are then unused) and runs
+ * the byte-lookup kernel: per block of 128 columns it builds, in fp32, the
+ * sum of q_i x_i over each column group of four for all 81 valid code bytes,
+ * then adds one table entry per code byte and multiplies each block's sum by
+ * its scale, all in fp32; y is written without atomics (deterministic). A code
+ * byte holding a code 11 contributes 0. Small launches split each matrix's
+ * blocks over a cluster of up to 8 CTAs.
+ */
 int qmv_run_int4(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
                  float* y, int64_t ldy, void* stream);
 

@@ -29,6 +29,20 @@ two's complement, values -7 .. 7) share one arrangement:
                     ((n // 16) * S + b // 8) * 128 + (n % 16) * 8 + b % 8,
                     with S = ceil(K / 1024) steps per row.
 
+Ternary in the byte-lookup layout (the same codes and scales, arranged for a
+matvec that reads one code byte per table lookup): rows go in NG = ceil(N/32)
+groups of 32 (the last padded with zero codes and zero scales), KB = K/128.
+
+  section 0 codes : NG * KB * 1024 bytes. Byte c of a row's block holds the
+                    codes of columns 4c .. 4c+3 of the block, column 4c + i at
+                    bits 2i, 2i+1. A row's 32 bytes of a block are rotated by
+                    n % 32: the byte at position t is byte (t + n) % 32. The
+                    1024-byte record of (block b, row group G) starts at
+                    (b * NG + G) * 1024; position t of row n lies at
+                    (t // 16) * 512 + (n % 32) * 16 + t % 16 inside it.
+  section 1 scales: fp16 bits [KB][NG * 32]; (row n, block b) is element
+                    b * NG * 32 + n.
+
 Cassandra split (see ``oracle.cassandra`` for the contents):
   0 bitmap    : N x K/32 uint32, bit (j % 32) of word j // 32 = kept(n, j)
   1 signmant  : N x (K/2)/8 uint32, nibble i (bits 4(i%8)..) = S<<3 | M>>4 of
@@ -148,6 +162,28 @@ def rows_from_records(flat, N: int, K: int, block_words: int, cols_per_word: int
                 flat[pos:pos + n].reshape(ROW_GROUP, nbk * block_words)
             pos += n
     return rows[:N]
+
+
+LUT_ROW_GROUP = 32
+
+
+def lut_groups(N: int) -> int:
+    return (N + LUT_ROW_GROUP - 1) // LUT_ROW_GROUP
+
+
+def ternary_lut_sizes(N: int, K: int):
+    NG, KB = lut_groups(N), K // 128
+    return [NG * KB * 1024, KB * NG * LUT_ROW_GROUP * 2]
+
+
+def lut_byte_offset(n: int, b: int, t: int, N: int) -> int:
+    """Offset in section 0 of position t of (row n, block b)."""
+    NG = lut_groups(N)
+    return (b * NG + n // LUT_ROW_GROUP) * 1024 + (t // 16) * 512 + (n % LUT_ROW_GROUP) * 16 + t % 16
+
+
+def lut_scale_index(n: int, b: int, N: int) -> int:
+    return b * lut_groups(N) * LUT_ROW_GROUP + n
 
 
 def ternary_bit_pos(k):

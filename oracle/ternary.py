@@ -77,6 +77,53 @@ def unpack(buf: bytes, N: int, K: int):
     return q, s16.copy()
 
 
+def pack_lut(q: np.ndarray, s16: np.ndarray) -> bytes:
+    """Packed ternary buffer in the byte-lookup layout (``oracle.layout``), by plain loops
+    over rows, blocks and byte positions."""
+    N, K = q.shape
+    KB = K // BLOCK
+    c = codes_of(q).reshape(N, KB, 32, 4)              # [row][block][column group][column in group]
+    group_bytes = np.zeros((N, KB, 32), dtype=np.uint32)
+    for i in range(4):
+        group_bytes |= c[:, :, :, i] << np.uint32(2 * i)
+    offs, total = layout.sections(layout.ternary_lut_sizes(N, K))
+    buf = bytearray(total)
+    for n in range(N):
+        for b in range(KB):
+            for t in range(32):
+                buf[offs[0] + layout.lut_byte_offset(n, b, t, N)] = int(group_bytes[n, b, (t + n) % 32])
+    s16 = np.asarray(s16, dtype=np.uint16)
+    for n in range(N):
+        for b in range(KB):
+            pos = offs[1] + 2 * layout.lut_scale_index(n, b, N)
+            buf[pos:pos + 2] = int(s16[n, b]).to_bytes(2, "little")
+    return bytes(buf)
+
+
+def unpack_lut(buf: bytes, N: int, K: int):
+    """Inverse of ``pack_lut``: (q int8 [N][K], s16 uint16 [N][K/128]). Code 11 is rejected."""
+    KB = K // BLOCK
+    offs, total = layout.sections(layout.ternary_lut_sizes(N, K))
+    assert len(buf) >= total
+    raw = np.frombuffer(buf, dtype=np.uint8)
+    q = np.zeros((N, K), dtype=np.int8)
+    s16 = np.zeros((N, KB), dtype=np.uint16)
+    value = {0: 0, 1: 1, 2: -1}
+    for n in range(N):
+        for b in range(KB):
+            for t in range(32):
+                byte = int(raw[offs[0] + layout.lut_byte_offset(n, b, t, N)])
+                grp = (t + n) % 32
+                for i in range(4):
+                    code = (byte >> (2 * i)) & 3
+                    if code == 3:
+                        raise ValueError("invalid ternary code 11")
+                    q[n, b * BLOCK + 4 * grp + i] = value[code]
+            pos = offs[1] + 2 * layout.lut_scale_index(n, b, N)
+            s16[n, b] = int.from_bytes(bytes(raw[pos:pos + 2]), "little")
+    return q, s16
+
+
 def dequant(q: np.ndarray, s16: np.ndarray) -> np.ndarray:
     """w_hat = q * fp16 scale of its block, float64 [N][K]."""
     N, K = q.shape

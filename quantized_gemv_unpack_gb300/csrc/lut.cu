@@ -1,0 +1,523 @@
+// Batch-1 matvec over block-128 ternary weights in the lookup layout
+// (QMV_TERNARY2_LUT): y = W_hat x for one activation row, with W_hat = q * s,
+// q in {-1, 0, +1} per weight ("Ternary Bonsai 2", section 1.2) and one fp16
+// scale s per block of 128 columns.
+//
+// Decode by table lookup. A code byte holds the codes of four consecutive
+// columns (2 bits each), so it takes one of 81 valid values e. Per block of
+// 128 columns the CTA builds, from x, the table
+//     T[e][c] = sum_{i<4} q_i(e) * x[128 b + 4 c + i]     (c = 0..31 column groups)
+// in fp32 in shared memory; then every row's block costs one lookup per byte:
+// 32 lookups and fp32 adds per row and block, and one multiply by the block's
+// scale. The table is stored with a row of 64 four-byte slots per e (slot c
+// and slot c + 32 hold the same value), so the address of T[e][c] for the
+// lane that owns row n at byte position t is e*256 + 4*(n%32) + 4*t with
+// c = (t + n) % 32: one byte permute builds e*256 + 4*(n%32) from the code
+// word and the lane's offset, and 4*t is the load's immediate offset. The
+// packer rotates each row's 32 code bytes by n % 32 to match, so at every
+// position t the 32 lanes of a warp read 32 distinct banks (no conflicts).
+// Rows of invalid bytes (a code 11) are zeroed once per launch and never
+// rebuilt, so such a byte contributes 0.
+//
+// Work split. A unit is up to 2048 rows of one matvec (unit_rows) over all of
+// its blocks (a cluster of C CTAs splits the blocks, each CTA a contiguous
+// share, and CTA rank 0 adds the C partial sums in rank order through
+// distributed shared memory). The host assigns units to clusters largest
+// first, each to the least loaded cluster, and passes the lists in the launch
+// parameters. Each of the 512 threads owns up to four rows of a unit (rows
+// r0 + 512 j + tid); lane = row % 32.
+//
+// Streaming. The codes of (block, 32-row group) are 1 KB records, rows of a
+// unit contiguous per block, so a thread's row is two coalesced 16-byte loads.
+// The next step's codes and scales are loaded into a second register set
+// while the current step is looked up, and one thread asks the copy engine to
+// prefetch the step after next into L2 (cp.async.bulk.prefetch), so the
+// register loads hit L2. No wait in this kernel spins: it synchronizes only
+// with CTA and cluster barriers.
+#include <algorithm>
+#include <cstring>
+#include <queue>
+#include <vector>
+
+#include "qmv_internal.cuh"
+
+namespace qmv {
+namespace {
+
+constexpr int kThreadsL = 512;
+constexpr int kRpt = 4;                          // rows per thread and unit
+constexpr int kUnitRowsMax = kThreadsL * kRpt;   // 2048
+constexpr int kMaxUnitsL = 4096;
+constexpr int kMaxWorkersL = 256;
+constexpr int kTableBytes = 65536;
+constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of partial sums
+// the table needs a 64 KB aligned shared window address; the dynamic shared
+// memory base is not assumed, so 64 KB of slack is requested for the round-up
+constexpr size_t kSmemL = 2 * kTableBytes + kPartBytes;
+
+struct LutTask {
+  const unsigned char* codes;  // section 0; the scales follow at NG * KB * 1024 bytes
+  const uint16_t* x;           // bf16 [K]
+  float* y;                    // fp32 [N]
+  int32_t N, NG, KB, unit0;    // NG 32-row groups, KB blocks, first unit of this task
+};
+
+struct LutBatch {
+  int32_t n_tasks, n_units, unit_rows, n_workers;
+  int32_t sched_n;             // 0: unit u goes to worker u % n_workers
+  int32_t pad;
+  int* err;
+  uint16_t sched_off[kMaxWorkersL + 1];
+  uint16_t sched[kMaxUnitsL];
+  LutTask t[kMaxTasks];
+};
+static_assert(sizeof(LutBatch) <= 32000, "launch parameters must stay below the 32 KB limit");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+template <int IMM>
+__device__ __forceinline__ float lds_at(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(IMM));
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ void l1_prefetch(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+// Predicated loads: when pred is false the destination keeps its old value (no branch).
+__device__ __forceinline__ void ldg16_if(uint4& v, const uint4* p, bool pred) {
+  asm("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "l"(p), "r"((int)pred));
+}
+__device__ __forceinline__ void ldg2_if(uint32_t& v, const uint16_t* p, bool pred) {
+  asm("{\n\t.reg .pred q;\n\t.reg .b16 h;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.nc.b16 h, [%1];\n\t@q cvt.u32.u16 %0, h;\n\t}"
+      : "+r"(v)
+      : "l"(p), "r"((int)pred));
+}
+__device__ __forceinline__ float code_val(int d, float x) { return d == 1 ? x : (d == 2 ? -x : 0.f); }
+
+// One step = one block of one unit for this CTA.
+struct Step {
+  int k;        // position in this worker's unit list (past the end: no step)
+  int ti, r0;   // task, first row of the unit
+  int bk, kb1;  // current block, end of this CTA's blocks
+  int nrows;    // rows of the unit
+  bool valid;
+  __device__ __forceinline__ int nrows32() const { return (nrows + 31) & ~31; }
+};
+
+struct Item {
+  uint4 lo, hi;  // the row's 32 code bytes of the block
+  uint32_t s;    // the row's fp16 scale of the block (low 16 bits)
+};
+
+__device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
+  int lo = 0, hi = b.n_tasks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (b.t[mid].unit0 <= unit) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant__ LutBatch b) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  const uint32_t T0 = (base + 65535u) & ~65535u;
+  const uint32_t part = T0 + kTableBytes;     // [2][kRpt][512] fp32
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const uint32_t L = T0 | (uint32_t)(lane * 4);
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const int worker = (int)cluster_id();
+
+  // zero the table rows of invalid code bytes (any 2-bit field equal to 3)
+  for (int i = tid; i < 256 * 64; i += kThreadsL) {
+    const int e = i >> 6;
+    if ((e & (e >> 1)) & 0x55) sts_f32(T0 + 4u * (uint32_t)i, 0.f);
+  }
+
+  // this worker's units
+  int k_end, k_beg;
+  if (b.sched_n) {
+    k_beg = b.sched_off[worker];
+    k_end = b.sched_off[worker + 1];
+  } else {
+    k_beg = 0;
+    k_end = worker < b.n_units ? (b.n_units - 1 - worker) / b.n_workers + 1 : 0;
+  }
+  auto unit_at = [&](int k) { return b.sched_n ? (int)b.sched[k] : worker + k * b.n_workers; };
+  // first step of the unit at list position k (valid = false past the end)
+  auto unit_step = [&](int k) {
+    Step s = {};  // every field defined, also past the end of the list
+    s.k = k;
+    s.valid = k < k_end;
+    if (!s.valid) return s;
+    const int unit = unit_at(k);
+    s.ti = find_lut_task(b, unit);
+    const LutTask& T = b.t[s.ti];
+    s.r0 = (unit - T.unit0) * b.unit_rows;
+    s.nrows = min(b.unit_rows, T.N - s.r0);
+    s.bk = (int)(rank * (uint32_t)T.KB / C);
+    s.kb1 = (int)((rank + 1) * (uint32_t)T.KB / C);
+    return s;
+  };
+  auto advance = [&](Step s) {
+    if (!s.valid) return s;
+    if (++s.bk < s.kb1) return s;
+    return unit_step(s.k + 1);
+  };
+  auto prefetch_step = [&](const Step& s) {
+    if (!s.valid) return;
+    const LutTask& T = b.t[s.ti];
+    const int g0 = s.r0 >> 5;
+    const int ng = s.nrows32() >> 5;
+    l2_prefetch(T.codes + ((size_t)s.bk * T.NG + g0) * 1024, (uint32_t)ng * 1024u);
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
+    l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
+  };
+  // pull a step's codes and scales into L1 (one 128-byte line per thread)
+  auto prefetch_l1 = [&](const Step& s) {
+    if (!s.valid) return;
+    const LutTask& T = b.t[s.ti];
+    const int ng = s.nrows32() >> 5;
+    if (tid < ng * 8) l1_prefetch(T.codes + ((size_t)s.bk * T.NG + (s.r0 >> 5)) * 1024 + (size_t)tid * 128);
+    if (tid < ng) {
+      const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
+      l1_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0 + tid * 32);
+    }
+  };
+  // the rows r0 + 512 j + tid of a step: from one base address per step, item j
+  // is 16 row groups (16 KB of codes, 1 KB of scales) further on; warps past the
+  // unit's rows load nothing
+  auto load_items = [&](const Step& s, Item (&it)[kRpt]) {
+    const LutTask& T = b.t[s.ti];
+    const uint4* cw = reinterpret_cast<const uint4*>(T.codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024) +
+                         (size_t)s.bk * T.NG * 32 + s.r0 + tid;
+    const int n32 = s.nrows32() - (tid & ~31);
+#pragma unroll
+    for (int j = 0; j < kRpt; ++j) {
+      const bool on = j * kThreadsL < n32;
+      ldg16_if(it[j].lo, cw + j * 1024, on);
+      ldg16_if(it[j].hi, cw + j * 1024 + 32, on);
+      ldg2_if(it[j].s, sc + j * kThreadsL, on);
+    }
+  };
+  // builders: threads 0..287 (warps 0..8), column group g = tid % 32, high digit pair hi = tid / 32
+  const int g = tid & 31, hi = tid >> 5;
+  const bool builder = hi < 9;
+  auto load_x = [&](const Step& s) -> uint2 {
+    if (builder && s.valid) return *reinterpret_cast<const uint2*>(b.t[s.ti].x + (size_t)s.bk * 128 + 4 * g);
+    return make_uint2(0u, 0u);
+  };
+
+  float acc[kRpt];
+#pragma unroll
+  for (int j = 0; j < kRpt; ++j) acc[j] = 0.f;
+  int parity = 0;
+
+  // the table of a step's block, from its x, into the table at tb
+  auto build = [&](uint2 xw, uint32_t tb) {
+    if (!builder) return;
+    const float x0 = __uint_as_float(xw.x << 16), x1 = __uint_as_float(xw.x & 0xFFFF0000u);
+    const float x2 = __uint_as_float(xw.y << 16), x3 = __uint_as_float(xw.y & 0xFFFF0000u);
+    const int d2 = hi % 3, d3 = hi / 3;
+    const float p23 = code_val(d2, x2) + code_val(d3, x3);
+    const uint32_t row_hi = tb + (uint32_t)((16 * d2 + 64 * d3) * 256 + 4 * g);
+#pragma unroll
+    for (int lo = 0; lo < 9; ++lo) {
+      const int d0 = lo % 3, d1 = lo / 3;
+      const float v = (code_val(d0, x0) + code_val(d1, x1)) + p23;
+      const uint32_t a = row_hi + (uint32_t)((d0 + 4 * d1) * 256);
+      sts_f32(a, v);
+      sts_f32(a + 128u, v);
+    }
+  };
+  // this thread's rows of a step, looked up in table buffer tb (lane offset in Lt)
+  auto lookups = [&](const Step& s, const Item (&it)[kRpt], uint32_t Lt) {
+    const int n32 = s.nrows32() - (tid & ~31);
+#pragma unroll
+    for (int j = 0; j < kRpt; ++j) {
+      if (j * kThreadsL < n32) {
+        const uint32_t w[8] = {it[j].lo.x, it[j].lo.y, it[j].lo.z, it[j].lo.w,
+                               it[j].hi.x, it[j].hi.y, it[j].hi.z, it[j].hi.w};
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          // result bytes: lane offset, code byte t, table window high bytes
+          const uint32_t a0 = prmt(w[t >> 2], Lt, 0x7604u | ((uint32_t)(t & 3) << 4));
+          const uint32_t a1 = prmt(w[(t + 1) >> 2], Lt, 0x7604u | ((uint32_t)((t + 1) & 3) << 4));
+          float v0, v1;
+          switch (t) {
+#define QMV_LUT_CASE(T) \
+  case T:               \
+    v0 = lds_at<4 * T>(a0); \
+    v1 = lds_at<4 * (T + 1)>(a1); \
+    break;
+            QMV_LUT_CASE(0) QMV_LUT_CASE(2) QMV_LUT_CASE(4) QMV_LUT_CASE(6)
+            QMV_LUT_CASE(8) QMV_LUT_CASE(10) QMV_LUT_CASE(12) QMV_LUT_CASE(14)
+            QMV_LUT_CASE(16) QMV_LUT_CASE(18) QMV_LUT_CASE(20) QMV_LUT_CASE(22)
+            QMV_LUT_CASE(24) QMV_LUT_CASE(26) QMV_LUT_CASE(28) QMV_LUT_CASE(30)
+#undef QMV_LUT_CASE
+          }
+          s0 += v0;
+          s1 += v1;
+        }
+        acc[j] = fmaf(s0 + s1, __half2float(__ushort_as_half((unsigned short)it[j].s)), acc[j]);
+      }
+    }
+  };
+  // the unit of s is complete in this CTA: write y (C == 1) or add the
+  // cluster's partial sums in rank order (rank 0 writes)
+  auto finish = [&](const Step& s) {
+    const LutTask& T = b.t[s.ti];
+    if (C == 1) {
+#pragma unroll
+      for (int j = 0; j < kRpt; ++j) {
+        const int row = s.r0 + j * kThreadsL + tid;
+        if (j * kThreadsL + tid < s.nrows) T.y[row] = acc[j];
+      }
+    } else {
+      const uint32_t pbase = part + (uint32_t)(parity * kRpt * kThreadsL * 4);
+#pragma unroll
+      for (int j = 0; j < kRpt; ++j) sts_f32(pbase + (uint32_t)((j * kThreadsL + tid) * 4), acc[j]);
+      cluster_sync();
+      if (rank == 0) {
+#pragma unroll
+        for (int j = 0; j < kRpt; ++j) {
+          const int row = s.r0 + j * kThreadsL + tid;
+          if (j * kThreadsL + tid < s.nrows) {
+            const uint32_t a = pbase + (uint32_t)((j * kThreadsL + tid) * 4);
+            float v = acc[j];
+            for (uint32_t r = 1; r < C; ++r) v += ld_cluster_f32(a, r);
+            T.y[row] = v;
+          }
+        }
+      }
+      parity ^= 1;
+    }
+#pragma unroll
+    for (int j = 0; j < kRpt; ++j) acc[j] = 0.f;
+  };
+
+  // Per step: load this step's codes and scales (L1 hits: they were pulled into
+  // L1 during the previous step, and into L2 the step before), pull the next
+  // step into L1 and the one after into L2, load the next step's activations
+  // (builders); then, between two CTA barriers, build the table, and look up.
+  Step cur = unit_step(k_beg);
+  Step nxt = advance(cur);
+  if (cur.valid) {
+    if (tid == 0) {
+      prefetch_step(cur);
+      prefetch_step(nxt);
+    }
+    prefetch_l1(cur);
+  }
+  Item A[kRpt];
+#pragma unroll
+  for (int j = 0; j < kRpt; ++j) {
+    A[j].lo = A[j].hi = make_uint4(0u, 0u, 0u, 0u);
+    A[j].s = 0u;
+  }
+  uint2 xc = load_x(cur);
+  while (cur.valid) {
+    load_items(cur, A);
+    const Step nn = advance(nxt);
+    prefetch_l1(nxt);
+    if (tid == 0) prefetch_step(nn);
+    const uint2 xn = load_x(nxt);
+    __syncthreads();  // every lookup of the previous step is done
+    build(xc, T0);
+    __syncthreads();  // the table is complete
+    lookups(cur, A, L);
+    if (!nxt.valid || nxt.k != cur.k) finish(cur);
+    cur = nxt;
+    nxt = nn;
+    xc = xn;
+  }
+  // no CTA leaves while a peer may still read its partial sums
+  if (C > 1) cluster_sync();
+}
+
+}  // namespace
+
+int check_lut_desc(const qmv_desc* d) {
+  if (!d) return fail(QMV_ERR_ARG, "desc is NULL");
+  if (d->abi_version != QMV_ABI_VERSION)
+    return fail(QMV_ERR_ARG, "desc abi_version %u, library %d", d->abi_version, QMV_ABI_VERSION);
+  if (d->format != QMV_TERNARY2_LUT) return fail(QMV_ERR_ARG, "desc format %u is not QMV_TERNARY2_LUT", d->format);
+  if (d->N <= 0 || d->K <= 0 || d->group != QMV_GROUP || d->K % QMV_GROUP)
+    return fail(QMV_ERR_ARG, "desc N=%lld K=%lld group=%d", (long long)d->N, (long long)d->K, d->group);
+  if (d->N > (1 << 26) || d->K > (1 << 26)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
+  qmv_desc ref;
+  qmv_pack_desc(QMV_TERNARY2_LUT, d->N, d->K, d->group, &ref);
+  for (int i = 0; i < 2; ++i)
+    if (ref.off[i] != d->off[i] || ref.bytes[i] != d->bytes[i])
+      return fail(QMV_ERR_ARG, "desc section %d does not match the lookup layout of a %lld x %lld matrix", i,
+                  (long long)d->N, (long long)d->K);
+  return QMV_OK;
+}
+
+int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
+  static thread_local LutBatch b;
+  if (n < 1 || n > kMaxTasks) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n, kMaxTasks);
+  int min_kb = 1 << 30;
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    const qmv_task& t = tasks[i];
+    int rc = check_lut_desc(t.desc);
+    if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
+    if (!t.w || !t.x || !t.y) return fail(QMV_ERR_ARG, "task %d: NULL w, x or y", i);
+    if (!aligned16(t.w) || !aligned16(t.x) || !aligned16(t.y))
+      return fail(QMV_ERR_ALIGN, "task %d: w, x and y must be 16-byte aligned", i);
+    LutTask& T = b.t[i];
+    T.codes = static_cast<const unsigned char*>(t.w) + t.desc->off[0];
+    T.x = static_cast<const uint16_t*>(t.x);
+    T.y = t.y;
+    T.N = (int32_t)t.desc->N;
+    T.NG = (int32_t)((t.desc->N + 31) / 32);
+    T.KB = (int32_t)(t.desc->K / QMV_GROUP);
+    min_kb = std::min(min_kb, T.KB);
+    total += t.desc->N * t.desc->K;
+  }
+  b.n_tasks = n;
+  const int sms = sm_count();
+  auto units_for = [&](int rows) {
+    int64_t u = 0;
+    for (int i = 0; i < n; ++i) u += (b.t[i].N + rows - 1) / rows;
+    return u;
+  };
+  // Rows per unit and CTAs per cluster: whole 2048-row units on single CTAs
+  // when there are enough of them; otherwise smaller units whose blocks a
+  // cluster of up to 8 CTAs shares, until the launch covers the SMs.
+  int rows = kUnitRowsMax, C = 1;
+  if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
+    bool done = false;
+    for (int r : {kUnitRowsMax, 1024, 512, 256}) {
+      for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
+        rows = r;
+        C = c;
+        if (units_for(r) * c >= sms) {
+          done = true;
+          break;
+        }
+      }
+      if (done) break;
+    }
+  }
+  int64_t n_units = 0;
+  for (int i = 0; i < n; ++i) {
+    b.t[i].unit0 = (int32_t)n_units;
+    n_units += (b.t[i].N + rows - 1) / rows;
+  }
+  if (n_units > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
+  b.n_units = (int32_t)n_units;
+  b.unit_rows = rows;
+  b.err = device_error_word();
+  if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+
+  const void* kern = (const void*)lut_kernel;
+  int per_sm = 0;
+  int rc = kernel_fit(kern, kThreadsL, kSmemL, &per_sm);
+  if (rc) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreadsL);
+  cfg.dynamicSmemBytes = kSmemL;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = C > 1 ? 1 : 0;
+  int workers = sms * per_sm;
+  if (C > 1) {
+    cfg.gridDim = dim3((unsigned)(C * 8));
+    int nc = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&nc, lut_kernel, &cfg);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+    if (nc < 1) return fail(QMV_ERR_UNSUPPORTED, "no cluster of %d CTAs fits the device", C);
+    workers = nc;
+  }
+  workers = (int)std::min<int64_t>(std::min(workers, kMaxWorkersL), n_units);
+  b.n_workers = workers;
+
+  // largest units first, each to the least loaded worker
+  if (n_units <= kMaxUnitsL) {
+    std::vector<std::pair<int64_t, int>> cost((size_t)n_units);
+    for (int i = 0; i < n; ++i) {
+      const LutTask& T = b.t[i];
+      const int nu = (T.N + rows - 1) / rows;
+      for (int u = 0; u < nu; ++u) {
+        const int64_t r = std::min(rows, T.N - u * rows);
+        cost[(size_t)(T.unit0 + u)] = {r * T.KB, T.unit0 + u};
+      }
+    }
+    std::stable_sort(cost.begin(), cost.end(), [](const auto& a, const auto& c) { return a.first > c.first; });
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int w = 0; w < workers; ++w) heap.push({0, w});
+    std::vector<std::vector<int>> lists((size_t)workers);
+    for (const auto& c : cost) {
+      Load l = heap.top();
+      heap.pop();
+      lists[(size_t)l.second].push_back(c.second);
+      l.first += c.first;
+      heap.push(l);
+    }
+    int pos = 0;
+    for (int w = 0; w < workers; ++w) {
+      b.sched_off[w] = (uint16_t)pos;
+      for (int u : lists[(size_t)w]) b.sched[pos++] = (uint16_t)u;
+    }
+    b.sched_off[workers] = (uint16_t)pos;
+    b.sched_n = pos;
+  } else {
+    b.sched_n = 0;
+  }
+  cfg.gridDim = dim3((unsigned)(workers * C));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lut_kernel, b);
+  if (e != cudaSuccess) return cuda_fail(e, "lookup matvec launch");
+  return QMV_OK;
+}
+
+}  // namespace qmv

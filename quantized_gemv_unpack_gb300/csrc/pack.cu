@@ -40,6 +40,14 @@ __device__ __forceinline__ int64_t record_word(int64_t n, int64_t b, int64_t K, 
   return ((g * 16 * KB + st * 16 * 8) + r * nbk + j) * block_words;
 }
 
+// Byte offset of byte t of (row n, block b) in the lookup layout's codes
+// section (QMV_TERNARY2_LUT): 1 KB records of (block, 32-row group), each
+// row's 32 bytes rotated by n % 32 (byte t holds column group (t + n) % 32).
+__host__ __device__ __forceinline__ int64_t lut_byte(int64_t n, int64_t b, int t, int64_t NG) {
+  return (b * NG + n / 32) * 1024 + (t / 16) * 512 + (n % 32) * 16 + t % 16;
+}
+
+template <bool LUT>
 __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
                                     uint16_t* __restrict__ scales) {
   const int64_t nb = K / 128;
@@ -72,10 +80,40 @@ __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int6
       words[k >> 4] |= code << pos;
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 8));
-  dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-  dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-  scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
+  if constexpr (LUT) {
+    // group c (columns 4c..4c+3) as one byte, column 4c + i at bits 2i
+    uint32_t gb[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = 4 * c + i, rr = k & 15;
+        const int pos = (rr & 1) ? 15 + rr : rr;
+        v |= ((words[k >> 4] >> pos) & 3u) << (2 * i);
+      }
+      gb[c] = v;
+    }
+    const int64_t NG = (N + 31) / 32;
+    const int rot = (int)(n % 32);
+    uint32_t out[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) v |= gb[(4 * u + kk + rot) & 31] << (8 * kk);
+      out[u] = v;
+    }
+    unsigned char* cb = reinterpret_cast<unsigned char*>(codes);
+    *reinterpret_cast<uint4*>(cb + lut_byte(n, b, 0, NG)) = make_uint4(out[0], out[1], out[2], out[3]);
+    *reinterpret_cast<uint4*>(cb + lut_byte(n, b, 16, NG)) = make_uint4(out[4], out[5], out[6], out[7]);
+    scales[b * NG * 32 + n] = f64_to_f16_rne(s);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 8));
+    dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+    dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+    scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
+  }
 }
 
 __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
@@ -125,10 +163,26 @@ __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, co
   const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= N * KB) return;
   const int64_t n = blk / KB, b = blk % KB;
-  const int bw = format == QMV_TERNARY2 ? 8 : 16;
-  const uint32_t* src = codes + record_word(n, b, K, bw);
   int8_t* out = q + n * K + b * 128;
   bool bad = false;
+  if (format == QMV_TERNARY2_LUT) {
+    const int64_t NG = (N + 31) / 32;
+    const unsigned char* cb = reinterpret_cast<const unsigned char*>(codes);
+    for (int t = 0; t < 32; ++t) {
+      const uint32_t v = cb[lut_byte(n, b, t, NG)];
+      const int c = (int)((t + n) % 32);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t code = (v >> (2 * i)) & 3u;
+        bad |= code == 3u;
+        out[4 * c + i] = code == 1u ? 1 : (code == 2u ? -1 : 0);
+      }
+    }
+    if (bad) atomicCAS(err, 0, QMV_ERR_CORRUPT);
+    if (scales_out) scales_out[n * KB + b] = scales[b * NG * 32 + n];
+    return;
+  }
+  const int bw = format == QMV_TERNARY2 ? 8 : 16;
+  const uint32_t* src = codes + record_word(n, b, K, bw);
   for (int wi = 0; wi < bw; ++wi) {
     const uint32_t w = src[wi];
     if (format == QMV_TERNARY2) {
@@ -151,7 +205,8 @@ __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, co
 }
 
 int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, void* stream) {
-  int rc = check_desc(desc, format);
+  const bool lut = format == QMV_TERNARY2 && desc && desc->format == QMV_TERNARY2_LUT;
+  int rc = lut ? check_lut_desc(desc) : check_desc(desc, format);
   if (rc) return rc;
   if (!w || !packed) return fail(QMV_ERR_ARG, "NULL w or packed");
   if (!aligned16(w) || !aligned16(packed)) return fail(QMV_ERR_ALIGN, "w and packed must be 16-byte aligned");
@@ -166,11 +221,11 @@ int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, 
   // zero the padding rows of the last row group, the padding scales (rows past
   // N, blocks past K/128) and the alignment padding after each section, so
   // every byte is determined
-  if (desc->N % 16) {
+  if (desc->N % (lut ? 32 : 16)) {
     cudaError_t e = cudaMemsetAsync(base + desc->off[0], 0, (size_t)desc->bytes[0], s);
     if (e != cudaSuccess) return cuda_fail(e, "zero padding rows");
   }
-  if (desc->N % 16 || (desc->K / 128) % 8) {
+  if (desc->N % (lut ? 32 : 16) || (!lut && (desc->K / 128) % 8)) {
     cudaError_t e = cudaMemsetAsync(base + desc->off[1], 0, (size_t)desc->bytes[1], s);
     if (e != cudaSuccess) return cuda_fail(e, "zero padding scales");
   }
@@ -182,8 +237,10 @@ int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, 
       if (e != cudaSuccess) return cuda_fail(e, "zero section padding");
     }
   }
-  if (format == QMV_TERNARY2)
-    pack_ternary_kernel<<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+  if (lut)
+    pack_ternary_kernel<true><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+  else if (format == QMV_TERNARY2)
+    pack_ternary_kernel<false><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
   else
     pack_int4_kernel<<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
   cudaError_t e = cudaGetLastError();
@@ -209,8 +266,9 @@ int qmv_pack_int4(const qmv_desc* desc, const float* w, void* packed, void* stre
 int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* scales, void* stream) {
   if (!desc) return fail(QMV_ERR_ARG, "desc is NULL");
   const int format = (int)desc->format;
-  if (format != QMV_TERNARY2 && format != QMV_INT4) return fail(QMV_ERR_UNSUPPORTED, "qmv_unpack serves ternary and INT4");
-  int rc = check_desc(desc, format);
+  if (format != QMV_TERNARY2 && format != QMV_INT4 && format != QMV_TERNARY2_LUT)
+    return fail(QMV_ERR_UNSUPPORTED, "qmv_unpack serves ternary (either layout) and INT4");
+  int rc = format == QMV_TERNARY2_LUT ? check_lut_desc(desc) : check_desc(desc, format);
   if (rc) return rc;
   if (!packed || !q) return fail(QMV_ERR_ARG, "NULL packed or q");
   if (!aligned16(packed) || !aligned16(q) || (scales && !aligned16(scales)))

@@ -61,8 +61,35 @@ def test_desc_matches_oracle_layout(L):
             assert d.abi_version == q.QMV_ABI_VERSION and d.group == 128
 
 
+def test_lut_desc_matches_oracle_layout(L):
+    for N, K in [(1, 128), (31, 384), (33, 256), (4096, 4096), (1024, 5120), (5120, 25600)]:
+        d = q.qmv_pack_desc(q.QMV_TERNARY2_LUT, N, K)
+        offs, total = layout.sections(layout.ternary_lut_sizes(N, K))
+        assert [d.off[i] for i in range(2)] == offs
+        assert [d.bytes[i] for i in range(2)] == layout.ternary_lut_sizes(N, K)
+        assert d.total_bytes == total and d.format == q.QMV_TERNARY2_LUT
+
+
+def test_lut_run_rejects_bad_arguments_on_the_host(L):
+    d = q.qmv_pack_desc(q.QMV_TERNARY2_LUT, 64, 256)
+    rec = q.qmv_pack_desc(q.QMV_TERNARY2, 64, 256)
+    # the lookup layout serves one activation row
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, 256, 2, 256, 256, 64, None) == q.QMV_ERR_UNSUPPORTED
+    assert "M = 1" in q.qmv_last_error()
+    assert L.qmv_run_ternary(ctypes.byref(d), 264, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ALIGN
+    assert L.qmv_run_ternary(ctypes.byref(d), 256, None, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    bad = q.qmv_desc.from_buffer_copy(d)
+    bad.bytes[1] -= 2
+    assert L.qmv_run_ternary(ctypes.byref(bad), 256, 256, 1, 256, 256, 64, None) == q.QMV_ERR_ARG
+    # a record-layout desc in a lookup batch is rejected
+    tasks = (q.qmv_task * 2)(q.qmv_task(ctypes.pointer(d), 256, 256, 256, 256, 64),
+                             q.qmv_task(ctypes.pointer(rec), 256, 256, 256, 256, 64))
+    assert L.qmv_run_batch(q.QMV_TERNARY2_LUT, tasks, 2, 1, None) == q.QMV_ERR_ARG
+    assert "task 1" in q.qmv_last_error()
+
+
 @pytest.mark.parametrize("args", [(q.QMV_TERNARY2, 0, 128), (q.QMV_TERNARY2, 4, 100), (q.QMV_INT4, 4, -128),
-                                  (9, 4, 128)])
+                                  (9, 4, 128), (q.QMV_TERNARY2_LUT, 4, 192), (q.QMV_TERNARY2_LUT, 4, 128, 64)])
 def test_pack_desc_rejects_bad_shapes(L, args):
     with pytest.raises(q.QmvError) as e:
         q.qmv_pack_desc(*args)
