@@ -590,13 +590,14 @@ class Moe(Workload):
 
 def make_workload(name, q, torch, dev, a):
     if name == "stack":
-        return Stack(q, torch, dev, a.layers, path=a.path, layout=a.layout)
+        return Stack(q, torch, dev, a.layers, path=a.path, layout=a.layout or "lut")
     if name == "stack-sparse":
         return SparseStack(q, torch, dev, a.layers)
     if name == "kv-encode":
         return KvEncode(q, torch, dev)
     if name == "ternary-4096":
-        return Ternary4096(q, torch, dev, a.M or 1, path=a.path, layout=a.layout if (a.M or 1) == 1 else "record")
+        return Ternary4096(q, torch, dev, a.M or 1, path=a.path,
+                           layout=(a.layout or "record") if (a.M or 1) == 1 else "record")
     if name == "int4-layer":
         return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
@@ -620,8 +621,9 @@ def main():
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
-    ap.add_argument("--layout", default="lut", choices=["lut", "record"],
-                    help="ternary at M = 1 (stack, ternary-4096): byte-lookup layout or row-group records")
+    ap.add_argument("--layout", default=None, choices=["lut", "record"],
+                    help="ternary at M = 1: byte-lookup layout or row-group records (default: lookup for the "
+                         "stack, records for the single 4096 x 4096 matrix, where the record kernel is ahead)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
@@ -644,7 +646,7 @@ def main():
         line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": base["seconds_per_pass"] * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-                "config": Stack.stack_config(LAYERS, a.layout), "impl": "reference",
+                "config": Stack.stack_config(LAYERS, a.layout or "lut"), "impl": "reference",
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
                                  "unit": UNIT},
                 "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

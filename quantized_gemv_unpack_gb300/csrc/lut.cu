@@ -53,7 +53,8 @@ constexpr int kTableBytes = 65536;
 constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of partial sums
 // the table needs a 64 KB aligned shared window address; the dynamic shared
 // memory base is not assumed, so 64 KB of slack is requested for the round-up
-constexpr size_t kSmemL = 2 * kTableBytes + kPartBytes;
+constexpr size_t kSmemNeed = kTableBytes + kPartBytes;
+constexpr size_t kSmemL = kTableBytes + kSmemNeed;
 
 struct LutTask {
   const unsigned char* codes;  // section 0; the scales follow at NG * KB * 1024 bytes
@@ -65,7 +66,7 @@ struct LutTask {
 struct LutBatch {
   int32_t n_tasks, n_units, unit_rows, n_workers;
   int32_t sched_n;             // 0: unit u goes to worker u % n_workers
-  int32_t pad;
+  uint32_t smem_bytes;         // dynamic shared memory of the launch
   int* err;
   uint16_t sched_off[kMaxWorkersL + 1];
   uint16_t sched[kMaxUnitsL];
@@ -87,9 +88,6 @@ __device__ __forceinline__ float lds_at(uint32_t a) {
 }
 __device__ __forceinline__ void sts_f32(uint32_t a, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-__device__ __forceinline__ void l1_prefetch(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -160,6 +158,10 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   const uint32_t T0 = (base + 65535u) & ~65535u;
+  if (T0 + kSmemNeed > base + b.smem_bytes) {  // the launch did not reserve the round-up
+    if (threadIdx.x == 0) atomicCAS(b.err, 0, (int)QMV_ERR_UNSUPPORTED);
+    return;
+  }
   const uint32_t part = T0 + kTableBytes;     // [2][kRpt][512] fp32
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -213,33 +215,17 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
     l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
   };
-  // pull a step's codes and scales into L1 (one 128-byte line per thread)
-  auto prefetch_l1 = [&](const Step& s) {
-    if (!s.valid) return;
-    const LutTask& T = b.t[s.ti];
-    const int ng = s.nrows32() >> 5;
-    if (tid < ng * 8) l1_prefetch(T.codes + ((size_t)s.bk * T.NG + (s.r0 >> 5)) * 1024 + (size_t)tid * 128);
-    if (tid < ng) {
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
-      l1_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0 + tid * 32);
-    }
-  };
-  // the rows r0 + 512 j + tid of a step: from one base address per step, item j
-  // is 16 row groups (16 KB of codes, 1 KB of scales) further on; warps past the
-  // unit's rows load nothing
-  auto load_items = [&](const Step& s, Item (&it)[kRpt]) {
+  // item j of a step: the row r0 + 512 j + tid (16 row groups, i.e. 16 KB of
+  // codes and 1 KB of scales, per j); warps past the unit's rows load nothing
+  auto load_item = [&](const Step& s, int j, Item& it) {
     const LutTask& T = b.t[s.ti];
     const uint4* cw = reinterpret_cast<const uint4*>(T.codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024) +
                          (size_t)s.bk * T.NG * 32 + s.r0 + tid;
-    const int n32 = s.nrows32() - (tid & ~31);
-#pragma unroll
-    for (int j = 0; j < kRpt; ++j) {
-      const bool on = j * kThreadsL < n32;
-      ldg16_if(it[j].lo, cw + j * 1024, on);
-      ldg16_if(it[j].hi, cw + j * 1024 + 32, on);
-      ldg2_if(it[j].s, sc + j * kThreadsL, on);
-    }
+    const bool on = s.valid && j * kThreadsL < s.nrows32() - (tid & ~31);
+    ldg16_if(it.lo, cw + j * 1024, on);
+    ldg16_if(it.hi, cw + j * 1024 + 32, on);
+    ldg2_if(it.s, sc + j * kThreadsL, on);
   };
   // builders: threads 0..287 (warps 0..8), column group g = tid % 32, high digit pair hi = tid / 32
   const int g = tid & 31, hi = tid >> 5;
@@ -271,37 +257,49 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
       sts_f32(a + 128u, v);
     }
   };
-  // this thread's rows of a step, looked up in table buffer tb (lane offset in Lt)
-  auto lookups = [&](const Step& s, const Item (&it)[kRpt], uint32_t Lt) {
-    const int n32 = s.nrows32() - (tid & ~31);
+  // one row's block: 32 lookups and adds, times the block's scale, into acc
+  auto row_block = [&](const Item& it, float& a) {
+    const uint32_t w[8] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w, it.hi.x, it.hi.y, it.hi.z, it.hi.w};
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < kRpt; ++j) {
-      if (j * kThreadsL < n32) {
-        const uint32_t w[8] = {it[j].lo.x, it[j].lo.y, it[j].lo.z, it[j].lo.w,
-                               it[j].hi.x, it[j].hi.y, it[j].hi.z, it[j].hi.w};
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          // result bytes: lane offset, code byte t, table window high bytes
-          const uint32_t a0 = prmt(w[t >> 2], Lt, 0x7604u | ((uint32_t)(t & 3) << 4));
-          const uint32_t a1 = prmt(w[(t + 1) >> 2], Lt, 0x7604u | ((uint32_t)((t + 1) & 3) << 4));
-          float v0, v1;
-          switch (t) {
+    for (int t = 0; t < 32; t += 2) {
+      // result bytes: lane offset, code byte t, table window high bytes
+      const uint32_t a0 = prmt(w[t >> 2], L, 0x7604u | ((uint32_t)(t & 3) << 4));
+      const uint32_t a1 = prmt(w[(t + 1) >> 2], L, 0x7604u | ((uint32_t)((t + 1) & 3) << 4));
+      float v0, v1;
+      switch (t) {
 #define QMV_LUT_CASE(T) \
   case T:               \
     v0 = lds_at<4 * T>(a0); \
     v1 = lds_at<4 * (T + 1)>(a1); \
     break;
-            QMV_LUT_CASE(0) QMV_LUT_CASE(2) QMV_LUT_CASE(4) QMV_LUT_CASE(6)
-            QMV_LUT_CASE(8) QMV_LUT_CASE(10) QMV_LUT_CASE(12) QMV_LUT_CASE(14)
-            QMV_LUT_CASE(16) QMV_LUT_CASE(18) QMV_LUT_CASE(20) QMV_LUT_CASE(22)
-            QMV_LUT_CASE(24) QMV_LUT_CASE(26) QMV_LUT_CASE(28) QMV_LUT_CASE(30)
+        QMV_LUT_CASE(0) QMV_LUT_CASE(2) QMV_LUT_CASE(4) QMV_LUT_CASE(6)
+        QMV_LUT_CASE(8) QMV_LUT_CASE(10) QMV_LUT_CASE(12) QMV_LUT_CASE(14)
+        QMV_LUT_CASE(16) QMV_LUT_CASE(18) QMV_LUT_CASE(20) QMV_LUT_CASE(22)
+        QMV_LUT_CASE(24) QMV_LUT_CASE(26) QMV_LUT_CASE(28) QMV_LUT_CASE(30)
 #undef QMV_LUT_CASE
-          }
-          s0 += v0;
-          s1 += v1;
-        }
-        acc[j] = fmaf(s0 + s1, __half2float(__ushort_as_half((unsigned short)it[j].s)), acc[j]);
+      }
+      s0 += v0;
+      s1 += v1;
+    }
+    a = fmaf(s0 + s1, __half2float(__ushort_as_half((unsigned short)it.s)), a);
+  };
+  // this thread's rows of a step (all four in a full unit, else the rows of this
+  // warp's 32-row groups that the unit has); right after a row's block, its
+  // register slot is reloaded with the same slot of the next step
+  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Step& n) {
+    if (s.nrows32() == kUnitRowsMax) {
+#pragma unroll
+      for (int j = 0; j < kRpt; ++j) {
+        row_block(it[j], acc[j]);
+        load_item(n, j, it[j]);
+      }
+    } else {
+      const int n32 = s.nrows32() - (tid & ~31);
+#pragma unroll
+      for (int j = 0; j < kRpt; ++j) {
+        if (j * kThreadsL < n32) row_block(it[j], acc[j]);
+        load_item(n, j, it[j]);
       }
     }
   };
@@ -338,36 +336,31 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
     for (int j = 0; j < kRpt; ++j) acc[j] = 0.f;
   };
 
-  // Per step: load this step's codes and scales (L1 hits: they were pulled into
-  // L1 during the previous step, and into L2 the step before), pull the next
-  // step into L1 and the one after into L2, load the next step's activations
-  // (builders); then, between two CTA barriers, build the table, and look up.
+  // Per step: prefetch the step after next to L2 and load the next step's
+  // activations (builders); between two CTA barriers build the table; then look
+  // up this step's rows, each slot reloaded with the next step's row at once.
   Step cur = unit_step(k_beg);
   Step nxt = advance(cur);
-  if (cur.valid) {
-    if (tid == 0) {
-      prefetch_step(cur);
-      prefetch_step(nxt);
-    }
-    prefetch_l1(cur);
+  if (tid == 0 && cur.valid) {
+    prefetch_step(cur);
+    prefetch_step(nxt);
   }
   Item A[kRpt];
 #pragma unroll
   for (int j = 0; j < kRpt; ++j) {
     A[j].lo = A[j].hi = make_uint4(0u, 0u, 0u, 0u);
     A[j].s = 0u;
+    load_item(cur, j, A[j]);
   }
   uint2 xc = load_x(cur);
   while (cur.valid) {
-    load_items(cur, A);
     const Step nn = advance(nxt);
-    prefetch_l1(nxt);
     if (tid == 0) prefetch_step(nn);
     const uint2 xn = load_x(nxt);
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
     __syncthreads();  // the table is complete
-    lookups(cur, A, L);
+    lookups(cur, A, nxt);
     if (!nxt.valid || nxt.k != cur.k) finish(cur);
     cur = nxt;
     nxt = nn;
@@ -454,9 +447,11 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
 
+  const size_t smem = kSmemL;
+  b.smem_bytes = (uint32_t)smem;
   const void* kern = (const void*)lut_kernel;
   int per_sm = 0;
-  int rc = kernel_fit(kern, kThreadsL, kSmemL, &per_sm);
+  int rc = kernel_fit(kern, kThreadsL, smem, &per_sm);
   if (rc) return rc;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -465,7 +460,7 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreadsL);
-  cfg.dynamicSmemBytes = kSmemL;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
