@@ -6,7 +6,7 @@
 #include <mutex>
 #include <vector>
 
-#include "qmv_internal.cuh"
+#include "lut.cuh"
 
 namespace qmv {
 

@@ -39,7 +39,7 @@
 #include <queue>
 #include <vector>
 
-#include "qmv_internal.cuh"
+#include "lut.cuh"
 
 namespace qmv {
 namespace {
@@ -128,6 +128,18 @@ __device__ __forceinline__ void ldg2_if(uint32_t& v, const uint16_t* p, bool pre
       : "+r"(v)
       : "l"(p), "r"((int)pred));
 }
+// two fp32 adds in one instruction: (a.lo + lo, a.hi + hi)
+__device__ __forceinline__ uint64_t add2_f32(uint64_t a, float lo, float hi) {
+  uint64_t v, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(v));
+  return d;
+}
+__device__ __forceinline__ float sum2_f32(uint64_t a) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(a));
+  return __uint_as_float(lo) + __uint_as_float(hi);
+}
 __device__ __forceinline__ float code_val(int d, float x) { return d == 1 ? x : (d == 2 ? -x : 0.f); }
 
 // One step = one block of one unit for this CTA.
@@ -215,17 +227,32 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
     l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
   };
-  // item j of a step: the row r0 + 512 j + tid (16 row groups, i.e. 16 KB of
-  // codes and 1 KB of scales, per j); warps past the unit's rows load nothing
-  auto load_item = [&](const Step& s, int j, Item& it) {
+  // This thread's load addresses of a step: row r0 + tid of its codes and of
+  // its scales; item j (row r0 + 512 j + tid) is 16 row groups further on (16 KB
+  // of codes, 1 KB of scales). n32 > 512 j while item j has rows of this warp.
+  struct Src {
+    const uint4* cw;
+    const uint16_t* sc;
+    int n32;
+  };
+  auto src_of = [&](const Step& s) {
+    Src r;
+    r.cw = nullptr;
+    r.sc = nullptr;
+    r.n32 = 0;
+    if (!s.valid) return r;
     const LutTask& T = b.t[s.ti];
-    const uint4* cw = reinterpret_cast<const uint4*>(T.codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
-    const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024) +
-                         (size_t)s.bk * T.NG * 32 + s.r0 + tid;
-    const bool on = s.valid && j * kThreadsL < s.nrows32() - (tid & ~31);
-    ldg16_if(it.lo, cw + j * 1024, on);
-    ldg16_if(it.hi, cw + j * 1024 + 32, on);
-    ldg2_if(it.s, sc + j * kThreadsL, on);
+    r.cw = reinterpret_cast<const uint4*>(T.codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
+    r.sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024) + (size_t)s.bk * T.NG * 32 + s.r0 +
+           tid;
+    r.n32 = s.nrows32() - (tid & ~31);
+    return r;
+  };
+  auto load_item = [&](const Src& r, int j, Item& it) {
+    const bool on = j * kThreadsL < r.n32;
+    ldg16_if(it.lo, r.cw + j * 1024, on);
+    ldg16_if(it.hi, r.cw + j * 1024 + 32, on);
+    ldg2_if(it.s, r.sc + j * kThreadsL, on);
   };
   // builders: threads 0..287 (warps 0..8), column group g = tid % 32, high digit pair hi = tid / 32
   const int g = tid & 31, hi = tid >> 5;
@@ -260,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
   // one row's block: 32 lookups and adds, times the block's scale, into acc
   auto row_block = [&](const Item& it, float& a) {
     const uint32_t w[8] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w, it.hi.x, it.hi.y, it.hi.z, it.hi.w};
-    float s0 = 0.f, s1 = 0.f;
+    uint64_t s2 = 0;  // two partial sums (even and odd positions)
 #pragma unroll
     for (int t = 0; t < 32; t += 2) {
       // result bytes: lane offset, code byte t, table window high bytes
@@ -279,15 +306,14 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
         QMV_LUT_CASE(24) QMV_LUT_CASE(26) QMV_LUT_CASE(28) QMV_LUT_CASE(30)
 #undef QMV_LUT_CASE
       }
-      s0 += v0;
-      s1 += v1;
+      s2 = add2_f32(s2, v0, v1);
     }
-    a = fmaf(s0 + s1, __half2float(__ushort_as_half((unsigned short)it.s)), a);
+    a = fmaf(sum2_f32(s2), __half2float(__ushort_as_half((unsigned short)it.s)), a);
   };
   // this thread's rows of a step (all four in a full unit, else the rows of this
   // warp's 32-row groups that the unit has); right after a row's block, its
   // register slot is reloaded with the same slot of the next step
-  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Step& n) {
+  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Src& n) {
     if (s.nrows32() == kUnitRowsMax) {
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) {
@@ -350,7 +376,11 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
   for (int j = 0; j < kRpt; ++j) {
     A[j].lo = A[j].hi = make_uint4(0u, 0u, 0u, 0u);
     A[j].s = 0u;
-    load_item(cur, j, A[j]);
+  }
+  {
+    const Src first = src_of(cur);
+#pragma unroll
+    for (int j = 0; j < kRpt; ++j) load_item(first, j, A[j]);
   }
   uint2 xc = load_x(cur);
   while (cur.valid) {
@@ -360,7 +390,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
     __syncthreads();  // the table is complete
-    lookups(cur, A, nxt);
+    lookups(cur, A, src_of(nxt));
     if (!nxt.valid || nxt.k != cur.k) finish(cur);
     cur = nxt;
     nxt = nn;

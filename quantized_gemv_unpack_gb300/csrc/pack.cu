@@ -6,7 +6,7 @@
 // the fp16 scales are fully determined by the input (no reduction-order
 // freedom). The float64 -> fp16 rounding is done on the bit patterns,
 // nearest-even in one step, from the IEEE-754 binary16 definition.
-#include "qmv_internal.cuh"
+#include "lut.cuh"
 
 namespace qmv {
 namespace {

@@ -86,11 +86,6 @@ int check_sparse_desc(const qmv_desc* d);
 int run_sparse(const qmv_desc* const* descs, const void* const* ws, const void* const* xs, const int64_t* ldx,
                float* const* ys, const int64_t* ldy, int n, int M, cudaStream_t s);
 
-// Byte-lookup ternary matvec (lut.cu): descriptor check, and n matvecs at M = 1
-// in one launch (the tasks' descriptors are checked there).
-int check_lut_desc(const qmv_desc* d);
-int run_lut(const qmv_task* tasks, int n, cudaStream_t s);
-
 // From this many activation rows on, the entry points use the tensor-core
 // kernel (unless qmv_desc.flags forces one of the two): the fp16-FMA kernel's
 // cost grows with M; measured on the INT4 layer set and the ternary stack it is
