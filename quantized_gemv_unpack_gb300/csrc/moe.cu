@@ -347,6 +347,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   __shared__ int s_tok[kMaxTokens];
   __shared__ float s_prob[kMaxTokens];
   __shared__ MoeRoute R;
+  // the down launch may start on SMs this grid frees; it waits for this grid's
+  // results (g, u and the zeroed y) before it reads them
+  if (PHASE == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   route(a, R);
   if (PHASE == 0) {
     // y is accumulated by the down phase's atomics
@@ -400,6 +403,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   }
   __syncwarp();
   for (int i = 0; i < kMoeSlots; ++i) prod.issue();
+  // down: routing done and the first weight copies in flight; the gate|up grid's
+  // g, u and zeroed y are complete and visible after this
+  if (PHASE == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const DecodeK dk = load_decode_k(a.magic);
   float* gu = reinterpret_cast<float*>(a.ws + a.off_gu);
@@ -559,8 +565,19 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   moe_expert_kernel<0><<<std::min(sm_count(), units_gu), kMoeThreads, smem_gu, s>>>(a);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return cuda_fail(ce, "moe gate|up launch");
-  moe_expert_kernel<1><<<std::min(sm_count(), units_dn), kMoeThreads, smem_dn, s>>>(a);
-  ce = cudaGetLastError();
+  // programmatic dependent launch: the down grid's routing and first weight
+  // copies overlap the end of the gate|up grid
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)std::min(sm_count(), units_dn));
+  cfg.blockDim = dim3(kMoeThreads);
+  cfg.dynamicSmemBytes = smem_dn;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ce = cudaLaunchKernelEx(&cfg, moe_expert_kernel<1>, a);
   if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
   return QMV_OK;
 }

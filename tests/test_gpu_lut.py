@@ -191,3 +191,36 @@ def test_lut_stack_layer_sampled(env):
         xb = xs[K].view(torch.int16).cpu().numpy().view(np.uint16)
         yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
         _check(y[:, idx].cpu().numpy(), yr, B, name)
+
+
+def test_lut_more_units_than_the_schedule_holds(env):
+    """448 matvecs of 20480 x 128 give 4480 units of 2048 rows, more than the launch
+    parameters list, so units go round-robin to the CTAs; sampled rows of every 32nd task
+    against the oracle, and every output written."""
+    q, torch, dev = env
+    from oracle import ternary
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    gen = synth.torch_generator(12, dev)
+    N, K, T = 20480, 128, q.QMV_MAX_BATCH
+    tasks, keep = [], {}
+    for i in range(T):
+        w = synth.student_t4_torch(gen, (N, K), device=dev)
+        d, p = _pack(q, torch, dev, w)
+        x = synth.activations_bf16_torch(gen, (1, K), device=dev)
+        y = torch.full((1, N), float("nan"), device=dev)
+        tasks.append((d, p, x, y))
+        if i % 32 == 0 or i == T - 1:
+            keep[i] = w
+        del w
+    q.qmv_run_batch(q.QMV_TERNARY2_LUT, tasks, 1)
+    assert q.qmv_check_status() == 0
+    assert all(bool(torch.isfinite(t[3]).all()) for t in tasks)
+    rng = np.random.default_rng(6)
+    for i, w in keep.items():
+        rows = np.unique(np.concatenate(([0, N - 1], rng.choice(N, 32, replace=False))))
+        idx = torch.from_numpy(rows).to(dev)
+        qq, _, s16 = ternary.quantize(w[idx].cpu().numpy())
+        xb = tasks[i][2].view(torch.int16).cpu().numpy().view(np.uint16)
+        yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
+        _check(tasks[i][3][:, idx].cpu().numpy(), yr, B, f"task {i}")
