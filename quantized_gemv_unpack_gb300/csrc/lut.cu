@@ -44,17 +44,17 @@
 namespace qmv {
 namespace {
 
-constexpr int kThreadsL = 512;
+constexpr int kThreadsL = 256;                   // two CTAs per SM
 constexpr int kRpt = 4;                          // rows per thread and unit
-constexpr int kUnitRowsMax = kThreadsL * kRpt;   // 2048
+constexpr int kUnitRowsMax = kThreadsL * kRpt;   // 1024
 constexpr int kMaxUnitsL = 4096;
-constexpr int kMaxWorkersL = 256;
+constexpr int kMaxWorkersL = 512;
 constexpr int kTableBytes = 65536;
 constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of partial sums
-// the table needs a 64 KB aligned shared window address; the dynamic shared
-// memory base is not assumed, so 64 KB of slack is requested for the round-up
+// the table and the partial sums: 72 KB, so two CTAs share an SM and one's
+// table build overlaps the other's lookups
 constexpr size_t kSmemNeed = kTableBytes + kPartBytes;
-constexpr size_t kSmemL = kTableBytes + kSmemNeed;
+constexpr size_t kSmemL = kSmemNeed;
 
 struct LutTask {
   const unsigned char* codes;  // section 0; the scales follow at NG * KB * 1024 bytes
@@ -166,10 +166,10 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant__ LutBatch b) {
+__global__ void __launch_bounds__(kThreadsL, 2) lut_kernel(const __grid_constant__ LutBatch b) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
-  const uint32_t T0 = (base + 65535u) & ~65535u;
+  const uint32_t T0 = base;  // the table: 256 rows (code byte e) of 64 four-byte slots
   if (T0 + kSmemNeed > base + b.smem_bytes) {  // the launch did not reserve the round-up
     if (threadIdx.x == 0) atomicCAS(b.err, 0, (int)QMV_ERR_UNSUPPORTED);
     return;
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
   const uint32_t part = T0 + kTableBytes;     // [2][kRpt][512] fp32
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const uint32_t L = T0 | (uint32_t)(lane * 4);
+  const uint32_t L = (uint32_t)(lane * 4);
   const uint32_t C = cluster_size();
   const uint32_t rank = cluster_rank();
   const int worker = (int)cluster_id();
@@ -250,15 +250,16 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
   };
   auto load_item = [&](const Src& r, int j, Item& it) {
     const bool on = j * kThreadsL < r.n32;
-    ldg16_if(it.lo, r.cw + j * 1024, on);
-    ldg16_if(it.hi, r.cw + j * 1024 + 32, on);
+    ldg16_if(it.lo, r.cw + j * (kThreadsL / 32) * 64, on);
+    ldg16_if(it.hi, r.cw + j * (kThreadsL / 32) * 64 + 32, on);
     ldg2_if(it.s, r.sc + j * kThreadsL, on);
   };
-  // builders: threads 0..287 (warps 0..8), column group g = tid % 32, high digit pair hi = tid / 32
-  const int g = tid & 31, hi = tid >> 5;
-  const bool builder = hi < 9;
+  // table builders: thread (warp w, lane g) writes column group g's entries of
+  // the code bytes whose high digit pair (d2, d3) is hi = w (w < 8, nine bytes),
+  // and of hi = 8 the byte with low pair lo = w (warp 0 also lo = 8)
+  const int g = lane, warp = tid >> 5;
   auto load_x = [&](const Step& s) -> uint2 {
-    if (builder && s.valid) return *reinterpret_cast<const uint2*>(b.t[s.ti].x + (size_t)s.bk * 128 + 4 * g);
+    if (s.valid) return *reinterpret_cast<const uint2*>(b.t[s.ti].x + (size_t)s.bk * 128 + 4 * g);
     return make_uint2(0u, 0u);
   };
 
@@ -269,20 +270,23 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
 
   // the table of a step's block, from its x, into the table at tb
   auto build = [&](uint2 xw, uint32_t tb) {
-    if (!builder) return;
     const float x0 = __uint_as_float(xw.x << 16), x1 = __uint_as_float(xw.x & 0xFFFF0000u);
     const float x2 = __uint_as_float(xw.y << 16), x3 = __uint_as_float(xw.y & 0xFFFF0000u);
-    const int d2 = hi % 3, d3 = hi / 3;
-    const float p23 = code_val(d2, x2) + code_val(d3, x3);
-    const uint32_t row_hi = tb + (uint32_t)((16 * d2 + 64 * d3) * 256 + 4 * g);
-#pragma unroll
-    for (int lo = 0; lo < 9; ++lo) {
-      const int d0 = lo % 3, d1 = lo / 3;
+    auto put = [&](int d0, int d1, int d2, int d3, float p23) {
       const float v = (code_val(d0, x0) + code_val(d1, x1)) + p23;
-      const uint32_t a = row_hi + (uint32_t)((d0 + 4 * d1) * 256);
+      const uint32_t a = tb + (uint32_t)((d0 + 4 * d1 + 16 * d2 + 64 * d3) * 256 + 4 * g);
       sts_f32(a, v);
       sts_f32(a + 128u, v);
+    };
+    {
+      const int d2 = warp % 3, d3 = warp / 3;
+      const float p23 = code_val(d2, x2) + code_val(d3, x3);
+#pragma unroll
+      for (int lo = 0; lo < 9; ++lo) put(lo % 3, lo / 3, d2, d3, p23);
     }
+    const float p23 = -x2 - x3;  // hi = 8: d2 = d3 = 2 (codes 10, -1)
+    put(warp % 3, warp / 3, 2, 2, p23);
+    if (warp == 0) put(2, 2, 2, 2, p23);
   };
   // one row's block: 32 lookups and adds, times the block's scale, into acc
   auto row_block = [&](const Item& it, float& a) {
@@ -290,9 +294,9 @@ __global__ void __launch_bounds__(kThreadsL, 1) lut_kernel(const __grid_constant
     uint64_t s2 = 0;  // two partial sums (even and odd positions)
 #pragma unroll
     for (int t = 0; t < 32; t += 2) {
-      // result bytes: lane offset, code byte t, table window high bytes
-      const uint32_t a0 = prmt(w[t >> 2], L, 0x7604u | ((uint32_t)(t & 3) << 4));
-      const uint32_t a1 = prmt(w[(t + 1) >> 2], L, 0x7604u | ((uint32_t)((t + 1) & 3) << 4));
+      // result bytes: lane offset, code byte t, 0, 0; plus the table base
+      const uint32_t a0 = prmt(w[t >> 2], L, 0x7604u | ((uint32_t)(t & 3) << 4)) + T0;
+      const uint32_t a1 = prmt(w[(t + 1) >> 2], L, 0x7604u | ((uint32_t)((t + 1) & 3) << 4)) + T0;
       float v0, v1;
       switch (t) {
 #define QMV_LUT_CASE(T) \
