@@ -171,12 +171,16 @@ def qmv_run_int4(desc: qmv_desc, w, x, y, stream=None):
 
 
 class Batch:
-    """A prepared qmv_run_batch argument list (keeps the ctypes arrays alive)."""
+    """A prepared qmv_run_batch argument list. It keeps the descriptors, the ctypes
+    arrays and the tensors (packed weights, x, y) alive for as long as it exists: the
+    launch reads them through raw pointers, and memory that the caller's allocator took
+    back and handed out again would otherwise be read as weights."""
 
     def __init__(self, format: int, tasks, M: int):
         self.format = format
         self.M = M
         self.descs = [t[0] for t in tasks]
+        self.tensors = [tuple(t[1:]) for t in tasks]
         self.arr = (qmv_task * len(tasks))()
         for i, (d, w, x, y) in enumerate(tasks):
             _, ldx = _rows(x)

@@ -8,10 +8,10 @@
 // 128 columns the CTA builds, from x, the table
 //     T[e][c] = sum_{i<4} q_i(e) * x[128 b + 4 c + i]     (c = 0..31 column groups)
 // in fp32 in shared memory; then every row's block costs one lookup per byte:
-// 32 lookups and fp32 adds per row and block, and one multiply by the block's
-// scale. The table is stored with a row of 64 four-byte slots per e (slot c
-// and slot c + 32 hold the same value), so the address of T[e][c] for the
-// lane that owns row n at byte position t is e*256 + 4*(n%32) + 4*t with
+// 32 lookups, added in pairs by packed fp32x2 adds, and one multiply by the
+// block's scale. The table has a row of 64 four-byte slots per e (slot c and
+// slot c + 32 hold the same value), so the address of T[e][c] for the lane
+// that owns row n at byte position t is base + e*256 + 4*(n%32) + 4*t with
 // c = (t + n) % 32: one byte permute builds e*256 + 4*(n%32) from the code
 // word and the lane's offset, and 4*t is the load's immediate offset. The
 // packer rotates each row's 32 code bytes by n % 32 to match, so at every
@@ -19,21 +19,25 @@
 // Rows of invalid bytes (a code 11) are zeroed once per launch and never
 // rebuilt, so such a byte contributes 0.
 //
-// Work split. A unit is up to 2048 rows of one matvec (unit_rows) over all of
+// Occupancy. A CTA is 8 warps with 72 KB of shared memory (the table and the
+// cluster partial sums) and 80 registers per thread, so three CTAs share an
+// SM: their per-block barriers and table builds fall at different times and
+// the lookups of one CTA fill the shared-memory pipe while another builds.
+//
+// Work split. A unit is up to 1024 rows of one matvec (unit_rows) over all of
 // its blocks (a cluster of C CTAs splits the blocks, each CTA a contiguous
 // share, and CTA rank 0 adds the C partial sums in rank order through
-// distributed shared memory). The host assigns units to clusters largest
-// first, each to the least loaded cluster, and passes the lists in the launch
-// parameters. Each of the 512 threads owns up to four rows of a unit (rows
-// r0 + 512 j + tid); lane = row % 32.
+// distributed shared memory). The host assigns units to CTAs (clusters)
+// largest first, each to the least loaded one, and passes the lists in the
+// launch parameters. Each of the 256 threads owns up to four rows of a unit
+// (rows r0 + 256 j + tid); lane = row % 32.
 //
 // Streaming. The codes of (block, 32-row group) are 1 KB records, rows of a
 // unit contiguous per block, so a thread's row is two coalesced 16-byte loads.
-// The next step's codes and scales are loaded into a second register set
-// while the current step is looked up, and one thread asks the copy engine to
-// prefetch the step after next into L2 (cp.async.bulk.prefetch), so the
-// register loads hit L2. No wait in this kernel spins: it synchronizes only
-// with CTA and cluster barriers.
+// Right after a row's lookups its registers are reloaded with the same row slot
+// of the next step, and one thread asks the copy engine to prefetch the step
+// after next into L2 (cp.async.bulk.prefetch), so those loads hit L2. No wait
+// in this kernel spins: it synchronizes only with CTA and cluster barriers.
 #include <algorithm>
 #include <cstring>
 #include <queue>
@@ -44,15 +48,15 @@
 namespace qmv {
 namespace {
 
-constexpr int kThreadsL = 256;                   // two CTAs per SM
+constexpr int kThreadsL = 256;                   // three CTAs per SM
 constexpr int kRpt = 4;                          // rows per thread and unit
 constexpr int kUnitRowsMax = kThreadsL * kRpt;   // 1024
 constexpr int kMaxUnitsL = 4096;
 constexpr int kMaxWorkersL = 512;
 constexpr int kTableBytes = 65536;
 constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of partial sums
-// the table and the partial sums: 72 KB, so two CTAs share an SM and one's
-// table build overlaps the other's lookups
+// the table and the partial sums: 72 KB, so three CTAs (80 registers per
+// thread) share an SM and one's table build overlaps the others' lookups
 constexpr size_t kSmemNeed = kTableBytes + kPartBytes;
 constexpr size_t kSmemL = kSmemNeed;
 
@@ -166,7 +170,7 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreadsL, 2) lut_kernel(const __grid_constant__ LutBatch b) {
+__global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant__ LutBatch b) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   const uint32_t T0 = base;  // the table: 256 rows (code byte e) of 64 four-byte slots

@@ -130,3 +130,23 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         q.lib()
+
+
+def test_batch_keeps_its_tensors_alive(L):
+    """A prepared batch holds the tensors whose addresses it passes, so the caller's
+    allocator cannot hand their memory out again while the batch may still launch."""
+    import gc
+    import weakref
+    import torch
+    d = q.qmv_pack_desc(q.QMV_TERNARY2_LUT, 64, 256)
+    w = torch.zeros(d.total_bytes, dtype=torch.uint8)
+    x = torch.zeros((1, 256), dtype=torch.bfloat16)
+    y = torch.zeros((1, 64), dtype=torch.float32)
+    refs = [weakref.ref(t) for t in (w, x, y)]
+    batch = q.Batch(q.QMV_TERNARY2_LUT, [(d, w, x, y)], 1)
+    del w, x, y
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    del batch
+    gc.collect()
+    assert all(r() is None for r in refs)
