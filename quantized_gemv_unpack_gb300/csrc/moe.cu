@@ -30,23 +30,32 @@ namespace {
 
 using namespace core;
 
-constexpr int kMoeWarps = 20;                           // decode warps per CTA: 4-row warps fit 102
-constexpr int kMoeThreads = kMoeWarps * 32;             // registers, and the extra warps hide latency
-constexpr int kMoeRPW = 4;                              // rows per decode warp
-constexpr int kMoeTileRows = kMoeWarps * kMoeRPW;       // 80
+// Decode warps and rows per warp of the expert kernels, by the most tokens a
+// slot can have (MT <= M): one token decodes 16 rows per warp (an activation
+// load serves four rows, as in the matvec batch), two tokens 8, more tokens 4
+// (4-row warps fit 102 registers at eight tokens, and 20 of them hide latency).
+template <int MTMAX>
+struct MoeCfg {
+  static constexpr int W = MTMAX <= 2 ? 16 : 20;
+  static constexpr int RPW = MTMAX == 1 ? 16 : (MTMAX == 2 ? 8 : 4);
+  static constexpr int THREADS = W * 32;
+  static constexpr int TILE_ROWS = W * RPW;
+};
+constexpr int kMaxMoeWarps = 20;
 constexpr int kMaxTopk = 8;
 constexpr int kMaxTokens = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxPairs = kMaxTokens * kMaxTopk;
 constexpr int kMoeSlots = 2;                            // ring slots per decode warp
 
-// The expert kernels' ring: per warp kMoeSlots slots of one step of 4 rows (a
-// deeper ring measured slower at M = 1).
+// The expert kernels' ring: per warp kMoeSlots slots of one step of the warp's
+// rows (a deeper ring measured slower at M = 1).
+template <int W, int RPW>
 struct MoeRing {
-  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+  using G = Geometry<QMV_TERNARY2, RPW>;
   static constexpr int SLOT = G::SLOT;
-  static constexpr int RING = kMoeWarps * kMoeSlots * SLOT;
-  static constexpr int BARS = kMoeWarps * kMoeSlots * 8;
+  static constexpr int RING = W * kMoeSlots * SLOT;
+  static constexpr int BARS = W * kMoeSlots * 8;
 };
 
 // Workspace layout (all offsets in bytes from the workspace base).
@@ -92,7 +101,7 @@ struct MoeRoute {
   float pair_prob[kMaxPairs];
   int exp[kMaxTokens][kMaxTopk];
   float prob[kMaxTokens][kMaxTopk];
-  int wp[kMoeWarps], ws[kMoeWarps];
+  int wp[kMaxMoeWarps], ws[kMaxMoeWarps];
 };
 
 // Called by all threads of the CTA (blockDim.x >= E); ends with a CTA barrier.
@@ -215,6 +224,7 @@ struct SwiGlu {  // h = silu(g) * u from the workspace, pair rows [first + m]
 // tile): lane 0 copies the warp's 4 rows of one step of the unit's expert
 // matrix into the next ring slot (one bulk copy, completes on the slot's
 // mbarrier), two steps ahead of the decode.
+template <int W, int RPW>
 struct UnitProducer {
   const uint32_t* codes0;   // expert 0's codes; expert e at + e * stride_words
   int64_t stride_words;
@@ -225,14 +235,14 @@ struct UnitProducer {
   uint64_t* wfull;
   __device__ __forceinline__ void issue() {
     using F = Fmt<QMV_TERNARY2>;
-    using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+    using G = Geometry<QMV_TERNARY2, RPW>;
     constexpr int kStepWords = kBlocksPerStep * F::WPB;
     if (u >= u_end) return;
     const int nb = K / 128;
     const int nbk = min(kBlocksPerStep, nb - s * kBlocksPerStep);
-    const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
+    const int wrow0 = (u % tiles) * (W * RPW) + warp * RPW;
     const int N16 = (N + 15) / 16 * 16;
-    const uint32_t bytes = wrow0 < N16 ? (uint32_t)(kMoeRPW * nbk * G::BLOCK_BYTES) : 0u;
+    const uint32_t bytes = wrow0 < N16 ? (uint32_t)(RPW * nbk * G::BLOCK_BYTES) : 0u;
     const int slot = n_issued % kMoeSlots;
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -254,19 +264,20 @@ struct UnitProducer {
 
 // Decode the units [u, u_end) of one slot (all tiles of one expert matrix for
 // the slot's MT tokens); out(m, row, value) receives sum_k w_hat x.
-template <int MT, class Src, class Out>
+template <int W, int RPW, int MT, class Src, class Out>
 __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u, int u_end, const Src& src,
-                         const Out& out, unsigned char* smem_raw, const DecodeK& dk, UnitProducer& prod,
-                         uint32_t& it, int* err) {
+                         const Out& out, unsigned char* smem_raw, const DecodeK& dk, UnitProducer<W, RPW>& prod,
+                         uint32_t& it, int* err, bool restage) {
   constexpr int FMT = QMV_TERNARY2;
   using F = Fmt<FMT>;
-  using G = Geometry<FMT, kMoeRPW>;
-  constexpr int RQ = kMoeRPW / kGroups;
-  __shared__ float s_red[kMoeWarps][MT];
+  using G = Geometry<FMT, RPW>;
+  using Ring = MoeRing<W, RPW>;
+  constexpr int RQ = RPW / kGroups;
+  __shared__ float s_red[W][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
   const int S = (K + kStep - 1) / kStep;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw + MoeRing::RING + MoeRing::BARS);
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw + Ring::RING + Ring::BARS);
   __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 3, p = lane & 7;
@@ -274,11 +285,11 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
   const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
   const int KB = K / 128;
 
-  stage_chunk<FMT, MT, kMoeThreads>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
+  if (restage) stage_chunk<FMT, MT, W * 32>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
 
   const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;  // scale records per 16-row group
   for (; u < u_end; ++u) {
-    const int wrow0 = (u % tiles) * kMoeTileRows + warp * kMoeRPW;
+    const int wrow0 = (u % tiles) * (W * RPW) + warp * RPW;
     const unsigned short* sp[RQ];
 #pragma unroll
     for (int r = 0; r < RQ; ++r) {
@@ -340,9 +351,10 @@ struct DownOut {  // y[token] += p * value
 
 // Persistent: CTA c takes the contiguous unit range [c*U/G, (c+1)*U/G) of the
 // U = n_slots * tiles units of this phase (all units are the same size).
-template <int PHASE>
-__global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArgs a) {
-  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+template <int PHASE, int MTMAX>
+__global__ void __launch_bounds__(MoeCfg<MTMAX>::THREADS, 1) moe_expert_kernel(const MoeArgs a) {
+  constexpr int W = MoeCfg<MTMAX>::W, RPW = MoeCfg<MTMAX>::RPW;
+  using Ring = MoeRing<W, RPW>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ int s_tok[kMaxTokens];
   __shared__ float s_prob[kMaxTokens];
@@ -375,13 +387,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   const int* slot_count = R.slot_count;
   const int N = PHASE == 0 ? 2 * a.I : a.H;
   const int K = PHASE == 0 ? a.H : a.I;
-  const int tiles = (N + kMoeTileRows - 1) / kMoeTileRows;
+  const int tiles = (N + W * RPW - 1) / (W * RPW);
   const int total = ns * tiles;
   const int u_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int u_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   if (u_begin >= u_end) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  UnitProducer prod;
+  UnitProducer<W, RPW> prod;
   prod.codes0 = PHASE == 0 ? a.gu_codes : a.dn_codes;
   prod.stride_words = a.stride_words;
   prod.slot_expert = slot_expert;
@@ -395,8 +407,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   prod.warp = warp;
   prod.lane = lane;
   prod.n_issued = 0;
-  prod.wring = smem_raw + (size_t)warp * kMoeSlots * MoeRing::SLOT;
-  prod.wfull = reinterpret_cast<uint64_t*>(smem_raw + MoeRing::RING) + warp * kMoeSlots;
+  prod.wring = smem_raw + (size_t)warp * kMoeSlots * Ring::SLOT;
+  prod.wfull = reinterpret_cast<uint64_t*>(smem_raw + Ring::RING) + warp * kMoeSlots;
   if (lane == 0) {
     for (int i = 0; i < kMoeSlots; ++i) mbar_init(&prod.wfull[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -411,6 +423,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   float* gu = reinterpret_cast<float*>(a.ws + a.off_gu);
   const uint16_t* scales0 = PHASE == 0 ? a.gu_scales : a.dn_scales;
   uint32_t it = 0;
+  bool staged = false;  // gate|up at one token: every slot stages the same x, once
   for (int u = u_begin; u < u_end;) {
     const int slot = u / tiles;
     const int u_stop = min(u_end, (slot + 1) * tiles);
@@ -424,23 +437,26 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
     }
     __syncthreads();
     const uint16_t* scales = scales0 + (size_t)e * a.stride_halves;
+    const bool restage = !(PHASE == 0 && a.M == 1 && staged);
+    staged = true;
     if (PHASE == 0) {
       const GatherRows src{a.x, a.ldx, s_tok};
       const GuOut out{gu, 2 * a.I, first};
       switch (cnt) {
-#define QMV_MOE_CASE(m) \
-  case m: run_slot<m>(scales, N, K, tiles, u, u_stop, src, out, smem_raw, dk, prod, it, a.err); break;
+#define QMV_MOE_CASE(m)                                                                                          \
+  case m:                                                                                                        \
+    if (m <= MTMAX)                                                                                              \
+      run_slot<W, RPW, (m <= MTMAX ? m : 1)>(scales, N, K, tiles, u, u_stop, src, out, smem_raw, dk, prod, it, \
+                                             a.err, restage);                                                    \
+    break;
         QMV_MOE_CASE(1) QMV_MOE_CASE(2) QMV_MOE_CASE(3) QMV_MOE_CASE(4)
         QMV_MOE_CASE(5) QMV_MOE_CASE(6) QMV_MOE_CASE(7) QMV_MOE_CASE(8)
-#undef QMV_MOE_CASE
         default: break;
       }
     } else {
       const SwiGlu src{gu, a.I, first};
       const DownOut out{a.y, a.ldy, s_tok, s_prob};
       switch (cnt) {
-#define QMV_MOE_CASE(m) \
-  case m: run_slot<m>(scales, N, K, tiles, u, u_stop, src, out, smem_raw, dk, prod, it, a.err); break;
         QMV_MOE_CASE(1) QMV_MOE_CASE(2) QMV_MOE_CASE(3) QMV_MOE_CASE(4)
         QMV_MOE_CASE(5) QMV_MOE_CASE(6) QMV_MOE_CASE(7) QMV_MOE_CASE(8)
 #undef QMV_MOE_CASE
@@ -451,10 +467,44 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_expert_kernel(const MoeArg
   }
 }
 
+template <int MTMAX>
 size_t expert_smem(int64_t K) {
-  using G = Geometry<QMV_TERNARY2, kMoeRPW>;
+  using Ring = MoeRing<MoeCfg<MTMAX>::W, MoeCfg<MTMAX>::RPW>;
   const int64_t S = (K + kStep - 1) / kStep;
-  return MoeRing::RING + MoeRing::BARS + (size_t)kMaxTokens * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(kMaxTokens, S);
+  return Ring::RING + Ring::BARS + (size_t)MTMAX * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(MTMAX, S);
+}
+
+// The two expert launches for slots of at most MTMAX tokens (MTMAX >= M).
+template <int MTMAX>
+int launch_experts(const MoeArgs& a, int64_t H, int64_t I, cudaStream_t s) {
+  using Cfg = MoeCfg<MTMAX>;
+  const size_t smem_gu = expert_smem<MTMAX>(H), smem_dn = expert_smem<MTMAX>(I);
+  int per_sm = 0;
+  int rc = kernel_fit((const void*)moe_expert_kernel<0, MTMAX>, Cfg::THREADS, smem_gu, &per_sm);
+  if (rc) return rc;
+  rc = kernel_fit((const void*)moe_expert_kernel<1, MTMAX>, Cfg::THREADS, smem_dn, &per_sm);
+  if (rc) return rc;
+  // persistent grids: one CTA per SM, capped by the largest possible unit count
+  const int units_gu = a.max_slots * (int)((2 * I + Cfg::TILE_ROWS - 1) / Cfg::TILE_ROWS);
+  const int units_dn = a.max_slots * (int)((H + Cfg::TILE_ROWS - 1) / Cfg::TILE_ROWS);
+  moe_expert_kernel<0, MTMAX><<<std::min(sm_count(), units_gu), Cfg::THREADS, smem_gu, s>>>(a);
+  cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return cuda_fail(ce, "moe gate|up launch");
+  // programmatic dependent launch: the down grid's routing and first weight
+  // copies overlap the end of the gate|up grid
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)std::min(sm_count(), units_dn));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = smem_dn;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ce = cudaLaunchKernelEx(&cfg, moe_expert_kernel<1, MTMAX>, a);
+  if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
+  return QMV_OK;
 }
 
 // Scratch for moe_qmv_run_static: one fixed array per device, in the module's
@@ -518,8 +568,9 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   if (H > INT32_MAX || ldx > INT32_MAX || ldy > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "sizes too large");
   const MoeLayout L(E, topk, M, I);
   if (ws_bytes < (size_t)L.total) return fail(QMV_ERR_ARG, "workspace %zu < %lld bytes", ws_bytes, (long long)L.total);
-  const size_t smem_gu = expert_smem(H), smem_dn = expert_smem(I);
-  if (std::max(smem_gu, smem_dn) > 227 * 1024 - 1024) return fail(QMV_ERR_UNSUPPORTED, "hidden size too large for one CTA");
+  const size_t need_gu = M == 1 ? expert_smem<1>(H) : (M == 2 ? expert_smem<2>(H) : expert_smem<8>(H));
+  const size_t need_dn = M == 1 ? expert_smem<1>(I) : (M == 2 ? expert_smem<2>(I) : expert_smem<8>(I));
+  if (std::max(need_gu, need_dn) > 227 * 1024 - 1024) return fail(QMV_ERR_UNSUPPORTED, "hidden size too large for one CTA");
   int* err = device_error_word();
   if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
 
@@ -553,33 +604,9 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   a.err = err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t ce;
-  int per_sm = 0;
-  rc = kernel_fit((const void*)moe_expert_kernel<0>, kMoeThreads, smem_gu, &per_sm);
-  if (rc) return rc;
-  rc = kernel_fit((const void*)moe_expert_kernel<1>, kMoeThreads, smem_dn, &per_sm);
-  if (rc) return rc;
-  // persistent grids: one CTA per SM, capped by the largest possible unit count
-  const int units_gu = a.max_slots * (int)((I2 + kMoeTileRows - 1) / kMoeTileRows);
-  const int units_dn = a.max_slots * (int)((H + kMoeTileRows - 1) / kMoeTileRows);
-  moe_expert_kernel<0><<<std::min(sm_count(), units_gu), kMoeThreads, smem_gu, s>>>(a);
-  ce = cudaGetLastError();
-  if (ce != cudaSuccess) return cuda_fail(ce, "moe gate|up launch");
-  // programmatic dependent launch: the down grid's routing and first weight
-  // copies overlap the end of the gate|up grid
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3((unsigned)std::min(sm_count(), units_dn));
-  cfg.blockDim = dim3(kMoeThreads);
-  cfg.dynamicSmemBytes = smem_dn;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  ce = cudaLaunchKernelEx(&cfg, moe_expert_kernel<1>, a);
-  if (ce != cudaSuccess) return cuda_fail(ce, "moe down launch");
-  return QMV_OK;
+  if (M == 1) return launch_experts<1>(a, H, I, s);
+  if (M == 2) return launch_experts<2>(a, H, I, s);
+  return launch_experts<8>(a, H, I, s);
 }
 
 int moe_qmv_run_static(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts,
