@@ -339,6 +339,7 @@ class SparseStack(Workload):
         c = Stack.stack_config(self.layers)
         c["workload"] = c["workload"].replace("block-128 absmean ternary", "flagged sparse block-128 ternary "
                                               f"({100 * self.ZERO:.1f} % of 16 x 128 tiles zero)")
+        c["layout"] = "flagged sparse tiles (QMV_TERNARY2_SPARSE)"
         c["zero_tile_fraction"] = self.ZERO
         c["bits_per_weight"] = 8 * (self.nbytes - self.layers * (HIDDEN + INTER) * 2) / sum(
             N * K for _, N, K in synth_shapes()) / self.layers
