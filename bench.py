@@ -608,6 +608,22 @@ def make_workload(name, q, torch, dev, a):
     raise SystemExit(f"unknown workload {name}")
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(values, dist, device):
+    """Elementwise maximum of per-rank timings across the process group (the job is as
+    slow as its slowest replica)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(bytes_per_step_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job GB/s: every rank streams its own replica's bytes in the slowest rank's time."""
+    return bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9 * world
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -725,14 +741,12 @@ def main():
     e2e_bytes = sum(wl.bytes(i) for i in range(n_e2e)) / n_e2e
 
     if dist is not None:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+        ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, dev)
     if rank != 0:
         dist.destroy_process_group()
         return
     peak, peak_kind = peaks()
-    per_gpu = nbytes / (ms * 1e-3) / 1e9
+    per_gpu = job_throughput(nbytes, ms, 1)
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
     launches = {"stack": 1, "stack-sparse": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
                 "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "kv-encode": 1, "moe": 2}[a.workload]
