@@ -57,8 +57,7 @@ constexpr int kTableBytes = 65536;
 constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of partial sums
 // the table and the partial sums: 72 KB, so three CTAs (80 registers per
 // thread) share an SM and one's table build overlaps the others' lookups
-constexpr size_t kSmemNeed = kTableBytes + kPartBytes;
-constexpr size_t kSmemL = kSmemNeed;
+constexpr size_t kSmemL = kTableBytes + kPartBytes;
 
 struct LutTask {
   const unsigned char* codes;  // section 0; the scales follow at NG * KB * 1024 bytes
@@ -172,13 +171,13 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
 
 __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant__ LutBatch b) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const uint32_t base = smem_u32(smem_raw);
-  const uint32_t T0 = base;  // the table: 256 rows (code byte e) of 64 four-byte slots
-  if (T0 + kSmemNeed > base + b.smem_bytes) {  // the launch did not reserve the round-up
+  // the table: 256 rows (code byte e) of 64 four-byte slots, then the partial sums
+  const uint32_t T0 = smem_u32(smem_raw);
+  if (b.smem_bytes < kSmemL) {  // a launch without room for both: report, compute nothing
     if (threadIdx.x == 0) atomicCAS(b.err, 0, (int)QMV_ERR_UNSUPPORTED);
     return;
   }
-  const uint32_t part = T0 + kTableBytes;     // [2][kRpt][512] fp32
+  const uint32_t part = T0 + kTableBytes;     // [2][kRpt][kThreadsL] fp32
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const uint32_t L = (uint32_t)(lane * 4);
@@ -232,8 +231,8 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
   };
   // This thread's load addresses of a step: row r0 + tid of its codes and of
-  // its scales; item j (row r0 + 512 j + tid) is 16 row groups further on (16 KB
-  // of codes, 1 KB of scales). n32 > 512 j while item j has rows of this warp.
+  // its scales; item j (row r0 + 256 j + tid) is 8 row groups further on (8 KB
+  // of codes, 512 B of scales). n32 > 256 j while item j has rows of this warp.
   struct Src {
     const uint4* cw;
     const uint16_t* sc;
@@ -456,13 +455,13 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
     for (int i = 0; i < n; ++i) u += (b.t[i].N + rows - 1) / rows;
     return u;
   };
-  // Rows per unit and CTAs per cluster: whole 2048-row units on single CTAs
+  // Rows per unit and CTAs per cluster: whole 1024-row units on single CTAs
   // when there are enough of them; otherwise smaller units whose blocks a
   // cluster of up to 8 CTAs shares, until the launch covers the SMs.
   int rows = kUnitRowsMax, C = 1;
   if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
     bool done = false;
-    for (int r : {kUnitRowsMax, 1024, 512, 256}) {
+    for (int r : {kUnitRowsMax, 512, 256}) {
       for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
         rows = r;
         C = c;
