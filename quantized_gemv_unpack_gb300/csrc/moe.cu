@@ -302,11 +302,20 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
     for (int r = 0; r < RQ; ++r)
 #pragma unroll
       for (int m = 0; m < MT; ++m) accc[r][m] = 0.f;
+    // block scales run one step ahead of the decode (their load latency overlaps a step)
+    unsigned short scn[RQ];
+#pragma unroll
+    for (int r = 0; r < RQ; ++r) scn[r] = p < nb ? __ldg(sp[r]) : (unsigned short)0;
     for (int s = 0; s < nsteps; ++s, ++it) {
       const bool active = s * kBlocksPerStep + p < nb;
       unsigned short sc[RQ];
 #pragma unroll
-      for (int r = 0; r < RQ; ++r) sc[r] = active ? __ldg(sp[r] + s * 128) : (unsigned short)0;
+      for (int r = 0; r < RQ; ++r) sc[r] = scn[r];
+      if (s + 1 < nsteps) {
+        const bool next = (s + 1) * kBlocksPerStep + p < nb;
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) scn[r] = next ? __ldg(sp[r] + (s + 1) * 128) : (unsigned short)0;
+      }
       const int slot = it % kMoeSlots;
       mbar_wait(&prod.wfull[slot], (it / kMoeSlots) & 1u, err);
       if (active) {
