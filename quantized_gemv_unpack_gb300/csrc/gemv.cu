@@ -24,7 +24,7 @@
 //
 // Activations are staged per (x, chunk) in shared memory as fp16 pairs in
 // the order a lane consumes them, after scaling the chunk by a power of two
-// so its largest magnitude lies in [2^9, 2^10) (ternary) or [2^8, 2^9) (INT4);
+// so its largest magnitude lies in [2^9, 2^10) (ternary) or [2^5, 2^6) (INT4);
 // the scale is undone in fp32.
 //
 // Decode, per 32-bit code word, without lookup tables, one shift and one

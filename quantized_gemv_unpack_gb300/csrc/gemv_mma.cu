@@ -49,7 +49,7 @@
 // to q exactly.
 //
 // Activations are staged per chunk of K as fp16, scaled per row by a power of
-// two (largest magnitude in [2^9, 2^10) for ternary, [2^8, 2^9) for INT4), in
+// two (largest magnitude in [2^9, 2^10) for ternary, [2^5, 2^6) for INT4), in
 // 16-byte units whose index is XORed with (row & 7) so that the 32 lanes of a
 // load hit all banks.
 #include <algorithm>
