@@ -106,6 +106,30 @@ def test_lut_activation_range(env):
         _check(y.cpu().numpy(), yr, B, f"x scale {scale}")
 
 
+def test_lut_sparse_codes(env):
+    """One nonzero code per block against N(0,1) activations: a block's sum |w_hat x| is then a
+    single term. The lookup path adds table entries that hold only the products of nonzero codes,
+    so its error stays relative to that term (fp32 bound), unlike seeded fp16 chains."""
+    q, torch, dev = env
+    from oracle import ternary
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = 96, 5120
+    g = synth.rng(4243)
+    w = np.zeros((N, K), np.float32)
+    hit = g.integers(0, 128, size=(N, K // 128)) + 128 * np.arange(K // 128)[None, :]
+    w[np.arange(N)[:, None], hit] = np.float32(0.02) * np.where(g.random((N, K // 128)) < 0.5, -1, 1)
+    xb = synth.activations_bf16(g, (1, K))
+    d, p = _pack(q, torch, dev, w)
+    y = torch.full((1, N), float("nan"), device=dev)
+    q.qmv_run_ternary(d, p, _dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
+    qq, _, s16 = ternary.quantize(w)
+    assert np.all((qq != 0).reshape(N, K // 128, 128).sum(axis=2) == 1)
+    yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
+    _check(y.cpu().numpy(), yr, B, "sparse codes")
+
+
 def test_lut_invalid_byte_contributes_zero(env):
     """A code byte holding a code 11 adds nothing (its four columns count as 0); qmv_unpack flags it."""
     q, torch, dev = env
