@@ -446,6 +446,10 @@ int launch_mma_t(GemvBatch& b, int M, cudaStream_t s) {
   int kc = (int)(budget / per_col) / kStep * kStep;
   const int need = (max_K + kStep - 1) / kStep * kStep;
   if (kc > need) kc = need;
+  // One chunk that holds the longest K whole need not be a whole number of steps
+  // (chunks past the first start at multiples of the chunk, which must then be
+  // whole steps): at M = 4, K = 13824 fits in 108 KB but 14 steps do not.
+  if (kc < max_K && (size_t)max_K * per_col <= budget) kc = max_K;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", M);
   b.kc = kc;
   const size_t smem = ring + (size_t)M * kc * 2 + (FMT == QMV_TERNARY2 ? (size_t)(kc / 128) * MT * 4 : 0);
