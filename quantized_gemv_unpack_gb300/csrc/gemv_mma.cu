@@ -368,6 +368,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
               } else {
                 d[0] = d[1] = d[2] = d[3] = 0.f;
               }
+              // odd k-slices accumulate apart (two independent MMA chains per block)
+              float d2[4] = {0.f, 0.f, 0.f, 0.f};
               // k-slice kk: pairs 2kk and 2kk+1 (columns 32t + 4kk .. +3) of rows g and g+8
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
@@ -377,8 +379,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                                        h2u(decode_pair<FMT>(wg8[p0 / PPW], p0 % PPW, dk)),
                                        h2u(decode_pair<FMT>(wg[p1 / PPW], p1 % PPW, dk)),
                                        h2u(decode_pair<FMT>(wg8[p1 / PPW], p1 % PPW, dk))};
-                mma16816(d, a, xp[2 * kk], xp[2 * kk + 1]);
+                if (kk & 1) mma16816(d2, a, xp[2 * kk], xp[2 * kk + 1]);
+                else mma16816(d, a, xp[2 * kk], xp[2 * kk + 1]);
               }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d[e] += d2[e];
               tot[n][0] = fmaf(d[0], fg, tot[n][0]);
               tot[n][1] = fmaf(d[1], fg, tot[n][1]);
               tot[n][2] = fmaf(d[2], fg8, tot[n][2]);
