@@ -78,7 +78,7 @@ def copies_for(nbytes: int) -> int:
 
 
 PATH_FLAGS = {"auto": 0, "fma": 1, "mma": 2}   # qmv_desc.flags: QMV_FLAG_PATH_FMA / QMV_FLAG_PATH_MMA
-MMA_MIN_M = {"int4": 1, "ternary": 3}          # the library's automatic choice of the tensor-core kernel
+MMA_MIN_M = {"int4": 1, "ternary": 2}          # the library's automatic choice of the tensor-core kernel
 
 
 LUT_KERNEL = "lut_kernel (byte-lookup tables, fp32)"

@@ -48,7 +48,9 @@ typedef enum {
   QMV_ERR_UNSUPPORTED = -3,  /* valid request this build does not serve */
   QMV_ERR_CORRUPT = -4,      /* a kernel met packed data that breaks the format */
   QMV_ERR_CUDA = -5,         /* a CUDA runtime call failed (message has the CUDA error) */
-  QMV_ERR_TIMEOUT = -6       /* reserved: a bounded device wait gave up */
+  QMV_ERR_TIMEOUT = -6       /* a kernel's bounded device-side wait (a copy completion) gave up
+                                after its time limit; recorded in the device error word, read
+                                with qmv_check_status; the kernel's outputs are then invalid */
 } qmv_status;
 
 typedef enum {
@@ -149,11 +151,11 @@ typedef struct {
 /*
  * Kernel choice of the ternary/INT4 matvec entry points (qmv_desc.flags; the
  * packers leave it 0). With 0 the library picks: the tensor-core kernel
- * (mma.sync m16n8k16, decode cost independent of M) for INT4 and for ternary
- * from M = 3, the fp16-FMA kernel (cost grows with M) for ternary at M <= 2.
- * Setting one bit forces a kernel, for testing and tuning; both bits set is
- * QMV_ERR_ARG. Results of both kernels satisfy the same error bound; the
- * tensor-core kernel's are also reproducible bit for bit.
+ * (mma.sync m16n8k16 on bf16, decode cost independent of M) for INT4 and for
+ * ternary from M = 2, the fp16-FMA kernel (cost grows with M) for ternary at
+ * M = 1. Setting one bit forces a kernel, for testing and tuning; both path bits
+ * set is QMV_ERR_ARG. Results of both kernels satisfy the same error bound and
+ * are reproducible bit for bit.
  */
 #define QMV_FLAG_PATH_FMA 1u
 #define QMV_FLAG_PATH_MMA 2u
@@ -212,12 +214,17 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
  * of the packed ternary (qmv_run_ternary) or INT4 (qmv_run_int4) matrix.
  * M in 1..QMV_MAX_M, ldx >= K, ldy >= N (a QMV_TERNARY2_SPARSE desc in
  * qmv_run_ternary or qmv_run_batch: M in 1..8, the fp16-FMA kernel, and K must
- * fit shared memory in one piece). Activations are rounded to fp16 after
- * a power-of-two scaling per row and chunk of K; the fp16-FMA kernel sums
- * products in fp16 pairs over 16-32 columns and in fp32 beyond, the
- * tensor-core kernel (see QMV_FLAG_PATH_*) in fp32 from the start. Each
- * row's error stays within the library's documented bound
- * |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|.
+ * fit shared memory in one piece). Every kernel decodes a zero code to an
+ * exact 0, so an activation meeting a zero weight contributes nothing. The
+ * tensor-core kernel multiplies the bf16 activations as given (exact products)
+ * and sums in fp32. The fp16-FMA kernel (and the sparse kernel) scales each
+ * activation row and chunk of K by a power of two into fp16, where every value
+ * down to 2^-30 (ternary) or 2^-25 (INT4) of the chunk's largest magnitude is
+ * exact, forms exact products and sums them in fp16 chains of 8 columns (at
+ * most 3 * 2^-11 of the chain's sum of |terms|), then in fp32. Each row's
+ * error stays within the library's bound
+ * |y - y_exact| <= 2e-3 * sum_k |W_hat[n][k] x[m][k]|
+ * (for the fp16-FMA kernel: for activations within that range).
  */
 int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
                     float* y, int64_t ldy, void* stream);
@@ -340,7 +347,9 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
  * callers.
  *  - It allocates nothing and frees nothing. The first call on a device looks up
  *    the array's device address (cudaGetSymbolAddress) and keeps it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture. The kept address belongs to the
+ *    device's context: after cudaDeviceReset on that device do not call this
+ *    entry point again in the same process.
  *  - A call whose scratch need (moe_workspace_size) exceeds the array is
  *    rejected with QMV_ERR_ARG before any launch.
  *  - All calls share the one array and it keeps the previous call's contents;

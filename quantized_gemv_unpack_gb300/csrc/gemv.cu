@@ -24,30 +24,33 @@
 //
 // Activations are staged per (x, chunk) in shared memory as fp16 pairs in
 // the order a lane consumes them, after scaling the chunk by a power of two
-// so its largest magnitude lies in [2^9, 2^10) (ternary) or [2^5, 2^6) (INT4);
-// the scale is undone in fp32.
+// so its largest magnitude lies in [2^13, 2^14) (ternary) or [2^10, 2^11)
+// (INT4); the scale is undone in fp32.
 //
-// Decode, per 32-bit code word, without lookup tables, one shift and one
-// three-input logic op per column pair (mask and base live in registers).
-// The ALU pipe (logic ops, shifts) and the FMA pipe (integer multiply, fp16
-// FMA) each issue 16 lanes per clock per SM sub-partition on this GPU, so of
-// the eight ternary shifts per word four (the left shifts by 9, 7, 5, 1) are
-// integer multiplies by 2^s and four are funnel shifts; the multipliers and
-// amounts arrive as kernel parameters so the assembler keeps that split.
+// Decode, per 32-bit code word, without lookup tables: one shift, one
+// three-input logic op and one fp16 subtraction per column pair (mask and base
+// live in registers). The ALU pipe (logic ops, shifts) and the FMA pipe
+// (integer multiply, fp16 arithmetic) each issue 16 lanes per clock per SM
+// sub-partition on this GPU, so of the eight ternary shifts per word four (the
+// left shifts by 9, 7, 5, 1) are integer multiplies by 2^s and four are funnel
+// shifts; the multipliers and amounts arrive as kernel parameters so the
+// assembler keeps that split.
 //  * ternary: the low half holds even columns, the high half odd columns, so a
 //    word gives eight (even, odd) column pairs. Shifting pair i's two 2-bit
 //    codes to bits 9-10 and 25-26 and computing (t & 0x06000600) ^ 0x3C003C00
 //    yields two fp16 values v = 1 + q/2 (code 00 -> 1.0, 01 -> 1.5, 10 -> 0.5):
 //    bit 9 is the mantissa MSB (+0.5), bit 10 the exponent LSB (halves 1.0).
-//    Then sum_k v_k x_k = sum_k x_k + (1/2) sum_k q_k x_k; the fp16
-//    accumulator is seeded with -sum x over the block (computed once per staged
-//    chunk), leaving (1/2) sum q x; the factor 2 is applied at the end.
+//    Subtracting 1 gives q/2 exactly, so a zero code contributes exactly 0
+//    whatever its activation; the factor 2 is applied at the end.
 //  * INT4: (t & 0x000F000F) ^ 0x64086408 maps a two's-complement nibble q to
 //    the fp16 integer 1032 + q (1024 + offset-binary nibble); subtracting 1032
-//    gives q exactly, which is then multiplied into the fp16 accumulator.
-// Two fp16 pair accumulators per block (first and second half of the words)
-// are added, widened to fp32 and scaled by the block's fp16 scale; three warp
-// shuffles reduce the eight lanes of a row at the end of the tile.
+//    gives q exactly.
+// Products of these weights with the staged activations are exact. They are
+// summed in fp16 chains of four column pairs, and each chain is widened into
+// an fp32 block sum (two mixed-precision adds); the block sum is scaled by the
+// block's fp16 scale in fp32. A chain rounds three times, so each row stays
+// within 3 * 2^-11 (1.5e-3) of sum_k |w_hat_k x_k| plus fp32 rounding. Three
+// warp shuffles reduce the eight lanes of a row at the end of the tile.
 #include <algorithm>
 #include <cstdlib>
 
@@ -87,7 +90,6 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__
   using G = Geometry<FMT, RPW>;
   using R = FmaRing<FMT, RPW, W>;
   constexpr int WPB = F::WPB;
-  constexpr int JW = F::JW;
   constexpr int RQ = RPW / kGroups;          // row quads per decode warp
   constexpr bool TERN = FMT == QMV_TERNARY2;
 
@@ -97,7 +99,6 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__
   const int KC = b.kc;
   const int S = KC / kStep;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + R::BARS);        // [MT][S][WPB][JW][8]
-  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * WPB * JW * 8);  // [MT][S*8][seeds per block]
   __shared__ float s_red[W][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__
 
       if (x != staged_x || kc0 != staged_kc0 || K != staged_K) {
         // ---- stage the activations of this chunk
-        stage_chunk<FMT, MT, W * 32>(Bf16Rows{x, ldx, kc0}, kcn, S, xs, negs, s_red, s_xscale, s_xinv);
+        stage_chunk<FMT, MT, W * 32>(Bf16Rows{x, ldx, kc0}, kcn, S, xs, s_red, s_xscale, s_xinv);
         staged_x = x;
         staged_kc0 = kc0;
         staged_K = K;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__
           for (int r = 0; r < RQ; ++r) sc[r] = srec[(srow + r * kGroups) * kBlocksPerStep + p];
           // rows of the step are nbk blocks apart in the slot
           const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
-          decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, row_bytes, xs, negs, S, s, g, p, dk, sc, accc);
+          decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, row_bytes, xs, S, s, g, p, dk, sc, accc);
         }
         __syncwarp();  // every lane is done with the slot before it is refilled
         issue_one();
@@ -284,16 +285,15 @@ int launch_t(GemvBatch& b, cudaStream_t s) {
   b.n_tiles = tiles;
   b.rows_per_tile = R::TILE_ROWS;
   // activation chunk: as much of K as fits next to the ring, in whole steps;
-  // per staged column: MT fp16 values, plus the seeds (fp16 pairs per 128 columns and row)
+  // per staged column: MT fp16 values
   const size_t fixed = R::RING + R::BARS;
   const size_t budget = kSmemMax - fixed - 1024;
-  int kc_cap = (int)(budget / ((size_t)MT * kStep * 2 + seed_bytes<FMT>(MT, 1))) * kStep;
+  int kc_cap = (int)(budget / ((size_t)MT * kStep * 2)) * kStep;
   int kc = ((max_K + kStep - 1) / kStep) * kStep;
   if (kc > kc_cap) kc = kc_cap;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", MT);
   b.kc = kc;
-  const size_t S = kc / kStep;
-  const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<FMT>(MT, S);
+  const size_t smem = fixed + (size_t)MT * kc * 2;
   fill_magic<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");

@@ -19,7 +19,9 @@ struct Fmt<QMV_TERNARY2> {
   static constexpr int PPW = 8;    // column pairs per word
   static constexpr int CPW = 16;   // columns per word
   static constexpr int JW = 2;     // 16-byte activation pieces per word
-  static constexpr int XLOG2 = 9;  // staged |x| max in [2^9, 2^10)
+  // staged |x| max in [2^13, 2^14): a chain of four products |q/2 x| <= 2^13
+  // stays below 2^15, and values down to 2^-29 of the largest stay exact in fp16
+  static constexpr int XLOG2 = 13;
   static constexpr uint32_t MASK = 0x06000600u, BASE = 0x3C003C00u;
 };
 template <>
@@ -28,26 +30,18 @@ struct Fmt<QMV_INT4> {
   static constexpr int PPW = 4;
   static constexpr int CPW = 8;
   static constexpr int JW = 1;
-  // staged |x| max in [2^5, 2^6): a block half sums 64 products |q x| <= 8 * 64, so no
-  // fp16 partial sum can overflow (65504)
-  static constexpr int XLOG2 = 5;
+  // staged |x| max in [2^10, 2^11): a chain of four products |q x| <= 7 * 2^11
+  // stays below the fp16 maximum (65504)
+  static constexpr int XLOG2 = 10;
   static constexpr uint32_t MASK = 0x000F000Fu, BASE = 0x64086408u;
 };
 
-// fp16 accumulation chains of four code words: two per ternary block, each
-// seeded with -sum x over its own 64 columns (so that its partial sums stay
-// near the chain's own result), four per INT4 block. Chains are added into the
-// block's pair sum, which is widened to fp32 once per block.
-template <int FMT>
-struct Chain {
-  static constexpr int WORDS = 4;
-  static constexpr int SEEDS = FMT == QMV_TERNARY2 ? Fmt<FMT>::WPB / WORDS : 1;  // staged seeds per block
-};
-// Shared-memory bytes of the staged seeds for MT rows and S steps.
-template <int FMT>
-inline size_t seed_bytes(size_t MT, size_t S) {
-  return MT * S * kBlocksPerStepHost * Chain<FMT>::SEEDS * 4;
-}
+// fp16 accumulation chains of kChainPairs column pairs: each chain starts from
+// an exact product and takes three more fp16 FMAs, then its two halves are
+// added into an fp32 block sum (mixed-precision adds). With exact products the
+// chain's rounding error is at most 3 * 2^-11 of the sum of its |terms|, which
+// keeps every row within 1.5e-3 of sum_k |w_hat_k x_k|.
+constexpr int kChainPairs = 4;
 
 constexpr int kGroups = 4;            // lane groups (rows of a row quad)
 constexpr int kBlocksPerStep = kBlocksPerStepHost;  // lanes per row
@@ -95,11 +89,23 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_fl
 // 2^e as a float, e in [-126, 127]
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
+// fp32 a + the two fp16 halves of h (mixed-precision adds, exact widening)
+__device__ __forceinline__ float add_h2_f32(float a, __half2 h) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 t;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.f16 t, lo, %2;\n\tadd.rn.f32.f16 %0, hi, t;\n\t}"
+      : "=f"(d)
+      : "r"(*reinterpret_cast<const uint32_t*>(&h)), "f"(a));
+  return d;
+}
+
+// The two weights of column pair i of code word w as fp16, exactly: ternary
+// q/2 (code 00 -> 0, 01 -> +1/2, 10 -> -1/2), INT4 q.
 template <int FMT>
 __device__ __forceinline__ __half2 decode_pair(uint32_t w, int i, const DecodeK& k) {
   if constexpr (FMT == QMV_TERNARY2) {
     // pair i: even column code at bits 2i..2i+1, odd column code at 16+2i..17+2i;
-    // shift both to bits 9-10 / 25-26
+    // shift both to bits 9-10 / 25-26, where (t & mask) ^ base gives v = 1 + q/2
     uint32_t t;
     switch (i) {
       case 0: t = mul_lo(w, k.m9); break;
@@ -111,7 +117,7 @@ __device__ __forceinline__ __half2 decode_pair(uint32_t w, int i, const DecodeK&
       case 6: t = shr_r(w, k.s3); break;
       default: t = shr_r(w, k.s5); break;
     }
-    return as_h2(and_xor(t, k.mask, k.base));
+    return __hsub2(as_h2(and_xor(t, k.mask, k.base)), __floats2half2_rn(1.f, 1.f));
   } else {
     const uint32_t t = i == 0 ? w : shr_r(w, i == 1 ? k.s1 : (i == 2 ? k.s3 : k.s5));
     return __hsub2(as_h2(and_xor(t, k.mask, k.base)), __floats2half2_rn(1032.f, 1032.f));
@@ -192,13 +198,13 @@ struct Bf16Rows {  // x[m][ldx], bf16
 
 // Stage columns [kc0, kc0 + kcn) of MT activation rows into shared memory: fp16
 // pairs in the order a lane consumes them, scaled by a power of two per row so
-// the largest magnitude lands in [2^XLOG2, 2^(XLOG2+1)); for ternary also the
-// negated per-chain sums (even and odd columns) that seed the accumulation
-// chains. Called by every thread of
-// the CTA (NT threads); begins and ends with a CTA barrier.
+// the largest magnitude lands in [2^XLOG2, 2^(XLOG2+1)). bf16 values have 8
+// significant bits, so the scaled values are exact in fp16 down to 2^-17
+// (subnormal spacing 2^-24). Called by every thread of the CTA (NT threads);
+// begins and ends with a CTA barrier.
 template <int FMT, int MT, int NT, class Src>
-__device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, __half2* negs, float (*s_red)[MT],
-                            float* s_xscale, float* s_xinv) {
+__device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, float (*s_red)[MT], float* s_xscale,
+                            float* s_xinv) {
   using F = Fmt<FMT>;
   constexpr int WPB = F::WPB;
   constexpr int JW = F::JW;
@@ -206,7 +212,6 @@ __device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, __half2* 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int nb = kcn / 128;
   const int ngroups = kcn / 8;
   __syncthreads();
 #pragma unroll
@@ -256,104 +261,72 @@ __device__ void stage_chunk(const Src& src, int kcn, int S, uint4* xs, __half2* 
       xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
     }
   }
-  if constexpr (FMT == QMV_TERNARY2) {
-    __syncthreads();
-    // seed q = ((m * S + s) * 8 + block) * (WPB / CW) + chain
-    constexpr int CW = Chain<FMT>::WORDS;
-    constexpr int NCH = WPB / CW;
-    for (int q = tid; q < MT * S * kBlocksPerStep * NCH; q += NT) {
-      const int c = q % NCH;
-      const int m = q / (S * kBlocksPerStep * NCH);
-      const int blk = (q / NCH) % (S * kBlocksPerStep);
-      const int s = blk / kBlocksPerStep, pp = blk % kBlocksPerStep;
-      float se = 0.f, so = 0.f;
-      if (blk < nb) {
-#pragma unroll
-        for (int h = c * CW; h < (c + 1) * CW; ++h)
-#pragma unroll
-          for (int j = 0; j < JW; ++j) {
-            const uint4 pc = xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + pp];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(as_h2(word_of(pc, e)));
-              se += f.x;
-              so += f.y;
-            }
-          }
-      }
-      negs[q] = __floats2half2_rn(-se, -so);
-    }
-  }
   __syncthreads();
 }
 
 // Decode one step (up to 8 blocks) of RQ row quads held in a shared-memory
 // slot and accumulate sum_k w_hat x per row and activation row into accc
-// (fp32, in units of the block scale times the staged activation scale).
-// sb points at the slot plus this lane's block; rows are row_bytes apart.
+// (fp32, in units of the block scale times the staged activation scale; for
+// ternary half of that, since the decode gives q/2). sb points at the slot plus
+// this lane's block; rows are row_bytes apart. The 16-byte activation piece j
+// of word h holds the word's column pairs 4j .. 4j+3, i.e. one chain.
 template <int FMT, int MT, int RQ>
-__device__ __forceinline__ void decode_step(const unsigned char* sb, int row_bytes, const uint4* xs,
-                                            const __half2* negs, int S, int s, int g, int p, const DecodeK& dk,
-                                            const unsigned short (&sc)[RQ], float (&accc)[RQ][MT]) {
+__device__ __forceinline__ void decode_step(const unsigned char* sb, int row_bytes, const uint4* xs, int S, int s,
+                                            int g, int p, const DecodeK& dk, const unsigned short (&sc)[RQ],
+                                            float (&accc)[RQ][MT]) {
   using F = Fmt<FMT>;
   constexpr int WPB = F::WPB;
   constexpr int JW = F::JW;
-  constexpr bool TERN = FMT == QMV_TERNARY2;
+  static_assert(F::PPW == JW * kChainPairs, "one chain per 16-byte activation piece");
   uint4 cw[RQ][WPB / 4];
 #pragma unroll
   for (int r = 0; r < RQ; ++r)
 #pragma unroll
     for (int u = 0; u < WPB / 4; ++u)
       cw[r][u] = *reinterpret_cast<const uint4*>(sb + (r * kGroups + g) * row_bytes + u * 16);
-  constexpr int CW = Chain<FMT>::WORDS;
-  __half2 blk[RQ][MT], ch[RQ][MT];
-  auto seed_of = [&](int m, int h) {
-    return TERN ? negs[(((size_t)m * S + s) * kBlocksPerStep + p) * (WPB / CW) + h / CW] : __floats2half2_rn(0.f, 0.f);
-  };
+  float bsum[RQ][MT];
+#pragma unroll
+  for (int r = 0; r < RQ; ++r)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) bsum[r][m] = 0.f;
   auto xload = [&](int m, int h, int j) { return xs[((((size_t)m * S + s) * WPB + h) * JW + j) * 8 + p]; };
+  // one chain: four exact products summed in fp16, then widened into the block sum
+  auto chain = [&](const __half2 (&v)[kChainPairs], const uint4& xw, float& acc) {
+    __half2 c = __hmul2(v[0], as_h2(xw.x));
+    c = __hfma2(v[1], as_h2(xw.y), c);
+    c = __hfma2(v[2], as_h2(xw.z), c);
+    c = __hfma2(v[3], as_h2(xw.w), c);
+    acc = add_h2_f32(acc, c);
+  };
 #pragma unroll
   for (int h = 0; h < WPB; ++h) {
     if constexpr (RQ == 1) {
       // one row: decode the word once, then stream each activation row through it
       const uint32_t w = word_of(cw[0][h / 4], h % 4);
-      __half2 v[F::PPW];
 #pragma unroll
-      for (int i = 0; i < F::PPW; ++i) v[i] = decode_pair<FMT>(w, i, dk);
+      for (int j = 0; j < JW; ++j) {
+        __half2 v[kChainPairs];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        uint4 xw[JW];
+        for (int i = 0; i < kChainPairs; ++i) v[i] = decode_pair<FMT>(w, j * kChainPairs + i, dk);
 #pragma unroll
-        for (int j = 0; j < JW; ++j) xw[j] = xload(m, h, j);
-        if (h % CW == 0) ch[0][m] = seed_of(m, h);
-#pragma unroll
-        for (int i = 0; i < F::PPW; ++i) ch[0][m] = __hfma2(v[i], as_h2(word_of(xw[i / 4], i % 4)), ch[0][m]);
-        if (h % CW == CW - 1) blk[0][m] = h == CW - 1 ? ch[0][m] : __hadd2(blk[0][m], ch[0][m]);
+        for (int m = 0; m < MT; ++m) chain(v, xload(m, h, j), bsum[0][m]);
       }
     } else {
       // several rows share each activation load
-      uint4 xw[MT][JW];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
+      for (int j = 0; j < JW; ++j) {
+        uint4 xw[MT];
 #pragma unroll
-        for (int j = 0; j < JW; ++j) xw[m][j] = xload(m, h, j);
-        if (h % CW == 0) {
-          const __half2 seed = seed_of(m, h);
+        for (int m = 0; m < MT; ++m) xw[m] = xload(m, h, j);
 #pragma unroll
-          for (int r = 0; r < RQ; ++r) ch[r][m] = seed;
+        for (int r = 0; r < RQ; ++r) {
+          const uint32_t w = word_of(cw[r][h / 4], h % 4);
+          __half2 v[kChainPairs];
+#pragma unroll
+          for (int i = 0; i < kChainPairs; ++i) v[i] = decode_pair<FMT>(w, j * kChainPairs + i, dk);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) chain(v, xw[m], bsum[r][m]);
         }
-      }
-#pragma unroll
-      for (int r = 0; r < RQ; ++r) {
-        const uint32_t w = word_of(cw[r][h / 4], h % 4);
-#pragma unroll
-        for (int i = 0; i < F::PPW; ++i) {
-          const __half2 v = decode_pair<FMT>(w, i, dk);
-#pragma unroll
-          for (int m = 0; m < MT; ++m) ch[r][m] = __hfma2(v, as_h2(word_of(xw[m][i / 4], i % 4)), ch[r][m]);
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (h % CW == CW - 1) blk[r][m] = h == CW - 1 ? ch[r][m] : __hadd2(blk[r][m], ch[r][m]);
       }
     }
   }
@@ -361,7 +334,7 @@ __device__ __forceinline__ void decode_step(const unsigned char* sb, int row_byt
   for (int r = 0; r < RQ; ++r) {
     const float scf = __half2float(__ushort_as_half(sc[r]));
 #pragma unroll
-    for (int m = 0; m < MT; ++m) accc[r][m] = fmaf(__low2float(blk[r][m]) + __high2float(blk[r][m]), scf, accc[r][m]);
+    for (int m = 0; m < MT; ++m) accc[r][m] = fmaf(bsum[r][m], scf, accc[r][m]);
   }
 }
 

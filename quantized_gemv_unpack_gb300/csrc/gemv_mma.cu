@@ -3,7 +3,7 @@
 //
 // The per-pair fp16 FMA of the matvec kernel in gemv.cu costs one instruction
 // per activation row, so its time grows with M. Here the decoded weights feed
-// mma.sync.m16n8k16 (fp16 operands, fp32 accumulation) as the A operand
+// mma.sync.m16n8k16 (bf16 operands, fp32 accumulation) as the A operand
 // straight from registers, with the activations as B (n = activation row, one
 // or two n8 tiles): the decode costs the same as for one row and the
 // contraction over M runs on the tensor pipe.
@@ -34,24 +34,29 @@
 // k-slices of a 128-column block are the 32 columns 32t..32t+31 (pair p =
 // columns 32t + 2p, +1): k-slice j takes pair 2j at k = 2t, 2t+1 and pair
 // 2j+1 at k = 2t+8, 2t+9. These 32 columns are two ternary code words (or four
-// INT4 words) of a row, decoded with the fixed shifts of gemv_core.cuh, and the
-// lane's B registers are the activation pairs of the same columns, i.e. 64
-// contiguous bytes of staged x. The 8 rows one code load touches share banks
+// INT4 words) of a row, and the lane's B registers are the activation pairs of
+// the same columns, i.e. 64 contiguous bytes of staged x. The 8 rows one code load touches share banks
 // (rows are 256 or 512 B apart in a slot); those loads stay well below the
 // shared-memory bandwidth.
+//
+// Operands are bf16 (mma.sync m16n8k16, bf16 x bf16 -> fp32). The activations
+// are the caller's bf16 values, copied unchanged into shared memory, so there is
+// no range limit and no rounding before the products. The weights decode to
+// bf16 exactly: ternary codes, shifted to bits 6-7 / 22-23, give
+// (t & 0x00C000C0) ^ 0x3F803F80 = 1 + q/2 (bit 6 is the mantissa MSB, bit 7 the
+// exponent LSB of bf16 1.0), and subtracting 1.0 leaves q/2 (a zero code is an
+// exact 0); INT4 nibbles give (t & 0x000F000F) ^ 0x43084308 = 136 + q (128 plus
+// the offset-binary nibble), and subtracting 136 leaves q. Every product is
+// exact in fp32 and only the fp32 accumulation rounds.
 //
 // Block scales. Each k-slice lies inside one 128-column block, so a warp's
 // eight MMAs of a block accumulate that block; the fp32 result is scaled by
 // the block's fp16 scale of row g / g + 8 (from the scale record in the slot)
-// and added to the running sum. Ternary codes decode to v = 1 + q/2 (see
-// gemv.cu); the accumulator starts at -sum(x) of the block, leaving
-// (1/2) sum q x, and the factor 2 is applied when y is written. INT4 decodes
-// to q exactly.
+// and added to the running sum. Ternary sums carry q/2, so the factor 2 is
+// applied when y is written.
 //
-// Activations are staged per chunk of K as fp16, scaled per row by a power of
-// two (largest magnitude in [2^9, 2^10) for ternary, [2^5, 2^6) for INT4), in
-// 16-byte units whose index is XORed with (row & 7) so that the 32 lanes of a
-// load hit all banks.
+// Activations are staged per chunk of K in 16-byte units whose index is XORed
+// with (row & 7) so that the 32 lanes of a load hit all banks.
 #include <algorithm>
 
 #include "gemv_core.cuh"
@@ -83,12 +88,62 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16 decode constants (kernel parameters, so they live in registers and the
+// shifts keep their unit): mask, base (also the value subtracted), the left
+// shift multipliers 2^6, 2^4, 2^2 and the right shift amounts 2, 4, 6, 8
+// (ternary) or, for INT4, right shifts 4, 8, 12 in r2, r4, r6.
+struct DecodeB {
+  uint32_t mask, base, m6, m4, m2, r2, r4, r6, r8;
+};
+template <int FMT>
+inline void fill_magic_bf16(uint32_t* magic) {
+  const bool tern = FMT == QMV_TERNARY2;
+  magic[0] = tern ? 0x00C000C0u : 0x000F000Fu;
+  magic[1] = tern ? 0x3F803F80u : 0x43084308u;
+  magic[2] = 1u << 6;
+  magic[3] = 1u << 4;
+  magic[4] = 1u << 2;
+  magic[5] = tern ? 2 : 4;
+  magic[6] = tern ? 4 : 8;
+  magic[7] = tern ? 6 : 12;
+  magic[8] = 8;
+  magic[9] = 0;
+}
+__device__ __forceinline__ DecodeB load_decode_b(const uint32_t* m) {
+  return DecodeB{m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], m[8]};
+}
+// Column pair i of code word w as two exact bf16 weights: ternary q/2, INT4 q.
+template <int FMT>
+__device__ __forceinline__ uint32_t decode_pair_bf16(uint32_t w, int i, const DecodeB& k) {
+  uint32_t t;
+  if constexpr (FMT == QMV_TERNARY2) {
+    // pair i's codes at bits 2i..2i+1 and 16+2i..17+2i, moved to bits 6-7 / 22-23
+    switch (i) {
+      case 0: t = mul_lo(w, k.m6); break;
+      case 1: t = mul_lo(w, k.m4); break;
+      case 2: t = mul_lo(w, k.m2); break;
+      case 3: t = w; break;
+      case 4: t = shr_r(w, k.r2); break;
+      case 5: t = shr_r(w, k.r4); break;
+      case 6: t = shr_r(w, k.r6); break;
+      default: t = shr_r(w, k.r8); break;
+    }
+  } else {
+    t = i == 0 ? w : shr_r(w, i == 1 ? k.r2 : (i == 2 ? k.r4 : k.r6));
+  }
+  return sub_bf16x2(and_xor(t, k.mask, k.base), k.base);
+}
 
 __device__ __forceinline__ int find_task_mma(const GemvBatch& b, int tile) {
   int lo = 0, hi = b.n_tasks - 1;
@@ -146,80 +201,16 @@ struct QuadWalk {
   }
 };
 
-// Stage columns [kc0, kc0 + kcn) of the M activation rows (only rows < M are
-// stored; lanes of rows past M read row 0 of their n-tile) and, for ternary,
-// -sum(x) of every 128-column block for rows < MT (0 past M).
-template <int FMT, int MT>
-__device__ void stage_mma(const uint16_t* __restrict__ x, int ldx, int kc0, int kcn, int M, int KCU, uint4* xs,
-                          float* xneg, float (*s_red)[MT], float* s_xinv) {
-  using F = Fmt<FMT>;
+// Stage columns [kc0, kc0 + kcn) of the M activation rows: the bf16 values
+// unchanged, 16-byte unit u of row m at m * KCU + (u ^ (m & 7)).
+__device__ void stage_mma(const uint16_t* __restrict__ x, int ldx, int kc0, int kcn, int M, int KCU, uint4* xs) {
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   constexpr int NT = kMmaWarps * 32;
   const int nu = kcn / 8;  // 16-byte units per row
   bar_consumers();
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    float mx = 0.f;
-    if (m < M)
-      for (int u = tid; u < nu; u += NT) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + kc0 + u * 8);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t w = word_of(raw, e);
-          mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(w & 0xFFFFu)), fabsf(bf16_to_f32(w >> 16))));
-        }
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_red[warp][m] = mx;
-  }
-  bar_consumers();
-  __shared__ float s_xscale[MT];
-  if (tid < MT) {
-    float mx = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w) mx = fmaxf(mx, s_red[w][tid]);
-    int e = 0;
-    if (mx > 0.f && mx <= 3.4e38f) {
-      int ex;
-      frexpf(mx, &ex);
-      e = max(-120, min(120, F::XLOG2 - (ex - 1)));
-    }
-    s_xscale[tid] = exp2i(e);
-    s_xinv[tid] = exp2i(-e);
-  }
-  bar_consumers();
   for (int q = tid; q < M * nu; q += NT) {
     const int m = q / nu, u = q - m * nu;
-    const float sc = s_xscale[m];
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + kc0 + u * 8);
-    uint32_t hv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t w = word_of(raw, e);
-      hv[e] = h2u(__floats2half2_rn(bf16_to_f32(w & 0xFFFFu) * sc, bf16_to_f32(w >> 16) * sc));
-    }
-    xs[(size_t)m * KCU + (u ^ (m & 7))] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-  }
-  if constexpr (FMT == QMV_TERNARY2) {
-    bar_consumers();
-    const int nblk = kcn / 128;
-    for (int q = tid; q < nblk * MT; q += NT) {
-      const int blk = q / MT, m = q - blk * MT;
-      float sum = 0.f;
-      if (m < M)
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint4 v = xs[(size_t)m * KCU + ((blk * 16 + u) ^ (m & 7))];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(as_h2(word_of(v, e)));
-          sum += f.x + f.y;
-        }
-      }
-      xneg[q] = -sum;
-    }
+    xs[(size_t)m * KCU + (u ^ (m & 7))] = *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + kc0 + u * 8);
   }
   bar_consumers();
 }
@@ -241,9 +232,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
   const int KC = b.kc;
   const int KCU = KC / 8;
   uint4* xs = reinterpret_cast<uint4*>(red + kQuads * 2 * 4 * kTileRows * MT);             // [M][KCU]
-  float* xneg = reinterpret_cast<float*>(xs + (size_t)M * KCU);                            // [KC/128][MT]
-  __shared__ float s_red[kMmaWarps][MT];
-  __shared__ float s_xinv[MT];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -291,7 +279,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
   }
 
   const int g = lane >> 2, t = lane & 3;
-  const DecodeK dk = load_decode_k(b.magic);
+  const DecodeB dk = load_decode_b(b.magic);
   const uint16_t* staged_x = nullptr;
   int staged_kc0 = -1, staged_K = -1;
   uint32_t it = 0, tile_no = 0;
@@ -307,7 +295,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     for (int kc0 = 0; kc0 < K; kc0 += KC) {
       const int kcn = min(KC, K - kc0);
       if (T.x != staged_x || kc0 != staged_kc0 || K != staged_K) {
-        stage_mma<FMT, MT>(T.x, T.ldx, kc0, kcn, M, KCU, xs, xneg, s_red, s_xinv);
+        stage_mma(T.x, T.ldx, kc0, kcn, M, KCU, xs);
         staged_x = T.x;
         staged_kc0 = kc0;
         staged_K = K;
@@ -360,14 +348,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                 const uint4 xv = xs[(size_t)m * KCU + ((u0 + v) ^ (m & 7))];
                 xp[4 * v] = xv.x; xp[4 * v + 1] = xv.y; xp[4 * v + 2] = xv.z; xp[4 * v + 3] = xv.w;
               }
-              float d[4];
-              if constexpr (TERN) {
-                // -sum x over the block
-                const float2 xn = *reinterpret_cast<const float2*>(xneg + (size_t)(s * 8 + bk) * MT + n * 8 + 2 * t);
-                d[0] = xn.x; d[1] = xn.y; d[2] = xn.x; d[3] = xn.y;
-              } else {
-                d[0] = d[1] = d[2] = d[3] = 0.f;
-              }
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
               // odd k-slices accumulate apart (two independent MMA chains per block)
               float d2[4] = {0.f, 0.f, 0.f, 0.f};
               // k-slice kk: pairs 2kk and 2kk+1 (columns 32t + 4kk .. +3) of rows g and g+8
@@ -375,10 +356,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
               for (int kk = 0; kk < 8; ++kk) {
                 constexpr int PPW = F::PPW;
                 const int p0 = 2 * kk, p1 = 2 * kk + 1;
-                const uint32_t a[4] = {h2u(decode_pair<FMT>(wg[p0 / PPW], p0 % PPW, dk)),
-                                       h2u(decode_pair<FMT>(wg8[p0 / PPW], p0 % PPW, dk)),
-                                       h2u(decode_pair<FMT>(wg[p1 / PPW], p1 % PPW, dk)),
-                                       h2u(decode_pair<FMT>(wg8[p1 / PPW], p1 % PPW, dk))};
+                const uint32_t a[4] = {decode_pair_bf16<FMT>(wg[p0 / PPW], p0 % PPW, dk),
+                                       decode_pair_bf16<FMT>(wg8[p0 / PPW], p0 % PPW, dk),
+                                       decode_pair_bf16<FMT>(wg[p1 / PPW], p1 % PPW, dk),
+                                       decode_pair_bf16<FMT>(wg8[p1 / PPW], p1 % PPW, dk)};
                 if (kk & 1) mma16816(d2, a, xp[2 * kk], xp[2 * kk + 1]);
                 else mma16816(d, a, xp[2 * kk], xp[2 * kk + 1]);
               }
@@ -420,7 +401,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
             const int row = row0 + r;
             if (row < N && m < M) {
               float* yp = T.y + (size_t)m * T.ldy + row;
-              const float val = kFactor * v * s_xinv[m];
+              const float val = kFactor * v;
               *yp = kc0 == 0 ? val : *yp + val;
             }
           }
@@ -445,9 +426,9 @@ int launch_mma_t(GemvBatch& b, int M, cudaStream_t s) {
   b.n_tiles = tiles;
   b.rows_per_tile = kTileRows;
   const size_t ring = (size_t)kQuads * G::RING * (G::SLOT + 256 + 16) + (size_t)kQuads * 2 * 4 * kTileRows * MT * 4;
-  const size_t budget = kSmemMax - ring - 2048;  // static shared memory (s_red, s_xinv, s_xscale) < 2 KB
-  // per staged column: M fp16 values, and for ternary MT floats per 128 columns
-  const size_t per_col = (size_t)M * 2 + (FMT == QMV_TERNARY2 ? ((size_t)MT * 4 + 127) / 128 : 0);
+  const size_t budget = kSmemMax - ring - 1024;
+  // per staged column: M bf16 values
+  const size_t per_col = (size_t)M * 2;
   int kc = (int)(budget / per_col) / kStep * kStep;
   const int need = (max_K + kStep - 1) / kStep * kStep;
   if (kc > need) kc = need;
@@ -457,8 +438,8 @@ int launch_mma_t(GemvBatch& b, int M, cudaStream_t s) {
   if (kc < max_K && (size_t)max_K * per_col <= budget) kc = max_K;
   if (kc < kStep) return fail(QMV_ERR_UNSUPPORTED, "activation chunk does not fit shared memory for M=%d", M);
   b.kc = kc;
-  const size_t smem = ring + (size_t)M * kc * 2 + (FMT == QMV_TERNARY2 ? (size_t)(kc / 128) * MT * 4 : 0);
-  fill_magic<FMT>(b.magic);
+  const size_t smem = ring + (size_t)M * kc * 2;
+  fill_magic_bf16<FMT>(b.magic);
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   auto kern = gemv_mma_kernel<FMT, NT>;

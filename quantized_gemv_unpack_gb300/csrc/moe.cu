@@ -278,14 +278,13 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
   __shared__ float s_xscale[MT];
   const int S = (K + kStep - 1) / kStep;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw + Ring::RING + Ring::BARS);
-  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 3, p = lane & 7;
   const int nb = K / 128;
   const int nsteps = (nb + kBlocksPerStep - 1) / kBlocksPerStep;
   const int KB = K / 128;
 
-  if (restage) stage_chunk<FMT, MT, W * 32>(src, K, S, xs, negs, s_red, s_xscale, s_xinv);
+  if (restage) stage_chunk<FMT, MT, W * 32>(src, K, S, xs, s_red, s_xscale, s_xinv);
 
   const int SS = (KB + kBlocksPerStep - 1) / kBlocksPerStep;  // scale records per 16-row group
   for (; u < u_end; ++u) {
@@ -320,7 +319,7 @@ __device__ void run_slot(const uint16_t* scales, int N, int K, int tiles, int u,
       mbar_wait(&prod.wfull[slot], (it / kMoeSlots) & 1u, err);
       if (active) {
         const int row_bytes = min(kBlocksPerStep, nb - s * kBlocksPerStep) * G::BLOCK_BYTES;
-        decode_step<FMT, MT, RQ>(prod.wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, negs, S,
+        decode_step<FMT, MT, RQ>(prod.wring + (size_t)slot * G::SLOT + p * G::BLOCK_BYTES, row_bytes, xs, S,
                                  s, g, p, dk, sc, accc);
       }
       __syncwarp();
@@ -480,7 +479,7 @@ template <int MTMAX>
 size_t expert_smem(int64_t K) {
   using Ring = MoeRing<MoeCfg<MTMAX>::W, MoeCfg<MTMAX>::RPW>;
   const int64_t S = (K + kStep - 1) / kStep;
-  return Ring::RING + Ring::BARS + (size_t)MTMAX * S * kStep * 2 + seed_bytes<QMV_TERNARY2>(MTMAX, S);
+  return Ring::RING + Ring::BARS + (size_t)MTMAX * S * kStep * 2;
 }
 
 // The two expert launches for slots of at most MTMAX tokens (MTMAX >= M).

@@ -88,9 +88,10 @@ int run_sparse(const qmv_desc* const* descs, const void* const* ws, const void* 
 
 // From this many activation rows on, the entry points use the tensor-core
 // kernel (unless qmv_desc.flags forces one of the two): the fp16-FMA kernel's
-// cost grows with M; measured on the INT4 layer set and the ternary stack it is
-// ahead only for ternary at M <= 2 (INT4 decodes more words per weight byte, so
-// the tensor-core kernel wins there from M = 1).
-inline int mma_min_m(int format) { return format == QMV_INT4 ? 1 : 3; }
+// cost grows with M; measured on the INT4 layer set, the 4096 x 4096 ternary
+// matrix and the ternary stack it is ahead only for ternary at M = 1 (INT4
+// decodes more words per weight byte, so the tensor-core kernel wins there from
+// M = 1).
+inline int mma_min_m(int format) { return format == QMV_INT4 ? 1 : 2; }
 
 }  // namespace qmv

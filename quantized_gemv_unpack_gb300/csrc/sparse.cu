@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(SparseWarps<MT>::value * 32, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + R::RING);
   const int S = b.kc / kStep;
   uint4* xs = reinterpret_cast<uint4*>(smem_raw + R::RING + R::BARS);
-  __half2* negs = reinterpret_cast<__half2*>(xs + (size_t)MT * S * F::WPB * F::JW * 8);
   __shared__ float s_red[W][MT];
   __shared__ float s_xinv[MT];
   __shared__ float s_xscale[MT];
@@ -175,7 +174,7 @@ __global__ void __launch_bounds__(SparseWarps<MT>::value * 32, 1)
     const int ti = find_sparse_task(b, tile);
     const SparseTask& T = b.t[ti];
     if (T.x != staged_x || T.K != staged_K) {
-      stage_chunk<FMT, MT, W * 32>(Bf16Rows{T.x, T.ldx, 0}, T.K, S, xs, negs, s_red, s_xscale, s_xinv);
+      stage_chunk<FMT, MT, W * 32>(Bf16Rows{T.x, T.ldx, 0}, T.K, S, xs, s_red, s_xscale, s_xinv);
       staged_x = T.x;
       staged_K = T.K;
     }
@@ -213,7 +212,7 @@ __global__ void __launch_bounds__(SparseWarps<MT>::value * 32, 1)
         unsigned short sc[RQ];
 #pragma unroll
         for (int r = 0; r < RQ; ++r) sc[r] = srec[p * 16 + half * RPW + r * kGroups + g];
-        decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, nbk * G::BLOCK_BYTES, xs, negs, S, blk / kBlocksPerStep, g,
+        decode_step<FMT, MT, RQ>(sb + p * G::BLOCK_BYTES, nbk * G::BLOCK_BYTES, xs, S, blk / kBlocksPerStep, g,
                                  blk % kBlocksPerStep, dk, sc, accc);
       }
       __syncwarp();
@@ -252,8 +251,7 @@ int launch_sparse_t(SparseBatch& b, cudaStream_t s) {
   b.rows_per_tile = TILE_ROWS;
   const size_t fixed = SparseRing<RPW, W>::RING + SparseRing<RPW, W>::BARS;
   const int kc = (max_K + kStep - 1) / kStep * kStep;
-  const size_t S = kc / kStep;
-  const size_t smem = fixed + (size_t)MT * kc * 2 + seed_bytes<QMV_TERNARY2>(MT, S);
+  const size_t smem = fixed + (size_t)MT * kc * 2;
   if (smem > kSmemMax - 1024)
     return fail(QMV_ERR_UNSUPPORTED, "sparse ternary: K=%d with M=%d does not fit shared memory in one piece", max_K, MT);
   b.kc = kc;

@@ -17,6 +17,11 @@ Distributions follow the workloads the pages measure on:
   rounding, so that the Wanda norm sees outlier channels ("Cassandra" page,
   section 3.2).
 * MoE router logits: N(0, 1) in float32.
+* outlier activations (parity edge cases): LLM activations carry a few
+  channels far larger than the rest (the "Cassandra" page's calibration scales
+  1 % of the channels by 20); `outlier_case` makes 1 % of the channels 1000x
+  the rest, or one channel 2^24x, with zero weights on those columns in every
+  even row, or spreads magnitudes log-uniformly over a 2^24 range.
 
 Two back ends produce the same distributions from different streams: NumPy
 (PCG64) on the host for sizes the oracle can handle, and torch (Philox) on the
@@ -79,6 +84,42 @@ def calibration_bf16(g: np.random.Generator, rows: int, K: int,
 
 def router_logits(g: np.random.Generator, M: int, E: int) -> np.ndarray:
     return g.standard_normal((M, E), dtype=np.float32)
+
+
+OUTLIER_KINDS = ("channels", "huge", "range")
+
+
+def outlier_activations(g: np.random.Generator, kind: str, M: int, K: int):
+    """float32 activations [M][K] with an extreme range inside each row, and the columns
+    whose weights the caller should zero in some rows (empty for "range").
+
+    "channels": floor(1 % of K) channels (at least one, a seeded permutation) 1000x an
+    N(0, 1) draw; "huge": one channel at +-2^24; "range": sign of an N(0, 1) draw times
+    2^u, u uniform on [-12, 12]."""
+    x = g.standard_normal((M, K)).astype(np.float32)
+    if kind == "channels":
+        ch = np.sort(g.permutation(K)[: max(1, K // 100)])
+        x[:, ch] *= np.float32(1000.0)
+    elif kind == "huge":
+        ch = np.array([int(g.integers(0, K))])
+        x[:, ch] = np.float32(2.0 ** 24) * np.where(g.random((M, 1)) < 0.5, -1, 1).astype(np.float32)
+    elif kind == "range":
+        ch = np.zeros(0, dtype=np.int64)
+        x = (np.sign(x) * np.exp2(g.uniform(-12, 12, size=(M, K)))).astype(np.float32)
+    else:
+        raise ValueError(kind)
+    return x, ch
+
+
+def outlier_case(kind: str, N: int, K: int, M: int, seed: int):
+    """Student-t weights [N][K] (float32) whose outlier columns are 0 in every even row,
+    and `outlier_activations` of that kind as bf16 bits [M][K]."""
+    g = rng(seed)
+    w = student_t4(g, (N, K))
+    x, ch = outlier_activations(g, kind, M, K)
+    if len(ch):
+        w[0::2, :][:, ch] = 0.0
+    return w, to_bf16_bits(x)
 
 
 # ----------------------------------------------------------------------------- torch

@@ -130,6 +130,28 @@ def test_lut_sparse_codes(env):
     _check(y.cpu().numpy(), yr, B, "sparse codes")
 
 
+@pytest.mark.parametrize("kind", ["channels", "huge", "range"])
+@pytest.mark.parametrize("K", [4096, 25600])
+def test_lut_activation_outliers(env, kind, K):
+    """Outlier channels (1000x, or one at 2^24) on columns whose codes are 0 in half of the rows,
+    and a 2^24 range of magnitudes inside one row, at the full K of the stack (5120 / 25600) and
+    of the single 4096 x 4096 matrix: zero codes add exactly 0 to a table entry, so the fp32
+    bound holds."""
+    q, torch, dev = env
+    from oracle import ternary
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    N = 96
+    w, xb = synth.outlier_case(kind, N, K, 1, seed=K + 5)
+    d, p = _pack(q, torch, dev, w)
+    y = torch.full((1, N), float("nan"), device=dev)
+    q.qmv_run_ternary(d, p, _dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
+    qq, _, s16 = ternary.quantize(w)
+    yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
+    _check(y.cpu().numpy(), yr, B, f"{kind} K={K}")
+
+
 def test_lut_invalid_byte_contributes_zero(env):
     """A code byte holding a code 11 adds nothing (its four columns count as 0); qmv_unpack flags it."""
     q, torch, dev = env

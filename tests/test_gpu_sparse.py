@@ -60,6 +60,81 @@ def test_sparse_matvec_matches_oracle(env, N, K, frac, M):
     assert np.all(np.abs(yy - yr) <= RTOL * B), f"worst {np.max(np.abs(yy - yr) / np.maximum(B, 1e-300)):.3e}"
 
 
+def _run_sparse(q, torch, dev, w, xb):
+    from oracle import ternary, ternary_sparse as ts
+    from oracle.matvec import matvec_bf16x
+    M, N = xb.shape[0], w.shape[0]
+    d, packed = _pack_sparse(q, torch, dev, w)
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.full((M, N), float("nan"), device=dev)
+    q.qmv_run_ternary(d, packed, x, y)
+    assert q.qmv_check_status() == 0
+    qs, ss = ts.quantize(w)
+    yr, B = matvec_bf16x(ternary.dequant(qs, ss), xb)
+    return y.cpu().numpy(), yr, B
+
+
+def _check(yy, yr, B, what):
+    err = np.abs(yy.astype(np.float64) - yr)
+    assert np.all(err <= RTOL * B), f"{what}: worst |err|/B = {np.max(err / np.maximum(B, 1e-300)):.3e}"
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_sparse_saturated_blocks(env, M):
+    """Identical codes against identical activations just under a power of two (the fp16 chains'
+    roundings all point the same way), with zero tiles in between."""
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = 48, 1024
+    w = _weights(N, K, 0.3, 77)
+    w[0] = 0.02
+    w[1] = -0.02
+    w[2, : K // 2], w[2, K // 2:] = 0.02, -0.02
+    w[3, 0::2], w[3, 1::2] = 0.02, -0.02
+    x = np.full((M, K), 0.99, np.float32)
+    if M > 1:
+        x[1] = -0.99
+    if M > 2:
+        x[2, 0::2], x[2, 1::2] = 0.99, -0.99
+        x[3] = np.float32(0.99) * np.sign(synth.rng(78).standard_normal(K)).astype(np.float32)
+    yy, yr, B = _run_sparse(q, torch, dev, w, synth.to_bf16_bits(x))
+    assert np.all(np.isfinite(yy))
+    _check(yy, yr, B, f"saturated M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_sparse_one_code_per_block(env, M):
+    """One nonzero code per block of the stored tiles: a zero code must add exactly nothing."""
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = 64, 5120
+    g = synth.rng(4244 + M)
+    w = np.zeros((N, K), np.float32)
+    hit = g.integers(0, 128, size=(N, K // 128)) + 128 * np.arange(K // 128)[None, :]
+    w[np.arange(N)[:, None], hit] = np.float32(0.02) * np.where(g.random((N, K // 128)) < 0.5, -1, 1)
+    w[16:32, 128 * 5:128 * 9] = 0.0                     # a few zero tiles
+    yy, yr, B = _run_sparse(q, torch, dev, w, synth.activations_bf16(g, (M, K)))
+    _check(yy, yr, B, f"one code per block M={M}")
+
+
+@pytest.mark.parametrize("kind", ["channels", "huge", "range"])
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_sparse_activation_outliers(env, kind, M):
+    """Outlier channels on columns whose codes are 0 in half of the rows, and a 2^24 range of
+    magnitudes inside one row, at K = 13824 (the longest K whose activations fit shared memory in
+    one piece at M <= 4) and K = 5120 at M = 8."""
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = 96, (13824 if M <= 4 else 5120)
+    w, xb = synth.outlier_case(kind, N, K, M, seed=31 + M)
+    g = synth.rng(32)
+    zero = g.random(((N + 15) // 16, K // 128)) < 0.2
+    for gi, b in zip(*np.nonzero(zero)):
+        w[16 * gi:16 * gi + 16, 128 * b:128 * b + 128] = 0.0
+    yy, yr, B = _run_sparse(q, torch, dev, w, xb)
+    _check(yy, yr, B, f"{kind} M={M}")
+
+
 def test_sparse_batch_equals_separate_calls(env):
     q, torch, dev = env
     from quantized_gemv_unpack_gb300 import synth
