@@ -353,14 +353,14 @@ class SparseStack(Workload):
     def host_io(self):
         return [self.x_all], [self.y_all]
 
+    def traffic(self):
+        # captured on 3 layers; every layer's stored tiles are read once, so traffic grows with the layer count
+        return captured_traffic("stack-sparse", self.layers / LAYERS)
+
 
 def synth_shapes():
     from quantized_gemv_unpack_gb300 import synth
     return synth.gqa_layer_shapes(HIDDEN, NQ, NKV, HD, INTER)
-
-    def traffic(self):
-        # captured on 3 layers; every layer's stored tiles are read once, so traffic grows with the layer count
-        return captured_traffic("stack-sparse", self.layers / LAYERS)
 
 
 
@@ -473,6 +473,7 @@ class Cassandra(Workload):
         self.name = ("cass-mx-" if mx else "cass-") + ("target" if target else "draft")
         self.dense = N * K * 2
         self.spec_bytes, self.verif_bytes = spec, verif
+        self.stats = None if mx else exponent_statistics(W, buf, self.d)
 
     def config(self):
         if self.mx:
@@ -481,10 +482,13 @@ class Cassandra(Workload):
         else:
             path = "target (speculation + verification, bit-exact rebuild)" if self.target else "draft (speculation only)"
             name = "Cassandra split"
-        return {"workload": f"{name} 14336 x 4096 MLP matrix, {path}, M={self.M}", "M": self.M, "seed": 2,
-                "dense_bf16_bytes": self.dense, "speculation_bytes": self.spec_bytes,
-                "verification_bytes": self.verif_bytes, "n_symbols": self.d.n_symbols,
-                "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
+        c = {"workload": f"{name} 14336 x 4096 MLP matrix, {path}, M={self.M}", "M": self.M, "seed": 2,
+             "dense_bf16_bytes": self.dense, "speculation_bytes": self.spec_bytes,
+             "verification_bytes": self.verif_bytes, "n_symbols": self.d.n_symbols,
+             "l2": f"rotating {self.copies} copies of the packed matrix (>= 3x L2)"}
+        if self.stats:
+            c["kept_exponents"] = self.stats
+        return c
 
     def step(self, i, stream):
         self.fn(self.d, self.ps[i % self.copies], self.x, self.y, None, stream)
@@ -494,6 +498,59 @@ class Cassandra(Workload):
 
     def traffic(self):
         return captured_traffic(f"{self.name} M={self.M}")
+
+
+def exponent_statistics(W, buf, d):
+    """Entropy and mean unary code length (bits) of the kept exponents of a packed Cassandra
+    matrix, next to the figures the "Cassandra" page quotes for trained models (section 3.3).
+    Read from the packed bitmap (section 0) and the original bf16 weights."""
+    import numpy as np
+    N, K = W.shape
+    words = np.frombuffer(buf, dtype=np.uint32, count=N * K // 32, offset=int(d.off[0])).reshape(N, K // 32)
+    keep = ((words[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool).reshape(N, K)
+    E = ((W[keep] >> 7) & 0xFF).astype(np.int64)
+    counts = np.bincount(E, minlength=256)
+    p = counts[counts > 0] / counts.sum()
+    order = np.lexsort((np.arange(256), -counts))          # rank: count descending, then exponent
+    rank = np.empty(256, np.int64)
+    rank[order] = np.arange(256)
+    return {"entropy_bits": float(-(p * np.log2(p)).sum()), "mean_unary_bits": float((rank[E] + 1).mean()),
+            "distinct": int((counts > 0).sum()), "page_trained_models": {"entropy_bits": [2.58, 2.64],
+                                                                         "mean_unary_bits": 2.85}}
+
+
+class CassSpeculate(Cassandra):
+    """One draft-then-verify step on the Cassandra matrix: 4 draft matvecs at M = 1 (speculation
+    data only), then one target pass at M = 5 (1 + 4 draft tokens) over both streams."""
+    name = "cass-speculate"
+    kernel = "cass_kernel (4 draft launches at M = 1 + 1 target launch at M = 5)"
+    N_DRAFT = 4
+
+    def __init__(self, q, torch, dev):
+        super().__init__(q, torch, dev, target=True)
+        self.name = "cass-speculate"
+        self.kernel = CassSpeculate.kernel
+        N, K = 14336, 4096
+        self.yd = torch.empty((self.N_DRAFT, N), device=dev)
+        self.nbytes = (self.N_DRAFT * (self.spec_bytes + K * 2 + N * 4)
+                       + self.spec_bytes + self.verif_bytes + self.M * (K * 2 + N * 4))
+        self.q = q
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("Cassandra split 14336 x 4096 MLP matrix, one self-speculative step: 4 draft matvecs "
+                         "(M=1, speculation data) then one target verification (M=5, both streams)")
+        c["n_draft"] = self.N_DRAFT
+        return c
+
+    def step(self, i, stream):
+        self.q.cass_speculate_step(self.d, self.ps[i % self.copies], self.x, self.yd, self.y, stream)
+
+    def host_io(self):
+        return [self.x], [self.yd, self.y]
+
+    def traffic(self):
+        return None
 
 
 class KvEncode(Workload):
@@ -545,19 +602,25 @@ class Moe(Workload):
     name = "moe"
     kernel = "moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
 
+    _experts = None   # (gen, buffer) shared by the MoE workloads of one process (seed 3)
+
     def __init__(self, q, torch, dev, M=1, n_logits=64):
         from quantized_gemv_unpack_gb300 import synth
         E, H, I, topk = 128, 4096, 2048, 8
-        gen = synth.torch_generator(3, dev)
         self.gu = q.qmv_pack_desc(q.QMV_TERNARY2, 2 * I, H)
         self.dn = q.qmv_pack_desc(q.QMV_TERNARY2, H, I)
         self.down_off = self.gu.total_bytes
         self.stride = self.down_off + self.dn.total_bytes
-        self.buf = torch.empty(E * self.stride, dtype=torch.uint8, device=dev)
-        for e in range(E):
-            rec = self.buf[e * self.stride:(e + 1) * self.stride]
-            q.qmv_pack_ternary(self.gu, synth.student_t4_torch(gen, (2 * I, H), device=dev), rec[:self.down_off])
-            q.qmv_pack_ternary(self.dn, synth.student_t4_torch(gen, (H, I), device=dev), rec[self.down_off:])
+        if Moe._experts is None:
+            gen = synth.torch_generator(3, dev)
+            buf = torch.empty(E * self.stride, dtype=torch.uint8, device=dev)
+            for e in range(E):
+                rec = buf[e * self.stride:(e + 1) * self.stride]
+                q.qmv_pack_ternary(self.gu, synth.student_t4_torch(gen, (2 * I, H), device=dev), rec[:self.down_off])
+                q.qmv_pack_ternary(self.dn, synth.student_t4_torch(gen, (H, I), device=dev), rec[self.down_off:])
+            Moe._experts = (gen, buf)
+        self.buf = Moe._experts[1]
+        gen = synth.torch_generator(30 + M, dev)
         self.logits = [synth.router_logits_torch(gen, M, E, device=dev) for _ in range(n_logits)]
         self.active = [len(set(torch.topk(lg, topk, dim=1).indices.flatten().tolist())) for lg in self.logits]
         self.x = synth.activations_bf16_torch(gen, (M, H), device=dev)
@@ -601,6 +664,8 @@ def make_workload(name, q, torch, dev, a):
                            layout=(a.layout or "record") if (a.M or 1) == 1 else "record")
     if name == "int4-layer":
         return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
+    if name == "cass-speculate":
+        return CassSpeculate(q, torch, dev)
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
         return Cassandra(q, torch, dev, target=name.endswith("target"), mx="-mx-" in name)
     if name == "moe":
@@ -624,6 +689,65 @@ def job_throughput(bytes_per_step_per_rank: float, ms_per_step: float, world: in
     return bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9 * world
 
 
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(wl, steps, warmup, stream, torch):
+    """Mean device time (ms) of `steps` steps after `warmup` untimed ones, CUDA events on `stream`."""
+    for i in range(warmup):
+        wl.step(i, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        wl.step(i, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+CONFIGS = [  # (key, workload, M): the other four configurations, each on its own workload
+    ("cfg1 ternary 4096x4096 M=1", "ternary-4096", 1),
+    ("cfg2 INT4 GQA layer set M=1", "int4-layer", 1),
+    ("cfg2 INT4 GQA layer set M=4", "int4-layer", 4),
+    ("cfg3 Cassandra draft M=1", "cass-draft", 1),
+    ("cfg3 Cassandra target M=5", "cass-target", 5),
+    ("cfg3 Cassandra 4 drafts + verify M=5", "cass-speculate", 5),
+    ("cfg4 MoE 128 experts top-8 M=1", "moe", 1),
+    ("cfg4 MoE 128 experts top-8 M=2", "moe", 2),
+    ("cfg4 MoE 128 experts top-8 M=4", "moe", 4),
+    ("cfg4 MoE 128 experts top-8 M=8", "moe", 8),
+]
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measure_configs(q, torch, dev, stream, steps, warmup, peak):
+    """Every other configuration, measured in this process under one clock record: time per step,
+    GB/s on the algorithmic bytes, fractions of the measured copy peak and of the nominal 8 TB/s,
+    and the ncu DRAM traffic per step where a current capture exists."""
+    out = {}
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    for key, name, M in CONFIGS:
+        args = argparse.Namespace(M=M, path="auto", layout=None, layers=LAYERS)
+        wl = make_workload(name, q, torch, dev, args)
+        ms = time_steps(wl, steps, warmup, stream, torch)
+        nb = sum(wl.bytes(i) for i in range(steps)) / steps
+        gbs = nb / (ms * 1e-3) / 1e9
+        out[key] = {"us_per_step": ms * 1e3, "GB_s": gbs, "frac_of_measured_copy": gbs / peak,
+                    "frac_of_nominal_8TB_s": gbs / NOMINAL_HBM_GBS, "algorithmic_bytes_per_step": nb,
+                    "traffic": wl.traffic(), "kernel": wl.kernel, "workload": wl.config()["workload"]}
+        if name.startswith("cass"):
+            st = wl.config().get("kept_exponents")
+            if st:
+                out[key]["kept_exponents"] = st
+        del wl
+        torch.cuda.empty_cache()
+    assert q.qmv_check_status() == 0
+    out["clocks"] = clocks.stop()
+    out["steps_each"] = steps
+    return out
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -634,7 +758,7 @@ def main():
     ap.add_argument("--impl", default="qmv", choices=["qmv", "reference"])
     ap.add_argument("--workload", default="stack",
                     choices=["stack", "stack-sparse", "ternary-4096", "int4-layer", "cass-draft", "cass-target",
-                             "cass-mx-draft", "cass-mx-target", "kv-encode", "moe"])
+                             "cass-mx-draft", "cass-mx-target", "cass-speculate", "kv-encode", "moe"])
     ap.add_argument("--M", type=int, default=0, help="activation rows (int4-layer, ternary-4096, moe)")
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
@@ -642,6 +766,8 @@ def main():
                     help="ternary at M = 1: byte-lookup layout or row-group records (default: lookup for the "
                          "stack, records for the single 4096 x 4096 matrix, where the record kernel is ahead)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload only: skip measuring the other configurations in the same run")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     a = ap.parse_args()
@@ -746,10 +872,14 @@ def main():
         dist.destroy_process_group()
         return
     peak, peak_kind = peaks()
+    configs = None
+    if a.workload == "stack" and not a.no_configs:
+        configs = measure_configs(q, torch, dev, stream, steps=20, warmup=3, peak=peak)
     per_gpu = job_throughput(nbytes, ms, 1)
     fma_split = 1 if ((a.M or 1) <= 8 or "mma" in wl.kernel) else 2   # fp16-FMA launches cover 8 rows each
     launches = {"stack": 1, "stack-sparse": 1, "ternary-4096": fma_split, "int4-layer": fma_split, "cass-draft": 1,
-                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "kv-encode": 1, "moe": 2}[a.workload]
+                "cass-target": 1, "cass-mx-draft": 1, "cass-mx-target": 1, "cass-speculate": 5, "kv-encode": 1,
+                "moe": 2}[a.workload]
     line = {
         "metric": METRIC, "value": per_gpu * world, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -767,6 +897,8 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if configs is not None:
+        line["configs"] = configs
     if wl.tok_s:
         line["tok_s"] = 1000.0 / ms * world
     print(json.dumps(line))

@@ -159,6 +159,15 @@ typedef struct {
  */
 #define QMV_FLAG_PATH_FMA 1u
 #define QMV_FLAG_PATH_MMA 2u
+/*
+ * Testing only (ternary/INT4 matvec): the kernel's first wait is on a barrier
+ * that nothing completes, limited to 1 ms, before any copy is issued. The wait
+ * gives up, the kernel records QMV_ERR_TIMEOUT in the device error word and
+ * ends without writing y, and qmv_check_status returns QMV_ERR_TIMEOUT. It
+ * shows how a lost copy is reported without making the GPU fault. Any other
+ * unknown flag bit is QMV_ERR_ARG.
+ */
+#define QMV_FLAG_TEST_WAIT_TIMEOUT 0x100u
 
 /* One matvec of a batch: y[M][ldy] = W x[M][ldx] for the matrix packed in w. */
 typedef struct {
@@ -315,6 +324,25 @@ int cass_decode_draft(const qmv_desc* desc, const void* packed, const void* x_bf
  */
 int cass_reconstruct(const qmv_desc* desc, const void* packed, const void* x_bf16, int M,
                      int64_t ldx, float* y, int64_t ldy, uint16_t* w_out, void* stream);
+
+/*
+ * One draft-then-verify step of self-speculative decoding on one Cassandra
+ * matrix ("Cassandra", section 2 and 3.2 figures b and c: draft tokens come from
+ * the speculation data alone, then one target pass over speculation and
+ * verification data checks the current token and every draft token at once).
+ * Activation row 0 of x is the current token, rows 1..n_draft the draft tokens.
+ * Issues, in stream order, n_draft draft matvecs at M = 1 (y_draft[d] = W_draft
+ * x[d] for d < n_draft: draft token d + 1 is produced from row d) and then one
+ * target matvec at M = n_draft + 1 (y_target[m] = W x[m], W the original
+ * bf16 weights rebuilt bit for bit). x: device bf16 [n_draft + 1][ldx];
+ * y_draft: device fp32 [n_draft][ldy]; y_target: device fp32
+ * [n_draft + 1][ldy]; the two must not overlap. 1 <= n_draft <= 7 (the
+ * "Nemotron 3.5 Bolt" drafts are 7 tokens long). QMV_CASS or QMV_CASS_MX.
+ * Every argument is checked before the first launch; errors as
+ * cass_decode_draft.
+ */
+int cass_speculate_step(const qmv_desc* desc, const void* packed, const void* x_bf16, int n_draft, int64_t ldx,
+                        float* y_draft, float* y_target, int64_t ldy, void* stream);
 
 /*
  * Mixture-of-experts decode over ternary SwiGLU experts ("Nemotron 3.5 Bolt",

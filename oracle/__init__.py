@@ -23,7 +23,8 @@ division, round-half-even), written from the pages' definitions:
 * ``layout``    - the packed byte layout of each format, written from its
                   specification (section offsets, bit positions).
 
-Pins live in ``tests/test_oracle_*.py``. Parity unpinned: the exponent entropy
-and mean unary code length statistics (``cassandra.exponent_stats``) are only
-reported, as the pages' figures come from trained models.
+Pins live in ``tests/test_oracle_*.py``. Every function has one; the exponent
+entropy and mean unary code length (``cassandra.exponent_stats``) are pinned by
+closed forms and the source-coding bound (the pages' own figures for them come
+from trained models and are quoted as context only).
 """

@@ -244,8 +244,9 @@ def verification_bytes(meta) -> int:
 def exponent_stats(E_kept: np.ndarray):
     """(Shannon entropy in bits, mean unary code length in bits) of the kept exponents.
 
-    Reported only ("Cassandra" 3.3 quotes 2.58-2.64 bit entropy and a 2.85 bit mean
-    for trained models); parity unpinned.
+    "Cassandra" 3.3 quotes 2.58-2.64 bit entropy and a 2.85 bit mean for trained
+    models. Pinned by closed forms (uniform, {2, 1, 1}, single symbol, a dyadic
+    distribution) and the source-coding bound mean >= entropy.
     """
     _, rank_of, counts = exponent_codebook(E_kept)
     p = counts[counts > 0] / counts.sum()

@@ -24,11 +24,12 @@ QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
 QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
 QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX, QMV_TERNARY2_SPARSE, QMV_TERNARY2_LUT = 1, 2, 3, 4, 5, 6
 QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-FMA or the tensor-core matvec kernel
+QMV_FLAG_TEST_WAIT_TIMEOUT = 0x100           # qmv_desc.flags, testing only: the matvec's first wait gives up
 
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
            "qmv_run_int4", "qmv_run_batch", "qmv_sparse_pack_host", "cass_pack_host", "cass_mx_pack_host", "cass_kv_encode", "cass_decode_draft", "cass_reconstruct",
-           "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
+           "cass_speculate_step", "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
 
 
 class QmvError(RuntimeError):
@@ -73,6 +74,7 @@ _SIGS = {
     "cass_kv_encode": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _DESC, _P, _I64, _P]),
     "cass_decode_draft": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
     "cass_reconstruct": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _I64, _P, _P]),
+    "cass_speculate_step": (_I32, [_DESC, _P, _P, _I32, _I64, _P, _P, _I64, _P]),
     "moe_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I64, _I64]),
     "moe_qmv_run": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P,
                            ctypes.c_size_t, _P]),
@@ -261,6 +263,18 @@ def cass_reconstruct(desc: qmv_desc, packed, x, y=None, w_out=None, stream=None)
     ldy = _rows(y)[1] if y is not None else 0
     _check(lib().cass_reconstruct(ctypes.byref(desc), _ptr(packed), _ptr(x), M, ldx, _ptr(y), ldy,
                                   _ptr(w_out), _stream(stream)))
+
+
+def cass_speculate_step(desc: qmv_desc, packed, x, y_draft, y_target, stream=None):
+    """x: bf16 [n_draft + 1][ldx] (row 0 the current token); y_draft [n_draft][ldy]; y_target
+    [n_draft + 1][ldy] with the same ldy."""
+    M, ldx = _rows(x)
+    nd, ldy = _rows(y_draft)
+    mt, ldy2 = _rows(y_target)
+    if nd != M - 1 or mt != M or ldy2 != ldy:
+        raise ValueError("x must have n_draft + 1 rows, y_draft n_draft and y_target n_draft + 1, one ldy")
+    _check(lib().cass_speculate_step(ctypes.byref(desc), _ptr(packed), _ptr(x), nd, ldx, _ptr(y_draft),
+                                     _ptr(y_target), ldy, _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- MoE

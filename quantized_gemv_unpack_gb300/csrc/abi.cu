@@ -182,6 +182,9 @@ int run_tasks(int format, GemvTask* tasks, int n, int M, uint64_t flags, cudaStr
   static thread_local GemvBatch b;
   const uint64_t path = flags & (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA);
   if (path == (QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA)) return fail(QMV_ERR_ARG, "both QMV_FLAG_PATH_FMA and _MMA set");
+  if (flags & ~(uint64_t)(QMV_FLAG_PATH_FMA | QMV_FLAG_PATH_MMA | QMV_FLAG_TEST_WAIT_TIMEOUT))
+    return fail(QMV_ERR_ARG, "unknown qmv_desc.flags bits 0x%llx", (unsigned long long)flags);
+  b.test_wait_us = (flags & QMV_FLAG_TEST_WAIT_TIMEOUT) ? 1000u : 0u;
   if (path == QMV_FLAG_PATH_MMA || (path == 0 && M >= mma_min_m(format))) {
     for (int i = 0; i < n; ++i) b.t[i] = tasks[i];
     b.n_tasks = n;
@@ -344,7 +347,8 @@ int qmv_check_status(void* stream, int32_t* device_code) {
     if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
   }
   if (device_code) *device_code = v;
-  if (v) return fail(v, "a kernel reported status %d (corrupt packed data)", v);
+  if (v) return fail(v, "a kernel reported status %d (%s)", v,
+                     v == QMV_ERR_TIMEOUT ? "a bounded device wait gave up" : "corrupt packed data");
   return QMV_OK;
 }
 

@@ -958,8 +958,9 @@ int check_cassmx_desc(const qmv_desc* d) {
   return QMV_OK;
 }
 
-int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, int M, int64_t ldx, float* y,
-             int64_t ldy, uint16_t* w_out, void* stream) {
+// Argument checks shared by the draft, target and draft-then-verify calls.
+int check_cass_call(const qmv_desc* d, const void* packed, const void* x, int M, int64_t ldx, const float* y,
+                    int64_t ldy, const uint16_t* w_out) {
   if (!d) return fail(QMV_ERR_ARG, "desc is NULL");
   const bool mx = d->abi_version == QMV_ABI_VERSION && d->format == QMV_CASS_MX;
   int rc = mx ? check_cassmx_desc(d) : check_cass_desc(d);
@@ -969,7 +970,16 @@ int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, 
   if (!aligned16(packed) || !aligned16(x) || (y && !aligned16(y)) || (w_out && !aligned16(w_out)))
     return fail(QMV_ERR_ALIGN, "buffers must be 16-byte aligned");
   if (ldx < d->K || (y && ldy < d->N)) return fail(QMV_ERR_ARG, "ldx < K or ldy < N");
+  if (ldx % 8) return fail(QMV_ERR_ALIGN, "ldx=%lld must be a multiple of 8 (16-byte rows)", (long long)ldx);
   if (ldx > INT32_MAX || ldy > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "leading dimension too large");
+  return QMV_OK;
+}
+
+int run_cass(bool target, const qmv_desc* d, const void* packed, const void* x, int M, int64_t ldx, float* y,
+             int64_t ldy, uint16_t* w_out, void* stream) {
+  int rc = check_cass_call(d, packed, x, M, ldx, y, ldy, w_out);
+  if (rc) return rc;
+  const bool mx = d->format == QMV_CASS_MX;
   int* err = device_error_word();
   if (!err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
   const char* b = static_cast<const char*>(packed);
@@ -1283,6 +1293,26 @@ int cass_decode_draft(const qmv_desc* desc, const void* packed, const void* x_bf
 int cass_reconstruct(const qmv_desc* desc, const void* packed, const void* x_bf16, int M, int64_t ldx, float* y,
                      int64_t ldy, uint16_t* w_out, void* stream) {
   return run_cass(true, desc, packed, x_bf16, M, ldx, y, ldy, w_out, stream);
+}
+
+int cass_speculate_step(const qmv_desc* desc, const void* packed, const void* x_bf16, int n_draft, int64_t ldx,
+                        float* y_draft, float* y_target, int64_t ldy, void* stream) {
+  if (n_draft < 1 || n_draft > 7) return fail(QMV_ERR_ARG, "n_draft=%d outside 1..7", n_draft);
+  if (!y_draft || !y_target) return fail(QMV_ERR_ARG, "NULL y_draft or y_target");
+  // all arguments are checked before the first launch
+  int rc = check_cass_call(desc, packed, x_bf16, n_draft + 1, ldx, y_target, ldy, nullptr);
+  if (rc) return rc;
+  if (!aligned16(y_draft)) return fail(QMV_ERR_ALIGN, "y_draft must be 16-byte aligned");
+  if (y_draft + (size_t)(n_draft - 1) * ldy + desc->N > y_target && y_target + (size_t)n_draft * ldy + desc->N > y_draft)
+    return fail(QMV_ERR_ARG, "y_draft and y_target overlap");
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  // the draft tokens in order: draft token d is produced from activation row d
+  for (int d = 0; d < n_draft; ++d) {
+    rc = run_cass(false, desc, packed, x + (size_t)d * ldx, 1, ldx, y_draft + (size_t)d * ldy, ldy, nullptr, stream);
+    if (rc) return rc;
+  }
+  // one target pass verifies the current token and all draft tokens
+  return run_cass(true, desc, packed, x, n_draft + 1, ldx, y_target, ldy, nullptr, stream);
 }
 
 }  // extern "C"

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kernel(const __grid_constant__
   unsigned char* wring = ring + (size_t)warp * kSlots * R::SLOT;
   uint64_t* wfull = full + warp * kSlots;
 
+  if (b.test_wait_us && test_wait_times_out(b.err, b.test_wait_us)) return;
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&wfull[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

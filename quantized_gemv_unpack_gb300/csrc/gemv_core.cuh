@@ -147,20 +147,36 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Bounded wait: false (and QMV_ERR_TIMEOUT in the device error word) if the
-// phase does not complete within kWaitNs. Once the error word holds a timeout,
+// phase does not complete within limit_ns. Once the error word holds a timeout,
 // later waits give up after a few hundred polls, so a launch that lost a
 // barrier ends quickly instead of timing out wait after wait.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t polls = 1;; ++polls) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((polls & 255u) == 0u &&
-        (global_ns() - t0 > kWaitNs || *reinterpret_cast<volatile int*>(err) == (int)QMV_ERR_TIMEOUT))
+        (global_ns() - t0 > limit_ns || *reinterpret_cast<volatile int*>(err) == (int)QMV_ERR_TIMEOUT))
       break;
   }
   atomicCAS(err, 0, (int)QMV_ERR_TIMEOUT);
   return false;
+}
+// Testing hook (QMV_FLAG_TEST_WAIT_TIMEOUT): before any copy is issued, thread
+// 0 waits on a barrier that nothing completes, with a limit of `us`
+// microseconds, so the wait gives up and records QMV_ERR_TIMEOUT; true means
+// the kernel must return at once (nothing is in flight). Called by every
+// thread of the CTA.
+__device__ __forceinline__ bool test_wait_times_out(int* err, uint32_t us) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int gave_up;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    gave_up = mbar_wait(&bar, 0u, err, (uint64_t)us * 1000ull) ? 0 : 1;
+  }
+  __syncthreads();
+  return gave_up != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
   uint64_t* qempty = empty + quad * R;
   float* qred = red + (size_t)quad * 2 * 4 * kTileRows * MT;
 
+  if (b.test_wait_us && test_wait_times_out(b.err, b.test_wait_us)) return;
   if (tid < kQuads * R) {
     mbar_init(&full[tid], 1);
     mbar_init(&empty[tid], 4);

@@ -62,7 +62,9 @@ struct GemvBatch {
   int32_t kc;              // activation chunk staged in shared memory (elements)
   int32_t rows_per_tile;
   int32_t n_ctas;
-  int32_t pad0;
+  // testing only (QMV_FLAG_TEST_WAIT_TIMEOUT): > 0 makes the kernel's first
+  // wait one that nothing completes, limited to this many microseconds
+  uint32_t test_wait_us;
   // CTA c processes the contiguous tile range [cta_tile[c], cta_tile[c+1]),
   // cut so every CTA streams about the same number of bytes
   int32_t cta_tile[kMaxCtas + 1];

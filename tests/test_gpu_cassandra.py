@@ -193,3 +193,57 @@ def test_corrupt_streams_are_reported(env):
     # the untouched buffer is clean
     q.cass_decode_draft(d, _dev(torch, buf, dev), x, y)
     assert q.qmv_check_status() == 0
+
+
+@pytest.mark.parametrize("mx", [False, True])
+@pytest.mark.parametrize("n_draft", [1, 4, 7])
+def test_speculate_step_draft_then_verify(env, mx, n_draft):
+    """One self-speculative step ("Cassandra" 2, 3.2 figures b and c): n_draft draft matvecs at
+    M = 1 from the speculation data, then one target pass at M = n_draft + 1. The draft outputs
+    match the draft matvec of the oracle's draft weights, and the verification output matches
+    the dense bf16 matvec of the original weights (Cassandra-1: lossless rebuild) or of the
+    oracle's MX target values (Cassandra-2), each within the bound."""
+    q, torch, dev = env
+    from oracle import cassandra as cs
+    from oracle import cassandra_mx as cmx
+    from oracle.matvec import matvec_bf16x
+    from oracle.numerics import bf16_bits_to_f64
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(900 + n_draft)
+    N, K = 200, 1024
+    W = synth.to_bf16_bits(synth.student_t4(g, (N, K)))
+    X, _ = synth.calibration_bf16(g, 128, K)
+    d, buf = (q.cass_mx_pack_host if mx else q.cass_pack_host)(W, X)
+    packed = _dev(torch, buf, dev)
+    xb = synth.activations_bf16(g, (n_draft + 1, K))
+    x = _bf16(torch, xb, dev)
+    yd = torch.full((n_draft, N), float("nan"), device=dev)
+    yt = torch.full((n_draft + 1, N), float("nan"), device=dev)
+    q.cass_speculate_step(d, packed, x, yd, yt)
+    assert q.qmv_check_status() == 0
+    if mx:
+        ref, meta = cmx.pack(W, X)
+        w_draft, w_target = bf16_bits_to_f64(cmx.draft(ref, meta)), bf16_bits_to_f64(cmx.reconstruct(ref, meta))
+    else:
+        ref, meta = cs.pack(W, X)
+        w_draft, w_target = bf16_bits_to_f64(cs.draft(ref, meta)), bf16_bits_to_f64(W)
+    yr, B = matvec_bf16x(w_draft, xb[:n_draft])
+    assert np.all(np.abs(yd.cpu().numpy() - yr) <= RTOL * B)
+    yr, B = matvec_bf16x(w_target, xb)
+    assert np.all(np.abs(yt.cpu().numpy() - yr) <= RTOL * B)
+
+
+def test_speculate_step_rejects_bad_arguments(env):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(5)
+    W = synth.to_bf16_bits(synth.student_t4(g, (16, 256)))
+    X, _ = synth.calibration_bf16(g, 16, 256)
+    d, buf = q.cass_pack_host(W, X)
+    packed = _dev(torch, buf, dev)
+    x = torch.zeros((9, 256), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(q.QmvError):                      # n_draft = 8 > 7
+        q.cass_speculate_step(d, packed, x, torch.zeros((8, 16), device=dev), torch.zeros((9, 16), device=dev))
+    y = torch.zeros((9, 16), device=dev)
+    with pytest.raises(q.QmvError):                      # y_draft overlaps y_target
+        q.cass_speculate_step(d, packed, x[:5], y[1:5], y[0:5])

@@ -352,3 +352,45 @@ def test_smaller_launch_does_not_break_a_larger_one(env, path):
         qq, _, s16 = int4.quantize(w)
         yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
         _check_bound(y.cpu().numpy(), yr, B, f"K={w.shape[1]}")
+
+
+@pytest.mark.parametrize("path", ["fma", "mma"])
+def test_bounded_wait_timeout_is_reported(env, path):
+    """QMV_FLAG_TEST_WAIT_TIMEOUT makes the kernel's first wait one that nothing completes (1 ms
+    limit): the call returns, y is left unwritten, qmv_check_status reports QMV_ERR_TIMEOUT once,
+    and the next clean call on the same context gives 0 and the oracle's result."""
+    q, torch, dev = env
+    from oracle import ternary
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(606)
+    N, K, M = 64, 2048, 1
+    w = synth.student_t4(g, (N, K))
+    xb = synth.activations_bf16(g, (M, K))
+    d, packed = _pack(q, torch, dev, "ternary", w, path)
+    x = _to_dev_bf16(torch, xb, dev)
+    d.flags |= q.QMV_FLAG_TEST_WAIT_TIMEOUT
+    y = torch.full((M, N), float("nan"), device=dev)
+    q.qmv_run_ternary(d, packed, x, y)
+    code = q.qmv_check_status()
+    assert code == q.QMV_ERR_TIMEOUT
+    assert torch.isnan(y).all()                          # the kernel gave up before writing
+    assert q.qmv_check_status() == 0                     # the word was cleared
+    d.flags &= ~q.QMV_FLAG_TEST_WAIT_TIMEOUT
+    q.qmv_run_ternary(d, packed, x, y)
+    assert q.qmv_check_status() == 0
+    qq, _, s16 = ternary.quantize(w)
+    yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
+    _check_bound(y.cpu().numpy(), yr, B, f"after timeout {path}")
+
+
+def test_unknown_flag_bits_are_rejected(env):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    w = synth.student_t4(synth.rng(607), (16, 256))
+    d, packed = _pack(q, torch, dev, "int4", w)
+    d.flags = 0x40
+    x = torch.zeros((1, 256), dtype=torch.bfloat16, device=dev)
+    y = torch.zeros((1, 16), device=dev)
+    with pytest.raises(q.QmvError):
+        q.qmv_run_int4(d, packed, x, y)

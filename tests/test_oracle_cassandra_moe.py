@@ -145,6 +145,42 @@ def test_corrupt_stream_is_rejected():
 
 # ----------------------------------------------------------------------------- MoE
 
+def test_exponent_stats_closed_forms():
+    """Entropy and mean unary length of the kept exponents ("Cassandra" 3.3) on distributions
+    whose values follow from the definitions: four equally frequent exponents give H = 2 bit and
+    ranks 0..3, i.e. codes of 1..4 bits, mean 2.5; counts {2, 1, 1} give H = 1.5 bit and lengths
+    1 (twice), 2, 3 (equal counts: smaller exponent first), mean 7/4; one exponent gives H = 0 and
+    the one-bit code."""
+    from oracle import cassandra as c
+    H, L = c.exponent_stats(np.array([120, 121, 122, 123] * 5, dtype=np.uint8))
+    assert H == pytest.approx(2.0, abs=1e-12) and L == pytest.approx(2.5, abs=1e-12)
+    H, L = c.exponent_stats(np.array([130, 127, 127, 125], dtype=np.uint8))
+    assert H == pytest.approx(1.5, abs=1e-12) and L == pytest.approx(1.75, abs=1e-12)
+    # which of the two single exponents gets rank 1 does not change the mean, but the order does:
+    _, rank_of, _ = c.exponent_codebook(np.array([130, 127, 127, 125], dtype=np.uint8))
+    assert (rank_of[127], rank_of[125], rank_of[130]) == (0, 1, 2)
+    H, L = c.exponent_stats(np.full(7, 126, dtype=np.uint8))
+    assert H == 0.0 and L == 1.0
+
+
+def test_exponent_stats_source_coding_bound():
+    """The unary code of the frequency rank is a prefix code, so its mean length is at least the
+    entropy (source coding theorem); for a dyadic geometric distribution p_r = 2^-(r+1) the bound
+    is met with equality except for the last symbol, which needs one bit more than the tail."""
+    from oracle import cassandra as c
+    g = np.random.default_rng(5)
+    for _ in range(20):
+        E = g.choice(np.arange(110, 140), size=500, p=g.dirichlet(np.ones(30)))
+        H, L = c.exponent_stats(E.astype(np.uint8))
+        assert L >= H - 1e-12
+    counts = [16, 8, 4, 2, 1, 1]                       # p = 1/2, 1/4, 1/8, 1/16, 1/32, 1/32
+    E = np.concatenate([np.full(n, 120 + i) for i, n in enumerate(counts)]).astype(np.uint8)
+    H, L = c.exponent_stats(E)
+    assert H == pytest.approx(1 / 2 + 2 / 4 + 3 / 8 + 4 / 16 + 2 * 5 / 32, abs=1e-12)
+    assert L == pytest.approx((16 * 1 + 8 * 2 + 4 * 3 + 2 * 4 + 5 + 6) / 32, abs=1e-12)
+    assert L - H == pytest.approx(1 / 32, abs=1e-12)
+
+
 def test_route_matches_brute_force_and_ties():
     g = synth.rng(8)
     L = synth.router_logits(g, 5, 16)
