@@ -392,6 +392,46 @@ int moe_qmv_run_static(const qmv_desc* gateup_desc, const qmv_desc* down_desc, c
                        const void* x_bf16, int M, int64_t ldx, float* y, int64_t ldy, void* stream);
 
 /*
+ * Packed-weight files ("Ternary Bonsai 2", section 3.6: the packed indices,
+ * scales and flags are exported as the file that inference loads). A file
+ * holds named packed matrices of any format above, each with its qmv_desc and
+ * a CRC-32 per section (reflected polynomial 0xEDB88320, as zip), behind a
+ * versioned header whose own fields and entry table carry CRC-32s too; the byte
+ * layout is described in the library source (file.cu). Tensors start on 4096-byte
+ * boundaries. Host-side calls; only qmv_file_load touches the GPU.
+ *
+ * qmv_file_write: names[i] (NUL-terminated, < QMV_FILE_NAME_BYTES bytes,
+ *   unique), descs[i] and buffers[i] (host, descs[i].total_bytes bytes) of n
+ *   tensors; the descriptors' flags are stored as 0. Overwrites `path`.
+ * qmv_file_open: maps the file read-only and checks magic, version, header and
+ *   table CRCs and that every entry lies inside the file with a valid
+ *   descriptor (QMV_ERR_CORRUPT otherwise; QMV_ERR_UNSUPPORTED for a newer
+ *   version). *out is freed by qmv_file_close.
+ * qmv_file_tensor: name (nullable, QMV_FILE_NAME_BYTES bytes) and descriptor
+ *   (nullable) of tensor `index`; qmv_file_find: the index of a name, or
+ *   QMV_ERR_ARG if absent.
+ * qmv_file_load: checks the CRC of every section of tensor `index` on the host
+ *   (QMV_ERR_CORRUPT on a mismatch, nothing copied), then copies the packed
+ *   buffer into `dst` (device, caller-owned, >= desc.total_bytes bytes,
+ *   16-byte aligned) on `stream`. When the call returns the source bytes are
+ *   staged, so the file may be closed while the copy is in flight.
+ * qmv_file_read_host: the same check, then a copy into host memory.
+ * qmv_crc32: CRC-32 of n bytes continuing from `crc` (0 to start).
+ */
+#define QMV_FILE_NAME_BYTES 64
+typedef struct qmv_file qmv_file;
+int qmv_file_write(const char* path, int n, const char* const* names, const qmv_desc* descs,
+                   const void* const* buffers);
+int qmv_file_open(const char* path, qmv_file** out);
+int qmv_file_count(const qmv_file* f);
+int qmv_file_tensor(const qmv_file* f, int index, char* name, qmv_desc* desc);
+int qmv_file_find(const qmv_file* f, const char* name);
+int qmv_file_load(const qmv_file* f, int index, void* dst, int64_t capacity, void* stream);
+int qmv_file_read_host(const qmv_file* f, int index, void* dst, int64_t capacity);
+void qmv_file_close(qmv_file* f);
+uint32_t qmv_crc32(const void* data, size_t n, uint32_t crc);
+
+/*
  * Synchronize `stream`, then read and clear the current device's error word.
  * *device_code (nullable) receives 0 or a qmv_status the kernels recorded.
  * Returns QMV_ERR_CUDA if the synchronization failed, else the recorded status.

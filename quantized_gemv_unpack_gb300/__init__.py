@@ -29,7 +29,9 @@ QMV_FLAG_TEST_WAIT_TIMEOUT = 0x100           # qmv_desc.flags, testing only: the
 # the exported C symbols (one per declaration in include/qmv.h)
 EXPORTS = ("qmv_pack_desc", "qmv_pack_ternary", "qmv_pack_int4", "qmv_unpack", "qmv_run_ternary",
            "qmv_run_int4", "qmv_run_batch", "qmv_sparse_pack_host", "cass_pack_host", "cass_mx_pack_host", "cass_kv_encode", "cass_decode_draft", "cass_reconstruct",
-           "cass_speculate_step", "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static", "qmv_check_status", "qmv_last_error")
+           "cass_speculate_step", "moe_workspace_size", "moe_qmv_run", "moe_qmv_run_static",
+           "qmv_file_write", "qmv_file_open", "qmv_file_count", "qmv_file_tensor", "qmv_file_find", "qmv_file_load",
+           "qmv_file_read_host", "qmv_file_close", "qmv_crc32", "qmv_check_status", "qmv_last_error")
 
 
 class QmvError(RuntimeError):
@@ -79,6 +81,15 @@ _SIGS = {
     "moe_qmv_run": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P,
                            ctypes.c_size_t, _P]),
     "moe_qmv_run_static": (_I32, [_DESC, _DESC, _P, _I64, _I64, _I32, _P, _I32, _P, _I32, _I64, _P, _I64, _P]),
+    "qmv_file_write": (_I32, [ctypes.c_char_p, _I32, ctypes.POINTER(ctypes.c_char_p), _DESC, ctypes.POINTER(_P)]),
+    "qmv_file_open": (_I32, [ctypes.c_char_p, ctypes.POINTER(_P)]),
+    "qmv_file_count": (_I32, [_P]),
+    "qmv_file_tensor": (_I32, [_P, _I32, ctypes.c_char_p, _DESC]),
+    "qmv_file_find": (_I32, [_P, ctypes.c_char_p]),
+    "qmv_file_load": (_I32, [_P, _I32, _P, _I64, _P]),
+    "qmv_file_read_host": (_I32, [_P, _I32, _P, _I64]),
+    "qmv_file_close": (None, [_P]),
+    "qmv_crc32": (ctypes.c_uint32, [_P, ctypes.c_size_t, ctypes.c_uint32]),
     "qmv_check_status": (_I32, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "qmv_last_error": (ctypes.c_char_p, []),
 }
@@ -308,6 +319,78 @@ def moe_qmv_run_static(gateup_desc: qmv_desc, down_desc: qmv_desc, experts, expe
 
 
 # ----------------------------------------------------------------------------- status
+
+# ----------------------------------------------------------------------------- packed-weight files
+
+QMV_FILE_NAME_BYTES = 64
+
+
+def qmv_crc32(data, crc: int = 0) -> int:
+    """CRC-32 (zip polynomial) of a bytes-like object or a host NumPy array."""
+    import numpy as np
+    a = np.ascontiguousarray(np.frombuffer(data, dtype=np.uint8) if isinstance(data, (bytes, bytearray)) else data)
+    return int(lib().qmv_crc32(_ptr(a), a.nbytes, crc))
+
+
+def qmv_file_write(path: str, items):
+    """items: [(name, qmv_desc, host buffer of desc.total_bytes bytes: NumPy array or CPU tensor)]."""
+    n = len(items)
+    names = (ctypes.c_char_p * n)(*[nm.encode() for nm, _, _ in items])
+    descs = (qmv_desc * n)(*[d for _, d, _ in items])
+    for _, d, b in items:
+        nb = b.nbytes if hasattr(b, "nbytes") else b.numel() * b.element_size()
+        if nb < d.total_bytes:
+            raise ValueError("buffer smaller than desc.total_bytes")
+        if hasattr(b, "is_cuda") and b.is_cuda:
+            raise ValueError("qmv_file_write takes host buffers")
+    bufs = (_P * n)(*[_ptr(b) for _, _, b in items])
+    _check(lib().qmv_file_write(path.encode(), n, names, descs, bufs))
+
+
+class QmvFile:
+    """An open packed-weight file (qmv_file_open ... qmv_file_close)."""
+
+    def __init__(self, path: str):
+        h = _P()
+        _check(lib().qmv_file_open(path.encode(), ctypes.byref(h)))
+        self._h = h
+
+    def __len__(self):
+        return int(lib().qmv_file_count(self._h))
+
+    def tensor(self, index: int):
+        """(name, qmv_desc) of tensor `index`."""
+        name = ctypes.create_string_buffer(QMV_FILE_NAME_BYTES)
+        d = qmv_desc()
+        _check(lib().qmv_file_tensor(self._h, index, name, ctypes.byref(d)))
+        return name.value.decode(), d
+
+    def find(self, name: str) -> int:
+        i = lib().qmv_file_find(self._h, name.encode())
+        if i < 0:
+            _check(i)
+        return int(i)
+
+    def load(self, index: int, dst, stream=None):
+        """Copy tensor `index` (CRC-checked) into the device buffer dst."""
+        nb = dst.numel() * dst.element_size()
+        _check(lib().qmv_file_load(self._h, index, _ptr(dst), nb, _stream(stream)))
+
+    def read_host(self, index: int, dst):
+        nb = dst.nbytes if hasattr(dst, "nbytes") else dst.numel() * dst.element_size()
+        _check(lib().qmv_file_read_host(self._h, index, _ptr(dst), nb))
+
+    def close(self):
+        if self._h:
+            lib().qmv_file_close(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
 
 def qmv_check_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device error word; raises on CUDA failure."""
