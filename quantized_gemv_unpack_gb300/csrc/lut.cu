@@ -9,20 +9,23 @@
 //     T[e][c] = sum_{i<4} q_i(e) * x[128 b + 4 c + i]     (c = 0..31 column groups)
 // in fp32 in shared memory; then every row's block costs one lookup per byte:
 // 32 lookups, added in pairs by packed fp32x2 adds, and one multiply by the
-// block's scale. The table has a row of 64 four-byte slots per e (slot c and
-// slot c + 32 hold the same value), so the address of T[e][c] for the lane
-// that owns row n at byte position t is base + e*256 + 4*(n%32) + 4*t with
-// c = (t + n) % 32: one byte permute builds e*256 + 4*(n%32) from the code
-// word and the lane's offset, and 4*t is the load's immediate offset. The
-// packer rotates each row's 32 code bytes by n % 32 to match, so at every
-// position t the 32 lanes of a warp read 32 distinct banks (no conflicts).
+// block's scale. The table has a 256-byte row per e, of which the first 32
+// four-byte slots hold T[e][0..31]. The packer rotates each row's 32 code bytes
+// by n % 32 (position t holds column group (t + n) % 32), so the lane that owns
+// row n reads position t at slot (lane + t) mod 32: at every t the 32 lanes of
+// a warp read 32 distinct banks (no conflicts). One byte permute builds the
+// address e*256 + 4*((lane + t) mod 32) from the code word and a register whose
+// bytes hold the lane's wrapped offsets of four consecutive positions (lane
+// offsets plus 16 per code word, masked to 0..124: no carries between bytes).
 // Rows of invalid bytes (a code 11) are zeroed once per launch and never
 // rebuilt, so such a byte contributes 0.
 //
 // Occupancy. A CTA is 8 warps with 72 KB of shared memory (the table and the
 // cluster partial sums) and 80 registers per thread, so three CTAs share an
 // SM: their per-block barriers and table builds fall at different times and
-// the lookups of one CTA fill the shared-memory pipe while another builds.
+// the lookups of one CTA fill the shared-memory pipe while another builds. One
+// slot per entry (rather than a second copy at slot c + 32 to avoid the wrap)
+// halves the table stores, which share the L1 data path with the lookups.
 //
 // Work split. A unit is up to 1024 rows of one matvec (unit_rows) over all of
 // its blocks (a cluster of C CTAs splits the blocks, each CTA a contiguous
@@ -171,7 +174,7 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
 
 __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant__ LutBatch b) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // the table: 256 rows (code byte e) of 64 four-byte slots, then the partial sums
+  // the table: 256 rows (code byte e) of 256 bytes (slots 0..31 used), then the partial sums
   const uint32_t T0 = smem_u32(smem_raw);
   if (b.smem_bytes < kSmemL) {  // a launch without room for both: report, compute nothing
     if (threadIdx.x == 0) atomicCAS(b.err, 0, (int)QMV_ERR_UNSUPPORTED);
@@ -180,7 +183,8 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   const uint32_t part = T0 + kTableBytes;     // [2][kRpt][kThreadsL] fp32
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const uint32_t L = (uint32_t)(lane * 4);
+  // byte j of L0: 4 lane + 4 j (at most 136, so adding 16 k to every byte never carries)
+  const uint32_t L0 = (uint32_t)(4 * lane) * 0x01010101u + 0x0C080400u;
   const uint32_t C = cluster_size();
   const uint32_t rank = cluster_rank();
   const int worker = (int)cluster_id();
@@ -279,7 +283,6 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
       const float v = (code_val(d0, x0) + code_val(d1, x1)) + p23;
       const uint32_t a = tb + (uint32_t)((d0 + 4 * d1 + 16 * d2 + 64 * d3) * 256 + 4 * g);
       sts_f32(a, v);
-      sts_f32(a + 128u, v);
     };
     {
       const int d2 = warp % 3, d3 = warp / 3;
@@ -292,27 +295,19 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     if (warp == 0) put(2, 2, 2, 2, p23);
   };
   // one row's block: 32 lookups and adds, times the block's scale, into acc
-  auto row_block = [&](const Item& it, float& a) {
+  auto row_block = [&](const Item& it, float& a, uint32_t tb) {
     const uint32_t w[8] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w, it.hi.x, it.hi.y, it.hi.z, it.hi.w};
     uint64_t s2 = 0;  // two partial sums (even and odd positions)
 #pragma unroll
     for (int t = 0; t < 32; t += 2) {
-      // result bytes: lane offset, code byte t, 0, 0; plus the table base
-      const uint32_t a0 = prmt(w[t >> 2], L, 0x7604u | ((uint32_t)(t & 3) << 4)) + T0;
-      const uint32_t a1 = prmt(w[(t + 1) >> 2], L, 0x7604u | ((uint32_t)((t + 1) & 3) << 4)) + T0;
-      float v0, v1;
-      switch (t) {
-#define QMV_LUT_CASE(T) \
-  case T:               \
-    v0 = lds_at<4 * T>(a0); \
-    v1 = lds_at<4 * (T + 1)>(a1); \
-    break;
-        QMV_LUT_CASE(0) QMV_LUT_CASE(2) QMV_LUT_CASE(4) QMV_LUT_CASE(6)
-        QMV_LUT_CASE(8) QMV_LUT_CASE(10) QMV_LUT_CASE(12) QMV_LUT_CASE(14)
-        QMV_LUT_CASE(16) QMV_LUT_CASE(18) QMV_LUT_CASE(20) QMV_LUT_CASE(22)
-        QMV_LUT_CASE(24) QMV_LUT_CASE(26) QMV_LUT_CASE(28) QMV_LUT_CASE(30)
-#undef QMV_LUT_CASE
-      }
+      // result bytes: wrapped lane offset, code byte t, 0, 0; plus the table base
+      const uint32_t j0 = (uint32_t)(t & 3), j1 = (uint32_t)((t + 1) & 3);
+      // byte j of Lk: (4 lane + 4 (4k + j)) mod 128, the wrapped slot offset of position 4k + j
+      const uint32_t Lk = (L0 + (uint32_t)(t >> 2) * 0x10101010u) & 0x7C7C7C7Cu;
+      const uint32_t a0 = prmt(w[t >> 2], Lk, (4u + j0) | (j0 << 4) | ((12u + j0) << 8) | ((12u + j0) << 12)) + tb;
+      const uint32_t a1 = prmt(w[(t + 1) >> 2], Lk, (4u + j1) | (j1 << 4) | ((12u + j1) << 8) | ((12u + j1) << 12)) + tb;
+      const float v0 = lds_at<0>(a0);
+      const float v1 = lds_at<0>(a1);
       s2 = add2_f32(s2, v0, v1);
     }
     a = fmaf(sum2_f32(s2), __half2float(__ushort_as_half((unsigned short)it.s)), a);
@@ -320,18 +315,18 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   // this thread's rows of a step (all four in a full unit, else the rows of this
   // warp's 32-row groups that the unit has); right after a row's block, its
   // register slot is reloaded with the same slot of the next step
-  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Src& n) {
+  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Src& n, uint32_t tb) {
     if (s.nrows32() == kUnitRowsMax) {
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) {
-        row_block(it[j], acc[j]);
+        row_block(it[j], acc[j], tb);
         load_item(n, j, it[j]);
       }
     } else {
       const int n32 = s.nrows32() - (tid & ~31);
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) {
-        if (j * kThreadsL < n32) row_block(it[j], acc[j]);
+        if (j * kThreadsL < n32) row_block(it[j], acc[j], tb);
         load_item(n, j, it[j]);
       }
     }
@@ -397,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
     __syncthreads();  // the table is complete
-    lookups(cur, A, src_of(nxt));
+    lookups(cur, A, src_of(nxt), T0);
     if (!nxt.valid || nxt.k != cur.k) finish(cur);
     cur = nxt;
     nxt = nn;
