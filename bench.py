@@ -602,23 +602,32 @@ class Moe(Workload):
     name = "moe"
     kernel = "moe_expert_kernel<gate|up> + moe_expert_kernel<down> (one step, timed together)"
 
-    _experts = None   # (gen, buffer) shared by the MoE workloads of one process (seed 3)
+    _experts = None   # (layout, buffer) shared by the MoE workloads of one process (seed 3)
 
-    def __init__(self, q, torch, dev, M=1, n_logits=64):
+    @staticmethod
+    def kernel_name(layout):
+        return ("lut_kernel<gate|up> + lut_kernel<down> (byte-lookup experts, one step, timed together)"
+                if layout == "lut" else None)
+
+    def __init__(self, q, torch, dev, M=1, n_logits=64, layout="lut"):
         from quantized_gemv_unpack_gb300 import synth
         E, H, I, topk = 128, 4096, 2048, 8
-        self.gu = q.qmv_pack_desc(q.QMV_TERNARY2, 2 * I, H)
-        self.dn = q.qmv_pack_desc(q.QMV_TERNARY2, H, I)
+        fmt = q.QMV_TERNARY2_LUT if layout == "lut" else q.QMV_TERNARY2
+        self.gu = q.qmv_pack_desc(fmt, 2 * I, H)
+        self.dn = q.qmv_pack_desc(fmt, H, I)
         self.down_off = self.gu.total_bytes
         self.stride = self.down_off + self.dn.total_bytes
-        if Moe._experts is None:
+        self.layout = layout
+        if self.kernel_name(layout):
+            self.kernel = self.kernel_name(layout)
+        if Moe._experts is None or Moe._experts[0] != layout:
             gen = synth.torch_generator(3, dev)
             buf = torch.empty(E * self.stride, dtype=torch.uint8, device=dev)
             for e in range(E):
                 rec = buf[e * self.stride:(e + 1) * self.stride]
                 q.qmv_pack_ternary(self.gu, synth.student_t4_torch(gen, (2 * I, H), device=dev), rec[:self.down_off])
                 q.qmv_pack_ternary(self.dn, synth.student_t4_torch(gen, (H, I), device=dev), rec[self.down_off:])
-            Moe._experts = (gen, buf)
+            Moe._experts = (layout, buf)
         self.buf = Moe._experts[1]
         gen = synth.torch_generator(30 + M, dev)
         self.logits = [synth.router_logits_torch(gen, M, E, device=dev) for _ in range(n_logits)]
@@ -632,7 +641,7 @@ class Moe(Workload):
 
     def config(self):
         return {"workload": f"MoE decode, 128 ternary SwiGLU experts (hidden 4096, 2048), top-8 softmax, M={self.M}",
-                "M": self.M, "seed": 3, "mean_active_experts": sum(self.active) / len(self.active),
+                "M": self.M, "seed": 3, "layout": self.layout, "mean_active_experts": sum(self.active) / len(self.active),
                 "l2": f"router logits rotate over {len(self.logits)} draws; experts total "
                       f"{self.E * self.stride / 1e6:.0f} MB (> L2)"}
 
@@ -648,7 +657,7 @@ class Moe(Workload):
 
     def traffic(self):
         # the capture is of the first timed step (logits draw 0): scale to the mean active expert count
-        t = captured_traffic(f"moe M={self.M}")
+        t = captured_traffic(f"moe M={self.M}" + (" lut" if self.layout == "lut" else ""))
         return None if t is None else t * (sum(self.active) / len(self.active)) / self.active[0]
 
 
@@ -669,7 +678,7 @@ def make_workload(name, q, torch, dev, a):
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
         return Cassandra(q, torch, dev, target=name.endswith("target"), mx="-mx-" in name)
     if name == "moe":
-        return Moe(q, torch, dev, a.M or 1)
+        return Moe(q, torch, dev, a.M or 1, layout=a.layout or "lut")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -763,8 +772,9 @@ def main():
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
     ap.add_argument("--layout", default=None, choices=["lut", "record"],
-                    help="ternary at M = 1: byte-lookup layout or row-group records (default: lookup for the "
-                         "stack, records for the single 4096 x 4096 matrix, where the record kernel is ahead)")
+                    help="ternary at M = 1 and MoE experts: byte-lookup layout or row-group records (default: lookup "
+                         "for the stack and the MoE experts, records for the single 4096 x 4096 matrix, where the "
+                         "record kernel is ahead)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="default workload only: skip measuring the other configurations in the same run")

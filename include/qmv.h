@@ -353,7 +353,11 @@ int cass_speculate_step(const qmv_desc* desc, const void* packed, const void* x_
  * experts: device; expert e's record starts at experts + e * expert_stride and
  * holds the packed [gate; up] matrix (2I x H, described by gateup_desc, rows
  * 0..I-1 gate and I..2I-1 up) followed, at byte offset down_off, by the packed
- * down matrix (H x I, down_desc). Both ternary. logits: device fp32 [M][E].
+ * down matrix (H x I, down_desc). Both ternary, in one layout: QMV_TERNARY2
+ * (row-group records; fp16-FMA expert kernels, one slot per active expert with
+ * all its tokens) or QMV_TERNARY2_LUT (byte-lookup layout; the lookup kernel, one
+ * task per (token, expert) pair, H and I multiples of 128; y is added into in a
+ * run-dependent order, within the same bound). logits: device fp32 [M][E].
  * x_bf16: device [M][ldx]; y: device fp32 [M][ldy], overwritten.
  * workspace: device, >= moe_workspace_size(E, topk, M, H, I) bytes.
  * 1 <= topk <= 8, topk <= E <= 256, M in 1..8.

@@ -35,18 +35,32 @@
 // launch parameters. Each of the 256 threads owns up to four rows of a unit
 // (rows r0 + 256 j + tid); lane = row % 32.
 //
+// MoE experts (lut_kernel<1>, <2>): the same kernel runs the gate|up and the down
+// phase of the MoE decode over experts in this layout ("Nemotron 3.5 Bolt",
+// expert top-K routing). Every CTA routes the tokens in shared memory; task i is
+// the i-th (token, expert) pair in expert order, whose codes are its expert's
+// matrix, whose activations are its token's x (gate|up) or h = silu(g) * u of
+// its own gate|up outputs (down), and whose output goes to the workspace
+// (gate|up) or is added, times the pair's routing weight, into y by fp32
+// atomics (down). The down launch is a programmatic dependent of the gate|up
+// launch: it routes, loads its first weights and asks L2 for the rest while
+// gate|up runs, and waits for it before reading g and u.
+//
 // Streaming. The codes of (block, 32-row group) are 1 KB records, rows of a
 // unit contiguous per block, so a thread's row is two coalesced 16-byte loads.
 // Right after a row's lookups its registers are reloaded with the same row slot
 // of the next step, and one thread asks the copy engine to prefetch the step
-// after next into L2 (cp.async.bulk.prefetch), so those loads hit L2. No wait
-// in this kernel spins: it synchronizes only with CTA and cluster barriers.
+// after next into L2 (cp.async.bulk.prefetch), so those loads hit L2; a launch
+// whose weights fit half of L2 asks for all of a CTA's steps at its start. No
+// wait in this kernel spins: it synchronizes only with CTA and cluster barriers
+// and the dependent-launch wait.
 #include <algorithm>
 #include <cstring>
 #include <queue>
 #include <vector>
 
 #include "lut.cuh"
+#include "moe_route.cuh"
 
 namespace qmv {
 namespace {
@@ -69,11 +83,28 @@ struct LutTask {
   int32_t N, NG, KB, unit0;    // NG 32-row groups, KB blocks, first unit of this task
 };
 
+// The MoE expert phases (lut_kernel<1> gate|up, lut_kernel<2> down): task i is
+// the i-th (token, expert) pair of the routing each CTA computes, its codes are
+// expert e's matrix at codes + e * stride, and its activations and outputs are
+// found from the pair.
+struct LutMoe {
+  MoeRouting routing;          // logits [M][E], E, topk, M
+  const uint16_t* x;           // bf16 [M][ldx]
+  float* y;                    // fp32 [M][ldy]: zeroed by gate|up, added into by down
+  float* gu;                   // workspace: g (rows 0..I-1) and u (I..2I-1) of pair i at i * 2I
+  unsigned char* ws;           // workspace base: gate|up's CTA 0 leaves the routing there
+  int64_t off_slot_expert, off_slot_first, off_slot_count, off_pair_token, off_pair_prob;
+  int64_t stride;              // bytes between experts' records
+  int32_t I, H, ldx, ldy;
+};
+
 struct LutBatch {
   int32_t n_tasks, n_units, unit_rows, n_workers;
   int32_t sched_n;             // 0: unit u goes to worker u % n_workers
   uint32_t smem_bytes;         // dynamic shared memory of the launch
+  int32_t prefetch_all;        // 1: each CTA asks L2 for all of its steps at its start (small launches)
   int* err;
+  LutMoe moe;
   uint16_t sched_off[kMaxWorkersL + 1];
   uint16_t sched[kMaxUnitsL];
   LutTask t[kMaxTasks];
@@ -172,8 +203,16 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
   return lo;
 }
 
+__device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
+
+
+// PHASE 0: the tasks' matvecs; 1 / 2: the MoE gate|up / down phase (see LutMoe).
+template <int PHASE>
 __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant__ LutBatch b) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // the down phase may start on SMs the gate|up grid frees; it waits for that
+  // grid's g, u and zeroed y before reading them
+  if (PHASE == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the table: 256 rows (code byte e) of 256 bytes (slots 0..31 used), then the partial sums
   const uint32_t T0 = smem_u32(smem_raw);
   if (b.smem_bytes < kSmemL) {  // a launch without room for both: report, compute nothing
@@ -189,11 +228,43 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   const uint32_t rank = cluster_rank();
   const int worker = (int)cluster_id();
 
-  // zero the table rows of invalid code bytes (any 2-bit field equal to 3)
-  for (int i = tid; i < 256 * 64; i += kThreadsL) {
-    const int e = i >> 6;
-    if ((e & (e >> 1)) & 0x55) sts_f32(T0 + 4u * (uint32_t)i, 0.f);
+  // MoE phases: the routing of the M tokens, in shared memory (every CTA gets the
+  // same result), and the expert of each pair
+  MoeRoute* R = nullptr;
+  int* pair_expert = nullptr;
+  if constexpr (PHASE > 0) {
+    __shared__ MoeRoute s_route;
+    __shared__ int s_pair_expert[kMaxPairs];
+    R = &s_route;
+    pair_expert = s_pair_expert;
+    route(b.moe.routing, *R);
+    for (int sl = tid; sl < R->n_slots; sl += kThreadsL)
+      for (int j = R->slot_first[sl]; j < R->slot_first[sl] + R->slot_count[sl]; ++j) pair_expert[j] = R->slot_expert[sl];
+    if constexpr (PHASE == 1) {
+      const LutMoe& mo = b.moe;
+      for (int i = blockIdx.x * kThreadsL + tid; i < mo.routing.M * mo.H; i += gridDim.x * kThreadsL)
+        mo.y[(size_t)(i / mo.H) * mo.ldy + i % mo.H] = 0.f;
+      if (blockIdx.x == 0) {  // the routing, for inspection, in the workspace layout
+        const int np = mo.routing.M * mo.routing.topk;
+        for (int i = tid; i < np; i += kThreadsL) {
+          reinterpret_cast<int*>(mo.ws + mo.off_pair_token)[i] = R->pair_token[i];
+          reinterpret_cast<float*>(mo.ws + mo.off_pair_prob)[i] = R->pair_prob[i];
+        }
+        for (int i = tid; i < R->n_slots; i += kThreadsL) {
+          reinterpret_cast<int*>(mo.ws + mo.off_slot_expert)[i] = R->slot_expert[i];
+          reinterpret_cast<int*>(mo.ws + mo.off_slot_first)[i] = R->slot_first[i];
+          reinterpret_cast<int*>(mo.ws + mo.off_slot_count)[i] = R->slot_count[i];
+        }
+        if (tid == 0) *reinterpret_cast<int*>(mo.ws) = R->n_slots;
+      }
+    }
+    __syncthreads();
   }
+  // the codes of task ti (MoE: of its pair's expert)
+  auto codes_of = [&](int ti) -> const unsigned char* {
+    if constexpr (PHASE == 0) return b.t[ti].codes;
+    else return b.t[ti].codes + (size_t)pair_expert[ti] * (size_t)b.moe.stride;
+  };
 
   // this worker's units
   int k_end, k_beg;
@@ -228,10 +299,11 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   auto prefetch_step = [&](const Step& s) {
     if (!s.valid) return;
     const LutTask& T = b.t[s.ti];
+    const unsigned char* codes = codes_of(s.ti);
     const int g0 = s.r0 >> 5;
     const int ng = s.nrows32() >> 5;
-    l2_prefetch(T.codes + ((size_t)s.bk * T.NG + g0) * 1024, (uint32_t)ng * 1024u);
-    const uint16_t* sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024);
+    l2_prefetch(codes + ((size_t)s.bk * T.NG + g0) * 1024, (uint32_t)ng * 1024u);
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * 1024);
     l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
   };
   // This thread's load addresses of a step: row r0 + tid of its codes and of
@@ -249,8 +321,9 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     r.n32 = 0;
     if (!s.valid) return r;
     const LutTask& T = b.t[s.ti];
-    r.cw = reinterpret_cast<const uint4*>(T.codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
-    r.sc = reinterpret_cast<const uint16_t*>(T.codes + (size_t)T.NG * T.KB * 1024) + (size_t)s.bk * T.NG * 32 + s.r0 +
+    const unsigned char* codes = codes_of(s.ti);
+    r.cw = reinterpret_cast<const uint4*>(codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
+    r.sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * 1024) + (size_t)s.bk * T.NG * 32 + s.r0 +
            tid;
     r.n32 = s.nrows32() - (tid & ~31);
     return r;
@@ -265,9 +338,20 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   // the code bytes whose high digit pair (d2, d3) is hi = w (w < 8, nine bytes),
   // and of hi = 8 the byte with low pair lo = w (warp 0 also lo = 8)
   const int g = lane, warp = tid >> 5;
-  auto load_x = [&](const Step& s) -> uint2 {
-    if (s.valid) return *reinterpret_cast<const uint2*>(b.t[s.ti].x + (size_t)s.bk * 128 + 4 * g);
-    return make_uint2(0u, 0u);
+  // activations 4g .. 4g+3 of a step's block (MoE down: h = silu(g) * u of the pair)
+  auto load_x = [&](const Step& s) -> float4 {
+    if (!s.valid) return make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (PHASE == 2) {
+      const float* gr = b.moe.gu + (size_t)s.ti * 2 * b.moe.I + (size_t)s.bk * 128 + 4 * g;
+      const float4 gg = *reinterpret_cast<const float4*>(gr);
+      const float4 uu = *reinterpret_cast<const float4*>(gr + b.moe.I);
+      return make_float4(silu(gg.x) * uu.x, silu(gg.y) * uu.y, silu(gg.z) * uu.z, silu(gg.w) * uu.w);
+    } else {
+      const uint16_t* xr = PHASE == 0 ? b.t[s.ti].x : b.moe.x + (size_t)R->pair_token[s.ti] * b.moe.ldx;
+      const uint2 xw = *reinterpret_cast<const uint2*>(xr + (size_t)s.bk * 128 + 4 * g);
+      return make_float4(__uint_as_float(xw.x << 16), __uint_as_float(xw.x & 0xFFFF0000u),
+                         __uint_as_float(xw.y << 16), __uint_as_float(xw.y & 0xFFFF0000u));
+    }
   };
 
   float acc[kRpt];
@@ -276,9 +360,8 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   int parity = 0;
 
   // the table of a step's block, from its x, into the table at tb
-  auto build = [&](uint2 xw, uint32_t tb) {
-    const float x0 = __uint_as_float(xw.x << 16), x1 = __uint_as_float(xw.x & 0xFFFF0000u);
-    const float x2 = __uint_as_float(xw.y << 16), x3 = __uint_as_float(xw.y & 0xFFFF0000u);
+  auto build = [&](float4 xv, uint32_t tb) {
+    const float x0 = xv.x, x1 = xv.y, x2 = xv.z, x3 = xv.w;
     auto put = [&](int d0, int d1, int d2, int d3, float p23) {
       const float v = (code_val(d0, x0) + code_val(d1, x1)) + p23;
       const uint32_t a = tb + (uint32_t)((d0 + 4 * d1 + 16 * d2 + 64 * d3) * 256 + 4 * g);
@@ -333,13 +416,17 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   };
   // the unit of s is complete in this CTA: write y (C == 1) or add the
   // cluster's partial sums in rank order (rank 0 writes)
+  auto store = [&](const Step& s, int row, float v) {
+    if constexpr (PHASE == 0) b.t[s.ti].y[row] = v;
+    else if constexpr (PHASE == 1) b.moe.gu[(size_t)s.ti * 2 * b.moe.I + row] = v;
+    else atomicAdd(b.moe.y + (size_t)R->pair_token[s.ti] * b.moe.ldy + row, R->pair_prob[s.ti] * v);
+  };
   auto finish = [&](const Step& s) {
-    const LutTask& T = b.t[s.ti];
     if (C == 1) {
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) {
         const int row = s.r0 + j * kThreadsL + tid;
-        if (j * kThreadsL + tid < s.nrows) T.y[row] = acc[j];
+        if (j * kThreadsL + tid < s.nrows) store(s, row, acc[j]);
       }
     } else {
       const uint32_t pbase = part + (uint32_t)(parity * kRpt * kThreadsL * 4);
@@ -354,7 +441,7 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
             const uint32_t a = pbase + (uint32_t)((j * kThreadsL + tid) * 4);
             float v = acc[j];
             for (uint32_t r = 1; r < C; ++r) v += ld_cluster_f32(a, r);
-            T.y[row] = v;
+            store(s, row, v);
           }
         }
       }
@@ -384,11 +471,24 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
 #pragma unroll
     for (int j = 0; j < kRpt; ++j) load_item(first, j, A[j]);
   }
-  uint2 xc = load_x(cur);
+  // zero the table rows of invalid code bytes (any 2-bit field equal to 3) while
+  // the first loads are in flight (the loop's first barrier orders the zeros
+  // before any lookup)
+  for (int i = tid; i < 256 * 32; i += kThreadsL) {
+    const int e = i >> 5;
+    if ((e & (e >> 1)) & 0x55) sts_f32(T0 + (uint32_t)(e * 256 + 4 * (i & 31)), 0.f);
+  }
+  // a small launch asks L2 for all of its weights now (the MoE down phase does so
+  // while the gate|up grid still runs); a large one keeps two steps ahead
+  if (b.prefetch_all && tid == 0)
+    for (Step p = nxt; p.valid; p = advance(p)) prefetch_step(p);
+  // MoE down: the weights above do not depend on the gate|up grid; g and u do
+  if (PHASE == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
+  float4 xc = load_x(cur);
   while (cur.valid) {
     const Step nn = advance(nxt);
-    if (tid == 0) prefetch_step(nn);
-    const uint2 xn = load_x(nxt);
+    if (tid == 0 && !b.prefetch_all) prefetch_step(nn);
+    const float4 xn = load_x(nxt);
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
     __syncthreads();  // the table is complete
@@ -421,28 +521,13 @@ int check_lut_desc(const qmv_desc* d) {
   return QMV_OK;
 }
 
-int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
-  static thread_local LutBatch b;
-  if (n < 1 || n > kMaxTasks) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n, kMaxTasks);
-  int min_kb = 1 << 30;
-  int64_t total = 0;
-  for (int i = 0; i < n; ++i) {
-    const qmv_task& t = tasks[i];
-    int rc = check_lut_desc(t.desc);
-    if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
-    if (!t.w || !t.x || !t.y) return fail(QMV_ERR_ARG, "task %d: NULL w, x or y", i);
-    if (!aligned16(t.w) || !aligned16(t.x) || !aligned16(t.y))
-      return fail(QMV_ERR_ALIGN, "task %d: w, x and y must be 16-byte aligned", i);
-    LutTask& T = b.t[i];
-    T.codes = static_cast<const unsigned char*>(t.w) + t.desc->off[0];
-    T.x = static_cast<const uint16_t*>(t.x);
-    T.y = t.y;
-    T.N = (int32_t)t.desc->N;
-    T.NG = (int32_t)((t.desc->N + 31) / 32);
-    T.KB = (int32_t)(t.desc->K / QMV_GROUP);
-    min_kb = std::min(min_kb, T.KB);
-    total += t.desc->N * t.desc->K;
-  }
+namespace {
+
+// Units, clusters and the schedule of the n tasks in b.t, then the launch of
+// lut_kernel<PHASE> (as a programmatic dependent of the previous launch on the
+// stream when pdl is set).
+template <int PHASE>
+int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   b.n_tasks = n;
   const int sms = sm_count();
   auto units_for = [&](int rows) {
@@ -468,11 +553,14 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
       if (done) break;
     }
   }
-  int64_t n_units = 0;
+  int64_t n_units = 0, weight_bytes = 0;
   for (int i = 0; i < n; ++i) {
     b.t[i].unit0 = (int32_t)n_units;
     n_units += (b.t[i].N + rows - 1) / rows;
+    weight_bytes += (int64_t)b.t[i].NG * b.t[i].KB * (1024 + 64);
   }
+  // launches whose weights fit half of L2 are latency-bound: fetch them all at once
+  b.prefetch_all = weight_bytes <= (int64_t)64 << 20 ? 1 : 0;
   if (n_units > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
   b.n_units = (int32_t)n_units;
   b.unit_rows = rows;
@@ -481,26 +569,30 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
 
   const size_t smem = kSmemL;
   b.smem_bytes = (uint32_t)smem;
-  const void* kern = (const void*)lut_kernel;
+  auto kernel = lut_kernel<PHASE>;
   int per_sm = 0;
-  int rc = kernel_fit(kern, kThreadsL, smem, &per_sm);
+  int rc = kernel_fit((const void*)kernel, kThreadsL, smem, &per_sm);
   if (rc) return rc;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (C > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.blockDim = dim3(kThreadsL);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = C > 1 ? 1 : 0;
+  cfg.numAttrs = na;
   int workers = sms * per_sm;
   if (C > 1) {
     cfg.gridDim = dim3((unsigned)(C * 8));
     int nc = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&nc, lut_kernel, &cfg);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
     if (nc < 1) return fail(QMV_ERR_UNSUPPORTED, "no cluster of %d CTAs fits the device", C);
     workers = nc;
@@ -541,10 +633,82 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
   } else {
     b.sched_n = 0;
   }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = ++na;
+  }
   cfg.gridDim = dim3((unsigned)(workers * C));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lut_kernel, b);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, b);
   if (e != cudaSuccess) return cuda_fail(e, "lookup matvec launch");
   return QMV_OK;
+}
+
+}  // namespace
+
+int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
+  static thread_local LutBatch b;
+  if (n < 1 || n > kMaxTasks) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n, kMaxTasks);
+  int min_kb = 1 << 30;
+  for (int i = 0; i < n; ++i) {
+    const qmv_task& t = tasks[i];
+    int rc = check_lut_desc(t.desc);
+    if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
+    if (!t.w || !t.x || !t.y) return fail(QMV_ERR_ARG, "task %d: NULL w, x or y", i);
+    if (!aligned16(t.w) || !aligned16(t.x) || !aligned16(t.y))
+      return fail(QMV_ERR_ALIGN, "task %d: w, x and y must be 16-byte aligned", i);
+    LutTask& T = b.t[i];
+    T.codes = static_cast<const unsigned char*>(t.w) + t.desc->off[0];
+    T.x = static_cast<const uint16_t*>(t.x);
+    T.y = t.y;
+    T.N = (int32_t)t.desc->N;
+    T.NG = (int32_t)((t.desc->N + 31) / 32);
+    T.KB = (int32_t)(t.desc->K / QMV_GROUP);
+    min_kb = std::min(min_kb, T.KB);
+  }
+  return launch_lut<0>(b, n, min_kb, s, false);
+}
+
+int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
+  static thread_local LutBatch b;
+  const int P = c.M * c.topk;
+  LutMoe& mo = b.moe;
+  mo.routing = MoeRouting{c.logits, c.E, c.topk, c.M};
+  mo.x = c.x;
+  mo.y = c.y;
+  mo.gu = reinterpret_cast<float*>(c.ws + c.off_gu);
+  mo.ws = c.ws;
+  mo.off_slot_expert = c.off_slot_expert;
+  mo.off_slot_first = c.off_slot_first;
+  mo.off_slot_count = c.off_slot_count;
+  mo.off_pair_token = c.off_pair_token;
+  mo.off_pair_prob = c.off_pair_prob;
+  mo.stride = c.stride;
+  mo.I = (int32_t)c.I;
+  mo.H = (int32_t)c.H;
+  mo.ldx = (int32_t)c.ldx;
+  mo.ldy = (int32_t)c.ldy;
+  // gate|up: pair i reads its expert's [gate; up] matrix (2I x H) and writes g|u
+  for (int i = 0; i < P; ++i) {
+    LutTask& T = b.t[i];
+    T.codes = c.gu_codes;
+    T.x = nullptr;
+    T.y = nullptr;
+    T.N = (int32_t)(2 * c.I);
+    T.NG = (int32_t)((2 * c.I + 31) / 32);
+    T.KB = (int32_t)(c.H / QMV_GROUP);
+  }
+  int rc = launch_lut<1>(b, P, (int)(c.H / QMV_GROUP), s, false);
+  if (rc) return rc;
+  // down: pair i reads its expert's down matrix (H x I) and adds p * W_down h into y
+  for (int i = 0; i < P; ++i) {
+    LutTask& T = b.t[i];
+    T.codes = c.dn_codes;
+    T.N = (int32_t)c.H;
+    T.NG = (int32_t)((c.H + 31) / 32);
+    T.KB = (int32_t)(c.I / QMV_GROUP);
+  }
+  return launch_lut<2>(b, P, (int)(c.I / QMV_GROUP), s, true);
 }
 
 }  // namespace qmv

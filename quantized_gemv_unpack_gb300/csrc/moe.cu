@@ -24,6 +24,8 @@
 #include <vector>
 
 #include "gemv_core.cuh"
+#include "lut.cuh"
+#include "moe_route.cuh"
 
 namespace qmv {
 namespace {
@@ -41,11 +43,6 @@ struct MoeCfg {
   static constexpr int THREADS = W * 32;
   static constexpr int TILE_ROWS = W * RPW;
 };
-constexpr int kMaxMoeWarps = 20;
-constexpr int kMaxTopk = 8;
-constexpr int kMaxTokens = 8;
-constexpr int kMaxExperts = 256;
-constexpr int kMaxPairs = kMaxTokens * kMaxTopk;
 constexpr int kMoeSlots = 2;                            // ring slots per decode warp
 
 // The expert kernels' ring: per warp kMoeSlots slots of one step of the warp's
@@ -92,110 +89,6 @@ struct MoeArgs {
   uint32_t magic[10];
   int* err;
 };
-
-// Routing of the M tokens, in shared memory.
-struct MoeRoute {
-  int n_slots;
-  int slot_expert[kMaxPairs], slot_first[kMaxPairs], slot_count[kMaxPairs];
-  int pair_token[kMaxPairs];
-  float pair_prob[kMaxPairs];
-  int exp[kMaxTokens][kMaxTopk];
-  float prob[kMaxTokens][kMaxTopk];
-  int wp[kMaxMoeWarps], ws[kMaxMoeWarps];
-};
-
-// Called by all threads of the CTA (blockDim.x >= E); ends with a CTA barrier.
-__device__ void route(const MoeArgs& a, MoeRoute& R) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < a.M) {
-    // the lane's logits in registers and a bit mask of the entries taken (or past
-    // E), so that nothing is indexed at run time
-    const float* lg = a.logits + (size_t)warp * a.E;
-    float v[kMaxExperts / 32];
-    uint32_t taken = 0u;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = i * 32 + lane;
-      v[i] = e < a.E ? lg[e] : -INFINITY;
-      if (e >= a.E) taken |= 1u << i;
-    }
-    for (int r = 0; r < a.topk; ++r) {
-      // best remaining (value, index) of this lane, then across the warp; equal
-      // values keep the lower index
-      float bv = -INFINITY;
-      int bi = 1 << 30;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i)
-        if (!((taken >> i) & 1u) && (bi == (1 << 30) || v[i] > bv)) bv = v[i], bi = i * 32 + lane;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) bv = ov, bi = oi;
-      }
-      if (bi < a.E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        R.exp[warp][r] = bi < a.E ? bi : 0;
-        R.prob[warp][r] = bv;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      const float mx = R.prob[warp][0];
-      float z = 0.f;
-      for (int r = 0; r < a.topk; ++r) {
-        R.prob[warp][r] = expf(R.prob[warp][r] - mx);
-        z += R.prob[warp][r];
-      }
-      for (int r = 0; r < a.topk; ++r) R.prob[warp][r] /= z;
-    }
-  }
-  __syncthreads();
-  // pairs ordered by expert, then token: thread e counts expert e's pairs, a
-  // block-wide exclusive scan of (pairs, active) gives its first pair and its
-  // slot, and it writes its pairs in token order
-  const int e = threadIdx.x;
-  int cnt = 0;
-  if (e < a.E)
-    for (int t = 0; t < a.M; ++t)
-      for (int r = 0; r < a.topk; ++r) cnt += R.exp[t][r] == e;
-  const int act = cnt > 0;
-  int pc = cnt, sc = act;  // inclusive scans within the warp
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int up = __shfl_up_sync(0xffffffffu, pc, o), us = __shfl_up_sync(0xffffffffu, sc, o);
-    if (lane >= o) {
-      pc += up;
-      sc += us;
-    }
-  }
-  if (lane == 31) {
-    R.wp[warp] = pc;
-    R.ws[warp] = sc;
-  }
-  __syncthreads();
-  int base_p = 0, base_s = 0;
-  for (int w = 0; w < warp; ++w) {
-    base_p += R.wp[w];
-    base_s += R.ws[w];
-  }
-  if (act) {
-    int np = base_p + pc - cnt;
-    const int slot = base_s + sc - 1;
-    R.slot_expert[slot] = e;
-    R.slot_first[slot] = np;
-    R.slot_count[slot] = cnt;
-    for (int t = 0; t < a.M; ++t)
-      for (int r = 0; r < a.topk; ++r)
-        if (R.exp[t][r] == e) {
-          R.pair_token[np] = t;
-          R.pair_prob[np] = R.prob[t][r];
-          ++np;
-        }
-  }
-  if (threadIdx.x == blockDim.x - 1) R.n_slots = base_s + sc;
-  __syncthreads();
-}
 
 // activation sources of the two expert phases
 struct GatherRows {  // x rows of the slot's tokens
@@ -370,7 +263,7 @@ __global__ void __launch_bounds__(MoeCfg<MTMAX>::THREADS, 1) moe_expert_kernel(c
   // the down launch may start on SMs this grid frees; it waits for this grid's
   // results (g, u and the zeroed y) before it reads them
   if (PHASE == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  route(a, R);
+  route(MoeRouting{a.logits, a.E, a.topk, a.M}, R);
   if (PHASE == 0) {
     // y is accumulated by the down phase's atomics
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.M * a.H; i += gridDim.x * blockDim.x)
@@ -555,9 +448,11 @@ size_t moe_workspace_size(int E, int topk, int M, int64_t H, int64_t I) {
 int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const void* experts, int64_t expert_stride,
                 int64_t down_off, int E, const float* logits, int topk, const void* x_bf16, int M, int64_t ldx,
                 float* y, int64_t ldy, void* workspace, size_t ws_bytes, void* stream) {
-  int rc = check_desc(gateup_desc, QMV_TERNARY2);
+  // experts in the byte-lookup layout run on the lookup kernel, in the record layout on the FMA kernels
+  const bool lut = gateup_desc && gateup_desc->format == QMV_TERNARY2_LUT;
+  int rc = lut ? check_lut_desc(gateup_desc) : check_desc(gateup_desc, QMV_TERNARY2);
   if (rc) return fail(rc, "gate|up descriptor: %s", qmv_last_error());
-  rc = check_desc(down_desc, QMV_TERNARY2);
+  rc = lut ? check_lut_desc(down_desc) : check_desc(down_desc, QMV_TERNARY2);
   if (rc) return fail(rc, "down descriptor: %s", qmv_last_error());
   const int64_t H = gateup_desc->K, I2 = gateup_desc->N;
   if (I2 % 2 || down_desc->N != H || down_desc->K != I2 / 2)
@@ -576,6 +471,32 @@ int moe_qmv_run(const qmv_desc* gateup_desc, const qmv_desc* down_desc, const vo
   if (H > INT32_MAX || ldx > INT32_MAX || ldy > INT32_MAX) return fail(QMV_ERR_UNSUPPORTED, "sizes too large");
   const MoeLayout L(E, topk, M, I);
   if (ws_bytes < (size_t)L.total) return fail(QMV_ERR_ARG, "workspace %zu < %lld bytes", ws_bytes, (long long)L.total);
+  if (lut) {
+    if (!device_error_word()) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
+    const unsigned char* base = static_cast<const unsigned char*>(experts);
+    LutMoeCall c;
+    c.gu_codes = base + gateup_desc->off[0];
+    c.dn_codes = base + down_off + down_desc->off[0];
+    c.stride = expert_stride;
+    c.logits = logits;
+    c.E = E;
+    c.topk = topk;
+    c.M = M;
+    c.H = H;
+    c.I = I;
+    c.x = static_cast<const uint16_t*>(x_bf16);
+    c.ldx = ldx;
+    c.y = y;
+    c.ldy = ldy;
+    c.ws = static_cast<unsigned char*>(workspace);
+    c.off_slot_expert = L.slot_expert;
+    c.off_slot_first = L.slot_first;
+    c.off_slot_count = L.slot_count;
+    c.off_pair_token = L.pair_token;
+    c.off_pair_prob = L.pair_prob;
+    c.off_gu = L.gu;
+    return run_lut_moe(c, static_cast<cudaStream_t>(stream));
+  }
   const size_t need_gu = M == 1 ? expert_smem<1>(H) : (M == 2 ? expert_smem<2>(H) : expert_smem<8>(H));
   const size_t need_dn = M == 1 ? expert_smem<1>(I) : (M == 2 ? expert_smem<2>(I) : expert_smem<8>(I));
   if (std::max(need_gu, need_dn) > 227 * 1024 - 1024) return fail(QMV_ERR_UNSUPPORTED, "hidden size too large for one CTA");

@@ -29,11 +29,12 @@ def env():
 class Experts:
     """E ternary SwiGLU experts packed as [gate; up] (2I x H) + down (H x I) records, fp32 masters kept on the GPU."""
 
-    def __init__(self, q, torch, dev, E, H, I, seed, zero_cols=None):
+    def __init__(self, q, torch, dev, E, H, I, seed, zero_cols=None, layout="record"):
         from quantized_gemv_unpack_gb300 import synth
         gen = synth.torch_generator(seed, dev)
-        self.gu_desc = q.qmv_pack_desc(q.QMV_TERNARY2, 2 * I, H)
-        self.dn_desc = q.qmv_pack_desc(q.QMV_TERNARY2, H, I)
+        fmt = q.QMV_TERNARY2_LUT if layout == "lut" else q.QMV_TERNARY2
+        self.gu_desc = q.qmv_pack_desc(fmt, 2 * I, H)
+        self.dn_desc = q.qmv_pack_desc(fmt, H, I)
         self.down_off = self.gu_desc.total_bytes
         self.stride = self.down_off + self.dn_desc.total_bytes
         self.buf = torch.empty(E * self.stride, dtype=torch.uint8, device=dev)
@@ -114,9 +115,10 @@ def _check_routing(logits, topk, W):
 FP32_SLACK = 2e-6   # silu(g) * u and the combine in fp32: a few roundings of 2^-24 each
 
 
+@pytest.mark.parametrize("layout", ["record", "lut"])
 @pytest.mark.parametrize("M", [1, 2, 3, 8])
 @pytest.mark.parametrize("outliers", [None, "channels", "range"])
-def test_moe_small_end_to_end(env, M, outliers):
+def test_moe_small_end_to_end(env, M, outliers, layout):
     q, torch, dev = env
     from oracle import moe
     from oracle.numerics import bf16_bits_to_f64
@@ -126,7 +128,7 @@ def test_moe_small_end_to_end(env, M, outliers):
     if outliers:
         xf, ch = synth.outlier_activations(synth.rng(60 + M), outliers, M, H)
         xin = torch.from_numpy(synth.to_bf16_bits(xf).view(np.int16)).to(dev).view(torch.bfloat16)
-    ex = Experts(q, torch, dev, E, H, I, seed=30 + M, zero_cols=ch)
+    ex = Experts(q, torch, dev, E, H, I, seed=30 + M, zero_cols=ch, layout=layout)
     logits, xb, y, W = _run(q, torch, dev, ex, M, topk, seed=M, x=xin)
     idx, p, pairs = _check_routing(logits, topk, W)
     x = bf16_bits_to_f64(xb)
@@ -158,12 +160,15 @@ def test_moe_small_end_to_end(env, M, outliers):
     assert np.all(np.abs(y - yr) <= bound + 1e-30), f"worst |err|/bound = {np.max(np.abs(y - yr) / np.maximum(bound, 1e-300)):.3f}"
 
 
+@pytest.mark.parametrize("layout", ["record", "lut"])
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
-def test_moe_full_size_staged(env, M):
-    """128 experts, hidden 4096, SwiGLU 2048, top-8: routing exact, g|u and down+combine on sampled rows."""
+def test_moe_full_size_staged(env, M, layout):
+    """128 experts, hidden 4096, SwiGLU 2048, top-8: routing exact, g|u and down+combine on sampled rows,
+    with the experts in the record layout (fp16-FMA expert kernels) or the byte-lookup layout
+    (lookup kernel, one (token, expert) pair per task)."""
     q, torch, dev = env
     E, H, I, topk = 128, 4096, 2048, 8
-    ex = Experts(q, torch, dev, E, H, I, seed=3)
+    ex = Experts(q, torch, dev, E, H, I, seed=3, layout=layout)
     logits, xb, y, W = _run(q, torch, dev, ex, M, topk, seed=100 + M)
     idx, p, pairs = _check_routing(logits, topk, W)
     from oracle.numerics import bf16_bits_to_f64
