@@ -550,7 +550,7 @@ class CassSpeculate(Cassandra):
         return [self.x], [self.yd, self.y]
 
     def traffic(self):
-        return None
+        return captured_traffic("cass-speculate M=5")
 
 
 class KvEncode(Workload):

@@ -64,6 +64,47 @@ def unpack(buf: bytes, N: int, K: int):
     return q.reshape(N, K), s16.copy()
 
 
+def pack_lut(q: np.ndarray, s16: np.ndarray) -> bytes:
+    """Packed INT4 buffer in the byte-lookup layout (``oracle.layout``), by plain loops over
+    rows, blocks and byte positions."""
+    N, K = q.shape
+    KB = K // GROUP
+    nib = (np.asarray(q).astype(np.int32) & 0xF).reshape(N, KB, 64, 2)   # [row][block][pair][column]
+    pair_bytes = nib[:, :, :, 0] | (nib[:, :, :, 1] << 4)
+    offs, total = layout.sections(layout.int4_lut_sizes(N, K))
+    buf = bytearray(total)
+    for n in range(N):
+        for b in range(KB):
+            for t in range(64):
+                buf[offs[0] + layout.lut4_byte_offset(n, b, t, N)] = int(pair_bytes[n, b, layout.lut4_pair_at(n, t)])
+    s16 = np.asarray(s16, dtype=np.uint16)
+    for n in range(N):
+        for b in range(KB):
+            pos = offs[1] + 2 * layout.lut_scale_index(n, b, N)
+            buf[pos:pos + 2] = int(s16[n, b]).to_bytes(2, "little")
+    return bytes(buf)
+
+
+def unpack_lut(buf: bytes, N: int, K: int):
+    """Inverse of ``pack_lut``: (q int8 [N][K], s16 uint16 [N][K/128])."""
+    KB = K // GROUP
+    offs, total = layout.sections(layout.int4_lut_sizes(N, K))
+    assert len(buf) >= total
+    raw = np.frombuffer(buf, dtype=np.uint8)
+    q = np.zeros((N, K), dtype=np.int8)
+    s16 = np.zeros((N, KB), dtype=np.uint16)
+    for n in range(N):
+        for b in range(KB):
+            for t in range(64):
+                byte = int(raw[offs[0] + layout.lut4_byte_offset(n, b, t, N)])
+                p = layout.lut4_pair_at(n, t)
+                for i, v in enumerate((byte & 0xF, byte >> 4)):
+                    q[n, b * GROUP + 2 * p + i] = v - 16 if v >= 8 else v
+            pos = offs[1] + 2 * layout.lut_scale_index(n, b, N)
+            s16[n, b] = int.from_bytes(bytes(raw[pos:pos + 2]), "little")
+    return q, s16
+
+
 def dequant(q: np.ndarray, s16: np.ndarray) -> np.ndarray:
     N, K = q.shape
     s = f16_bits_to_f64(s16)

@@ -43,6 +43,21 @@ groups of 32 (the last padded with zero codes and zero scales), KB = K/128.
   section 1 scales: fp16 bits [KB][NG * 32]; (row n, block b) is element
                     b * NG * 32 + n.
 
+INT4 in the byte-lookup layout (the same codes and scales as INT4, arranged for
+a matvec that reads one code byte, a column pair, per table lookup): rows in
+NG = ceil(N/32) groups of 32 (the last padded with zero codes and zero scales),
+KB = K/128.
+
+  section 0 codes : NG * KB * 2048 bytes. Byte p of a row's block holds the
+                    codes of columns 2p (low nibble) and 2p + 1 (high nibble),
+                    4-bit two's complement. A row's 64 bytes of a block are
+                    read as two halves of 32, each rotated by n % 32: position
+                    t < 32 holds byte (t + n) % 32, position t >= 32 holds byte
+                    32 + (t - 32 + n) % 32. The 2048-byte record of (block b,
+                    row group G) starts at (b * NG + G) * 2048; position t of
+                    row n lies at (t // 16) * 512 + (n % 32) * 16 + t % 16.
+  section 1 scales: fp16 bits [KB][NG * 32], as in the ternary lookup layout.
+
 Cassandra split (see ``oracle.cassandra`` for the contents):
   0 bitmap    : N x K/32 uint32, bit (j % 32) of word j // 32 = kept(n, j)
   1 signmant  : N x (K/2)/8 uint32, nibble i (bits 4(i%8)..) = S<<3 | M>>4 of
@@ -184,6 +199,23 @@ def lut_byte_offset(n: int, b: int, t: int, N: int) -> int:
 
 def lut_scale_index(n: int, b: int, N: int) -> int:
     return b * lut_groups(N) * LUT_ROW_GROUP + n
+
+
+def int4_lut_sizes(N: int, K: int):
+    NG, KB = lut_groups(N), K // 128
+    return [NG * KB * 2048, KB * NG * LUT_ROW_GROUP * 2]
+
+
+def lut4_byte_offset(n: int, b: int, t: int, N: int) -> int:
+    """Offset in section 0 of position t (0..63) of (row n, block b), INT4 lookup layout."""
+    NG = lut_groups(N)
+    return (b * NG + n // LUT_ROW_GROUP) * 2048 + (t // 16) * 512 + (n % LUT_ROW_GROUP) * 16 + t % 16
+
+
+def lut4_pair_at(n: int, t: int) -> int:
+    """The column pair whose byte sits at position t of row n (two halves, each rotated by n % 32)."""
+    half = t // 32
+    return 32 * half + (t % 32 + n) % 32
 
 
 def ternary_bit_pos(k):
