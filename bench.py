@@ -82,6 +82,7 @@ MMA_MIN_M = {"int4": 1, "ternary": 2}          # the library's automatic choice 
 
 
 LUT_KERNEL = "lut_kernel (byte-lookup tables, fp32)"
+LUT4_KERNEL = "lut_kernel<INT4> (byte-lookup tables of column pairs, fp32)"
 
 
 def matvec_kernel(fmt: str, M: int, path: str, layout: str = "record") -> str:
@@ -406,15 +407,18 @@ class Int4Layer(Workload):
     name = "int4-layer"
     kernel = "gemv_kernel<int4, M>"
 
-    def __init__(self, q, torch, dev, M=1, path="auto"):
+    def __init__(self, q, torch, dev, M=1, path="auto", layout="record", layers=1):
         from quantized_gemv_unpack_gb300 import synth
-        self.kernel = matvec_kernel("int4", M, path)
+        if layout == "lut" and M != 1:
+            raise SystemExit("the INT4 lookup layout serves M = 1")
+        self.kernel = LUT4_KERNEL if layout == "lut" else matvec_kernel("int4", M, path)
+        fmt = q.QMV_INT4_LUT if layout == "lut" else q.QMV_INT4
         gen = synth.torch_generator(1, dev)
-        shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824)
+        shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824) * layers
         one = []
         for _, N, K in shapes:
-            d = q.qmv_pack_desc(q.QMV_INT4, N, K)
-            d.flags = PATH_FLAGS[path]
+            d = q.qmv_pack_desc(fmt, N, K)
+            d.flags = PATH_FLAGS[path] if layout == "record" else 0
             p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
             q.qmv_pack_int4(d, synth.student_t4_torch(gen, (N, K), device=dev), p)
             one.append((d, p, N, K))
@@ -425,14 +429,18 @@ class Int4Layer(Workload):
         self.batches = []
         for c in range(self.copies):
             tasks = [(d, p if c == 0 else p.clone(), self.xs[K], y) for (d, p, N, K), y in zip(one, self.ys)]
-            self.batches.append(q.Batch(q.QMV_INT4, tasks, M))
+            self.batches.append(q.Batch(fmt, tasks, M))
         self.nbytes = sum(d.bytes[0] + N * (K // 128) * 2 + M * N * 4 for d, _, N, K in one) + M * (5120 + 13824) * 2
         self.M = M
         self.path = path
+        self.layout = layout
+        self.layers = layers
 
     def config(self):
         return {"workload": f"INT4 GQA layer set (hidden 5120, 40/8 heads x 128, SwiGLU 13824), group-128 absmax/7, "
-                            f"M={self.M}", "M": self.M, "seed": 1, "matvecs_per_step": 7,
+                            f"M={self.M}" + (f", {self.layers} layers" if self.layers > 1 else ""),
+                "M": self.M, "seed": 1, "matvecs_per_step": 7 * self.layers,
+                "layout": {"lut": "byte-lookup (QMV_INT4_LUT)", "record": "row-group records (QMV_INT4)"}[self.layout],
                 "l2": f"rotating {self.copies} copies of the layer (>= 3x L2)"}
 
     def step(self, i, stream):
@@ -442,7 +450,8 @@ class Int4Layer(Workload):
         return list(self.xs.values()), self.ys
 
     def traffic(self):
-        return captured_traffic(f"int4-layer M={self.M}") if self.path == "auto" else None
+        key = f"int4-layer M={self.M}" + (" lut" if self.layout == "lut" else "")
+        return captured_traffic(key) if self.path == "auto" and self.layers == 1 else None
 
 
 class Cassandra(Workload):
@@ -672,7 +681,7 @@ def make_workload(name, q, torch, dev, a):
         return Ternary4096(q, torch, dev, a.M or 1, path=a.path,
                            layout=(a.layout or "record") if (a.M or 1) == 1 else "record")
     if name == "int4-layer":
-        return Int4Layer(q, torch, dev, a.M or 1, path=a.path)
+        return Int4Layer(q, torch, dev, a.M or 1, path=a.path, layout=a.layout or "record", layers=a.int4_layers)
     if name == "cass-speculate":
         return CassSpeculate(q, torch, dev)
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
@@ -737,7 +746,7 @@ def measure_configs(q, torch, dev, stream, steps, warmup, peak):
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
     for key, name, M in CONFIGS:
-        args = argparse.Namespace(M=M, path="auto", layout=None, layers=LAYERS)
+        args = argparse.Namespace(M=M, path="auto", layout=None, layers=LAYERS, int4_layers=1)
         wl = make_workload(name, q, torch, dev, args)
         ms = time_steps(wl, steps, warmup, stream, torch)
         nb = sum(wl.bytes(i) for i in range(steps)) / steps
@@ -779,6 +788,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="default workload only: skip measuring the other configurations in the same run")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
+    ap.add_argument("--int4-layers", type=int, default=1, help="INT4 layer sets per step (int4-layer workload)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     a = ap.parse_args()
     if a.oracle_child:

@@ -59,7 +59,8 @@ typedef enum {
   QMV_CASS = 3,              /* Cassandra lossless bf16 split (speculation + verification) */
   QMV_CASS_MX = 4,           /* Cassandra-2: the split with MX shared exponents (slightly lossy) */
   QMV_TERNARY2_SPARSE = 5,   /* ternary with flagged all-zero tiles left out */
-  QMV_TERNARY2_LUT = 6       /* QMV_TERNARY2's codes and scales in the byte-lookup layout (M = 1) */
+  QMV_TERNARY2_LUT = 6,      /* QMV_TERNARY2's codes and scales in the byte-lookup layout (M = 1) */
+  QMV_INT4_LUT = 7           /* QMV_INT4's codes and scales in the byte-lookup layout (M = 1) */
 } qmv_format;
 
 /*
@@ -135,6 +136,19 @@ typedef enum {
  *             * 16 + t % 16.
  *   1 scales: fp16 [KB][NG * 32]; the scale of (row n, block b) is element
  *             b * NG * 32 + n.
+ * QMV_INT4_LUT ("GPT-5.4 ..." section 3.2: the same codes and fp16 scales as
+ * QMV_INT4, arranged for the byte-lookup matvec at one activation row). Rows go
+ * in NG = ceil(N/32) groups of 32 (the last padded with zero codes and zero
+ * scales); KB = K/128 blocks.
+ *   0 codes : NG * KB * 2048 bytes. Code byte p of a row's block holds columns
+ *             2p (low nibble) and 2p + 1 (high nibble), 4-bit two's complement.
+ *             A row's 64 bytes of a block are two halves of 32, each rotated by
+ *             n % 32: position t < 32 holds byte (t + n) % 32, position t >= 32
+ *             byte 32 + (t - 32 + n) % 32. They lie in the 2048-byte record of
+ *             (block b, row group n / 32), which starts at (b * NG + n / 32) *
+ *             2048; inside it position t of row n is at (t / 16) * 512 + (n % 32)
+ *             * 16 + t % 16.
+ *   1 scales: fp16 [KB][NG * 32], as QMV_TERNARY2_LUT.
  */
 typedef struct {
   uint32_t abi_version;      /* QMV_ABI_VERSION */
@@ -179,8 +193,8 @@ typedef struct {
 } qmv_task;
 
 /*
- * Layout math only (host, no GPU needed): fill `out` for a ternary (either
- * layout) or INT4 matrix of N x K with the given group (must be 128). K must be a positive
+ * Layout math only (host, no GPU needed): fill `out` for a ternary or INT4
+ * matrix (either layout) of N x K with the given group (must be 128). K must be a positive
  * multiple of 128 and N positive; for QMV_CASS_MX (group 32) K must be a
  * multiple of 64. Returns QMV_ERR_UNSUPPORTED for QMV_CASS, whose stream
  * length depends on the data (use cass_pack_host).
@@ -189,7 +203,8 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
 
 /*
  * Quantize and pack on the GPU (offline step). w: device fp32 [N][K] row-major.
- * qmv_pack_ternary writes QMV_TERNARY2 or QMV_TERNARY2_LUT, after desc->format.
+ * qmv_pack_ternary writes QMV_TERNARY2 or QMV_TERNARY2_LUT, qmv_pack_int4
+ * QMV_INT4 or QMV_INT4_LUT, after desc->format.
  * packed: device buffer of desc->total_bytes. Ternary follows block_ternary
  * ("Ternary Bonsai 2", 1.2): scale* = (sum_k |w_k|)/128 + 1e-8 summed in float64
  * in column order, q = clamp(rint(w/scale*), -1, 1) in float64, stored scale =
@@ -211,7 +226,7 @@ int qmv_sparse_pack_host(const qmv_desc* dense, const void* dense_packed, qmv_de
                          int64_t out_capacity);
 
 /*
- * Decode a packed ternary (QMV_TERNARY2 or QMV_TERNARY2_LUT) or INT4 matrix
+ * Decode a packed ternary (QMV_TERNARY2 or QMV_TERNARY2_LUT) or INT4 (QMV_INT4 or QMV_INT4_LUT) matrix
  * to int8 q [N][K] (device) and its fp16 scales [N][K/128] (device, nullable)
  * for bit-exact checks. A ternary code 11 writes 0 to q and sets
  * QMV_ERR_CORRUPT in the device error word.
@@ -238,6 +253,9 @@ int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* sc
 int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx,
                     float* y, int64_t ldy, void* stream);
 /*
+ * A QMV_INT4_LUT desc in qmv_run_int4 or qmv_run_batch serves M = 1 only and
+ * runs the same byte-lookup kernel with one table entry per column pair (256
+ * code bytes per pair, q_lo x_2p + q_hi x_2p+1 in fp32).
  * A QMV_TERNARY2_LUT desc in qmv_run_ternary or qmv_run_batch serves M = 1
  * only (QMV_ERR_UNSUPPORTED otherwise; ldx and ldy are then unused) and runs
  * the byte-lookup kernel: per block of 128 columns it builds, in fp32, the

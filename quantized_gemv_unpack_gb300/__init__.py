@@ -22,7 +22,7 @@ QMV_MAX_BATCH = 448
 
 QMV_OK, QMV_ERR_ARG, QMV_ERR_ALIGN, QMV_ERR_UNSUPPORTED = 0, -1, -2, -3
 QMV_ERR_CORRUPT, QMV_ERR_CUDA, QMV_ERR_TIMEOUT = -4, -5, -6
-QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX, QMV_TERNARY2_SPARSE, QMV_TERNARY2_LUT = 1, 2, 3, 4, 5, 6
+QMV_TERNARY2, QMV_INT4, QMV_CASS, QMV_CASS_MX, QMV_TERNARY2_SPARSE, QMV_TERNARY2_LUT, QMV_INT4_LUT = 1, 2, 3, 4, 5, 6, 7
 QMV_FLAG_PATH_FMA, QMV_FLAG_PATH_MMA = 1, 2   # qmv_desc.flags: force the fp16-FMA or the tensor-core matvec kernel
 QMV_FLAG_TEST_WAIT_TIMEOUT = 0x100           # qmv_desc.flags, testing only: the matvec's first wait gives up
 

@@ -240,8 +240,9 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
     fill_sections(out, sizes, 6);
     return QMV_OK;
   }
-  if (format == QMV_TERNARY2_LUT) {
-    // byte-lookup layout, see qmv.h: 1 KB records of (block, 32-row group), scales [KB][NG * 32]
+  if (format == QMV_TERNARY2_LUT || format == QMV_INT4_LUT) {
+    // byte-lookup layouts, see qmv.h: 1 KB (ternary) or 2 KB (INT4) records of
+    // (block, 32-row group), scales [KB][NG * 32]
     if (group != QMV_GROUP) return fail(QMV_ERR_ARG, "group must be 128");
     if (N <= 0 || K <= 0 || K % QMV_GROUP) return fail(QMV_ERR_ARG, "N=%lld K=%lld (K must be a positive multiple of 128)", (long long)N, (long long)K);
     memset(out, 0, sizeof(*out));
@@ -251,7 +252,7 @@ int qmv_pack_desc(int format, int64_t N, int64_t K, int32_t group, qmv_desc* out
     out->K = K;
     out->group = group;
     const int64_t NG = (N + 31) / 32, KB = K / QMV_GROUP;
-    const int64_t sizes[2] = {NG * KB * 1024, KB * NG * 32 * 2};
+    const int64_t sizes[2] = {NG * KB * (format == QMV_INT4_LUT ? 2048 : 1024), KB * NG * 32 * 2};
     fill_sections(out, sizes, 2);
     return QMV_OK;
   }
@@ -282,13 +283,20 @@ int qmv_run_ternary(const qmv_desc* desc, const void* w, const void* x_bf16, int
 
 int qmv_run_int4(const qmv_desc* desc, const void* w, const void* x_bf16, int M, int64_t ldx, float* y,
                  int64_t ldy, void* stream) {
+  if (desc && desc->format == QMV_INT4_LUT) {
+    qmv_task t{desc, w, x_bf16, y, ldx, ldy};
+    return qmv_run_batch(QMV_INT4_LUT, &t, 1, M, stream);
+  }
   return run_one(QMV_INT4, desc, w, x_bf16, M, ldx, y, ldy, stream);
 }
 
 int qmv_run_batch(int format, const qmv_task* tasks, int n_tasks, int M, void* stream) {
-  if (format == QMV_TERNARY2_LUT) {
+  if (format == QMV_TERNARY2_LUT || format == QMV_INT4_LUT) {
     if (!tasks || n_tasks < 1 || n_tasks > QMV_MAX_BATCH) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n_tasks, QMV_MAX_BATCH);
     if (M != 1) return fail(QMV_ERR_UNSUPPORTED, "the lookup layout serves M = 1 (got M=%d)", M);
+    for (int i = 0; i < n_tasks; ++i)
+      if (!tasks[i].desc || (int)tasks[i].desc->format != format)
+        return fail(QMV_ERR_ARG, "task %d: descriptor format differs from the batch's", i);
     return run_lut(tasks, n_tasks, static_cast<cudaStream_t>(stream));
   }
   if (format == QMV_TERNARY2_SPARSE) {

@@ -109,7 +109,7 @@ uint64_t get_u64(const unsigned char* p) {
 // its total size.
 bool desc_is_sane(const qmv_desc& d) {
   if (d.abi_version != QMV_ABI_VERSION) return false;
-  if (d.format < QMV_TERNARY2 || d.format > QMV_TERNARY2_LUT) return false;
+  if (d.format < QMV_TERNARY2 || d.format > QMV_INT4_LUT) return false;
   if (d.N <= 0 || d.K <= 0 || d.total_bytes <= 0) return false;
   for (int i = 0; i < QMV_MAX_SECTIONS; ++i) {
     if (d.off[i] < 0 || d.bytes[i] < 0) return false;

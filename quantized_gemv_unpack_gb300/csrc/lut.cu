@@ -1,7 +1,8 @@
 // Batch-1 matvec over block-128 ternary weights in the lookup layout
 // (QMV_TERNARY2_LUT): y = W_hat x for one activation row, with W_hat = q * s,
 // q in {-1, 0, +1} per weight ("Ternary Bonsai 2", section 1.2) and one fp16
-// scale s per block of 128 columns.
+// scale s per block of 128 columns; and the same for group-128 INT4 weights
+// in their lookup layout (QMV_INT4_LUT, "GPT-5.4" section 3.2), below.
 //
 // Decode by table lookup. A code byte holds the codes of four consecutive
 // columns (2 bits each), so it takes one of 81 valid values e. Per block of
@@ -34,6 +35,14 @@
 // largest first, each to the least loaded one, and passes the lists in the
 // launch parameters. Each of the 256 threads owns up to four rows of a unit
 // (rows r0 + 256 j + tid); lane = row % 32.
+//
+// INT4 (lut_kernel<QMV_INT4_LUT, 0>): a code byte is one column pair (two
+// nibbles), so a block's table has 256 rows of 64 pair slots, T[lo + 16 hi][p] =
+// q(lo) x[2p] + q(hi) x[2p + 1] (both products exact in fp32), built by all
+// 256 threads (a pair and 64 byte values each); a row's block is 64 lookups,
+// its 64 bytes read as two halves of 32, each rotated by n % 32 like the ternary
+// bytes, the second half's slots 128 bytes on. 64 + 64 bytes of codes per row
+// item need 128 registers, so two CTAs share an SM.
 //
 // MoE experts (lut_kernel<1>, <2>): the same kernel runs the gate|up and the down
 // phase of the MoE decode over experts in this layout ("Nemotron 3.5 Bolt",
@@ -76,8 +85,22 @@ constexpr int kPartBytes = 2 * kRpt * kThreadsL * 4;  // two unit parities of pa
 // thread) share an SM and one's table build overlaps the others' lookups
 constexpr size_t kSmemL = kTableBytes + kPartBytes;
 
+// Geometry of the two lookup layouts: bytes of a (block, 32-row group) record,
+// code bytes of a row's block (table lookups per row and block), uint4 pieces
+// of a row's block.
+template <int FMT>
+struct LutFmt;
+template <>
+struct LutFmt<QMV_TERNARY2_LUT> {
+  static constexpr int REC = 1024, NPOS = 32, PIECES = 2, MIN_CTAS = 3;
+};
+template <>
+struct LutFmt<QMV_INT4_LUT> {
+  static constexpr int REC = 2048, NPOS = 64, PIECES = 4, MIN_CTAS = 2;
+};
+
 struct LutTask {
-  const unsigned char* codes;  // section 0; the scales follow at NG * KB * 1024 bytes
+  const unsigned char* codes;  // section 0; the scales follow at NG * KB * record bytes
   const uint16_t* x;           // bf16 [K]
   float* y;                    // fp32 [N]
   int32_t N, NG, KB, unit0;    // NG 32-row groups, KB blocks, first unit of this task
@@ -189,9 +212,10 @@ struct Step {
   __device__ __forceinline__ int nrows32() const { return (nrows + 31) & ~31; }
 };
 
+template <int PIECES>
 struct Item {
-  uint4 lo, hi;  // the row's 32 code bytes of the block
-  uint32_t s;    // the row's fp16 scale of the block (low 16 bits)
+  uint4 c[PIECES];  // the row's code bytes of the block (32 ternary, 64 INT4)
+  uint32_t s;       // the row's fp16 scale of the block (low 16 bits)
 };
 
 __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
@@ -206,9 +230,12 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
 
-// PHASE 0: the tasks' matvecs; 1 / 2: the MoE gate|up / down phase (see LutMoe).
-template <int PHASE>
-__global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant__ LutBatch b) {
+// FMT: QMV_TERNARY2_LUT or QMV_INT4_LUT. PHASE 0: the tasks' matvecs; 1 / 2: the
+// MoE gate|up / down phase (see LutMoe; ternary only).
+template <int FMT, int PHASE>
+__global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(const __grid_constant__ LutBatch b) {
+  using LF = LutFmt<FMT>;
+  using ItemT = Item<LF::PIECES>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // the down phase may start on SMs the gate|up grid frees; it waits for that
   // grid's g, u and zeroed y before reading them
@@ -302,8 +329,8 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     const unsigned char* codes = codes_of(s.ti);
     const int g0 = s.r0 >> 5;
     const int ng = s.nrows32() >> 5;
-    l2_prefetch(codes + ((size_t)s.bk * T.NG + g0) * 1024, (uint32_t)ng * 1024u);
-    const uint16_t* sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * 1024);
+    l2_prefetch(codes + ((size_t)s.bk * T.NG + g0) * LF::REC, (uint32_t)ng * LF::REC);
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * LF::REC);
     l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
   };
   // This thread's load addresses of a step: row r0 + tid of its codes and of
@@ -322,16 +349,18 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     if (!s.valid) return r;
     const LutTask& T = b.t[s.ti];
     const unsigned char* codes = codes_of(s.ti);
-    r.cw = reinterpret_cast<const uint4*>(codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * 64 + lane;
-    r.sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * 1024) + (size_t)s.bk * T.NG * 32 + s.r0 +
+    r.cw = reinterpret_cast<const uint4*>(codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * (LF::REC / 16) +
+           lane;
+    r.sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * LF::REC) + (size_t)s.bk * T.NG * 32 + s.r0 +
            tid;
     r.n32 = s.nrows32() - (tid & ~31);
     return r;
   };
-  auto load_item = [&](const Src& r, int j, Item& it) {
+  // piece i of a row holds its bytes 16i .. 16i+15, 512 bytes after piece i - 1
+  auto load_item = [&](const Src& r, int j, ItemT& it) {
     const bool on = j * kThreadsL < r.n32;
-    ldg16_if(it.lo, r.cw + j * (kThreadsL / 32) * 64, on);
-    ldg16_if(it.hi, r.cw + j * (kThreadsL / 32) * 64 + 32, on);
+#pragma unroll
+    for (int i = 0; i < LF::PIECES; ++i) ldg16_if(it.c[i], r.cw + j * (kThreadsL / 32) * (LF::REC / 16) + 32 * i, on);
     ldg2_if(it.s, r.sc + j * kThreadsL, on);
   };
   // table builders: thread (warp w, lane g) writes column group g's entries of
@@ -346,6 +375,10 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
       const float4 gg = *reinterpret_cast<const float4*>(gr);
       const float4 uu = *reinterpret_cast<const float4*>(gr + b.moe.I);
       return make_float4(silu(gg.x) * uu.x, silu(gg.y) * uu.y, silu(gg.z) * uu.z, silu(gg.w) * uu.w);
+    } else if constexpr (FMT == QMV_INT4_LUT) {
+      // columns 2p, 2p + 1 of the thread's pair p = lane + 32 (warp & 1)
+      const uint32_t xw = *reinterpret_cast<const uint32_t*>(b.t[s.ti].x + (size_t)s.bk * 128 + 2 * (g + 32 * (warp & 1)));
+      return make_float4(__uint_as_float(xw << 16), __uint_as_float(xw & 0xFFFF0000u), 0.f, 0.f);
     } else {
       const uint16_t* xr = PHASE == 0 ? b.t[s.ti].x : b.moe.x + (size_t)R->pair_token[s.ti] * b.moe.ldx;
       const uint2 xw = *reinterpret_cast<const uint2*>(xr + (size_t)s.bk * 128 + 4 * g);
@@ -362,6 +395,24 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   // the table of a step's block, from its x, into the table at tb
   auto build = [&](float4 xv, uint32_t tb) {
     const float x0 = xv.x, x1 = xv.y, x2 = xv.z, x3 = xv.w;
+    if constexpr (FMT == QMV_INT4_LUT) {
+      // INT4: thread (warp w, lane) writes pair p = lane + 32 (w & 1) of the 64 code
+      // bytes whose high nibble is one of 4 (w >> 1) .. 4 (w >> 1) + 3:
+      // T[lo + 16 hi][p] = q(lo) x0 + q(hi) x1, q the 4-bit two's complement value;
+      // both products are exact in fp32
+      const uint32_t slot = 4u * (uint32_t)(g + 32 * (warp & 1));
+      float a[16];
+#pragma unroll
+      for (int lo = 0; lo < 16; ++lo) a[lo] = (float)(lo < 8 ? lo : lo - 16) * x0;
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const int hi = 4 * (warp >> 1) + hh;
+        const float bh = (float)(hi < 8 ? hi : hi - 16) * x1;
+#pragma unroll
+        for (int lo = 0; lo < 16; ++lo) sts_f32(tb + (uint32_t)((hi * 16 + lo) * 256) + slot, a[lo] + bh);
+      }
+      return;
+    }
     auto put = [&](int d0, int d1, int d2, int d3, float p23) {
       const float v = (code_val(d0, x0) + code_val(d1, x1)) + p23;
       const uint32_t a = tb + (uint32_t)((d0 + 4 * d1 + 16 * d2 + 64 * d3) * 256 + 4 * g);
@@ -377,18 +428,28 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     put(warp % 3, warp / 3, 2, 2, p23);
     if (warp == 0) put(2, 2, 2, 2, p23);
   };
-  // one row's block: 32 lookups and adds, times the block's scale, into acc
-  auto row_block = [&](const Item& it, float& a, uint32_t tb) {
-    const uint32_t w[8] = {it.lo.x, it.lo.y, it.lo.z, it.lo.w, it.hi.x, it.hi.y, it.hi.z, it.hi.w};
+  // one row's block: one lookup per code byte (32 ternary, 64 INT4) and the adds,
+  // times the block's scale, into acc. Positions 32..63 (INT4) are the second half,
+  // rotated like the first, whose table slots are 32..63 (128 bytes on).
+  auto row_block = [&](const ItemT& it, float& a, uint32_t tb) {
+    uint32_t w[4 * LF::PIECES];
+#pragma unroll
+    for (int i = 0; i < LF::PIECES; ++i) {
+      w[4 * i] = it.c[i].x;
+      w[4 * i + 1] = it.c[i].y;
+      w[4 * i + 2] = it.c[i].z;
+      w[4 * i + 3] = it.c[i].w;
+    }
     uint64_t s2 = 0;  // two partial sums (even and odd positions)
 #pragma unroll
-    for (int t = 0; t < 32; t += 2) {
+    for (int t = 0; t < LF::NPOS; t += 2) {
       // result bytes: wrapped lane offset, code byte t, 0, 0; plus the table base
       const uint32_t j0 = (uint32_t)(t & 3), j1 = (uint32_t)((t + 1) & 3);
       // byte j of Lk: (4 lane + 4 (4k + j)) mod 128, the wrapped slot offset of position 4k + j
-      const uint32_t Lk = (L0 + (uint32_t)(t >> 2) * 0x10101010u) & 0x7C7C7C7Cu;
-      const uint32_t a0 = prmt(w[t >> 2], Lk, (4u + j0) | (j0 << 4) | ((12u + j0) << 8) | ((12u + j0) << 12)) + tb;
-      const uint32_t a1 = prmt(w[(t + 1) >> 2], Lk, (4u + j1) | (j1 << 4) | ((12u + j1) << 8) | ((12u + j1) << 12)) + tb;
+      const uint32_t Lk = (L0 + (uint32_t)((t >> 2) & 7) * 0x10101010u) & 0x7C7C7C7Cu;
+      const uint32_t tbh = tb + (t >= 32 ? 128u : 0u);
+      const uint32_t a0 = prmt(w[t >> 2], Lk, (4u + j0) | (j0 << 4) | ((12u + j0) << 8) | ((12u + j0) << 12)) + tbh;
+      const uint32_t a1 = prmt(w[(t + 1) >> 2], Lk, (4u + j1) | (j1 << 4) | ((12u + j1) << 8) | ((12u + j1) << 12)) + tbh;
       const float v0 = lds_at<0>(a0);
       const float v1 = lds_at<0>(a1);
       s2 = add2_f32(s2, v0, v1);
@@ -398,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   // this thread's rows of a step (all four in a full unit, else the rows of this
   // warp's 32-row groups that the unit has); right after a row's block, its
   // register slot is reloaded with the same slot of the next step
-  auto lookups = [&](const Step& s, Item (&it)[kRpt], const Src& n, uint32_t tb) {
+  auto lookups = [&](const Step& s, ItemT (&it)[kRpt], const Src& n, uint32_t tb) {
     if (s.nrows32() == kUnitRowsMax) {
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) {
@@ -460,10 +521,11 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
     prefetch_step(cur);
     prefetch_step(nxt);
   }
-  Item A[kRpt];
+  ItemT A[kRpt];
 #pragma unroll
   for (int j = 0; j < kRpt; ++j) {
-    A[j].lo = A[j].hi = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < LF::PIECES; ++i) A[j].c[i] = make_uint4(0u, 0u, 0u, 0u);
     A[j].s = 0u;
   }
   {
@@ -474,10 +536,11 @@ __global__ void __launch_bounds__(kThreadsL, 3) lut_kernel(const __grid_constant
   // zero the table rows of invalid code bytes (any 2-bit field equal to 3) while
   // the first loads are in flight (the loop's first barrier orders the zeros
   // before any lookup)
-  for (int i = tid; i < 256 * 32; i += kThreadsL) {
-    const int e = i >> 5;
-    if ((e & (e >> 1)) & 0x55) sts_f32(T0 + (uint32_t)(e * 256 + 4 * (i & 31)), 0.f);
-  }
+  if constexpr (FMT == QMV_TERNARY2_LUT)
+    for (int i = tid; i < 256 * 32; i += kThreadsL) {
+      const int e = i >> 5;
+      if ((e & (e >> 1)) & 0x55) sts_f32(T0 + (uint32_t)(e * 256 + 4 * (i & 31)), 0.f);
+    }
   // a small launch asks L2 for all of its weights now (the MoE down phase does so
   // while the gate|up grid still runs); a large one keeps two steps ahead
   if (b.prefetch_all && tid == 0)
@@ -508,12 +571,13 @@ int check_lut_desc(const qmv_desc* d) {
   if (!d) return fail(QMV_ERR_ARG, "desc is NULL");
   if (d->abi_version != QMV_ABI_VERSION)
     return fail(QMV_ERR_ARG, "desc abi_version %u, library %d", d->abi_version, QMV_ABI_VERSION);
-  if (d->format != QMV_TERNARY2_LUT) return fail(QMV_ERR_ARG, "desc format %u is not QMV_TERNARY2_LUT", d->format);
+  if (d->format != QMV_TERNARY2_LUT && d->format != QMV_INT4_LUT)
+    return fail(QMV_ERR_ARG, "desc format %u is not a lookup layout (QMV_TERNARY2_LUT, QMV_INT4_LUT)", d->format);
   if (d->N <= 0 || d->K <= 0 || d->group != QMV_GROUP || d->K % QMV_GROUP)
     return fail(QMV_ERR_ARG, "desc N=%lld K=%lld group=%d", (long long)d->N, (long long)d->K, d->group);
   if (d->N > (1 << 26) || d->K > (1 << 26)) return fail(QMV_ERR_UNSUPPORTED, "matrix too large");
   qmv_desc ref;
-  qmv_pack_desc(QMV_TERNARY2_LUT, d->N, d->K, d->group, &ref);
+  qmv_pack_desc((int)d->format, d->N, d->K, d->group, &ref);
   for (int i = 0; i < 2; ++i)
     if (ref.off[i] != d->off[i] || ref.bytes[i] != d->bytes[i])
       return fail(QMV_ERR_ARG, "desc section %d does not match the lookup layout of a %lld x %lld matrix", i,
@@ -526,7 +590,7 @@ namespace {
 // Units, clusters and the schedule of the n tasks in b.t, then the launch of
 // lut_kernel<PHASE> (as a programmatic dependent of the previous launch on the
 // stream when pdl is set).
-template <int PHASE>
+template <int FMT, int PHASE>
 int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   b.n_tasks = n;
   const int sms = sm_count();
@@ -537,7 +601,9 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   };
   // Rows per unit and CTAs per cluster: whole 1024-row units on single CTAs
   // when there are enough of them; otherwise smaller units whose blocks a
-  // cluster of up to 8 CTAs shares, until the launch covers the SMs.
+  // cluster of up to 8 CTAs shares, until the launch covers twice the SMs
+  // (measured: the INT4 layer set 74 -> 46 us against covering the SMs once,
+  // the small ternary launches unchanged).
   int rows = kUnitRowsMax, C = 1;
   if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
     bool done = false;
@@ -545,7 +611,7 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
       for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
         rows = r;
         C = c;
-        if (units_for(r) * c >= sms) {
+        if (units_for(r) * c >= 2 * sms) {
           done = true;
           break;
         }
@@ -557,7 +623,7 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   for (int i = 0; i < n; ++i) {
     b.t[i].unit0 = (int32_t)n_units;
     n_units += (b.t[i].N + rows - 1) / rows;
-    weight_bytes += (int64_t)b.t[i].NG * b.t[i].KB * (1024 + 64);
+    weight_bytes += (int64_t)b.t[i].NG * b.t[i].KB * (LutFmt<FMT>::REC + 64);
   }
   // launches whose weights fit half of L2 are latency-bound: fetch them all at once
   b.prefetch_all = weight_bytes <= (int64_t)64 << 20 ? 1 : 0;
@@ -569,7 +635,7 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
 
   const size_t smem = kSmemL;
   b.smem_bytes = (uint32_t)smem;
-  auto kernel = lut_kernel<PHASE>;
+  auto kernel = lut_kernel<FMT, PHASE>;
   int per_sm = 0;
   int rc = kernel_fit((const void*)kernel, kThreadsL, smem, &per_sm);
   if (rc) return rc;
@@ -649,11 +715,14 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
 int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
   static thread_local LutBatch b;
   if (n < 1 || n > kMaxTasks) return fail(QMV_ERR_ARG, "n_tasks=%d outside 1..%d", n, kMaxTasks);
+  if (!tasks || !tasks[0].desc) return fail(QMV_ERR_ARG, "NULL task or desc");
+  const uint32_t fmt = tasks[0].desc->format;
   int min_kb = 1 << 30;
   for (int i = 0; i < n; ++i) {
     const qmv_task& t = tasks[i];
     int rc = check_lut_desc(t.desc);
     if (rc) return fail(rc, "task %d: %s", i, qmv_last_error());
+    if (t.desc->format != fmt) return fail(QMV_ERR_ARG, "task %d: one launch serves one lookup layout", i);
     if (!t.w || !t.x || !t.y) return fail(QMV_ERR_ARG, "task %d: NULL w, x or y", i);
     if (!aligned16(t.w) || !aligned16(t.x) || !aligned16(t.y))
       return fail(QMV_ERR_ALIGN, "task %d: w, x and y must be 16-byte aligned", i);
@@ -666,7 +735,8 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
     T.KB = (int32_t)(t.desc->K / QMV_GROUP);
     min_kb = std::min(min_kb, T.KB);
   }
-  return launch_lut<0>(b, n, min_kb, s, false);
+  return fmt == QMV_INT4_LUT ? launch_lut<QMV_INT4_LUT, 0>(b, n, min_kb, s, false)
+                              : launch_lut<QMV_TERNARY2_LUT, 0>(b, n, min_kb, s, false);
 }
 
 int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
@@ -698,7 +768,7 @@ int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
     T.NG = (int32_t)((2 * c.I + 31) / 32);
     T.KB = (int32_t)(c.H / QMV_GROUP);
   }
-  int rc = launch_lut<1>(b, P, (int)(c.H / QMV_GROUP), s, false);
+  int rc = launch_lut<QMV_TERNARY2_LUT, 1>(b, P, (int)(c.H / QMV_GROUP), s, false);
   if (rc) return rc;
   // down: pair i reads its expert's down matrix (H x I) and adds p * W_down h into y
   for (int i = 0; i < P; ++i) {
@@ -708,7 +778,7 @@ int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
     T.NG = (int32_t)((c.H + 31) / 32);
     T.KB = (int32_t)(c.I / QMV_GROUP);
   }
-  return launch_lut<2>(b, P, (int)(c.I / QMV_GROUP), s, true);
+  return launch_lut<QMV_TERNARY2_LUT, 2>(b, P, (int)(c.I / QMV_GROUP), s, true);
 }
 
 }  // namespace qmv

@@ -47,6 +47,12 @@ __host__ __device__ __forceinline__ int64_t lut_byte(int64_t n, int64_t b, int t
   return (b * NG + n / 32) * 1024 + (t / 16) * 512 + (n % 32) * 16 + t % 16;
 }
 
+// Byte offset of position t (0..63) of (row n, block b) in the INT4 lookup
+// layout's codes section (QMV_INT4_LUT): 2 KB records of (block, 32-row group).
+__host__ __device__ __forceinline__ int64_t lut4_byte(int64_t n, int64_t b, int t, int64_t NG) {
+  return (b * NG + n / 32) * 2048 + (t / 16) * 512 + (n % 32) * 16 + t % 16;
+}
+
 template <bool LUT>
 __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
                                     uint16_t* __restrict__ scales) {
@@ -116,6 +122,7 @@ __global__ void pack_ternary_kernel(const float* __restrict__ w, int64_t N, int6
   }
 }
 
+template <bool LUT>
 __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t K, uint32_t* __restrict__ codes,
                                  uint16_t* __restrict__ scales) {
   const int64_t nb = K / 128;
@@ -148,10 +155,46 @@ __global__ void pack_int4_kernel(const float* __restrict__ w, int64_t N, int64_t
       words[k >> 3] |= ((uint32_t)q & 0xFu) << pos;
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 16));
+  if constexpr (LUT) {
+    // pair p (columns 2p, 2p + 1) as one byte, low nibble first; the two halves of
+    // 32 bytes each rotated by n % 32
+    uint32_t pb[64];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
-  scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
+    for (int p = 0; p < 64; ++p) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = 2 * p + i, rr = k & 7;
+        const int pos = (rr & 1) ? 14 + 2 * rr : 2 * rr;
+        v |= ((words[k >> 3] >> pos) & 0xFu) << (4 * i);
+      }
+      pb[p] = v;
+    }
+    const int64_t NG = (N + 31) / 32;
+    const int rot = (int)(n % 32);
+    unsigned char* cb = reinterpret_cast<unsigned char*>(codes);
+#pragma unroll
+    for (int piece = 0; piece < 4; ++piece) {
+      uint32_t out[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int t = 16 * piece + 4 * u + kk;
+          v |= pb[32 * (t >> 5) + ((t & 31) + rot) % 32] << (8 * kk);
+        }
+        out[u] = v;
+      }
+      *reinterpret_cast<uint4*>(cb + lut4_byte(n, b, 16 * piece, NG)) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    scales[b * NG * 32 + n] = f64_to_f16_rne(s);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(codes + record_word(n, b, K, 16));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
+    scales[scale_index(n, b, scale_steps(K))] = f64_to_f16_rne(s);
+  }
 }
 
 // One thread per (row, block): decodes the block's columns to int8 and copies
@@ -181,6 +224,20 @@ __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, co
     if (scales_out) scales_out[n * KB + b] = scales[b * NG * 32 + n];
     return;
   }
+  if (format == QMV_INT4_LUT) {
+    const int64_t NG = (N + 31) / 32;
+    const unsigned char* cb = reinterpret_cast<const unsigned char*>(codes);
+    for (int t = 0; t < 64; ++t) {
+      const uint32_t v = cb[lut4_byte(n, b, t, NG)];
+      const int p = 32 * (t >> 5) + (int)(((t & 31) + n) % 32);
+      for (int i = 0; i < 2; ++i) {
+        const int nib = (int)((v >> (4 * i)) & 0xFu);
+        out[2 * p + i] = (int8_t)(nib >= 8 ? nib - 16 : nib);
+      }
+    }
+    if (scales_out) scales_out[n * KB + b] = scales[b * NG * 32 + n];
+    return;
+  }
   const int bw = format == QMV_TERNARY2 ? 8 : 16;
   const uint32_t* src = codes + record_word(n, b, K, bw);
   for (int wi = 0; wi < bw; ++wi) {
@@ -205,7 +262,8 @@ __global__ void unpack_kernel(int format, const uint32_t* __restrict__ codes, co
 }
 
 int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, void* stream) {
-  const bool lut = format == QMV_TERNARY2 && desc && desc->format == QMV_TERNARY2_LUT;
+  const bool lut = desc && ((format == QMV_TERNARY2 && desc->format == QMV_TERNARY2_LUT) ||
+                            (format == QMV_INT4 && desc->format == QMV_INT4_LUT));
   int rc = lut ? check_lut_desc(desc) : check_desc(desc, format);
   if (rc) return rc;
   if (!w || !packed) return fail(QMV_ERR_ARG, "NULL w or packed");
@@ -237,12 +295,14 @@ int pack_common(int format, const qmv_desc* desc, const float* w, void* packed, 
       if (e != cudaSuccess) return cuda_fail(e, "zero section padding");
     }
   }
-  if (lut)
+  if (format == QMV_TERNARY2 && lut)
     pack_ternary_kernel<true><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
   else if (format == QMV_TERNARY2)
     pack_ternary_kernel<false><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+  else if (lut)
+    pack_int4_kernel<true><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
   else
-    pack_int4_kernel<<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
+    pack_int4_kernel<false><<<(unsigned)grid, threads, 0, s>>>(w, desc->N, desc->K, codes, scales);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
   return QMV_OK;
@@ -266,9 +326,10 @@ int qmv_pack_int4(const qmv_desc* desc, const float* w, void* packed, void* stre
 int qmv_unpack(const qmv_desc* desc, const void* packed, int8_t* q, uint16_t* scales, void* stream) {
   if (!desc) return fail(QMV_ERR_ARG, "desc is NULL");
   const int format = (int)desc->format;
-  if (format != QMV_TERNARY2 && format != QMV_INT4 && format != QMV_TERNARY2_LUT)
-    return fail(QMV_ERR_UNSUPPORTED, "qmv_unpack serves ternary (either layout) and INT4");
-  int rc = format == QMV_TERNARY2_LUT ? check_lut_desc(desc) : check_desc(desc, format);
+  if (format != QMV_TERNARY2 && format != QMV_INT4 && format != QMV_TERNARY2_LUT && format != QMV_INT4_LUT)
+    return fail(QMV_ERR_UNSUPPORTED, "qmv_unpack serves ternary and INT4 (either layout)");
+  const bool lutf = format == QMV_TERNARY2_LUT || format == QMV_INT4_LUT;
+  int rc = lutf ? check_lut_desc(desc) : check_desc(desc, format);
   if (rc) return rc;
   if (!packed || !q) return fail(QMV_ERR_ARG, "NULL packed or q");
   if (!aligned16(packed) || !aligned16(q) || (scales && !aligned16(scales)))

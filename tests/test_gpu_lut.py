@@ -277,3 +277,128 @@ def test_lut_more_units_than_the_schedule_holds(env):
         xb = tasks[i][2].view(torch.int16).cpu().numpy().view(np.uint16)
         yr, B = matvec_bf16x(ternary.dequant(qq, s16), xb)
         _check(tasks[i][3][:, idx].cpu().numpy(), yr, B, f"task {i}")
+
+
+# ----------------------------------------------------------------------------- INT4 lookup layout
+
+def _pack4(q, torch, dev, w):
+    N, K = w.shape
+    d = q.qmv_pack_desc(q.QMV_INT4_LUT, N, K)
+    p = torch.empty(d.total_bytes, dtype=torch.uint8, device=dev)
+    q.qmv_pack_int4(d, w if isinstance(w, torch.Tensor) else torch.from_numpy(w).to(dev), p)
+    return d, p
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (31, 384), (33, 256), (200, 1152), (64, 4096)])
+def test_int4_lut_packer_is_bit_exact(env, N, K):
+    q, torch, dev = env
+    from oracle import int4
+    from quantized_gemv_unpack_gb300 import synth
+    w = synth.student_t4(synth.rng(N * 17 + K), (N, K))
+    w[0, :128] = 0.0
+    d, p = _pack4(q, torch, dev, w)
+    qq, _, s16 = int4.quantize(w)
+    assert np.array_equal(p.cpu().numpy(), np.frombuffer(int4.pack_lut(qq, s16), np.uint8))
+    qd = torch.empty((N, K), dtype=torch.int8, device=dev)
+    sd = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+    q.qmv_unpack(d, p, qd, sd)
+    assert q.qmv_check_status() == 0
+    assert np.array_equal(qd.cpu().numpy(), qq)
+    assert np.array_equal(sd.cpu().numpy().view(np.uint16), s16)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (33, 256), (200, 1152), (96, 5120), (40, 13824), (4096, 4096)])
+def test_int4_lut_matvec_matches_oracle(env, N, K):
+    q, torch, dev = env
+    from oracle import int4
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    g = synth.rng(7 * N + K)
+    w = synth.student_t4(g, (N, K))
+    xb = synth.activations_bf16(g, (1, K))
+    d, p = _pack4(q, torch, dev, w)
+    y = torch.full((1, N), float("nan"), device=dev)
+    q.qmv_run_int4(d, p, _dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
+    qq, _, s16 = int4.quantize(w)
+    yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+    _check(y.cpu().numpy(), yr, B, f"int4 lut N={N} K={K}")
+
+
+@pytest.mark.parametrize("case", ["saturated", "one_code", "channels", "huge", "range"])
+def test_int4_lut_hard_inputs(env, case):
+    """Saturated groups (every code at +-7 against activations just under a power of two), one
+    nonzero code per group, outlier channels on zero codes and a 2^24 range inside one row, at
+    K = 13824 (the INT4 layer set's down projection)."""
+    q, torch, dev = env
+    from oracle import int4
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    N, K = 96, 13824
+    if case == "saturated":
+        w = synth.student_t4(synth.rng(3), (N, K))
+        w[0], w[1] = 0.02, -0.02
+        w[2, 0::2], w[2, 1::2] = 0.02, -0.02
+        xb = synth.to_bf16_bits(np.full((1, K), 0.99, np.float32))
+    elif case == "one_code":
+        g = synth.rng(4)
+        w = np.zeros((N, K), np.float32)
+        hit = g.integers(0, 128, size=(N, K // 128)) + 128 * np.arange(K // 128)[None, :]
+        w[np.arange(N)[:, None], hit] = np.float32(0.02) * np.where(g.random((N, K // 128)) < 0.5, -1, 1)
+        xb = synth.activations_bf16(g, (1, K))
+    else:
+        w, xb = synth.outlier_case(case, N, K, 1, seed=K + 9)
+    d, p = _pack4(q, torch, dev, w)
+    y = torch.full((1, N), float("nan"), device=dev)
+    q.qmv_run_int4(d, p, _dev_bf16(torch, xb, dev), y)
+    assert q.qmv_check_status() == 0
+    qq, _, s16 = int4.quantize(w)
+    yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+    _check(y.cpu().numpy(), yr, B, f"int4 lut {case}")
+
+
+def test_int4_lut_layer_set_batched_sampled(env):
+    """The INT4 GQA layer set (hidden 5120, 40/8 heads, SwiGLU 13824) in the lookup layout, one
+    batched launch as the benchmark runs it, and each matrix alone (a smaller launch, whose blocks
+    a cluster may split differently); sampled rows of both against the oracle."""
+    q, torch, dev = env
+    from oracle import int4
+    from oracle.matvec import matvec_bf16x
+    from quantized_gemv_unpack_gb300 import synth
+    gen = synth.torch_generator(1, dev)
+    shapes = synth.gqa_layer_shapes(5120, 40, 8, 128, 13824)
+    mats, ws = [], []
+    for name, N, K in shapes:
+        w = synth.student_t4_torch(gen, (N, K), device=dev)
+        mats.append(_pack4(q, torch, dev, w))
+        ws.append(w)
+    xs = {K: synth.activations_bf16_torch(gen, (1, K), device=dev) for K in {5120, 13824}}
+    ys = [torch.empty((1, N), device=dev) for _, N, _ in shapes]
+    q.qmv_run_batch(q.QMV_INT4_LUT, [(d, p, xs[K], y) for (d, p), (_, N, K), y in zip(mats, shapes, ys)], 1)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    for (d, p), (name, N, K), w, y in zip(mats, shapes, ws, ys):
+        y1 = torch.empty_like(y)
+        q.qmv_run_int4(d, p, xs[K], y1)
+        rows = np.unique(np.concatenate(([0, N - 1], rng.choice(N, 24, replace=False))))
+        qq, _, s16 = int4.quantize(w[torch.from_numpy(rows).to(dev)].cpu().numpy())
+        xb = xs[K].view(torch.int16).cpu().numpy().view(np.uint16)
+        yr, B = matvec_bf16x(int4.dequant(qq, s16), xb)
+        idx = torch.from_numpy(rows).to(dev)
+        _check(y[:, idx].cpu().numpy(), yr, B, name)
+        _check(y1[:, idx].cpu().numpy(), yr, B, name + " alone")
+    assert q.qmv_check_status() == 0
+
+
+def test_int4_lut_rejects_mixed_batches_and_m_above_1(env):
+    q, torch, dev = env
+    from quantized_gemv_unpack_gb300 import synth
+    w = synth.student_t4(synth.rng(2), (32, 256))
+    d4, p4 = _pack4(q, torch, dev, w)
+    dt, pt = _pack(q, torch, dev, w)
+    x = torch.zeros((2, 256), dtype=torch.bfloat16, device=dev)
+    y = torch.zeros((2, 32), device=dev)
+    with pytest.raises(q.QmvError):
+        q.qmv_run_int4(d4, p4, x, y)                                   # M = 2
+    with pytest.raises(q.QmvError):
+        q.qmv_run_batch(q.QMV_INT4_LUT, [(d4, p4, x[:1], y[:1]), (dt, pt, x[:1], y[1:])], 1)
