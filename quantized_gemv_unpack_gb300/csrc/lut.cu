@@ -602,8 +602,11 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   // Rows per unit and CTAs per cluster: whole 1024-row units on single CTAs
   // when there are enough of them; otherwise smaller units whose blocks a
   // cluster of up to 8 CTAs shares, until the launch covers twice the SMs
-  // (measured: the INT4 layer set 74 -> 46 us against covering the SMs once,
-  // the small ternary launches unchanged).
+  // (matvec batches: the INT4 layer set 74 -> 46 us, the 4096 x 4096 ternary
+  // matrix 13.2 -> 12.0 us against covering them once) or the SMs once (the
+  // MoE phases, whose pairs at M >= 2 would otherwise run clusters of 8 beyond
+  // the resident CTAs: M = 8 140 -> 134 us).
+  const int64_t target = PHASE == 0 ? 2 * (int64_t)sms : (int64_t)sms;
   int rows = kUnitRowsMax, C = 1;
   if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
     bool done = false;
@@ -611,7 +614,7 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
       for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
         rows = r;
         C = c;
-        if (units_for(r) * c >= 2 * sms) {
+        if (units_for(r) * c >= target) {
           done = true;
           break;
         }
