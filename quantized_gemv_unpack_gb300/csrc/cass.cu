@@ -351,15 +351,17 @@ __host__ __device__ inline size_t cass_per_warp(size_t K, size_t scap, bool targ
   return (w * 4 + 15) / 16 * 16;
 }
 
-// Bytes of the (rank, nibble) -> draft bits table: bf16 bits S<<15 | E<<7 |
-// m_hi<<4 for every codebook rank and sign/high-mantissa nibble.
-__host__ __device__ inline size_t cass_tab_bytes(int n_symbols) { return ((size_t)n_symbols * 32 + 15) / 16 * 16; }
+// Bytes of the (rank, nibble) -> draft value table: the fp32 bits of the bf16
+// draft value S<<15 | E<<7 | m_hi<<4 (shifted left by 16) for every codebook rank
+// and sign/high-mantissa nibble; the target ORs the low mantissa nibble in at
+// bits 16..19.
+__host__ __device__ inline size_t cass_tab_bytes(int n_symbols) { return (size_t)n_symbols * 64; }
 
 // The staged row one lane walks.
 struct CassRow {
   const uint32_t *bm, *sm, *lo, *st;
   const uint16_t* prg;  // the row's pruned halves (global)
-  const uint16_t* tab;
+  const uint32_t* tab;
   const uint16_t* xs;
   uint16_t* wrow;
   int KW, nsw, nsym, sk;
@@ -389,9 +391,9 @@ __device__ __forceinline__ void cass_walk(const CassRow& r, float (&acc)[MT], bo
     }
     const int sh = (k & 7) * 4;
     uint32_t v = r.tab[rank * 16 + ((smw >> sh) & 0xFu)];
-    if (TARGET) v |= (low >> sh) & 0xFu;
-    if (WOUT) r.wrow[j] = (uint16_t)v;
-    accumulate<MT>(r.xs, j, r.sk, __uint_as_float(v << 16), acc);
+    if (TARGET) v |= ((low >> sh) & 0xFu) << 16;
+    if (WOUT) r.wrow[j] = (uint16_t)(v >> 16);
+    accumulate<MT>(r.xs, j, r.sk, __uint_as_float(v), acc);
     if (TARGET || WOUT) {
       const int jz = cursor_next<true, SAFE>(cz, r.bm, r.KW, bad);
       uint32_t pv = 0;
@@ -423,6 +425,9 @@ __device__ __forceinline__ void cass_walk8(const CassRow& r, float (&acc)[MT], b
   Cursor cz = cursor_at<true>(r.bm, r.KW, r.zpos);
   const uint32_t st_base = smem_u32(r.st), bm_base = smem_u32(r.bm);
   int send = r.send;
+  // ranks are clamped to the codebook for the lookup and their maximum checked once
+  unsigned rmax = 0;
+  const unsigned rlast = (unsigned)r.nsym - 1u;
   uint4 pnext = TARGET ? pruned_block(r.prg, r.k0) : make_uint4(0, 0, 0, 0);
   for (int k = r.k0; k < r.k0 + r.cnt; k += 8) {
     const uint32_t smw = r.sm[skew<3>(k >> 3)];
@@ -432,16 +437,17 @@ __device__ __forceinline__ void cass_walk8(const CassRow& r, float (&acc)[MT], b
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int sp = cursor_step<false>(cs, st_base);
-      int rank = sp - send;
+      const unsigned rank = (unsigned)(sp - send);
       send = sp + 1;
-      if ((unsigned)rank >= (unsigned)r.nsym) bad = true, rank = 0;
-      uint32_t v = r.tab[rank * 16 + ((smw >> (4 * u)) & 0xFu)];
-      if (TARGET) v |= (low >> (4 * u)) & 0xFu;
-      accumulate<MT>(r.xs, cursor_step<false>(ck, bm_base), r.sk, __uint_as_float(v << 16), acc);
+      rmax = max(rmax, rank);
+      uint32_t v = r.tab[min(rank, rlast) * 16 + ((smw >> (4 * u)) & 0xFu)];
+      if (TARGET) v |= ((low >> (4 * u)) & 0xFu) << 16;
+      accumulate<MT>(r.xs, cursor_step<false>(ck, bm_base), r.sk, __uint_as_float(v), acc);
       if (TARGET)
         accumulate<MT>(r.xs, cursor_step<true>(cz, bm_base), r.sk, __uint_as_float(block_half(pcur, u) << 16), acc);
     }
   }
+  if (rmax > rlast) bad = true;
 }
 
 template <int MT, bool TARGET, bool WOUT>
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(CassWarps<MT, TARGET>::value * 32) cass_kernel
   const int nwarps = blockDim.x >> 5;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   const size_t xb = xs_bytes(K, a.sk, P);
-  uint16_t* tab = reinterpret_cast<uint16_t*>(smem + xb);
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + xb);
   uint32_t* bm_s = reinterpret_cast<uint32_t*>(smem + xb + cass_tab_bytes(a.n_symbols) +
                                                (size_t)warp * cass_per_warp(K, a.scap, TARGET));
   uint32_t* sm_s = bm_s + KW + 2;
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(CassWarps<MT, TARGET>::value * 32) cass_kernel
 
   for (int i = threadIdx.x; i < a.n_symbols * 16; i += blockDim.x) {
     const uint32_t nib = i & 15;
-    tab[i] = (uint16_t)(((nib & 8u) << 12) | ((uint32_t)a.codebook[i >> 4] << 7) | ((nib & 7u) << 4));
+    tab[i] = (((nib & 8u) << 12) | ((uint32_t)a.codebook[i >> 4] << 7) | ((nib & 7u) << 4)) << 16;
   }
   stage_x<MT>(xs, a.x, a.ldx, K, a.sk);
   __syncthreads();
