@@ -147,13 +147,15 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- CPU oracle sample
 
 def oracle_sample_main():
-    """Child process: time the float64 oracle on a bounded sample of the stack (single thread).
+    """Child process: time the float64 oracle on a bounded sample of the stack (one thread).
 
     The sample unit is the k and v matrices of one layer (2 x 1024 x 5120 weights):
     the oracle decodes their packed bytes, dequantizes and forms y in float64.
-    Weights are generated and packed by the oracle before the clock starts.
-    QMV_ORACLE_PASSES fixes the number of passes; otherwise passes repeat until
-    QMV_ORACLE_SECONDS of CPU work have been timed.
+    Weights are generated and packed by the oracle before the clock starts; the child
+    then prints "ready" and starts its clock when the parent writes a line to its
+    standard input, so that all children run at the same time. QMV_ORACLE_PASSES
+    fixes the number of passes; otherwise passes repeat until QMV_ORACLE_SECONDS of
+    CPU work have been timed.
     """
     from oracle import matvec as o_mv
     from oracle import ternary as o_t
@@ -169,6 +171,8 @@ def oracle_sample_main():
         packed.append((o_t.pack(qq, s16), N, K))
     x = synth.activations_bf16(g, (1, HIDDEN))
     nbytes = sum(len(b) for b, _, _ in packed) + HIDDEN * 2 + sum(N for _, N, _ in packed) * 4
+    print("ready", flush=True)
+    sys.stdin.readline()
     done = 0
     t0 = time.perf_counter()
     while True:
@@ -179,23 +183,54 @@ def oracle_sample_main():
         el = time.perf_counter() - t0
         if (passes and done >= passes) or (not passes and el >= budget):
             break
-    print(json.dumps({"seconds": el / done, "passes": done, "bytes": nbytes,
-                      "weights": sum(N * K for _, N, K in packed)}))
+    print(json.dumps({"seconds": el, "passes": done, "bytes": nbytes,
+                      "weights": sum(N * K for _, N, K in packed)}), flush=True)
 
 
-def run_oracle_sample(passes=0, seconds=10.0):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_oracle_sample(passes=0, seconds=10.0, cores=None):
+    """The oracle's sample on every host core: one single-threaded child per core, all
+    started together; throughput = all children's bytes / the slowest child's time."""
+    cores = cores or host_cores()
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                QMV_ORACLE_PASSES=str(passes), QMV_ORACLE_SECONDS=str(seconds))
-    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child"], env=env,
-                       capture_output=True, text=True, cwd=ROOT)
-    if p.returncode:
-        raise RuntimeError("oracle sample failed: " + p.stderr[-2000:])
-    r = json.loads(p.stdout.strip().splitlines()[-1])
-    gbs = r["bytes"] / r["seconds"] / 1e9
-    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds_per_pass": r["seconds"],
-            "sample": f"k and v matrices of one stack layer ({r['weights'] / 1e6:.1f}M weights, "
-                      f"{r['bytes'] / 1e6:.2f} MB packed) decoded, dequantized and multiplied in float64 NumPy "
-                      f"on one thread; {r['passes']} passes, {r['seconds']:.3f} s each"}
+    kids = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-child"], env=env, cwd=ROOT,
+                             stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+            for _ in range(cores)]
+    try:
+        for k in kids:
+            if k.stdout.readline().strip() != "ready":
+                raise RuntimeError("oracle sample failed: " + k.stderr.read()[-2000:])
+        for k in kids:
+            k.stdin.write("go\n")
+            k.stdin.flush()
+        res = []
+        for k in kids:
+            out, err = k.communicate()
+            if k.returncode:
+                raise RuntimeError("oracle sample failed: " + err[-2000:])
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    finally:
+        for k in kids:
+            if k.poll() is None:
+                k.kill()
+                k.wait()
+    wall = max(r["seconds"] for r in res)
+    total = sum(r["bytes"] * r["passes"] for r in res)
+    gbs = total / wall / 1e9
+    r0 = res[0]
+    per_pass = wall / min(r["passes"] for r in res)
+    return {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle", "seconds_per_pass": per_pass,
+            "sample": f"k and v matrices of one stack layer ({r0['weights'] / 1e6:.1f}M weights, "
+                      f"{r0['bytes'] / 1e6:.2f} MB packed) decoded, dequantized and multiplied in float64 NumPy; "
+                      f"{cores} single-threaded processes (one per host core) at once, "
+                      f"{sum(r['passes'] for r in res)} passes in {wall:.2f} s"}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -810,7 +845,7 @@ def main():
                 "warmup": a.warmup, "ms_per_step": base["seconds_per_pass"] * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
                 "config": Stack.stack_config(LAYERS, a.layout or "lut"), "impl": "reference",
-                "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
+                "cpu_baseline": {"kind": "oracle", "cores": base["cores"], "sample": base["sample"], "value": base["value"],
                                  "unit": UNIT},
                 "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))

@@ -30,10 +30,12 @@
 //
 // Work split. A unit is up to 1024 rows of one matvec (unit_rows) over all of
 // its blocks (a cluster of C CTAs splits the blocks, each CTA a contiguous
-// share, and CTA rank 0 adds the C partial sums in rank order through
-// distributed shared memory). The host assigns units to CTAs (clusters)
-// largest first, each to the least loaded one, and passes the lists in the
-// launch parameters. Each of the 256 threads owns up to four rows of a unit
+// share; then each CTA adds a 1/C share of the unit's rows over the C partial
+// sums, in rank order, through distributed shared memory, so that the cluster
+// finishes together). The host assigns units to CTAs (clusters) largest first,
+// each to the least loaded one, and passes the lists in the launch parameters;
+// when all units cost the same the device takes them round robin itself (no
+// list to read), and tasks of one shape find their unit's task by a division. Each of the 256 threads owns up to four rows of a unit
 // (rows r0 + 256 j + tid); lane = row % 32.
 //
 // INT4 (lut_kernel<QMV_INT4_LUT, 0>): a code byte is one column pair (two
@@ -59,8 +61,10 @@
 // unit contiguous per block, so a thread's row is two coalesced 16-byte loads.
 // Right after a row's lookups its registers are reloaded with the same row slot
 // of the next step, and one thread asks the copy engine to prefetch the step
-// after next into L2 (cp.async.bulk.prefetch), so those loads hit L2; a launch
-// whose weights fit half of L2 asks for all of a CTA's steps at its start. No
+// after next into L2 (cp.async.bulk.prefetch), so those loads hit L2. At its
+// start a CTA asks for its second step (and, when the launch's weights fit half
+// of L2, all of its steps) by one L2 line prefetch per thread: the copy engine,
+// busy with every CTA's requests at once, would hold its one thread back. No
 // wait in this kernel spins: it synchronizes only with CTA and cluster barriers
 // and the dependent-launch wait.
 #include <algorithm>
@@ -124,6 +128,7 @@ struct LutMoe {
 struct LutBatch {
   int32_t n_tasks, n_units, unit_rows, n_workers;
   int32_t sched_n;             // 0: unit u goes to worker u % n_workers
+  int32_t upt;                 // units per task when every task has the same N (task = unit / upt), else 0
   uint32_t smem_bytes;         // dynamic shared memory of the launch
   int32_t prefetch_all;        // 1: each CTA asks L2 for all of its steps at its start (small launches)
   int* err;
@@ -149,7 +154,10 @@ __device__ __forceinline__ float lds_at(uint32_t a) {
 __device__ __forceinline__ void sts_f32(uint32_t a, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+__device__ __forceinline__ void l2_prefetch_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -219,6 +227,7 @@ struct Item {
 };
 
 __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
+  if (b.upt) return unit / b.upt;
   int lo = 0, hi = b.n_tasks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -228,7 +237,6 @@ __device__ __forceinline__ int find_lut_task(const LutBatch& b, int unit) {
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
-
 
 // FMT: QMV_TERNARY2_LUT or QMV_INT4_LUT. PHASE 0: the tasks' matvecs; 1 / 2: the
 // MoE gate|up / down phase (see LutMoe; ternary only).
@@ -261,12 +269,9 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
   int* pair_expert = nullptr;
   if constexpr (PHASE > 0) {
     __shared__ MoeRoute s_route;
-    __shared__ int s_pair_expert[kMaxPairs];
     R = &s_route;
-    pair_expert = s_pair_expert;
     route(b.moe.routing, *R);
-    for (int sl = tid; sl < R->n_slots; sl += kThreadsL)
-      for (int j = R->slot_first[sl]; j < R->slot_first[sl] + R->slot_count[sl]; ++j) pair_expert[j] = R->slot_expert[sl];
+    pair_expert = R->pair_expert;
     if constexpr (PHASE == 1) {
       const LutMoe& mo = b.moe;
       for (int i = blockIdx.x * kThreadsL + tid; i < mo.routing.M * mo.H; i += gridDim.x * kThreadsL)
@@ -290,7 +295,15 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
   // the codes of task ti (MoE: of its pair's expert)
   auto codes_of = [&](int ti) -> const unsigned char* {
     if constexpr (PHASE == 0) return b.t[ti].codes;
-    else return b.t[ti].codes + (size_t)pair_expert[ti] * (size_t)b.moe.stride;
+    else return b.t[0].codes + (size_t)pair_expert[ti] * (size_t)b.moe.stride;  // one base for every pair
+  };
+  // rows, 32-row groups and blocks of task ti
+  struct Geo {
+    int N, NG, KB;
+  };
+  auto geo = [&](int ti) -> Geo {
+    const LutTask& T = b.t[ti];
+    return Geo{T.N, T.NG, T.KB};
   };
 
   // this worker's units
@@ -323,15 +336,32 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
     if (++s.bk < s.kb1) return s;
     return unit_step(s.k + 1);
   };
-  auto prefetch_step = [&](const Step& s) {
+  // one thread: ask the copy engine to bring a step's code records (contiguous)
+  // and scales into L2; it issues no load of its own, so the lookups' L1 path
+  // stays free, but it may wait while the engine is busy
+  auto prefetch_step_bulk = [&](const Step& s) {
     if (!s.valid) return;
-    const LutTask& T = b.t[s.ti];
+    const Geo T = geo(s.ti);
     const unsigned char* codes = codes_of(s.ti);
     const int g0 = s.r0 >> 5;
     const int ng = s.nrows32() >> 5;
-    l2_prefetch(codes + ((size_t)s.bk * T.NG + g0) * LF::REC, (uint32_t)ng * LF::REC);
+    l2_prefetch_bulk(codes + ((size_t)s.bk * T.NG + g0) * LF::REC, (uint32_t)ng * LF::REC);
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(codes + (size_t)T.NG * T.KB * LF::REC);
-    l2_prefetch(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
+    l2_prefetch_bulk(sc + (size_t)s.bk * T.NG * 32 + s.r0, (uint32_t)ng * 64u);
+  };
+  // all threads: the same by one 128-byte line per thread and pass (never waits)
+  auto prefetch_step = [&](const Step& s) {
+    if (!s.valid) return;
+    const Geo T = geo(s.ti);
+    const unsigned char* codes = codes_of(s.ti);
+    const int g0 = s.r0 >> 5;
+    const int ng = s.nrows32() >> 5;
+    const unsigned char* c0 = codes + ((size_t)s.bk * T.NG + g0) * LF::REC;
+    const uint32_t nc = (uint32_t)ng * LF::REC;
+    for (uint32_t o = (uint32_t)tid * 128u; o < nc; o += kThreadsL * 128u) l2_prefetch_line(c0 + o);
+    const unsigned char* s0 = codes + (size_t)T.NG * T.KB * LF::REC + ((size_t)s.bk * T.NG * 32 + s.r0) * 2;
+    const uint32_t ns = (uint32_t)ng * 64u;
+    if ((uint32_t)tid * 128u < ns + 128u) l2_prefetch_line(s0 + min((uint32_t)tid * 128u, ns - 1u));
   };
   // This thread's load addresses of a step: row r0 + tid of its codes and of
   // its scales; item j (row r0 + 256 j + tid) is 8 row groups further on (8 KB
@@ -347,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
     r.sc = nullptr;
     r.n32 = 0;
     if (!s.valid) return r;
-    const LutTask& T = b.t[s.ti];
+    const Geo T = geo(s.ti);
     const unsigned char* codes = codes_of(s.ti);
     r.cw = reinterpret_cast<const uint4*>(codes) + ((size_t)s.bk * T.NG + (s.r0 >> 5) + (tid >> 5)) * (LF::REC / 16) +
            lane;
@@ -494,17 +524,15 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
 #pragma unroll
       for (int j = 0; j < kRpt; ++j) sts_f32(pbase + (uint32_t)((j * kThreadsL + tid) * 4), acc[j]);
       cluster_sync();
-      if (rank == 0) {
-#pragma unroll
-        for (int j = 0; j < kRpt; ++j) {
-          const int row = s.r0 + j * kThreadsL + tid;
-          if (j * kThreadsL + tid < s.nrows) {
-            const uint32_t a = pbase + (uint32_t)((j * kThreadsL + tid) * 4);
-            float v = acc[j];
-            for (uint32_t r = 1; r < C; ++r) v += ld_cluster_f32(a, r);
-            store(s, row, v);
-          }
-        }
+      // CTA `rank` adds its share of the unit's rows over the C partial sums, in rank
+      // order, and stores them (every CTA of the cluster reads every other one's sums)
+      const int per = (s.nrows + (int)C - 1) / (int)C;
+      const int u_end = min((int)(rank + 1) * per, s.nrows);
+      for (int u = (int)rank * per + tid; u < u_end; u += kThreadsL) {
+        const uint32_t a = pbase + (uint32_t)(u * 4);
+        float v = 0.f;
+        for (uint32_t r = 0; r < C; ++r) v += ld_cluster_f32(a, r);
+        store(s, s.r0 + u, v);
       }
       parity ^= 1;
     }
@@ -517,10 +545,6 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
   // up this step's rows, each slot reloaded with the next step's row at once.
   Step cur = unit_step(k_beg);
   Step nxt = advance(cur);
-  if (tid == 0 && cur.valid) {
-    prefetch_step(cur);
-    prefetch_step(nxt);
-  }
   ItemT A[kRpt];
 #pragma unroll
   for (int j = 0; j < kRpt; ++j) {
@@ -533,6 +557,7 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
 #pragma unroll
     for (int j = 0; j < kRpt; ++j) load_item(first, j, A[j]);
   }
+  prefetch_step(nxt);
   // zero the table rows of invalid code bytes (any 2-bit field equal to 3) while
   // the first loads are in flight (the loop's first barrier orders the zeros
   // before any lookup)
@@ -543,14 +568,16 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
     }
   // a small launch asks L2 for all of its weights now (the MoE down phase does so
   // while the gate|up grid still runs); a large one keeps two steps ahead
-  if (b.prefetch_all && tid == 0)
-    for (Step p = nxt; p.valid; p = advance(p)) prefetch_step(p);
+  if (b.prefetch_all)
+    for (Step p = advance(nxt); p.valid; p = advance(p)) prefetch_step(p);
   // MoE down: the weights above do not depend on the gate|up grid; g and u do
   if (PHASE == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
   float4 xc = load_x(cur);
   while (cur.valid) {
     const Step nn = advance(nxt);
-    if (tid == 0 && !b.prefetch_all) prefetch_step(nn);
+    if (!b.prefetch_all) {
+      if (tid == 0) prefetch_step_bulk(nn);
+    }
     const float4 xn = load_x(nxt);
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
@@ -623,11 +650,19 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
     }
   }
   int64_t n_units = 0, weight_bytes = 0;
+  bool same_n = true, same_cost = true;
   for (int i = 0; i < n; ++i) {
     b.t[i].unit0 = (int32_t)n_units;
     n_units += (b.t[i].N + rows - 1) / rows;
     weight_bytes += (int64_t)b.t[i].NG * b.t[i].KB * (LutFmt<FMT>::REC + 64);
+    same_n = same_n && b.t[i].N == b.t[0].N;
+    same_cost = same_cost && b.t[i].KB == b.t[0].KB && (b.t[i].N % rows == 0 || b.t[i].N < rows);
   }
+  // tasks of one shape: the device finds a unit's task by a division (no search)
+  b.upt = same_n ? (b.t[0].N + rows - 1) / rows : 0;
+  // units of one cost: the greedy schedule below is the round robin, which the
+  // device computes itself (no list to read)
+  same_cost = same_cost && (same_n || n == 1);
   // launches whose weights fit half of L2 are latency-bound: fetch them all at once
   b.prefetch_all = weight_bytes <= (int64_t)64 << 20 ? 1 : 0;
   if (n_units > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
@@ -670,7 +705,7 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   b.n_workers = workers;
 
   // largest units first, each to the least loaded worker
-  if (n_units <= kMaxUnitsL) {
+  if (n_units <= kMaxUnitsL && !same_cost) {
     std::vector<std::pair<int64_t, int>> cost((size_t)n_units);
     for (int i = 0; i < n; ++i) {
       const LutTask& T = b.t[i];

@@ -11,8 +11,8 @@ int check_lut_desc(const qmv_desc* d);
 int run_lut(const qmv_task* tasks, int n, cudaStream_t s);
 
 // The MoE decode over experts in the lookup layout (arguments already checked
-// by moe_qmv_run): gate|up and down launches, one (token, expert) pair per
-// task, routing in every CTA, workspace offsets as moe_qmv_run's layout.
+// by moe_qmv_run): one (token, expert) pair per task, routing in every CTA,
+// workspace offsets as moe_qmv_run's layout; a gate|up and a down launch.
 struct LutMoeCall {
   const unsigned char* gu_codes;  // expert 0's [gate; up] codes (2I x H); expert e at + e * stride
   const unsigned char* dn_codes;  // expert 0's down codes (H x I)

@@ -41,3 +41,12 @@ def test_max_over_ranks_and_job_throughput():
     # 7.29 GB per replica in the slowest rank's 2 ms, two replicas
     assert bench.job_throughput(7.29e9, 2.0, world) == pytest.approx(2 * 7.29e9 / 2e-3 / 1e9)
     assert bench.job_throughput(7.29e9, 2.0, 1) == pytest.approx(3645.0)
+
+
+def test_oracle_sample_runs_one_child_per_core():
+    # two single-threaded children, one pass each, started together: the job's bytes are
+    # both children's, over the slower child's time
+    r = bench.run_oracle_sample(passes=1, cores=2)
+    assert r["cores"] == 2 and r["kind"] == "oracle" and r["unit"] == bench.UNIT
+    assert "2 single-threaded processes" in r["sample"] and "2 passes" in r["sample"]
+    assert r["value"] == pytest.approx(2 * 2.80e6 / r["seconds_per_pass"] / 1e9, rel=0.01)
