@@ -744,12 +744,29 @@ def job_throughput(bytes_per_step_per_rank: float, ms_per_step: float, world: in
 
 # ----------------------------------------------------------------------------- timing
 
-def time_steps(wl, steps, warmup, stream, torch):
-    """Mean device time (ms) of `steps` steps after `warmup` untimed ones, CUDA events on `stream`."""
+def time_steps(wl, steps, warmup, stream, torch, graph=False):
+    """Mean device time (ms) of `steps` steps after `warmup` untimed ones, CUDA events on `stream`.
+    graph: the steps are captured once into a CUDA graph (on torch's capture stream), which is
+    replayed once untimed and then timed, so that the kernels run back to back as in a decode loop
+    that replays its step graph; otherwise the steps are launched one by one from the host."""
     for i in range(warmup):
         wl.step(i, stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            for i in range(steps):
+                wl.step(i, cs)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) / steps
     e0.record(stream)
     for i in range(steps):
         wl.step(i, stream)
@@ -774,19 +791,22 @@ NOMINAL_HBM_GBS = 8000.0
 
 
 def measure_configs(q, torch, dev, stream, steps, warmup, peak):
-    """Every other configuration, measured in this process under one clock record: time per step,
-    GB/s on the algorithmic bytes, fractions of the measured copy peak and of the nominal 8 TB/s,
-    and the ncu DRAM traffic per step where a current capture exists."""
+    """Every other configuration, measured in this process under one clock record: time per step
+    (the steps replayed as one CUDA graph; the host-launched time beside it), GB/s on the
+    algorithmic bytes, fractions of the measured copy peak and of the nominal 8 TB/s, and the ncu
+    DRAM traffic per step where a current capture exists."""
     out = {}
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
     for key, name, M in CONFIGS:
         args = argparse.Namespace(M=M, path="auto", layout=None, layers=LAYERS, int4_layers=1)
         wl = make_workload(name, q, torch, dev, args)
-        ms = time_steps(wl, steps, warmup, stream, torch)
+        ms_host = time_steps(wl, steps, warmup, stream, torch)
+        ms = time_steps(wl, steps, warmup, stream, torch, graph=True)
         nb = sum(wl.bytes(i) for i in range(steps)) / steps
         gbs = nb / (ms * 1e-3) / 1e9
-        out[key] = {"us_per_step": ms * 1e3, "GB_s": gbs, "frac_of_measured_copy": gbs / peak,
+        out[key] = {"us_per_step": ms * 1e3, "us_per_step_host_launched": ms_host * 1e3,
+                    "GB_s": gbs, "frac_of_measured_copy": gbs / peak,
                     "frac_of_nominal_8TB_s": gbs / NOMINAL_HBM_GBS, "algorithmic_bytes_per_step": nb,
                     "traffic": wl.traffic(), "kernel": wl.kernel, "workload": wl.config()["workload"]}
         if name.startswith("cass"):
@@ -798,6 +818,8 @@ def measure_configs(q, torch, dev, stream, steps, warmup, peak):
     assert q.qmv_check_status() == 0
     out["clocks"] = clocks.stop()
     out["steps_each"] = steps
+    out["timing"] = (f"{steps} steps captured as one CUDA graph and replayed (us_per_step); the same steps "
+                     f"launched one by one from the host beside it (us_per_step_host_launched)")
     return out
 
 
@@ -820,6 +842,9 @@ def main():
                          "for the stack and the MoE experts, records for the single 4096 x 4096 matrix, where the "
                          "record kernel is ahead)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the steps as one replayed CUDA graph instead of host launches (not for the "
+                         "default line)")
     ap.add_argument("--no-configs", action="store_true",
                     help="default workload only: skip measuring the other configurations in the same run")
     ap.add_argument("--layers", type=int, default=LAYERS, help="stack depth (a smaller case for profiling)")
@@ -883,13 +908,17 @@ def main():
     clocks.start()
     time.sleep(0.3)
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(a.steps):
-        wl.step(i, stream)
-    ev1.record(stream)
-    barrier()
-    ms = ev0.elapsed_time(ev1) / a.steps
+    if a.graph:
+        ms = time_steps(wl, a.steps, 0, stream, torch, graph=True)
+        barrier()
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(a.steps):
+            wl.step(i, stream)
+        ev1.record(stream)
+        barrier()
+        ms = ev0.elapsed_time(ev1) / a.steps
     clk = clocks.stop()
     assert q.qmv_check_status() == 0
     nbytes = sum(wl.bytes(i) for i in range(a.steps)) / a.steps
@@ -941,7 +970,9 @@ def main():
         "dtype": "f32" if "lut_kernel" in wl.kernel else (
             "fp16x2-f32" if a.workload in ("stack", "stack-sparse", "ternary-4096", "int4-layer", "moe") else "f32"),
         "data": DATA,
-        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU", kernel_choice=a.path),
+        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "single GPU", kernel_choice=a.path,
+                       timing="steps captured as one CUDA graph and replayed" if a.graph else
+                       "steps launched one by one from the host"),
         "pct_of_peak": 100.0 * per_gpu / peak,
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,

@@ -68,6 +68,7 @@
 // wait in this kernel spins: it synchronizes only with CTA and cluster barriers
 // and the dependent-launch wait.
 #include <algorithm>
+#include <mutex>
 #include <cstring>
 #include <queue>
 #include <vector>
@@ -614,6 +615,43 @@ int check_lut_desc(const qmv_desc* d) {
 
 namespace {
 
+// Clusters of c CTAs of a lookup kernel (72 KB of shared memory, 256 threads)
+// that fit the device at once, looked up once per kernel, device and c.
+int active_clusters(const void* kernel, int c, int* out) {
+  struct Entry {
+    const void* k;
+    int dev, c, n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.k == kernel && e.dev == dev && e.c == c) {
+      *out = e.n;
+      return QMV_OK;
+    }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(c * 8));
+  cfg.blockDim = dim3(kThreadsL);
+  cfg.dynamicSmemBytes = kSmemL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nc = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+  if (nc < 1) return fail(QMV_ERR_UNSUPPORTED, "no cluster of %d CTAs fits the device", c);
+  cache.push_back({kernel, dev, c, nc});
+  *out = nc;
+  return QMV_OK;
+}
+
 // Units, clusters and the schedule of the n tasks in b.t, then the launch of
 // lut_kernel<PHASE> (as a programmatic dependent of the previous launch on the
 // stream when pdl is set).
@@ -626,13 +664,26 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
     for (int i = 0; i < n; ++i) u += (b.t[i].N + rows - 1) / rows;
     return u;
   };
+  auto kernel = lut_kernel<FMT, PHASE>;
+  int per_sm = 0;
+  int rc = kernel_fit((const void*)kernel, kThreadsL, kSmemL, &per_sm);
+  if (rc) return rc;
+  // CTAs (c = 1) or clusters of c CTAs resident at once
+  auto workers_for = [&](int c, int* w) -> int {
+    if (c == 1) {
+      *w = sms * per_sm;
+      return QMV_OK;
+    }
+    return active_clusters((const void*)kernel, c, w);
+  };
   // Rows per unit and CTAs per cluster: whole 1024-row units on single CTAs
   // when there are enough of them; otherwise smaller units whose blocks a
   // cluster of up to 8 CTAs shares, until the launch covers twice the SMs
   // (matvec batches: the INT4 layer set 74 -> 46 us, the 4096 x 4096 ternary
   // matrix 13.2 -> 12.0 us against covering them once) or the SMs once (the
   // MoE phases, whose pairs at M >= 2 would otherwise run clusters of 8 beyond
-  // the resident CTAs: M = 8 140 -> 134 us).
+  // the resident CTAs: M = 8 140 -> 134 us). A schedule-length model (units of
+  // 512 rows for the INT4 layer set) measured slower: 49.9 against 45.5 us.
   const int64_t target = PHASE == 0 ? 2 * (int64_t)sms : (int64_t)sms;
   int rows = kUnitRowsMax, C = 1;
   if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
@@ -673,10 +724,6 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
 
   const size_t smem = kSmemL;
   b.smem_bytes = (uint32_t)smem;
-  auto kernel = lut_kernel<FMT, PHASE>;
-  int per_sm = 0;
-  int rc = kernel_fit((const void*)kernel, kThreadsL, smem, &per_sm);
-  if (rc) return rc;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -692,15 +739,9 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  int workers = sms * per_sm;
-  if (C > 1) {
-    cfg.gridDim = dim3((unsigned)(C * 8));
-    int nc = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-    if (nc < 1) return fail(QMV_ERR_UNSUPPORTED, "no cluster of %d CTAs fits the device", C);
-    workers = nc;
-  }
+  int workers = 0;
+  rc = workers_for(C, &workers);
+  if (rc) return rc;
   workers = (int)std::min<int64_t>(std::min(workers, kMaxWorkersL), n_units);
   b.n_workers = workers;
 
