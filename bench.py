@@ -716,7 +716,10 @@ def make_workload(name, q, torch, dev, a):
         return Ternary4096(q, torch, dev, a.M or 1, path=a.path,
                            layout=(a.layout or "record") if (a.M or 1) == 1 else "record")
     if name == "int4-layer":
-        return Int4Layer(q, torch, dev, a.M or 1, path=a.path, layout=a.layout or "record", layers=a.int4_layers)
+        # batch 1: the byte-lookup layout (41.0 against 43.2 us on the tensor-core kernel, graph-replayed);
+        # M >= 2: the record layout (the lookup kernel serves M = 1)
+        lay = a.layout or ("lut" if (a.M or 1) == 1 and a.path == "auto" else "record")
+        return Int4Layer(q, torch, dev, a.M or 1, path=a.path, layout=lay, layers=a.int4_layers)
     if name == "cass-speculate":
         return CassSpeculate(q, torch, dev)
     if name in ("cass-draft", "cass-target", "cass-mx-draft", "cass-mx-target"):
@@ -838,9 +841,9 @@ def main():
     ap.add_argument("--path", default="auto", choices=list(PATH_FLAGS),
                     help="matvec kernel: the library's choice by M, or force fp16-FMA / tensor-core")
     ap.add_argument("--layout", default=None, choices=["lut", "record"],
-                    help="ternary at M = 1 and MoE experts: byte-lookup layout or row-group records (default: lookup "
-                         "for the stack and the MoE experts, records for the single 4096 x 4096 matrix, where the "
-                         "record kernel is ahead)")
+                    help="ternary and INT4 at M = 1 and MoE experts: byte-lookup layout or row-group records "
+                         "(default: lookup for the stack, the INT4 layer set at M = 1 and the MoE experts, records "
+                         "for the single 4096 x 4096 matrix, where the record kernel is ahead)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="time the steps as one replayed CUDA graph instead of host launches (not for the "
