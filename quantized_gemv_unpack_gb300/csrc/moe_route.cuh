@@ -95,8 +95,8 @@ __device__ __forceinline__ void route_topk_warp(const MoeRouting& a, MoeRoute& R
   }
 }
 
-// Called by all threads of the CTA (blockDim.x >= max(E, 32 M), a multiple of
-// 32). Ends with a CTA barrier.
+// Called by all threads of the CTA (blockDim.x a multiple of 32, at least 32 M and
+// 64); E <= 256, k <= 8, M <= 8. Ends with a CTA barrier.
 __device__ inline void route(const MoeRouting& a, MoeRoute& R) {
   const int warp = threadIdx.x >> 5;
   if (warp < a.M) {

@@ -205,3 +205,57 @@ def test_moe_rejects_bad_arguments(env):
         q.moe_qmv_run(ex.gu_desc, ex.dn_desc, ex.buf, ex.stride, ex.down_off, 4, logits, 2, x, y, ws[:64])
     with pytest.raises(q.QmvError):
         q.moe_qmv_run(ex.dn_desc, ex.gu_desc, ex.buf, ex.stride, ex.down_off, 4, logits, 2, x, y, ws)
+
+
+def _edge_logits(kind, M, E, seed):
+    """Router logits with the hard cases of the selection: many equal logits (the lower
+    expert first), signed zeros (equal), NaN entries (ranked as -inf; every token keeps at
+    least k finite logits, so none is selected)."""
+    g = np.random.default_rng(seed)
+    if kind == "random":
+        return g.standard_normal((M, E)).astype(np.float32)
+    if kind == "ties":
+        return g.choice(np.array([-1.0, 0.0, 0.5, 1.0], np.float32), size=(M, E))
+    if kind == "zeros":
+        z = g.choice(np.array([0.0, -0.0, 0.25], np.float32), size=(M, E))
+        return z.astype(np.float32)
+    if kind == "nan":
+        lg = g.standard_normal((M, E)).astype(np.float32)
+        for t in range(M):
+            lg[t, g.choice(E, size=E // 3, replace=False)] = np.nan
+        return lg
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("layout", ["record", "lut"])
+@pytest.mark.parametrize("E,topk,M", [(1, 1, 1), (7, 3, 2), (40, 8, 8), (129, 2, 3), (200, 8, 5), (256, 8, 8)])
+@pytest.mark.parametrize("kind", ["random", "ties", "zeros", "nan"])
+def test_routing_edge_cases(env, layout, E, topk, M, kind):
+    # the routing every expert CTA computes, read back from the workspace, against the oracle's
+    # top-k (larger logit first, equal logits lower expert first) and softmax
+    q, torch, dev = env
+    H = I = 128
+    ex = _small_experts(q, torch, dev, E, H, I, layout)
+    lg = _edge_logits(kind, M, E, seed=E * 100 + M)
+    if kind == "nan":
+        assert all(np.isfinite(lg[t]).sum() >= topk for t in range(M))
+    logits = torch.from_numpy(lg).to(dev)
+    x = torch.from_numpy(np.zeros((M, H), np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((M, H), device=dev)
+    ws = torch.zeros(q.moe_workspace_size(E, topk, M, H, I), dtype=torch.uint8, device=dev)
+    q.moe_qmv_run(ex.gu_desc, ex.dn_desc, ex.buf, ex.stride, ex.down_off, E, logits, topk, x, y, ws)
+    assert q.qmv_check_status() == 0
+    lg_oracle = np.where(np.isnan(lg), -np.inf, lg).astype(np.float32)
+    _check_routing(lg_oracle, topk, _ws_views(q, ws, E, topk, M, I))
+    assert np.all(y.cpu().numpy() == 0.0)   # x = 0: every expert output is 0
+
+
+_SMALL = {}
+
+
+def _small_experts(q, torch, dev, E, H, I, layout):
+    key = (E, H, I, layout)
+    if key not in _SMALL:
+        _SMALL.clear()
+        _SMALL[key] = Experts(q, torch, dev, E, H, I, seed=E, layout=layout)
+    return _SMALL[key]
