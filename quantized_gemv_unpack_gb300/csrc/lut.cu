@@ -28,7 +28,7 @@
 // slot per entry (rather than a second copy at slot c + 32 to avoid the wrap)
 // halves the table stores, which share the L1 data path with the lookups.
 //
-// Work split. A unit is up to 1024 rows of one matvec (unit_rows) over all of
+// Work split. A unit is up to 1024 rows of one matvec (its task's rows) over all of
 // its blocks (a cluster of C CTAs splits the blocks, each CTA a contiguous
 // share; then each CTA adds a 1/C share of the unit's rows over the C partial
 // sums, in rank order, through distributed shared memory, so that the cluster
@@ -108,7 +108,7 @@ struct LutTask {
   const unsigned char* codes;  // section 0; the scales follow at NG * KB * record bytes
   const uint16_t* x;           // bf16 [K]
   float* y;                    // fp32 [N]
-  int32_t N, NG, KB, unit0;    // NG 32-row groups, KB blocks, first unit of this task
+  int32_t N, rows, KB, unit0;  // rows per unit of this task (set by the launch), KB blocks, first unit
 };
 
 // The MoE expert phases (lut_kernel<1> gate|up, lut_kernel<2> down): task i is
@@ -127,7 +127,7 @@ struct LutMoe {
 };
 
 struct LutBatch {
-  int32_t n_tasks, n_units, unit_rows, n_workers;
+  int32_t n_tasks, n_units, n_workers;
   int32_t sched_n;             // 0: unit u goes to worker u % n_workers
   int32_t upt;                 // units per task when every task has the same N (task = unit / upt), else 0
   uint32_t smem_bytes;         // dynamic shared memory of the launch
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
   };
   auto geo = [&](int ti) -> Geo {
     const LutTask& T = b.t[ti];
-    return Geo{T.N, T.NG, T.KB};
+    return Geo{T.N, (T.N + 31) >> 5, T.KB};
   };
 
   // this worker's units
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
     const int unit = unit_at(k);
     s.ti = find_lut_task(b, unit);
     const LutTask& T = b.t[s.ti];
-    s.r0 = (unit - T.unit0) * b.unit_rows;
-    s.nrows = min(b.unit_rows, T.N - s.r0);
+    s.r0 = (unit - T.unit0) * T.rows;
+    s.nrows = min(T.rows, T.N - s.r0);
     s.bk = (int)(rank * (uint32_t)T.KB / C);
     s.kb1 = (int)((rank + 1) * (uint32_t)T.KB / C);
     return s;
@@ -700,17 +700,41 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
       if (done) break;
     }
   }
+  // In a small launch, a task whose units cost more than twice the typical unit
+  // (rows x blocks, the median over units) takes units of half or a quarter the
+  // rows, so that its few long units do not set the launch's length (the INT4
+  // layer set's down projection, K = 13824 against 5120).
+  for (int i = 0; i < n; ++i) b.t[i].rows = rows;
+  if (units_for(kUnitRowsMax) < 2 * (int64_t)sms && n > 1) {
+    std::vector<std::pair<int64_t, int64_t>> uc;  // (unit cost, units)
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+      const int64_t nu = (b.t[i].N + rows - 1) / rows;
+      uc.push_back({(int64_t)rows * b.t[i].KB, nu});
+      total += nu;
+    }
+    std::sort(uc.begin(), uc.end());
+    int64_t acc = 0, median = uc.back().first;
+    for (const auto& p : uc)
+      if ((acc += p.second) * 2 >= total) {
+        median = p.first;
+        break;
+      }
+    for (int i = 0; i < n; ++i)
+      while (b.t[i].rows > 256 && (int64_t)b.t[i].rows * b.t[i].KB > 2 * median) b.t[i].rows /= 2;
+  }
   int64_t n_units = 0, weight_bytes = 0;
   bool same_n = true, same_cost = true;
   for (int i = 0; i < n; ++i) {
     b.t[i].unit0 = (int32_t)n_units;
-    n_units += (b.t[i].N + rows - 1) / rows;
-    weight_bytes += (int64_t)b.t[i].NG * b.t[i].KB * (LutFmt<FMT>::REC + 64);
+    n_units += (b.t[i].N + b.t[i].rows - 1) / b.t[i].rows;
+    weight_bytes += (int64_t)((b.t[i].N + 31) / 32) * b.t[i].KB * (LutFmt<FMT>::REC + 64);
     same_n = same_n && b.t[i].N == b.t[0].N;
-    same_cost = same_cost && b.t[i].KB == b.t[0].KB && (b.t[i].N % rows == 0 || b.t[i].N < rows);
+    same_n = same_n && b.t[i].rows == b.t[0].rows;
+    same_cost = same_cost && b.t[i].KB == b.t[0].KB && (b.t[i].N % b.t[i].rows == 0 || b.t[i].N < b.t[i].rows);
   }
   // tasks of one shape: the device finds a unit's task by a division (no search)
-  b.upt = same_n ? (b.t[0].N + rows - 1) / rows : 0;
+  b.upt = same_n ? (b.t[0].N + b.t[0].rows - 1) / b.t[0].rows : 0;
   // units of one cost: the greedy schedule below is the round robin, which the
   // device computes itself (no list to read)
   same_cost = same_cost && (same_n || n == 1);
@@ -718,7 +742,6 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   b.prefetch_all = weight_bytes <= (int64_t)64 << 20 ? 1 : 0;
   if (n_units > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
   b.n_units = (int32_t)n_units;
-  b.unit_rows = rows;
   b.err = device_error_word();
   if (!b.err) return fail(QMV_ERR_CUDA, "cannot locate the device error word");
 
@@ -750,9 +773,9 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
     std::vector<std::pair<int64_t, int>> cost((size_t)n_units);
     for (int i = 0; i < n; ++i) {
       const LutTask& T = b.t[i];
-      const int nu = (T.N + rows - 1) / rows;
+      const int nu = (T.N + T.rows - 1) / T.rows;
       for (int u = 0; u < nu; ++u) {
-        const int64_t r = std::min(rows, T.N - u * rows);
+        const int64_t r = std::min(T.rows, T.N - u * T.rows);
         cost[(size_t)(T.unit0 + u)] = {r * T.KB, T.unit0 + u};
       }
     }
@@ -810,7 +833,7 @@ int run_lut(const qmv_task* tasks, int n, cudaStream_t s) {
     T.x = static_cast<const uint16_t*>(t.x);
     T.y = t.y;
     T.N = (int32_t)t.desc->N;
-    T.NG = (int32_t)((t.desc->N + 31) / 32);
+    T.rows = kUnitRowsMax;
     T.KB = (int32_t)(t.desc->K / QMV_GROUP);
     min_kb = std::min(min_kb, T.KB);
   }
@@ -844,7 +867,7 @@ int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
     T.x = nullptr;
     T.y = nullptr;
     T.N = (int32_t)(2 * c.I);
-    T.NG = (int32_t)((2 * c.I + 31) / 32);
+    T.rows = kUnitRowsMax;
     T.KB = (int32_t)(c.H / QMV_GROUP);
   }
   int rc = launch_lut<QMV_TERNARY2_LUT, 1>(b, P, (int)(c.H / QMV_GROUP), s, false);
@@ -854,7 +877,7 @@ int run_lut_moe(const LutMoeCall& c, cudaStream_t s) {
     LutTask& T = b.t[i];
     T.codes = c.dn_codes;
     T.N = (int32_t)c.H;
-    T.NG = (int32_t)((c.H + 31) / 32);
+    T.rows = kUnitRowsMax;
     T.KB = (int32_t)(c.I / QMV_GROUP);
   }
   return launch_lut<QMV_TERNARY2_LUT, 2>(b, P, (int)(c.I / QMV_GROUP), s, true);
