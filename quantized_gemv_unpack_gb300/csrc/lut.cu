@@ -62,9 +62,10 @@
 // Right after a row's lookups its registers are reloaded with the same row slot
 // of the next step, and one thread asks the copy engine to prefetch the step
 // after next into L2 (cp.async.bulk.prefetch), so those loads hit L2. At its
-// start a CTA asks for its second step (and, when the launch's weights fit half
-// of L2, all of its steps) by one L2 line prefetch per thread: the copy engine,
-// busy with every CTA's requests at once, would hold its one thread back. No
+// start a CTA asks for its second step by one L2 line prefetch per thread: the
+// copy engine, busy with every CTA's requests at once, would hold its one thread
+// back. (Asking for all of a small launch's weights at the start queued the first
+// steps' loads behind them: MoE M = 1 29.5 against 28.6 us.) No
 // wait in this kernel spins: it synchronizes only with CTA and cluster barriers
 // and the dependent-launch wait.
 #include <algorithm>
@@ -131,7 +132,6 @@ struct LutBatch {
   int32_t sched_n;             // 0: unit u goes to worker u % n_workers
   int32_t upt;                 // units per task when every task has the same N (task = unit / upt), else 0
   uint32_t smem_bytes;         // dynamic shared memory of the launch
-  int32_t prefetch_all;        // 1: each CTA asks L2 for all of its steps at its start (small launches)
   int* err;
   LutMoe moe;
   uint16_t sched_off[kMaxWorkersL + 1];
@@ -567,18 +567,12 @@ __global__ void __launch_bounds__(kThreadsL, LutFmt<FMT>::MIN_CTAS) lut_kernel(c
       const int e = i >> 5;
       if ((e & (e >> 1)) & 0x55) sts_f32(T0 + (uint32_t)(e * 256 + 4 * (i & 31)), 0.f);
     }
-  // a small launch asks L2 for all of its weights now (the MoE down phase does so
-  // while the gate|up grid still runs); a large one keeps two steps ahead
-  if (b.prefetch_all)
-    for (Step p = advance(nxt); p.valid; p = advance(p)) prefetch_step(p);
   // MoE down: the weights above do not depend on the gate|up grid; g and u do
   if (PHASE == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
   float4 xc = load_x(cur);
   while (cur.valid) {
     const Step nn = advance(nxt);
-    if (!b.prefetch_all) {
-      if (tid == 0) prefetch_step_bulk(nn);
-    }
+    if (tid == 0) prefetch_step_bulk(nn);
     const float4 xn = load_x(nxt);
     __syncthreads();  // every lookup of the previous step is done
     build(xc, T0);
@@ -723,12 +717,11 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
     for (int i = 0; i < n; ++i)
       while (b.t[i].rows > 256 && (int64_t)b.t[i].rows * b.t[i].KB > 2 * median) b.t[i].rows /= 2;
   }
-  int64_t n_units = 0, weight_bytes = 0;
+  int64_t n_units = 0;
   bool same_n = true, same_cost = true;
   for (int i = 0; i < n; ++i) {
     b.t[i].unit0 = (int32_t)n_units;
     n_units += (b.t[i].N + b.t[i].rows - 1) / b.t[i].rows;
-    weight_bytes += (int64_t)((b.t[i].N + 31) / 32) * b.t[i].KB * (LutFmt<FMT>::REC + 64);
     same_n = same_n && b.t[i].N == b.t[0].N;
     same_n = same_n && b.t[i].rows == b.t[0].rows;
     same_cost = same_cost && b.t[i].KB == b.t[0].KB && (b.t[i].N % b.t[i].rows == 0 || b.t[i].N < b.t[i].rows);
@@ -738,8 +731,6 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   // units of one cost: the greedy schedule below is the round robin, which the
   // device computes itself (no list to read)
   same_cost = same_cost && (same_n || n == 1);
-  // launches whose weights fit half of L2 are latency-bound: fetch them all at once
-  b.prefetch_all = weight_bytes <= (int64_t)64 << 20 ? 1 : 0;
   if (n_units > INT32_MAX / 2) return fail(QMV_ERR_UNSUPPORTED, "batch too large");
   b.n_units = (int32_t)n_units;
   b.err = device_error_word();
