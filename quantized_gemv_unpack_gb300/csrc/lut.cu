@@ -680,7 +680,12 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
   // 512 rows for the INT4 layer set) measured slower: 49.9 against 45.5 us.
   const int64_t target = PHASE == 0 ? 2 * (int64_t)sms : (int64_t)sms;
   int rows = kUnitRowsMax, C = 1;
-  if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
+  if (PHASE > 0 && units_for(kUnitRowsMax) >= (int64_t)sms) {
+    // MoE phases with at least a unit per SM (M = 8: 256 pairs' units): clusters of
+    // 4 keep all three CTAs of an SM busy, 3 units of 8 steps per cluster against 2
+    // of 16 for single CTAs (M = 8 121.2 -> 107.6 us; clusters of 8: 114.6)
+    C = std::min(4, min_kb);
+  } else if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
     bool done = false;
     for (int r : {kUnitRowsMax, 512, 256}) {
       for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
