@@ -670,21 +670,29 @@ int launch_lut(LutBatch& b, int n, int min_kb, cudaStream_t s, bool pdl) {
     }
     return active_clusters((const void*)kernel, c, w);
   };
-  // Rows per unit and CTAs per cluster: whole 1024-row units on single CTAs
-  // when there are enough of them; otherwise smaller units whose blocks a
-  // cluster of up to 8 CTAs shares, until the launch covers twice the SMs
-  // (matvec batches: the INT4 layer set 74 -> 46 us, the 4096 x 4096 ternary
-  // matrix 13.2 -> 12.0 us against covering them once) or the SMs once (the
-  // MoE phases, whose pairs at M >= 2 would otherwise run clusters of 8 beyond
-  // the resident CTAs: M = 8 140 -> 134 us). A schedule-length model (units of
-  // 512 rows for the INT4 layer set) measured slower: 49.9 against 45.5 us.
-  const int64_t target = PHASE == 0 ? 2 * (int64_t)sms : (int64_t)sms;
+  // Rows per unit and CTAs per cluster (matvec batches): whole 1024-row units on
+  // single CTAs when there are enough of them; otherwise smaller units whose
+  // blocks a cluster of up to 8 CTAs shares, until the launch covers twice the SMs
+  // (the INT4 layer set 74 -> 46 us, the 4096 x 4096 ternary matrix 13.2 -> 12.0 us
+  // against covering them once). A schedule-length model (units of 512 rows for the
+  // INT4 layer set) measured slower: 49.9 against 45.5 us.
+  const int64_t target = 2 * (int64_t)sms;
   int rows = kUnitRowsMax, C = 1;
-  if (PHASE > 0 && units_for(kUnitRowsMax) >= (int64_t)sms) {
-    // MoE phases with at least a unit per SM (M = 8: 256 pairs' units): clusters of
-    // 4 keep all three CTAs of an SM busy, 3 units of 8 steps per cluster against 2
-    // of 16 for single CTAs (M = 8 121.2 -> 107.6 us; clusters of 8: 114.6)
-    C = std::min(4, min_kb);
+  if (PHASE > 0) {
+    // MoE phases (1024-row units of equal cost): the cluster size whose rounds of
+    // units (units over resident clusters) times steps per unit, plus two for the
+    // fill and the reduction, are fewest; ties to the larger cluster. Against
+    // covering the SMs once: M = 3 63.7 -> 52 us, M = 8 121.2 -> 107 us (graph-replayed),
+    // M = 1, 2, 4 unchanged.
+    const int64_t units = units_for(kUnitRowsMax);
+    int64_t best = INT64_MAX;
+    for (int c = 1; c <= 8 && c <= min_kb; c *= 2) {
+      int w = 0;
+      rc = workers_for(c, &w);
+      if (rc) return rc;
+      const int64_t t = (units + w - 1) / w * ((min_kb + c - 1) / c + 2);
+      if (t <= best) best = t, C = c;
+    }
   } else if (units_for(kUnitRowsMax) < 2 * (int64_t)sms) {
     bool done = false;
     for (int r : {kUnitRowsMax, 512, 256}) {
