@@ -365,7 +365,8 @@ int cass_speculate_step(const qmv_desc* desc, const void* packed, const void* x_
 /*
  * Mixture-of-experts decode over ternary SwiGLU experts ("Nemotron 3.5 Bolt",
  * expert top-K routing): per token, the top-k of E router logits (equal logits:
- * lower expert index first), p = softmax over the k selected logits, and
+ * lower expert index first; -0 equals +0 and a NaN logit ranks as -inf), p = softmax
+ * over the k selected logits (fp32), and
  *   y_t = sum_e p_{t,e} * W_down,e ( silu(W_gate,e x_t) * (W_up,e x_t) ).
  * Only the selected experts' packed weights are read.
  * experts: device; expert e's record starts at experts + e * expert_stride and
