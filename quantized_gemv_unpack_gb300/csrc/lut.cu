@@ -35,8 +35,10 @@
 // finishes together). The host assigns units to CTAs (clusters) largest first,
 // each to the least loaded one, and passes the lists in the launch parameters;
 // when all units cost the same the device takes them round robin itself (no
-// list to read), and tasks of one shape find their unit's task by a division. Each of the 256 threads owns up to four rows of a unit
-// (rows r0 + 256 j + tid); lane = row % 32.
+// list to read), and tasks of one shape find their unit's task by a division.
+// In a small batch a task whose units cost more than twice the median unit
+// takes units of half or a quarter the rows. Each of the 256 threads owns up to
+// four rows of a unit (rows r0 + 256 j + tid); lane = row % 32.
 //
 // INT4 (lut_kernel<QMV_INT4_LUT, 0>): a code byte is one column pair (two
 // nibbles), so a block's table has 256 rows of 64 pair slots, T[lo + 16 hi][p] =
@@ -53,9 +55,10 @@
 // matrix, whose activations are its token's x (gate|up) or h = silu(g) * u of
 // its own gate|up outputs (down), and whose output goes to the workspace
 // (gate|up) or is added, times the pair's routing weight, into y by fp32
-// atomics (down). The down launch is a programmatic dependent of the gate|up
-// launch: it routes, loads its first weights and asks L2 for the rest while
-// gate|up runs, and waits for it before reading g and u.
+// atomics (down). Each phase takes the cluster size whose rounds of units over
+// the resident clusters, times steps per unit plus two, are fewest. The down
+// launch is a programmatic dependent of the gate|up launch: it routes and loads
+// its first weights while gate|up runs, and waits for it before reading g and u.
 //
 // Streaming. The codes of (block, 32-row group) are 1 KB records, rows of a
 // unit contiguous per block, so a thread's row is two coalesced 16-byte loads.
@@ -65,12 +68,12 @@
 // start a CTA asks for its second step by one L2 line prefetch per thread: the
 // copy engine, busy with every CTA's requests at once, would hold its one thread
 // back. (Asking for all of a small launch's weights at the start queued the first
-// steps' loads behind them: MoE M = 1 29.5 against 28.6 us.) No
-// wait in this kernel spins: it synchronizes only with CTA and cluster barriers
-// and the dependent-launch wait.
+// steps' loads behind them: MoE M = 1 29.5 against 28.6 us.) No wait in this
+// kernel spins: it synchronizes only with CTA and cluster barriers and the
+// dependent-launch wait.
 #include <algorithm>
-#include <mutex>
 #include <cstring>
+#include <mutex>
 #include <queue>
 #include <vector>
 
