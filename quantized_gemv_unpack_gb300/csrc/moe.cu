@@ -3,11 +3,12 @@
 //
 // Two launches on the caller's stream; g and u pass between them in the
 // caller's workspace. Each CTA of both starts by routing in shared memory (the
-// same inputs and code give every CTA the same result): one warp per token takes
-// the top-k of its E logits (equal logits: lower expert first) by k rounds of a
-// warp arg-max, softmax over the k selected logits in fp32; then one thread per
-// expert counts its (token, expert) pairs, a block scan orders the pairs by
-// expert and token and lists each active expert once (a slot).
+// same inputs and code give every CTA the same result; moe_route.cuh): one warp
+// per token takes the top-k of its E logits (equal logits: lower expert first)
+// as k rounds of a warp maximum over keys each lane keeps sorted, softmax over
+// the k selected logits in fp32; then one thread per (token, expert) pair finds
+// its place in expert-then-token order, and each active expert is listed once
+// (a slot).
 //  1. gate|up: a persistent grid (one CTA per SM) splits the units (slot,
 //     tile of 80 rows of the [gate; up] matrix) into equal contiguous ranges;
 //     a CTA stages the slot's token rows of x (gathered) once per slot and
